@@ -1,0 +1,331 @@
+"""fp64 CPU oracle for the hyper-connection residual call -- TEST INFRASTRUCTURE.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package. The product path (the CUDA library and its Python
+binding) never imports it, and it imports nothing from the product path.
+
+The arithmetic lives in ``hc_oracle.c`` (plain double-precision loops); this
+module only compiles it, marshals arrays into it and strings the calls together
+the way the turbospark-runtime 0.3.0 pages describe:
+
+* ``hc_call`` / ``mixer``: families/qwen4/mod.rs, module doc, "## Hyper-
+  connections"; families/qwen4/hc.rs, ``encode_hyper_connection``.
+* ``inject_add``: families/qwen4/mod.rs, decoder-layer pseudocode and
+  "THE INJECTION TRAP".
+* ``prefill_pair``: families/qwen4/hc.rs, the ``inject_row_offset`` paragraph
+  (token t's gates at element t*C*2 of the gate buffer inside a micro-batch),
+  and families/qwen4/mod.rs, "Chunked prefill is wired".
+* ``stack``: families/qwen4/mod.rs decoder-layer pseudocode (entry
+  replication, two calls and two inject-adds per layer, the exit mixer).
+
+Every function is pinned by ``tests/test_oracle_pins.py`` (closed forms,
+invariants, library special cases); ``tests/test_oracle_mutants.py`` plants
+plausible mistakes in a copy of the C source and checks that a pin fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "hc_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liborc_hc.so")
+
+RMS_EPS = 1e-6  # families/qwen4/mod.rs, `RMS_EPS`
+
+
+def compile_library(src: str, out: str) -> str:
+    """gcc -> shared library. ``-ffp-contract=off`` keeps every multiply and add
+    separately rounded, so x86_64 and aarch64 builds agree bit for bit."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-fPIC", "-shared", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile ``hc_oracle.c`` into ``_build/liborc_hc.so`` if it is missing or stale."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(SOURCE)):
+        return _LIB_PATH
+    return compile_library(SOURCE, _LIB_PATH)
+
+
+class _OrcWeight(ctypes.Structure):
+    _fields_ = [
+        ("kind", ctypes.c_int32),
+        ("group", ctypes.c_int32),
+        ("rows", ctypes.c_int64),
+        ("cols", ctypes.c_int64),
+        ("bf16", ctypes.c_void_p),
+        ("packed", ctypes.c_void_p),
+        ("scale", ctypes.c_void_p),
+        ("bias", ctypes.c_void_p),
+    ]
+
+
+_D = ctypes.POINTER(ctypes.c_double)
+
+
+def default_threads() -> int:
+    if hasattr(os, "sched_getaffinity"):
+        return max(1, len(os.sched_getaffinity(0)))
+    return max(1, os.cpu_count() or 1)
+
+
+def _np_bits(t) -> np.ndarray:
+    """A torch tensor (bf16/fp16 viewed as int16) or numpy array, C-contiguous."""
+    if hasattr(t, "detach"):
+        import torch  # only to reinterpret 16-bit float storage as raw bits
+        t = t.detach().cpu().contiguous()
+        if t.dtype in (torch.bfloat16, torch.float16):
+            t = t.view(torch.int16)
+        t = t.numpy()
+    return np.ascontiguousarray(t)
+
+
+def _f64(x) -> np.ndarray:
+    """Values as float64. bf16 tensors are widened by torch, an exact conversion."""
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().double().numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _dptr(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    assert a.dtype == np.float64 and a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(_D)
+
+
+@dataclass
+class _Marshalled:
+    struct: _OrcWeight
+    keep: tuple
+
+
+def _weight(w) -> Optional[_Marshalled]:
+    """Marshal a weight given by attributes kind ('bf16' | 'int4'), rows, cols,
+    data, scale, bias, group (as the seeded input generators make them)."""
+    if w is None:
+        return None
+    s = _OrcWeight()
+    s.rows, s.cols = int(w.rows), int(w.cols)
+    if w.kind == "bf16":
+        data = _np_bits(w.data).view(np.uint16)
+        assert data.shape == (s.rows, s.cols)
+        s.kind, s.group = 0, 0
+        s.bf16 = data.ctypes.data
+        keep = (data,)
+    elif w.kind == "int4":
+        packed = _np_bits(w.data).view(np.uint8)
+        scale = _np_bits(w.scale).view(np.uint16)
+        bias = _np_bits(w.bias).view(np.uint16)
+        g = int(w.group)
+        assert packed.shape == (s.rows, s.cols // 2) and s.cols % g == 0
+        assert scale.shape == (s.rows, s.cols // g) and bias.shape == scale.shape
+        s.kind, s.group = 1, g
+        s.packed, s.scale, s.bias = packed.ctypes.data, scale.ctypes.data, bias.ctypes.data
+        keep = (packed, scale, bias)
+    else:
+        raise ValueError(f"unknown weight kind {w.kind!r}")
+    return _Marshalled(s, keep)
+
+
+def _wptr(m: Optional[_Marshalled]):
+    return None if m is None else ctypes.byref(m.struct)
+
+
+class Oracle:
+    """The oracle bound to one compiled copy of ``hc_oracle.c``."""
+
+    def __init__(self, lib_path: Optional[str] = None):
+        lib = ctypes.CDLL(lib_path or build())
+        lib.orc_bf16_value.argtypes = [ctypes.c_uint16]
+        lib.orc_bf16_value.restype = ctypes.c_double
+        lib.orc_f16_value.argtypes = [ctypes.c_uint16]
+        lib.orc_f16_value.restype = ctypes.c_double
+        lib.orc_round_to_bf16.argtypes = [ctypes.c_double]
+        lib.orc_round_to_bf16.restype = ctypes.c_double
+        lib.orc_round_to_bf16_array.argtypes = [_D, _D, ctypes.c_int64]
+        lib.orc_weight_at.argtypes = [ctypes.POINTER(_OrcWeight), ctypes.c_int64, ctypes.c_int64]
+        lib.orc_weight_at.restype = ctypes.c_double
+        lib.orc_gemv.argtypes = [ctypes.POINTER(_OrcWeight), _D, _D, ctypes.c_int]
+        lib.orc_hc_call.argtypes = (
+            [ctypes.c_int64] * 4 + [ctypes.c_double, _D, _D]
+            + [ctypes.POINTER(_OrcWeight)] * 3
+            + [_D, _D, ctypes.c_int64, _D, _D, _D, ctypes.c_int])
+        lib.orc_hc_call.restype = ctypes.c_int
+        lib.orc_inject_add.argtypes = [ctypes.c_int64] * 3 + [_D, _D, _D, ctypes.c_int64, _D]
+        lib.orc_replicate_entry.argtypes = [ctypes.c_int64] * 3 + [_D, _D]
+        self.lib = lib
+
+    # ------------------------------------------------------------ scalars
+
+    def bf16_value(self, bits: int) -> float:
+        return self.lib.orc_bf16_value(bits & 0xFFFF)
+
+    def f16_value(self, bits: int) -> float:
+        return self.lib.orc_f16_value(bits & 0xFFFF)
+
+    def round_to_bf16(self, x) -> np.ndarray:
+        x = _f64(x)
+        y = np.empty_like(x)
+        self.lib.orc_round_to_bf16_array(_dptr(x.reshape(-1)), _dptr(y.reshape(-1)), x.size)
+        return y
+
+    def weight_values(self, w) -> np.ndarray:
+        """Every element of a weight as float64, through the oracle's decoder."""
+        m = _weight(w)
+        rows, cols = m.struct.rows, m.struct.cols
+        out = np.empty((rows, cols), dtype=np.float64)
+        for o in range(rows):
+            for i in range(cols):
+                out[o, i] = self.lib.orc_weight_at(ctypes.byref(m.struct), o, i)
+        return out
+
+    def gemv(self, w, x, threads: int = 1) -> np.ndarray:
+        m = _weight(w)
+        x = _f64(x)
+        assert x.shape == (m.struct.cols,)
+        y = np.empty(m.struct.rows, dtype=np.float64)
+        self.lib.orc_gemv(ctypes.byref(m.struct), _dptr(x), _dptr(y), threads)
+        return y
+
+    # ------------------------------------------------------------ the call
+
+    def hc_call(self, raw, g, down, up, inject, *, H: int, C: int, L: int,
+                eps: float = RMS_EPS, gate=None, gate_stride: Optional[int] = None,
+                threads: Optional[int] = None, want_w: bool = False) -> dict:
+        """One hyper-connection call on M tokens; ``inject=None`` gives the final mixer.
+
+        raw: [M, C*H] values; g: [C*H]. Returns float64 ``mixed`` [M, H],
+        ``inv_rms`` [M, C], ``a`` [M, L] (the silu output), ``w`` [M, C*H] (the
+        sigmoid output) if asked, and ``gate`` [M, C] -- or, when a strided
+        ``gate`` buffer is given, that buffer filled in place.
+        """
+        raw = _f64(raw).reshape(-1, C * H)
+        M = raw.shape[0]
+        g = _f64(g).reshape(C * H)
+        md, mu, mi = _weight(down), _weight(up), _weight(inject)
+        mixed = np.empty((M, H), dtype=np.float64)
+        inv_rms = np.empty((M, C), dtype=np.float64)
+        a = np.empty((M, L), dtype=np.float64)
+        w = np.empty((M, C * H), dtype=np.float64) if want_w else None
+        own_gate = gate is None
+        if own_gate:
+            gate_stride = C
+            gate = np.full(max(M * C, 1), np.nan, dtype=np.float64)
+        else:
+            assert gate.dtype == np.float64 and gate_stride is not None
+        rc = self.lib.orc_hc_call(M, H, C, L, eps, _dptr(raw), _dptr(g), _wptr(md), _wptr(mu),
+                                  _wptr(mi), _dptr(mixed), _dptr(gate), int(gate_stride),
+                                  _dptr(inv_rms), _dptr(a), _dptr(w), threads or default_threads())
+        if rc != 0:
+            raise ValueError("oracle: inconsistent shapes")
+        res = {"mixed": mixed, "inv_rms": inv_rms, "a": a}
+        if want_w:
+            res["w"] = w
+        if inject is not None:
+            res["gate"] = gate[: M * C].reshape(M, C) if own_gate else gate
+        return res
+
+    def mixer(self, raw, g, down, up, **kw) -> dict:
+        """The final hyper_connection_mixer: the call without block_inject_weight."""
+        return self.hc_call(raw, g, down, up, None, **kw)
+
+    def inject_add(self, raw, out, gate, *, H: int, C: int,
+                   gate_stride: Optional[int] = None) -> np.ndarray:
+        """raw + (out[:, None, :] * gate[:, :, None]).flatten(), onto the un-normalized raw."""
+        raw = _f64(raw).reshape(-1, C * H)
+        M = raw.shape[0]
+        out = _f64(out).reshape(M, H)
+        gate = _f64(gate).reshape(-1)
+        gate_stride = C if gate_stride is None else gate_stride
+        res = np.empty_like(raw)
+        self.lib.orc_inject_add(M, H, C, _dptr(raw), _dptr(out), _dptr(gate), gate_stride,
+                                _dptr(res))
+        return res
+
+    def replicate_entry(self, emb, *, H: int, C: int) -> np.ndarray:
+        emb = _f64(emb).reshape(-1, H)
+        raw = np.empty((emb.shape[0], C * H), dtype=np.float64)
+        self.lib.orc_replicate_entry(emb.shape[0], H, C, _dptr(emb), _dptr(raw))
+        return raw
+
+    # ------------------------------------------------------------ drivers
+
+    def prefill_pair(self, raw, attn, out_attn, mlp, out_mlp, *, H: int, C: int, L: int,
+                     eps: float = RMS_EPS, round_residual: bool = False,
+                     threads: Optional[int] = None) -> dict:
+        """attn_hc + inject-add, then mlp_hc + inject-add, on an M-token micro-batch.
+
+        ``attn`` / ``mlp`` carry attributes g, down, up, inject. Token t's
+        attn_hc gates go to element t*C*2 of one gate buffer and its mlp_hc
+        gates to t*C*2 + C, so no token's gate is overwritten before its
+        inject-add reads it (families/qwen4/hc.rs, ``inject_row_offset``).
+        ``round_residual`` stores the residual in bf16 after each inject-add.
+        """
+        raw = _f64(raw).reshape(-1, C * H)
+        M = raw.shape[0]
+        gates = np.full(M * 2 * C, np.nan, dtype=np.float64)
+        r1 = self.hc_call(raw, attn.g, attn.down, attn.up, attn.inject, H=H, C=C, L=L, eps=eps,
+                          gate=gates, gate_stride=2 * C, threads=threads)
+        raw1 = self.inject_add(raw, out_attn, gates, H=H, C=C, gate_stride=2 * C)
+        if round_residual:
+            raw1 = self.round_to_bf16(raw1)
+        gates_mlp = gates[C:]  # a view: its element t*2C is element t*2C + C of the buffer
+        r2 = self.hc_call(raw1, mlp.g, mlp.down, mlp.up, mlp.inject, H=H, C=C, L=L, eps=eps,
+                          gate=gates_mlp, gate_stride=2 * C, threads=threads)
+        raw2 = self.inject_add(raw1, out_mlp, gates_mlp, H=H, C=C, gate_stride=2 * C)
+        if round_residual:
+            raw2 = self.round_to_bf16(raw2)
+        return {"mixed_attn": r1["mixed"], "raw_after_attn": raw1, "mixed_mlp": r2["mixed"],
+                "raw_after_mlp": raw2, "gates": gates.reshape(M, 2, C),
+                "inv_rms_attn": r1["inv_rms"], "a_attn": r1["a"],
+                "inv_rms_mlp": r2["inv_rms"], "a_mlp": r2["a"]}
+
+    def stack(self, emb, layers: Sequence, outs: Sequence, final, *, H: int, C: int, L: int,
+              eps: float = RMS_EPS, round_residual: bool = True,
+              threads: Optional[int] = None) -> dict:
+        """The decoder stack's hyper-connection path on M tokens.
+
+        entry: raw = emb repeated C times; per layer l, with ``layers[l]`` =
+        (attn, mlp) and ``outs[l]`` = (out_attn, out_mlp): attn_hc + inject,
+        mlp_hc + inject; exit: the final mixer with ``final`` (g, down, up).
+
+        ``round_residual``: the residual is a bf16 tensor between calls, so it
+        is rounded to bf16 (ties to even) after every inject-add, as stored.
+        Each call itself is exact in fp64.
+        """
+        raw = self.replicate_entry(emb, H=H, C=C)
+        for (attn, mlp), (o_attn, o_mlp) in zip(layers, outs):
+            r = self.prefill_pair(raw, attn, o_attn, mlp, o_mlp, H=H, C=C, L=L, eps=eps,
+                                  round_residual=round_residual, threads=threads)
+            raw = r["raw_after_mlp"]
+        fin = self.mixer(raw, final.g, final.down, final.up, H=H, C=C, L=L, eps=eps,
+                         threads=threads)
+        return {"mixed": fin["mixed"], "raw": raw}
+
+
+_lock = threading.Lock()
+_default: Optional[Oracle] = None
+
+
+def get() -> Oracle:
+    """The oracle built from the committed ``hc_oracle.c``."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle()
+        return _default
