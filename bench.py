@@ -1,0 +1,396 @@
+"""Benchmark of the hyper-connection call on GB300.
+
+Workload (one GPU): the full-shape decode call, M=1 token, H=2560, C=4
+(wide 10240), hc_lowrank=320, bf16 weights: one attn_hc-style call
+(ts_hc_call) followed by its inject-add (ts_hc_inject_add), each call
+depending on the previous one through the residual, as in a decoder stack.
+
+One step = one replay of a CUDA graph that holds CALLS_PER_STEP dependent
+(call + inject-add) pairs cycling through WEIGHT_SETS distinct seeded weight
+sets (634 MB per pass, far larger than the 129 MB L2, so every call streams
+its weights from HBM). Inputs are resident in HBM when the timed region
+starts; ``e2e`` repeats the measurement with the step's inputs copied from
+pinned host memory and its results read back inside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). Under torchrun each rank runs an independent
+replica (no collective on the data path); value = calls of all ranks / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "hyper-connection calls/s and tokens/s at H=2560,C=4; achieved HBM GB/s vs peak"
+H, C, L, M = 2560, 4, 320, 1
+WEIGHT_SETS = 48
+CALLS_PER_STEP = 960
+CONFIG_SEED = 1  # the full-shape decode workload's seed
+
+# Algorithmic bytes of one call + inject-add at M = 1 (every tensor once):
+# down 6,553,600 + up 6,553,600 + inject 81,920 + g 20,480 + raw read 20,480
+# + mixed write 5,120 + gates 16 ; inject-add: raw read+write 40,960 + out 5,120 + gates 16.
+BYTES_PER_CALL = (2 * L * C * H + 2 * C * H * L + 2 * C * C * H + 2 * C * H + 2 * M * C * H
+                  + 2 * M * H + 4 * M * C) + (2 * 2 * M * C * H + 2 * M * H + 4 * M * C)
+assert BYTES_PER_CALL == 13_281_312
+KERNELS_PER_CALL = 3  # down, up (ts_hc_call) + inject-add
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "hyper_connection_residual_call_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def _recorded_traffic():
+    """DRAM bytes per call from the committed ncu summary, if taken on these sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_source_hash") != _kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_call")
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            time.sleep(0.25)
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l for (t, l) in self.lines if t0 - 0.15 <= t <= t1 + 0.15]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    """The fp64 CPU oracle on this host's cores, timed on a bounded sample per step."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    from hyper_connection_residual_call_gb300 import inputs
+
+    orc = oracle.get()
+    threads = oracle.default_threads()
+    w = inputs.make_hc_weights(H, C, L, CONFIG_SEED)
+    raw = inputs.make_residual(M, H, C, CONFIG_SEED)
+    out = inputs.make_sublayer_out(M, H, CONFIG_SEED)
+    calls_per_step = 1
+
+    def step(r):
+        res = orc.hc_call(r, w.g, w.down, w.up, w.inject, H=H, C=C, L=L, threads=threads)
+        return orc.inject_add(r, out, res["gate"], H=H, C=C)
+
+    r = raw.double().numpy()
+    for _ in range(args.warmup):
+        r = step(r)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = step(r)
+    dt = time.perf_counter() - t0
+    value = args.steps * calls_per_step / dt
+    sample = f"{args.steps} x 1 full-shape call + inject-add (M=1, H=2560, C=4, L=320), fp64 oracle"
+    line = {
+        "metric": METRIC, "value": value, "unit": "calls/s", "impl": "reference", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": _config(),
+        "cpu_baseline": {"value": value, "unit": "calls/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "calls/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config():
+    return {"workload": "full-shape decode hyper-connection call + inject-add: M=1, H=2560, C=4 "
+                        "(wide 10240), hc_lowrank=320, bf16 weights",
+            "M": M, "H": H, "C": C, "hc_lowrank": L, "calls_per_step": CALLS_PER_STEP,
+            "weight_sets": WEIGHT_SETS,
+            "l2": "inputs larger than L2: 48 distinct weight sets, 634 MB per pass, cycled",
+            "parallelism": "replicas"}
+
+
+def cpu_baseline(budget_s: float = 12.0):
+    import oracle
+    from hyper_connection_residual_call_gb300 import inputs
+
+    orc = oracle.get()
+    threads = oracle.default_threads()
+    w = inputs.make_hc_weights(H, C, L, CONFIG_SEED)
+    raw = inputs.make_residual(M, H, C, CONFIG_SEED).double().numpy()
+    out = inputs.make_sublayer_out(M, H, CONFIG_SEED)
+    n = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s and n < 2000:
+        res = orc.hc_call(raw, w.g, w.down, w.up, w.inject, H=H, C=C, L=L, threads=threads)
+        raw = orc.inject_add(raw, out, res["gate"], H=H, C=C)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "calls/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} full-shape calls + inject-adds (M=1, H=2560, C=4, L=320) in {dt:.1f} s, "
+                      f"fp64 oracle, OpenMP over output rows"}
+
+
+def parity_check(B, inputs, w0_d, w0, raw0, out0):
+    """The full-shape call on weight set 0 against the oracle, before timing."""
+    import numpy as np
+    import torch
+    import oracle
+
+    orc = oracle.get()
+    ref = orc.hc_call(raw0, w0.g, w0.down, w0.up, w0.inject, H=H, C=C, L=L)
+    ref_raw = orc.inject_add(raw0, out0, ref["gate"], H=H, C=C)
+    raw_d = raw0.cuda()
+    mixed, gates = B.hc_call(raw_d, w0_d, H=H, C=C)
+    B.hc_inject_add(raw_d, out0.cuda(), gates, H=H, C=C)
+    torch.cuda.synchronize()
+
+    def worst(g, r, atol, rtol):
+        g = g.detach().double().cpu().numpy().reshape(np.shape(r))
+        return float(np.max(np.abs(g - r) / (atol + rtol * np.abs(r))))
+
+    rms = float(np.sqrt(np.mean(ref["gate"] ** 2)))
+    res = {"mixed": worst(mixed, ref["mixed"], 1e-2, 1e-2),
+           "raw": worst(raw_d, ref_raw, 1e-2, 1e-2),
+           "gate": worst(gates, ref["gate"], 1e-5 * rms, 1e-3)}
+    ok = all(v <= 1.0 for v in res.values())
+    if not ok:
+        raise SystemExit(f"parity check failed before timing: {res}")
+    return {"checked": "full-shape call + inject-add vs fp64 oracle", "worst_err_over_limit": max(res.values())}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from hyper_connection_residual_call_gb300 import binding as B
+    from hyper_connection_residual_call_gb300 import inputs
+    from hyper_connection_residual_call_gb300.build import build
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build()
+    B.library()
+    dev = torch.device("cuda", local)
+
+    # Seeded inputs: weight sets, sublayer outputs, the initial residual.
+    sets_h = [inputs.make_hc_weights(H, C, L, CONFIG_SEED, i) for i in range(WEIGHT_SETS)]
+    outs_h = [inputs.make_sublayer_out(M, H, CONFIG_SEED, i) for i in range(WEIGHT_SETS)]
+    raw_h = inputs.make_residual(M, H, C, CONFIG_SEED)
+    sets = [w.to(dev) for w in sets_h]
+    outs = torch.stack([o.to(dev) for o in outs_h])          # [sets, M, H]
+    raw0 = raw_h.to(dev)
+
+    parity = parity_check(B, inputs, sets[0], sets_h[0], raw_h, outs_h[0]) if rank == 0 else None
+
+    raw = raw0.clone()
+    mixed = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    gates = torch.empty((M, C), dtype=torch.float32, device=dev)
+    wsp = B.workspace(M, H, C, L, dev)
+
+    def one_step():
+        for i in range(CALLS_PER_STEP):
+            k = i % WEIGHT_SETS
+            B.hc_call(raw, sets[k], H=H, C=C, mixed=mixed, inject_w=gates, inject_stride=C, ws=wsp)
+            B.hc_inject_add(raw, outs[k], gates, H=H, C=C)
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        one_step()  # eager warm-up (also initialises the library's per-device state)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        one_step()
+    torch.cuda.synchronize()
+
+    def timed(n_steps, body):
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n_steps):
+                body()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if ws > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            graph.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    t0 = time.time()
+    ms = timed(args.steps, graph.replay)
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1)
+
+    # e2e: per step, the step's inputs (initial residual + the 48 sublayer
+    # outputs) from pinned host memory, the graph, and the results read back.
+    raw_pin = raw_h.pin_memory()
+    outs_pin = torch.stack(outs_h).pin_memory()
+    mixed_pin = torch.empty((M, H), dtype=torch.bfloat16).pin_memory()
+    res_pin = torch.empty((M, C * H), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        raw.copy_(raw_pin, non_blocking=True)
+        outs.copy_(outs_pin, non_blocking=True)
+        graph.replay()
+        mixed_pin.copy_(mixed, non_blocking=True)
+        res_pin.copy_(raw, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    e2e_steps = max(1, args.steps // 2)
+    ms_e2e = timed(e2e_steps, e2e_step)
+    h2d = raw_pin.numel() * 2 + outs_pin.numel() * 2
+    d2h = mixed_pin.numel() * 2 + res_pin.numel() * 2
+
+    calls = args.steps * CALLS_PER_STEP * ws
+    value = calls / (ms / 1e3)
+    per_call_s = (ms / 1e3) / (args.steps * CALLS_PER_STEP)
+    achieved = BYTES_PER_CALL / per_call_s / 1e9
+    peak, peak_kind = _peaks()
+    e2e_value = e2e_steps * CALLS_PER_STEP * ws / (ms_e2e / 1e3)
+
+    if rank == 0:
+        base = cpu_baseline() if ws == 1 else None
+        line = {
+            "metric": METRIC, "value": value, "unit": "calls/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": _config(),
+            "tokens_per_s": value * M,
+            "hbm_gbs": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": _recorded_traffic(),
+                         "kernel": "one hyper-connection call (down + up kernels, PDL-overlapped) "
+                                   "+ its inject-add; 13,281,312 algorithmic bytes per call",
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                         else "fallback 6.8 TB/s"},
+            "e2e": {"value": e2e_value, "unit": "calls/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": KERNELS_PER_CALL * CALLS_PER_STEP * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": base,
+            "parity": parity,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,262 @@
+"""Thin Python binding of the C ABI in ``include/ts_hc.h`` (ctypes).
+
+Two layers, both argument marshalling only -- every step of the computation
+runs in the library's CUDA kernels:
+
+* ``ts_hc_*``: the C entry points under their own names, taking raw device
+  pointers (ints), a ``TsWeight`` struct and a CUDA stream handle; they return
+  the ``ts_status`` code.
+* ``hc_call`` / ``hc_mixer`` / ``hc_inject_add``: the same calls for torch
+  CUDA tensors. They allocate outputs/workspace with torch when not given,
+  pass the current torch stream, and raise ``HCError`` on any error status.
+
+There is no fallback: if the library is not built or cannot be loaded, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+from .build import LIB_PATH
+
+TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_CUDA, TS_ERR_WORKSPACE, TS_ERR_TIMEOUT = range(6)
+TS_W_BF16, TS_W_INT4_AFFINE = 0, 1
+RMS_EPS = 1e-6  # families/qwen4/mod.rs, RMS_EPS
+
+EXPORTS = ("ts_hc_workspace_bytes", "ts_hc_workspace_layout", "ts_hc_call", "ts_hc_inject_add",
+           "ts_hc_mixer", "ts_hc_replicate_entry", "ts_hc_last_error", "ts_hc_device_status")
+
+
+class HCError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"ts_hc status {status}: {message}")
+        self.status = status
+
+
+class TsWeight(ctypes.Structure):
+    _fields_ = [
+        ("type", ctypes.c_int32),
+        ("group", ctypes.c_int32),
+        ("data", ctypes.c_void_p),
+        ("scales", ctypes.c_void_p),
+        ("biases", ctypes.c_void_p),
+    ]
+
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+def library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load ``libts_hc.so`` (once). Raises if it is missing: there is no fallback."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"CUDA library {p} is not built; run hyper_connection_residual_call_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        vp, i, l, sz, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_size_t, ctypes.c_float
+        wp = ctypes.POINTER(TsWeight)
+        lib.ts_hc_workspace_bytes.argtypes = [i, i, i, i]
+        lib.ts_hc_workspace_bytes.restype = sz
+        lib.ts_hc_workspace_layout.argtypes = [i, i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+        lib.ts_hc_workspace_layout.restype = i
+        lib.ts_hc_call.argtypes = [vp, vp, wp, wp, wp, vp, vp, l, i, i, i, i, f, vp, sz, vp]
+        lib.ts_hc_call.restype = i
+        lib.ts_hc_mixer.argtypes = [vp, vp, wp, wp, vp, i, i, i, i, f, vp, sz, vp]
+        lib.ts_hc_mixer.restype = i
+        lib.ts_hc_inject_add.argtypes = [vp, vp, vp, l, i, i, i, vp]
+        lib.ts_hc_inject_add.restype = i
+        lib.ts_hc_replicate_entry.argtypes = [vp, vp, i, i, i, vp]
+        lib.ts_hc_replicate_entry.restype = i
+        lib.ts_hc_last_error.argtypes = []
+        lib.ts_hc_last_error.restype = ctypes.c_char_p
+        lib.ts_hc_device_status.argtypes = [vp, ctypes.POINTER(i)]
+        lib.ts_hc_device_status.restype = i
+        if path is None:
+            _lib = lib
+        return lib
+
+
+# ------------------------------------------------------------- C names
+
+def ts_hc_workspace_bytes(M: int, H: int, C: int, lowrank: int) -> int:
+    return library().ts_hc_workspace_bytes(M, H, C, lowrank)
+
+
+def ts_hc_workspace_layout(M: int, H: int, C: int, lowrank: int) -> Tuple[int, int]:
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    st = library().ts_hc_workspace_layout(M, H, C, lowrank, ctypes.byref(a), ctypes.byref(b))
+    _check(st)
+    return a.value, b.value
+
+
+def ts_hc_call(raw, hc_norm_w, down, up, inject, mixed, inject_w, inject_stride, M, H, C, lowrank,
+               eps, workspace, workspace_bytes, stream) -> int:
+    return library().ts_hc_call(raw, hc_norm_w, _wref(down), _wref(up), _wref(inject), mixed, inject_w,
+                                inject_stride, M, H, C, lowrank, eps, workspace, workspace_bytes, stream)
+
+
+def ts_hc_mixer(raw, hc_norm_w, down, up, mixed, M, H, C, lowrank, eps, workspace, workspace_bytes,
+                stream) -> int:
+    return library().ts_hc_mixer(raw, hc_norm_w, _wref(down), _wref(up), mixed, M, H, C, lowrank, eps,
+                                 workspace, workspace_bytes, stream)
+
+
+def ts_hc_inject_add(raw, out, inject_w, inject_stride, M, H, C, stream) -> int:
+    return library().ts_hc_inject_add(raw, out, inject_w, inject_stride, M, H, C, stream)
+
+
+def ts_hc_replicate_entry(emb, raw, M, H, C, stream) -> int:
+    return library().ts_hc_replicate_entry(emb, raw, M, H, C, stream)
+
+
+def ts_hc_last_error() -> str:
+    return library().ts_hc_last_error().decode()
+
+
+def ts_hc_device_status(stream) -> Tuple[int, int]:
+    v = ctypes.c_int()
+    st = library().ts_hc_device_status(stream, ctypes.byref(v))
+    return st, v.value
+
+
+def _wref(w: Optional[TsWeight]):
+    return None if w is None else ctypes.byref(w)
+
+
+def _check(st: int) -> None:
+    if st != TS_OK:
+        raise HCError(st, ts_hc_last_error())
+
+
+# ------------------------------------------------------------- torch layer
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def weight_struct(w) -> TsWeight:
+    """A ``TsWeight`` for a weight with attributes kind, data, scale, bias, group
+    (tensors already on the device)."""
+    s = TsWeight()
+    if w.kind == "bf16":
+        s.type, s.group = TS_W_BF16, 0
+        s.data = w.data.data_ptr()
+    elif w.kind == "int4":
+        s.type, s.group = TS_W_INT4_AFFINE, int(w.group)
+        s.data, s.scales, s.biases = w.data.data_ptr(), w.scale.data_ptr(), w.bias.data_ptr()
+    else:
+        raise ValueError(f"unknown weight kind {w.kind!r}")
+    return s
+
+
+def _need(t, name, dtype, shape=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise HCError(TS_ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise HCError(TS_ERR_INVALID_ARG, f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise HCError(TS_ERR_INVALID_ARG, f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise HCError(TS_ERR_INVALID_ARG, f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def workspace(M: int, H: int, C: int, L: int, device=None):
+    torch = _torch()
+    n = max(ts_hc_workspace_bytes(M, H, C, L), 256)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def hc_call(raw, weights, *, H: int, C: int, mixed=None, inject_w=None, inject_stride: Optional[int] = None,
+            eps: float = RMS_EPS, ws=None, stream=None):
+    """attn_hc / mlp_hc on raw [M, C*H] bf16 with ``weights`` (g, down, up, inject).
+
+    Returns (mixed [M, H] bf16, inject_w fp32). With a caller-given ``inject_w``
+    buffer and ``inject_stride``, token t's gates land at element t*inject_stride.
+    """
+    torch = _torch()
+    M = raw.shape[0]
+    L = weights.down.rows
+    _need(raw, "raw", torch.bfloat16, (M, C * H))
+    _need(weights.g, "hc_norm_w", torch.bfloat16, (C * H,))
+    if mixed is None:
+        mixed = torch.empty((M, H), dtype=torch.bfloat16, device=raw.device)
+    _need(mixed, "mixed", torch.bfloat16, (M, H))
+    if inject_w is None:
+        inject_stride = C
+        inject_w = torch.empty((max(M, 1), C), dtype=torch.float32, device=raw.device)
+    if inject_stride is None:
+        raise HCError(TS_ERR_INVALID_ARG, "inject_stride is required with a caller-given inject_w")
+    if ws is None:
+        ws = workspace(M, H, C, L, raw.device)
+    st = ts_hc_call(raw.data_ptr(), weights.g.data_ptr(), weight_struct(weights.down),
+                    weight_struct(weights.up), weight_struct(weights.inject), mixed.data_ptr(),
+                    inject_w.data_ptr(), inject_stride, M, H, C, L, eps, ws.data_ptr(),
+                    ws.numel() * ws.element_size(), _stream_handle(stream))
+    _check(st)
+    return mixed, inject_w
+
+
+def hc_mixer(raw, weights, *, H: int, C: int, mixed=None, eps: float = RMS_EPS, ws=None, stream=None):
+    """The final hyper_connection_mixer on raw [M, C*H] bf16; returns mixed [M, H] bf16."""
+    torch = _torch()
+    M = raw.shape[0]
+    L = weights.down.rows
+    _need(raw, "raw", torch.bfloat16, (M, C * H))
+    _need(weights.g, "hc_norm_w", torch.bfloat16, (C * H,))
+    if mixed is None:
+        mixed = torch.empty((M, H), dtype=torch.bfloat16, device=raw.device)
+    _need(mixed, "mixed", torch.bfloat16, (M, H))
+    if ws is None:
+        ws = workspace(M, H, C, L, raw.device)
+    st = ts_hc_mixer(raw.data_ptr(), weights.g.data_ptr(), weight_struct(weights.down),
+                     weight_struct(weights.up), mixed.data_ptr(), M, H, C, L, eps, ws.data_ptr(),
+                     ws.numel() * ws.element_size(), _stream_handle(stream))
+    _check(st)
+    return mixed
+
+
+def hc_inject_add(raw, out, inject_w, *, H: int, C: int, inject_stride: Optional[int] = None, stream=None):
+    """raw[m, c*H+h] += out[m, h] * inject_w[m*stride + c], in place; returns raw."""
+    torch = _torch()
+    M = raw.shape[0]
+    _need(raw, "raw", torch.bfloat16, (M, C * H))
+    _need(out, "out", torch.bfloat16, (M, H))
+    if not inject_w.is_cuda or inject_w.dtype != torch.float32:
+        raise HCError(TS_ERR_INVALID_ARG, "inject_w must be a CUDA float32 tensor")
+    st = ts_hc_inject_add(raw.data_ptr(), out.data_ptr(), inject_w.data_ptr(),
+                          C if inject_stride is None else inject_stride, M, H, C, _stream_handle(stream))
+    _check(st)
+    return raw
+
+
+def hc_replicate_entry(emb, *, C: int, raw=None, stream=None):
+    """raw [M, C*H] bf16 with every stream equal to emb [M, H] (repeat, not pad)."""
+    torch = _torch()
+    M, H = emb.shape
+    _need(emb, "emb", torch.bfloat16, (M, H))
+    if raw is None:
+        raw = torch.empty((M, C * H), dtype=torch.bfloat16, device=emb.device)
+    _need(raw, "raw", torch.bfloat16, (M, C * H))
+    _check(ts_hc_replicate_entry(emb.data_ptr(), raw.data_ptr(), M, H, C, _stream_handle(stream)))
+    return raw
+
+
+def device_status(stream=None) -> int:
+    st, v = ts_hc_device_status(_stream_handle(stream))
+    _check(st)
+    return v

@@ -1,0 +1,680 @@
+// hc_gemv.cu -- CUDA-core kernels of the hyper-connection call for small
+// token counts (weight-streaming GEMVs, HBM bound), the final mixer and the
+// inject-add.
+//
+// The call (families/qwen4/mod.rs, "## Hyper-connections"; families/qwen4/
+// hc.rs, encode_hyper_connection) runs as two kernels chained with
+// programmatic dependent launch:
+//
+//  hc_down_kernel  grouped RMSNorm folded into a split-K down GEMV (plus the C
+//                  block_inject_weight rows). A cluster of S CTAs shares a
+//                  block of output rows; CTA s streams the weight columns of
+//                  its chunk [s*KC, (s+1)*KC) into shared memory with bulk
+//                  copies issued before it waits on the previous kernel, then
+//                  forms x = raw * g for its chunk together with the chunk's
+//                  sum of squares. Partial dots and sums of squares meet in
+//                  distributed shared memory; rank q of the cluster finishes
+//                  rows q, q+S, ... as z = sum_s inv_rms[stream(s)] * P_s, and
+//                  writes silu(z / C) (down rows) or 2 sigmoid(z / C) (gate
+//                  rows). The normalised vector never goes to HBM.
+//  hc_up_kernel    CTA b streams up rows {c*H + h : h in its h-block} for all
+//                  C streams into shared memory before waiting, then forms
+//                  w = sigmoid(up . act) and the mean mix
+//                  mixed[h] = (1/C) sum_c w[c*H+h] * raw[c*H+h] * inv_rms[c] * g[c*H+h].
+//
+// Reductions run in a fixed order: results are bit-identical run to run.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "hc_kernels.h"
+#include "ptx.cuh"
+
+namespace tshc {
+
+namespace {
+
+// Elements per 16-byte vector of weight storage: 8 bf16 or 32 INT4 codes.
+template <int WT> struct Vec;
+template <> struct Vec<0> { static constexpr int kElems = 8; };
+template <> struct Vec<1> { static constexpr int kElems = 32; };
+
+__host__ __device__ constexpr int round_up(int x, int m) { return (x + m - 1) / m * m; }
+__host__ __device__ constexpr size_t round_up_sz(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+// Activations x_s are stored permuted so that lane l of a warp reading "its"
+// weight vector v = l + 32 i finds the matching activations as consecutive
+// float4s across lanes (no shared-memory bank conflicts). Element j of the
+// chunk, in vector v = j / VW at offset e = j % VW, sits at:
+template <int VW>
+__device__ __forceinline__ int xpos(int j)
+{
+    const int v = j / VW, e = j % VW;
+    return (v >> 5) * (32 * VW) + (e >> 2) * 128 + (v & 31) * 4 + (e & 3);
+}
+
+struct DownSmem {
+    size_t bar, w, sb, x, part, ssq, invr, red, total;
+};
+
+__host__ __device__ inline DownSmem down_layout(const DownParams &p, int mt)
+{
+    const int VW = p.down.type == 0 ? 8 : 32;
+    const int kcp = round_up(p.KC, 32 * VW);
+    const size_t seg = p.down.type == 0 ? (size_t)p.KC * 2 : (size_t)p.KC / 2;
+    const int ng = p.down.type == 0 ? 0 : p.KC / p.down.group;
+    DownSmem s;
+    s.bar = 0;
+    s.w = 128;
+    s.sb = round_up_sz(s.w + seg * p.rows_per_block, 128);
+    s.x = round_up_sz(s.sb + sizeof(float) * 2 * (size_t)ng * p.rows_per_block, 128);
+    s.part = round_up_sz(s.x + sizeof(float) * (size_t)mt * kcp, 128);
+    s.ssq = round_up_sz(s.part + sizeof(float) * (size_t)mt * p.rows_per_block, 16);
+    s.invr = round_up_sz(s.ssq + sizeof(float) * mt, 16);
+    s.red = round_up_sz(s.invr + sizeof(float) * (size_t)mt * p.C, 16);
+    s.total = round_up_sz(s.red + sizeof(float) * 32 * mt, 128);
+    return s;
+}
+
+struct UpSmem {
+    size_t bar, w, sb, act, wv, total;
+};
+
+__host__ __device__ inline UpSmem up_layout(const UpParams &p, int mt)
+{
+    const size_t row = p.up.type == 0 ? (size_t)p.L * 2 : (size_t)p.L / 2;
+    const int ng = p.up.type == 0 ? 0 : p.L / p.up.group;
+    UpSmem s;
+    s.bar = 0;
+    s.w = 128;
+    s.sb = round_up_sz(s.w + row * p.C * p.HB, 128);
+    s.act = round_up_sz(s.sb + sizeof(float) * 2 * (size_t)ng * p.C * p.HB, 128);
+    s.wv = round_up_sz(s.act + sizeof(float) * (size_t)mt * p.L, 128);
+    s.total = round_up_sz(s.wv + sizeof(float) * (size_t)mt * p.C * p.HB, 128);
+    return s;
+}
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&f)[8])
+{
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint16_t b)
+{
+    return __half2float(__ushort_as_half(b));
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ void record_timeout(unsigned *status)
+{
+    if (status)
+        atomicExch(status, kStatusTimeout);
+}
+
+// Dot of one weight row segment with MT activation rows, partial per lane.
+// bf16: lane handles vectors v = lane + 32 i of 8 elements.
+template <int MT>
+__device__ __forceinline__ void row_dot_bf16(const uint4 *wrow, int nvec, const float *x, int xstride,
+                                             int lane, float (&acc)[MT])
+{
+    for (int v = lane; v < nvec; v += 32) {
+        float wf[8];
+        unpack_bf16x8(wrow[v], wf);
+        const int p0 = xpos<8>(v * 8);
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            const float4 xa = *reinterpret_cast<const float4 *>(x + t * xstride + p0);
+            const float4 xb = *reinterpret_cast<const float4 *>(x + t * xstride + p0 + 128);
+            float a = acc[t];
+            a = fmaf(wf[0], xa.x, a); a = fmaf(wf[1], xa.y, a);
+            a = fmaf(wf[2], xa.z, a); a = fmaf(wf[3], xa.w, a);
+            a = fmaf(wf[4], xb.x, a); a = fmaf(wf[5], xb.y, a);
+            a = fmaf(wf[6], xb.z, a); a = fmaf(wf[7], xb.w, a);
+            acc[t] = a;
+        }
+    }
+}
+
+// INT4-affine: lane handles vectors of 32 codes (one group-aligned run of 32
+// inputs, so one scale and bias).
+template <int MT>
+__device__ __forceinline__ void row_dot_int4(const uint4 *wrow, int nvec, const float *sb, int group,
+                                             const float *x, int xstride, int lane, float (&acc)[MT])
+{
+    for (int v = lane; v < nvec; v += 32) {
+        const uint4 q = wrow[v];
+        const int gi = (v * 32) / group;
+        const float sc = sb[2 * gi], bi = sb[2 * gi + 1];
+        const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+        const int base = (v >> 5) * 1024 + (v & 31) * 4;
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {
+            float wf[8];
+#pragma unroll
+            for (int n = 0; n < 8; ++n)
+                wf[n] = fmaf((float)((words[wd] >> (4 * n)) & 0xFu), sc, bi);
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                // elements e = 8*wd .. 8*wd+7 sit in float4 groups e/4 = 2*wd, 2*wd+1
+                const float4 xa = *reinterpret_cast<const float4 *>(x + t * xstride + base + (2 * wd) * 128);
+                const float4 xb = *reinterpret_cast<const float4 *>(x + t * xstride + base + (2 * wd + 1) * 128);
+                float a = acc[t];
+                a = fmaf(wf[0], xa.x, a); a = fmaf(wf[1], xa.y, a);
+                a = fmaf(wf[2], xa.z, a); a = fmaf(wf[3], xa.w, a);
+                a = fmaf(wf[4], xb.x, a); a = fmaf(wf[5], xb.y, a);
+                a = fmaf(wf[6], xb.z, a); a = fmaf(wf[7], xb.w, a);
+                acc[t] = a;
+            }
+        }
+    }
+}
+
+template <int WT, int MT>
+__global__ void __launch_bounds__(512) hc_down_kernel(const DownParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int VW = Vec<WT>::kElems;
+    const DownSmem lay = down_layout(p, MT);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + lay.bar);
+    unsigned char *w_s = smem + lay.w;
+    float *sb_s = reinterpret_cast<float *>(smem + lay.sb);
+    float *x_s = reinterpret_cast<float *>(smem + lay.x);
+    float *part_s = reinterpret_cast<float *>(smem + lay.part);
+    float *ssq_s = reinterpret_cast<float *>(smem + lay.ssq);
+    float *invr_s = reinterpret_cast<float *>(smem + lay.invr);
+    float *red_s = reinterpret_cast<float *>(smem + lay.red);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    const int s = blockIdx.x;  // chunk index == rank in the cluster (gridDim.x == cluster size)
+    const int RPB = p.rows_per_block;
+    const int r0 = blockIdx.y * RPB;
+    const int nrows = min(RPB, p.R - r0);
+    const int KC = p.KC, k0 = s * KC;
+    const int kcp = round_up(KC, 32 * VW);
+    const int nvec = KC / VW;
+    const size_t seg = WT == 0 ? (size_t)KC * 2 : (size_t)KC / 2;
+
+    pdl_launch_dependents();
+
+    // Weights do not depend on the previous kernel: start streaming them now.
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar, (uint32_t)(seg * nrows));
+        for (int r = 0; r < nrows; ++r) {
+            const int gr = r0 + r;
+            const WeightView &wv = gr < p.L ? p.down : p.inject;
+            const int row = gr < p.L ? gr : gr - p.L;
+            const unsigned char *src = static_cast<const unsigned char *>(wv.data)
+                + (WT == 0 ? ((size_t)row * p.W + k0) * 2 : ((size_t)row * p.W + k0) / 2);
+            bulk_copy_g2s(w_s + r * seg, src, (uint32_t)seg, bar);
+        }
+    }
+    if constexpr (WT == 1) {
+        const int ng = KC / p.down.group;
+        for (int i = tid; i < nrows * ng; i += blockDim.x) {
+            const int r = i / ng, gi = i % ng;
+            const int gr = r0 + r;
+            const WeightView &wv = gr < p.L ? p.down : p.inject;
+            const int row = gr < p.L ? gr : gr - p.L;
+            const size_t off = (size_t)row * (p.W / wv.group) + k0 / wv.group + gi;
+            sb_s[2 * i] = half_bits_to_float(wv.scales[off]);
+            sb_s[2 * i + 1] = half_bits_to_float(wv.biases[off]);
+        }
+    }
+
+    // The residual is written by the previous kernel in the stream.
+    pdl_wait();
+
+    bool have_weights = false, timed_out = false;
+    for (int t0 = 0; t0 < p.M; t0 += MT) {
+        const int mt = min(MT, p.M - t0);
+
+        // x = raw * g over this chunk, and the chunk's sum of squares.
+        float ssq[MT];
+#pragma unroll
+        for (int t = 0; t < MT; ++t) ssq[t] = 0.f;
+        for (int v = tid; v < KC / 8; v += blockDim.x) {
+            float gf[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4 *>(p.g + k0 + v * 8), gf);
+            const int p0 = xpos<VW>(v * 8), p1 = xpos<VW>(v * 8 + 4);
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                float rf[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                if (t < mt)
+                    unpack_bf16x8(*reinterpret_cast<const uint4 *>(p.raw + (size_t)(t0 + t) * p.W + k0 + v * 8), rf);
+                float q = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q = fmaf(rf[e], rf[e], q);
+                ssq[t] += q;
+                *reinterpret_cast<float4 *>(x_s + t * kcp + p0) =
+                    make_float4(rf[0] * gf[0], rf[1] * gf[1], rf[2] * gf[2], rf[3] * gf[3]);
+                *reinterpret_cast<float4 *>(x_s + t * kcp + p1) =
+                    make_float4(rf[4] * gf[4], rf[5] * gf[5], rf[6] * gf[6], rf[7] * gf[7]);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            const float v = warp_sum(ssq[t]);
+            if (lane == 0) red_s[warp * MT + t] = v;
+        }
+        __syncthreads();
+        if (tid < MT) {
+            float v = 0.f;
+            for (int w = 0; w < nwarps; ++w) v += red_s[w * MT + tid];
+            ssq_s[tid] = v;
+        }
+        if (!have_weights) {
+            timed_out = !mbar_wait_bounded(bar, 0);
+            if (timed_out)
+                record_timeout(p.status);
+            have_weights = true;
+        }
+
+        // Partial dots of this CTA's rows over its chunk.
+        for (int r = warp; r < nrows; r += nwarps) {
+            float acc[MT];
+#pragma unroll
+            for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+            const uint4 *wrow = reinterpret_cast<const uint4 *>(w_s + r * seg);
+            if constexpr (WT == 0)
+                row_dot_bf16<MT>(wrow, nvec, x_s, kcp, lane, acc);
+            else
+                row_dot_int4<MT>(wrow, nvec, sb_s + 2 * r * (KC / p.down.group), p.down.group, x_s, kcp,
+                                 lane, acc);
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                const float v = warp_sum(acc[t]);
+                if (lane == 0) part_s[t * RPB + r] = v;
+            }
+        }
+
+        cluster_sync();  // every rank's partials and sums of squares are complete
+
+        if (tid < mt) {
+            for (int c = 0; c < p.C; ++c) {
+                float ss = 0.f;
+                for (int j = 0; j < p.sps; ++j)
+                    ss += dsmem_ld_f32(dsmem_addr(ssq_s + tid, c * p.sps + j));
+                invr_s[tid * p.C + c] = 1.0f / sqrtf(ss / (float)p.H + p.eps);
+            }
+        }
+        __syncthreads();
+        if (blockIdx.y == 0 && s == 0) {
+            for (int i = tid; i < mt * p.C; i += blockDim.x)
+                p.inv_rms[(size_t)t0 * p.C + i] = invr_s[i];
+        }
+
+        // Rank s finishes rows s, s+S, ... of the block.
+        const int my_rows = s < nrows ? (nrows - s + p.S - 1) / p.S : 0;
+        for (int i = tid; i < my_rows * mt; i += blockDim.x) {
+            const int r = s + p.S * (i / mt), t = i % mt;
+            float z = 0.f;
+            for (int q = 0; q < p.S; ++q)
+                z = fmaf(invr_s[t * p.C + q / p.sps], dsmem_ld_f32(dsmem_addr(part_s + t * RPB + r, q)), z);
+            const int gr = r0 + r;
+            const int m = t0 + t;
+            const float zc = z * p.inv_C;
+            if (gr < p.L)
+                p.act[(size_t)m * p.L + gr] = zc * sigmoidf_(zc);
+            else
+                p.gate[(size_t)m * p.gate_stride + (gr - p.L)] = 2.0f * sigmoidf_(zc);
+        }
+
+        cluster_sync();  // peers have read this CTA's partials before they are overwritten
+    }
+    if (timed_out)  // do not leave with a copy into this CTA's shared memory in flight
+        mbar_wait_bounded(bar, 0);
+}
+
+template <int WT, int MT>
+__global__ void __launch_bounds__(768) hc_up_kernel(const UpParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const UpSmem lay = up_layout(p, MT);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + lay.bar);
+    unsigned char *w_s = smem + lay.w;
+    float *sb_s = reinterpret_cast<float *>(smem + lay.sb);
+    float *act_s = reinterpret_cast<float *>(smem + lay.act);
+    float *wv_s = reinterpret_cast<float *>(smem + lay.wv);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    const int HB = p.HB, h0 = blockIdx.x * HB;
+    const int hb = min(HB, p.H - h0);
+    const int L = p.L;
+    const size_t row_bytes = WT == 0 ? (size_t)L * 2 : (size_t)L / 2;
+    const int ng = WT == 0 ? 0 : L / p.up.group;
+
+    pdl_launch_dependents();
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar, (uint32_t)(row_bytes * hb * p.C));
+        for (int c = 0; c < p.C; ++c)
+            bulk_copy_g2s(w_s + (size_t)c * HB * row_bytes,
+                          static_cast<const unsigned char *>(p.up.data) + ((size_t)c * p.H + h0) * row_bytes,
+                          (uint32_t)(row_bytes * hb), bar);
+    }
+    if constexpr (WT == 1) {
+        for (int i = tid; i < p.C * hb * ng; i += blockDim.x) {
+            const int c = i / (hb * ng), rem = i % (hb * ng), hl = rem / ng, gi = rem % ng;
+            const size_t off = ((size_t)c * p.H + h0 + hl) * ng + gi;
+            const int srow = c * HB + hl;
+            sb_s[2 * (srow * ng + gi)] = half_bits_to_float(p.up.scales[off]);
+            sb_s[2 * (srow * ng + gi) + 1] = half_bits_to_float(p.up.biases[off]);
+        }
+    }
+
+    // act and inv_rms come from the down kernel; raw from the kernel before it.
+    pdl_wait();
+
+    const int team = lane >> 3, tl = lane & 7;  // 8 lanes per up row
+    bool have_weights = false, timed_out = false;
+    for (int t0 = 0; t0 < p.M; t0 += MT) {
+        const int mt = min(MT, p.M - t0);
+        for (int i = tid; i < MT * L; i += blockDim.x) {
+            const int t = i / L, k = i % L;
+            act_s[i] = t < mt ? p.act[(size_t)(t0 + t) * L + k] : 0.f;
+        }
+        __syncthreads();
+        if (!have_weights) {
+            timed_out = !mbar_wait_bounded(bar, 0);
+            if (timed_out)
+                record_timeout(p.status);
+            have_weights = true;
+        }
+
+        for (int rr = warp * 4 + team; rr < p.C * hb; rr += nwarps * 4) {
+            const int c = rr / hb, hl = rr % hb;
+            const int srow = c * HB + hl;
+            const uint4 *wrow = reinterpret_cast<const uint4 *>(w_s + srow * row_bytes);
+            float acc[MT];
+#pragma unroll
+            for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+            if constexpr (WT == 0) {
+                for (int v = tl; v < L / 8; v += 8) {
+                    float wf[8];
+                    unpack_bf16x8(wrow[v], wf);
+#pragma unroll
+                    for (int t = 0; t < MT; ++t) {
+                        const float4 xa = *reinterpret_cast<const float4 *>(act_s + t * L + v * 8);
+                        const float4 xb = *reinterpret_cast<const float4 *>(act_s + t * L + v * 8 + 4);
+                        float a = acc[t];
+                        a = fmaf(wf[0], xa.x, a); a = fmaf(wf[1], xa.y, a);
+                        a = fmaf(wf[2], xa.z, a); a = fmaf(wf[3], xa.w, a);
+                        a = fmaf(wf[4], xb.x, a); a = fmaf(wf[5], xb.y, a);
+                        a = fmaf(wf[6], xb.z, a); a = fmaf(wf[7], xb.w, a);
+                        acc[t] = a;
+                    }
+                }
+            } else {
+                const float *sb = sb_s + 2 * srow * ng;
+                for (int v = tl; v < L / 32; v += 8) {
+                    const uint4 q = wrow[v];
+                    const int gi = (v * 32) / p.up.group;
+                    const float sc = sb[2 * gi], bi = sb[2 * gi + 1];
+                    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int wd = 0; wd < 4; ++wd) {
+                        float wf[8];
+#pragma unroll
+                        for (int n = 0; n < 8; ++n)
+                            wf[n] = fmaf((float)((words[wd] >> (4 * n)) & 0xFu), sc, bi);
+#pragma unroll
+                        for (int t = 0; t < MT; ++t) {
+                            const float *xr = act_s + t * L + v * 32 + wd * 8;
+                            const float4 xa = *reinterpret_cast<const float4 *>(xr);
+                            const float4 xb = *reinterpret_cast<const float4 *>(xr + 4);
+                            float a = acc[t];
+                            a = fmaf(wf[0], xa.x, a); a = fmaf(wf[1], xa.y, a);
+                            a = fmaf(wf[2], xa.z, a); a = fmaf(wf[3], xa.w, a);
+                            a = fmaf(wf[4], xb.x, a); a = fmaf(wf[5], xb.y, a);
+                            a = fmaf(wf[6], xb.z, a); a = fmaf(wf[7], xb.w, a);
+                            acc[t] = a;
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                float v = acc[t];
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                if (tl == 0) wv_s[(t * p.C + c) * HB + hl] = sigmoidf_(v);
+            }
+        }
+        __syncthreads();
+
+        for (int i = tid; i < mt * hb; i += blockDim.x) {
+            const int t = i / hb, hl = i % hb;
+            const int h = h0 + hl;
+            const size_t m = (size_t)(t0 + t);
+            float acc = 0.f;
+            for (int c = 0; c < p.C; ++c) {
+                const int j = c * p.H + h;
+                const float rv = __bfloat162float(__ushort_as_bfloat16(p.raw[m * p.W + j]));
+                const float gv = __bfloat162float(__ushort_as_bfloat16(p.g[j]));
+                const float nv = rv * p.inv_rms[m * p.C + c] * gv;
+                acc = fmaf(wv_s[(t * p.C + c) * HB + hl], nv, acc);
+            }
+            p.mixed[m * p.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(acc * p.inv_C));
+        }
+        __syncthreads();
+    }
+    if (timed_out)  // do not leave with a copy into this CTA's shared memory in flight
+        mbar_wait_bounded(bar, 0);
+}
+
+__global__ void __launch_bounds__(256) hc_inject_kernel(const InjectParams p)
+{
+    pdl_launch_dependents();
+    // The gates, and the guarantee that every reader of the old residual has
+    // finished, come with the previous kernel's completion.
+    pdl_wait();
+    const long per_tok = p.W / 8;
+    const long nvec = (long)p.M * per_tok;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < nvec; i += (long)gridDim.x * blockDim.x) {
+        const long m = i / per_tok;
+        const int e = (int)(i % per_tok) * 8;
+        const int c = e / p.H, h = e % p.H;
+        uint4 *rp = reinterpret_cast<uint4 *>(p.raw) + i;
+        const uint4 rv = *rp;
+        const uint4 ov = *reinterpret_cast<const uint4 *>(p.out + m * p.H + h);
+        const float gt = p.gate[m * p.gate_stride + c];
+        float rf[8], of[8];
+        unpack_bf16x8(rv, rf);
+        unpack_bf16x8(ov, of);
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(fmaf(of[2 * k], gt, rf[2 * k]),
+                                                           fmaf(of[2 * k + 1], gt, rf[2 * k + 1]));
+            o[k] = *reinterpret_cast<const uint32_t *>(&b);
+        }
+        *rp = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// raw[m][c*H + h] = emb[m][h]: one 16-byte vector of the wide row per thread.
+__global__ void __launch_bounds__(256) hc_replicate_kernel(const ReplicateParams p)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const long per_tok = (long)p.C * p.H / 8;
+    const long nvec = (long)p.M * per_tok;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < nvec; i += (long)gridDim.x * blockDim.x) {
+        const long m = i / per_tok;
+        const int h = (int)((i % per_tok) * 8) % p.H;
+        reinterpret_cast<uint4 *>(p.raw)[i] = *reinterpret_cast<const uint4 *>(p.emb + m * p.H + h);
+    }
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                      int cluster_x, bool pdl, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    int n = 0;
+    if (cluster_x > 0) {
+        attrs[n].id = cudaLaunchAttributeClusterDimension;
+        attrs[n].val.clusterDim.x = cluster_x;
+        attrs[n].val.clusterDim.y = 1;
+        attrs[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Raises a kernel's dynamic shared-memory limit once per device (to the
+// budget, which covers every launch the host logic allows).
+template <typename K>
+cudaError_t allow_smem(K kernel, size_t smem)
+{
+    if (smem <= 48 * 1024)
+        return cudaSuccess;
+    if (smem > kSmemBudget)
+        return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    static std::mutex mu;
+    static std::set<std::pair<const void *, int>> done;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_pair(reinterpret_cast<const void *>(kernel), dev);
+    if (done.count(key))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+    if (e == cudaSuccess)
+        done.insert(key);
+    return e;
+}
+
+template <int WT>
+cudaError_t launch_down_wt(const DownParams &p, const LaunchCfg &cfg, cudaStream_t stream)
+{
+    const int mt = p.mt;
+    const size_t smem = down_smem_bytes(p, mt);
+    const dim3 grid(p.S, (p.R + p.rows_per_block - 1) / p.rows_per_block, 1);
+    const dim3 block(down_threads(p));
+    void (*k)(DownParams) = nullptr;
+    switch (mt) {
+    case 1: k = hc_down_kernel<WT, 1>; break;
+    case 2: k = hc_down_kernel<WT, 2>; break;
+    case 4: k = hc_down_kernel<WT, 4>; break;
+    default: k = hc_down_kernel<WT, 8>; break;
+    }
+    cudaError_t e = allow_smem(k, smem);
+    if (e != cudaSuccess)
+        return e;
+    return launch_ex(k, grid, block, smem, stream, p.S, cfg.pdl, p);
+}
+
+template <int WT>
+cudaError_t launch_up_wt(const UpParams &p, const LaunchCfg &cfg, cudaStream_t stream)
+{
+    const int mt = p.mt;
+    const size_t smem = up_smem_bytes(p, mt);
+    const dim3 grid((p.H + p.HB - 1) / p.HB, 1, 1);
+    const dim3 block(up_threads(p));
+    void (*k)(UpParams) = nullptr;
+    switch (mt) {
+    case 1: k = hc_up_kernel<WT, 1>; break;
+    case 2: k = hc_up_kernel<WT, 2>; break;
+    case 4: k = hc_up_kernel<WT, 4>; break;
+    default: k = hc_up_kernel<WT, 8>; break;
+    }
+    cudaError_t e = allow_smem(k, smem);
+    if (e != cudaSuccess)
+        return e;
+    return launch_ex(k, grid, block, smem, stream, 0, cfg.pdl, p);
+}
+
+}  // namespace
+
+cudaError_t launch_replicate(const ReplicateParams &p, const LaunchCfg &cfg, cudaStream_t stream)
+{
+    const long nvec = (long)p.M * p.C * p.H / 8;
+    const int threads = 128;
+    long blocks = std::max<long>(1, std::min<long>((nvec + threads - 1) / threads, (long)cfg.sm_count * 8));
+    return launch_ex(hc_replicate_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, 0, cfg.pdl, p);
+}
+
+int gemv_token_tile(int M)
+{
+    return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8;
+}
+
+size_t down_smem_bytes(const DownParams &p, int mt) { return down_layout(p, mt).total; }
+size_t up_smem_bytes(const UpParams &p, int mt) { return up_layout(p, mt).total; }
+
+int down_threads(const DownParams &p)
+{
+    const int rounds = (p.rows_per_block + 15) / 16;
+    const int warps = std::max(4, (p.rows_per_block + rounds - 1) / rounds);
+    return 32 * warps;
+}
+
+int up_threads(const UpParams &p)
+{
+    const int warps = std::min(24, std::max(2, (p.C * p.HB + 3) / 4));
+    return 32 * warps;
+}
+
+cudaError_t launch_down(const DownParams &p, const LaunchCfg &cfg, cudaStream_t stream)
+{
+    return p.down.type == 0 ? launch_down_wt<0>(p, cfg, stream) : launch_down_wt<1>(p, cfg, stream);
+}
+
+cudaError_t launch_up(const UpParams &p, const LaunchCfg &cfg, cudaStream_t stream)
+{
+    return p.up.type == 0 ? launch_up_wt<0>(p, cfg, stream) : launch_up_wt<1>(p, cfg, stream);
+}
+
+cudaError_t launch_inject(const InjectParams &p, const LaunchCfg &cfg, cudaStream_t stream)
+{
+    const long nvec = (long)p.M * p.W / 8;
+    const int threads = 128;
+    long blocks = (nvec + threads - 1) / threads;
+    blocks = std::min<long>(blocks, (long)cfg.sm_count * 8);
+    blocks = std::max<long>(blocks, 1);
+    return launch_ex(hc_inject_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, 0, cfg.pdl, p);
+}
+
+}  // namespace tshc

@@ -1,0 +1,89 @@
+// hc_kernels.h -- launch parameters and launchers of the hyper-connection
+// kernels (internal to the library; the public ABI is include/ts_hc.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tshc {
+
+// A [rows][cols] weight in device memory (rows = outputs).
+struct WeightView {
+    int type;                 // 0 bf16, 1 INT4-affine
+    int group;                // INT4 group size
+    const void *data;         // bf16 [rows][cols] or uint8 [rows][cols/2]
+    const uint16_t *scales;   // fp16 [rows][cols/group]
+    const uint16_t *biases;   // fp16 [rows][cols/group]
+};
+
+// Split-K down projection: rows 0..L-1 are input_mix_weight_down, rows
+// L..L+Ci-1 block_inject_weight (Ci = C, or 0 for the mixer). A cluster of
+// S = C * sps CTAs shares one block of rows; CTA s of the cluster owns input
+// columns [s*KC, (s+1)*KC), which lie inside stream s / sps.
+struct DownParams {
+    const uint16_t *raw;      // bf16 [M][W]
+    const uint16_t *g;        // bf16 [W]
+    WeightView down;          // [L][W]
+    WeightView inject;        // [C][W]; data == nullptr for the mixer
+    float *act;               // [M][L]  silu(z / C)
+    float *inv_rms;           // [M][C]
+    float *gate;              // token m's gates at gate + m * gate_stride
+    long gate_stride;
+    int M, H, C, L, R, W;     // R = L + Ci rows
+    int sps, S, KC;           // chunks per stream, cluster size, chunk width
+    int rows_per_block;
+    int mt;                   // tokens per tile (1, 2, 4 or 8)
+    float eps, inv_C;
+    unsigned *status;
+};
+
+// Up projection + sigmoid + mean mix: CTA b owns h in [b*HB, b*HB + HB) of
+// every stream, i.e. up rows {c*H + h}.
+struct UpParams {
+    const uint16_t *raw;      // bf16 [M][W]
+    const uint16_t *g;        // bf16 [W]
+    WeightView up;            // [W][L]
+    const float *act;         // [M][L]
+    const float *inv_rms;     // [M][C]
+    uint16_t *mixed;          // bf16 [M][H]
+    int M, H, C, L, W;
+    int HB;
+    int mt;                   // tokens per tile (1, 2, 4 or 8)
+    float inv_C;
+    unsigned *status;
+};
+
+struct InjectParams {
+    uint16_t *raw;            // bf16 [M][W], in place
+    const uint16_t *out;      // bf16 [M][H]
+    const float *gate;        // token m's gates at gate + m * gate_stride
+    long gate_stride;
+    int M, H, C, W;
+};
+
+struct ReplicateParams {
+    const uint16_t *emb;      // bf16 [M][H]
+    uint16_t *raw;            // bf16 [M][C*H]
+    int M, H, C;
+};
+
+struct LaunchCfg {
+    int sm_count;
+    bool pdl;                 // launch as a programmatic dependent of the previous kernel
+};
+
+// Token-tile width for M tokens (1, 2, 4 or 8) before shared-memory limits.
+int gemv_token_tile(int M);
+// Shared memory one CTA may use (leaves room for a co-resident dependent CTA).
+constexpr size_t kSmemBudget = 200 * 1024;
+size_t down_smem_bytes(const DownParams &p, int mt);
+size_t up_smem_bytes(const UpParams &p, int mt);
+int down_threads(const DownParams &p);
+int up_threads(const UpParams &p);
+
+cudaError_t launch_down(const DownParams &p, const LaunchCfg &cfg, cudaStream_t stream);
+cudaError_t launch_up(const UpParams &p, const LaunchCfg &cfg, cudaStream_t stream);
+cudaError_t launch_inject(const InjectParams &p, const LaunchCfg &cfg, cudaStream_t stream);
+cudaError_t launch_replicate(const ReplicateParams &p, const LaunchCfg &cfg, cudaStream_t stream);
+
+}  // namespace tshc

@@ -1,0 +1,373 @@
+// ts_hc_api.cu -- the C ABI of include/ts_hc.h: argument validation on the
+// host, launch geometry, and the kernel launches. Allocates nothing.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "hc_kernels.h"
+#include "ts_hc.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+ts_status fail(ts_status st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+ts_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(TS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device-side status word: kernels record a timed-out wait here.
+__device__ unsigned int g_device_status;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxC = 8;
+constexpr int kMaxL = 1024;
+constexpr int kMaxH = 16384;
+
+struct DeviceInfo {
+    int sm_count = 0;
+    unsigned *status = nullptr;
+    bool ready = false;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+ts_status device_info(DeviceInfo *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(TS_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(MultiProcessorCount)");
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_device_status);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(device status)");
+        d.ready = true;
+    }
+    *out = d;
+    return TS_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+ts_status check_shape(int M, int H, int C, int L)
+{
+    if (M < 0)
+        return fail(TS_ERR_INVALID_ARG, "M = %d must be >= 0", M);
+    if (H < 8 || H % 8 != 0 || H > kMaxH)
+        return fail(TS_ERR_INVALID_ARG, "H = %d must be a multiple of 8 in [8, %d]", H, kMaxH);
+    if (C < 1 || C > kMaxC)
+        return fail(TS_ERR_INVALID_ARG, "C = %d must be in [1, %d]", C, kMaxC);
+    if (L < 8 || L % 8 != 0 || L > kMaxL)
+        return fail(TS_ERR_INVALID_ARG, "lowrank = %d must be a multiple of 8 in [8, %d]", L, kMaxL);
+    return TS_OK;
+}
+
+ts_status check_ptr(const void *p, const char *name, size_t align)
+{
+    if (!p)
+        return fail(TS_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!aligned(p, align))
+        return fail(TS_ERR_INVALID_ARG, "%s is not %zu-byte aligned", name, align);
+    return TS_OK;
+}
+
+ts_status check_weight(const ts_weight *w, const char *name, int rows, int cols)
+{
+    (void)rows;
+    if (!w)
+        return fail(TS_ERR_INVALID_ARG, "%s is NULL", name);
+    if (w->type == TS_W_BF16) {
+        if (!w->data || !aligned(w->data, 16))
+            return fail(TS_ERR_INVALID_ARG, "%s.data must be a 16-byte aligned device pointer", name);
+        return TS_OK;
+    }
+    if (w->type == TS_W_INT4_AFFINE) {
+        if (w->group != 32 && w->group != 64 && w->group != 128)
+            return fail(TS_ERR_UNSUPPORTED, "%s.group = %d: INT4 groups of 32, 64 or 128 are supported",
+                        name, w->group);
+        if (cols % w->group != 0 || cols % 32 != 0)
+            return fail(TS_ERR_UNSUPPORTED, "%s: %d inputs are not a multiple of the group %d and of 32",
+                        name, cols, w->group);
+        if (!w->data || !aligned(w->data, 16))
+            return fail(TS_ERR_INVALID_ARG, "%s.data must be a 16-byte aligned device pointer", name);
+        if (!w->scales || !aligned(w->scales, 2) || !w->biases || !aligned(w->biases, 2))
+            return fail(TS_ERR_INVALID_ARG, "%s.scales / %s.biases must be 2-byte aligned device pointers",
+                        name, name);
+        return TS_OK;
+    }
+    return fail(TS_ERR_INVALID_ARG, "%s.type = %d is not a ts_wtype", name, (int)w->type);
+}
+
+tshc::WeightView view(const ts_weight *w)
+{
+    tshc::WeightView v{};
+    if (!w)
+        return v;
+    v.type = w->type;
+    v.group = w->type == TS_W_INT4_AFFINE ? w->group : 0;
+    v.data = w->data;
+    v.scales = static_cast<const uint16_t *>(w->scales);
+    v.biases = static_cast<const uint16_t *>(w->biases);
+    return v;
+}
+
+// Chunks per stream for the split-K down kernel: the largest sps with
+// C * sps <= 8 (one portable cluster) whose chunk H / sps is a multiple of
+// `align` elements.
+int choose_sps(int H, int C, int align)
+{
+    int best = 0;
+    for (int sps = 1; C * sps <= 8; ++sps)
+        if (H % sps == 0 && (H / sps) % align == 0)
+            best = sps;
+    return best;
+}
+
+// The shared part of ts_hc_call and ts_hc_mixer.
+ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *down,
+                       const ts_weight *up, const ts_weight *inject, void *mixed, float *inject_w,
+                       long inject_stride, int M, int H, int C, int L, float eps, void *workspace,
+                       size_t workspace_bytes, cudaStream_t stream)
+{
+    ts_status st = check_shape(M, H, C, L);
+    if (st != TS_OK)
+        return st;
+    const int W = C * H;
+    if ((st = check_ptr(raw, "raw", 16)) != TS_OK) return st;
+    if ((st = check_ptr(hc_norm_w, "hc_norm_w", 16)) != TS_OK) return st;
+    if ((st = check_ptr(mixed, "mixed", 16)) != TS_OK) return st;
+    if ((st = check_weight(down, "down", L, W)) != TS_OK) return st;
+    if ((st = check_weight(up, "up", W, L)) != TS_OK) return st;
+    if (inject) {
+        if ((st = check_weight(inject, "inject", C, W)) != TS_OK) return st;
+        if (inject->type != down->type || (down->type == TS_W_INT4_AFFINE && inject->group != down->group))
+            return fail(TS_ERR_UNSUPPORTED, "inject must have the same storage format and group as down");
+        if ((st = check_ptr(inject_w, "inject_w", 4)) != TS_OK) return st;
+        if (inject_stride < C)
+            return fail(TS_ERR_INVALID_ARG, "inject_stride = %ld must be >= C = %d", inject_stride, C);
+    }
+    if (!(eps >= 0.0f) || eps > 1.0f)
+        return fail(TS_ERR_INVALID_ARG, "eps = %g must be in [0, 1]", (double)eps);
+    if (M == 0)
+        return TS_OK;
+    const size_t need = ts_hc_workspace_bytes(M, H, C, L);
+    if (!workspace || workspace_bytes < need)
+        return fail(TS_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+    if (!aligned(workspace, 256))
+        return fail(TS_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+
+    const int down_align = down->type == TS_W_BF16 ? 8 : std::max(32, down->group);
+    const int sps = choose_sps(H, C, down_align);
+    if (sps == 0)
+        return fail(TS_ERR_UNSUPPORTED, "H = %d is not a multiple of %d (INT4 down weights)", H, down_align);
+
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != TS_OK)
+        return st;
+
+    size_t inv_off = 0, act_off = 0;
+    ts_hc_workspace_layout(M, H, C, L, &inv_off, &act_off);
+    float *inv_rms = reinterpret_cast<float *>(static_cast<char *>(workspace) + inv_off);
+    float *act = reinterpret_cast<float *>(static_cast<char *>(workspace) + act_off);
+
+    tshc::DownParams d{};
+    d.raw = static_cast<const uint16_t *>(raw);
+    d.g = static_cast<const uint16_t *>(hc_norm_w);
+    d.down = view(down);
+    d.inject = view(inject);
+    d.act = act;
+    d.inv_rms = inv_rms;
+    d.gate = inject ? inject_w : nullptr;
+    d.gate_stride = inject ? inject_stride : 0;
+    d.M = M; d.H = H; d.C = C; d.L = L; d.W = W;
+    d.R = L + (inject ? C : 0);
+    d.sps = sps; d.S = C * sps; d.KC = H / sps;
+    d.eps = eps;
+    d.inv_C = 1.0f / (float)C;
+    d.status = dev.status;
+    const int target_blocks = std::max(1, dev.sm_count / d.S);
+    d.rows_per_block = (d.R + target_blocks - 1) / target_blocks;
+    d.mt = tshc::gemv_token_tile(M);
+    while (tshc::down_smem_bytes(d, d.mt) > tshc::kSmemBudget && d.mt > 1)
+        d.mt /= 2;
+    while (tshc::down_smem_bytes(d, d.mt) > tshc::kSmemBudget && d.rows_per_block > 1)
+        d.rows_per_block = (d.rows_per_block + 1) / 2;
+    if (tshc::down_smem_bytes(d, d.mt) > tshc::kSmemBudget)
+        return fail(TS_ERR_UNSUPPORTED, "shape H = %d, C = %d exceeds the shared-memory budget", H, C);
+
+    tshc::UpParams u{};
+    u.raw = d.raw;
+    u.g = d.g;
+    u.up = view(up);
+    u.act = act;
+    u.inv_rms = inv_rms;
+    u.mixed = static_cast<uint16_t *>(mixed);
+    u.M = M; u.H = H; u.C = C; u.L = L; u.W = W;
+    u.HB = (H + dev.sm_count - 1) / dev.sm_count;
+    u.inv_C = d.inv_C;
+    u.status = dev.status;
+    u.mt = tshc::gemv_token_tile(M);
+    while (tshc::up_smem_bytes(u, u.mt) > tshc::kSmemBudget && u.mt > 1)
+        u.mt /= 2;
+    while (tshc::up_smem_bytes(u, u.mt) > tshc::kSmemBudget && u.HB > 1)
+        u.HB = (u.HB + 1) / 2;
+    if (tshc::up_smem_bytes(u, u.mt) > tshc::kSmemBudget)
+        return fail(TS_ERR_UNSUPPORTED, "shape C = %d, lowrank = %d exceeds the shared-memory budget", C, L);
+
+    const tshc::LaunchCfg cfg{dev.sm_count, true};
+    cudaError_t e = tshc::launch_down(d, cfg, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launching the down kernel");
+    e = tshc::launch_up(u, cfg, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launching the up kernel");
+    return TS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ts_hc_workspace_bytes(int M, int H, int C, int lowrank)
+{
+    if (M < 0 || H < 1 || C < 1 || lowrank < 1)
+        return 0;
+    return align256(sizeof(float) * (size_t)M * C) + align256(sizeof(float) * (size_t)M * lowrank);
+}
+
+ts_status ts_hc_workspace_layout(int M, int H, int C, int lowrank, size_t *inv_rms_offset,
+                                 size_t *act_offset)
+{
+    if (M < 0 || H < 1 || C < 1 || lowrank < 1)
+        return fail(TS_ERR_INVALID_ARG, "invalid shape");
+    if (inv_rms_offset)
+        *inv_rms_offset = 0;
+    if (act_offset)
+        *act_offset = align256(sizeof(float) * (size_t)M * C);
+    return TS_OK;
+}
+
+ts_status ts_hc_call(const void *raw, const void *hc_norm_w, const ts_weight *down,
+                     const ts_weight *up, const ts_weight *inject, void *mixed, float *inject_w,
+                     long inject_stride, int M, int H, int C, int lowrank, float eps,
+                     void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    g_last_error.clear();
+    if (!inject)
+        return fail(TS_ERR_INVALID_ARG, "inject is NULL (use ts_hc_mixer for the final mixer)");
+    return hc_call_impl(raw, hc_norm_w, down, up, inject, mixed, inject_w, inject_stride, M, H, C,
+                        lowrank, eps, workspace, workspace_bytes, stream);
+}
+
+ts_status ts_hc_mixer(const void *raw, const void *hc_norm_w, const ts_weight *down,
+                      const ts_weight *up, void *mixed, int M, int H, int C, int lowrank, float eps,
+                      void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    g_last_error.clear();
+    return hc_call_impl(raw, hc_norm_w, down, up, nullptr, mixed, nullptr, 0, M, H, C, lowrank, eps,
+                        workspace, workspace_bytes, stream);
+}
+
+ts_status ts_hc_inject_add(void *raw, const void *out, const float *inject_w, long inject_stride,
+                           int M, int H, int C, cudaStream_t stream)
+{
+    g_last_error.clear();
+    if (M < 0)
+        return fail(TS_ERR_INVALID_ARG, "M = %d must be >= 0", M);
+    if (H < 8 || H % 8 != 0 || H > kMaxH)
+        return fail(TS_ERR_INVALID_ARG, "H = %d must be a multiple of 8 in [8, %d]", H, kMaxH);
+    if (C < 1 || C > kMaxC)
+        return fail(TS_ERR_INVALID_ARG, "C = %d must be in [1, %d]", C, kMaxC);
+    ts_status st;
+    if ((st = check_ptr(raw, "raw", 16)) != TS_OK) return st;
+    if ((st = check_ptr(out, "out", 16)) != TS_OK) return st;
+    if ((st = check_ptr(inject_w, "inject_w", 4)) != TS_OK) return st;
+    if (inject_stride < C)
+        return fail(TS_ERR_INVALID_ARG, "inject_stride = %ld must be >= C = %d", inject_stride, C);
+    if (M == 0)
+        return TS_OK;
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != TS_OK)
+        return st;
+    tshc::InjectParams p{};
+    p.raw = static_cast<uint16_t *>(raw);
+    p.out = static_cast<const uint16_t *>(out);
+    p.gate = inject_w;
+    p.gate_stride = inject_stride;
+    p.M = M; p.H = H; p.C = C; p.W = C * H;
+    const cudaError_t e = tshc::launch_inject(p, tshc::LaunchCfg{dev.sm_count, true}, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launching the inject-add kernel");
+    return TS_OK;
+}
+
+ts_status ts_hc_replicate_entry(const void *emb, void *raw, int M, int H, int C, cudaStream_t stream)
+{
+    g_last_error.clear();
+    if (M < 0)
+        return fail(TS_ERR_INVALID_ARG, "M = %d must be >= 0", M);
+    if (H < 8 || H % 8 != 0 || H > kMaxH)
+        return fail(TS_ERR_INVALID_ARG, "H = %d must be a multiple of 8 in [8, %d]", H, kMaxH);
+    if (C < 1 || C > kMaxC)
+        return fail(TS_ERR_INVALID_ARG, "C = %d must be in [1, %d]", C, kMaxC);
+    ts_status st;
+    if ((st = check_ptr(emb, "emb", 16)) != TS_OK) return st;
+    if ((st = check_ptr(raw, "raw", 16)) != TS_OK) return st;
+    if (M == 0)
+        return TS_OK;
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != TS_OK)
+        return st;
+    tshc::ReplicateParams p{static_cast<const uint16_t *>(emb), static_cast<uint16_t *>(raw), M, H, C};
+    const cudaError_t e = tshc::launch_replicate(p, tshc::LaunchCfg{dev.sm_count, true}, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launching the entry-replication kernel");
+    return TS_OK;
+}
+
+const char *ts_hc_last_error(void) { return g_last_error.c_str(); }
+
+ts_status ts_hc_device_status(cudaStream_t stream, int *status)
+{
+    g_last_error.clear();
+    if (!status)
+        return fail(TS_ERR_INVALID_ARG, "status is NULL");
+    unsigned v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_device_status, sizeof v, 0, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "reading the device status word");
+    *status = v == 0 ? TS_OK : (int)v;
+    return TS_OK;
+}
+
+}  // extern "C"

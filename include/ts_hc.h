@@ -1,0 +1,166 @@
+/*
+ * ts_hc.h -- C ABI of the GB300 (sm_103a) hyper-connection residual call.
+ *
+ * The operations are those of the qwen4_exp decode flow in the
+ * turbospark-runtime 0.3.0 source pages:
+ *   - families/qwen4/mod.rs, module doc, "## Hyper-connections": one call maps
+ *     the C*H-wide residual `raw` to the H-wide `mixed` and the C-wide gate
+ *     `inject_w`;
+ *   - families/qwen4/mod.rs, decoder-layer pseudocode and "THE INJECTION
+ *     TRAP": the inject-add onto the un-normalized residual;
+ *   - families/qwen4/mod.rs, the paragraph on the final
+ *     `hyper_connection_mixer` (the call without block_inject_weight);
+ *   - families/qwen4/hc.rs, `encode_hyper_connection`: step order, weight
+ *     shapes (rows = outputs, cols = inputs) and the per-token inject row.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *     allocates nothing and keeps no state beyond per-device attributes it
+ *     queries once. Every call is asynchronous on `stream` (0 = legacy default
+ *     stream).
+ *   - Row-major everywhere. A wide vector has C*H elements; stream c occupies
+ *     elements [c*H, (c+1)*H). Linear weights are [out][in] with no bias.
+ *   - bf16 tensors are 16-byte aligned; H is a multiple of 8, hc_lowrank (L)
+ *     a multiple of 8 (32 for INT4 weights); 1 <= C <= 8; 8 <= L <= 1024.
+ *   - Arguments are validated on the host before anything is launched; a bad
+ *     argument returns an error status without launching, and
+ *     ts_hc_last_error() names it. Launch failures return TS_ERR_CUDA.
+ *   - Results of the GPU path are deterministic: the same inputs give the same
+ *     bits on every run (fixed-order split-K reductions, no float atomics).
+ *   - A kernel that waits on an asynchronous copy gives up after about one
+ *     second, records TS_ERR_TIMEOUT in a device-side status word and returns
+ *     without hanging; read it with ts_hc_device_status().
+ */
+#ifndef TS_HC_H
+#define TS_HC_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TS_OK = 0,
+    TS_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size or stride */
+    TS_ERR_UNSUPPORTED = 2,   /* valid request outside what this build supports */
+    TS_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    TS_ERR_WORKSPACE = 4,     /* workspace missing or smaller than ts_hc_workspace_bytes() */
+    TS_ERR_TIMEOUT = 5        /* a device-side wait gave up (see ts_hc_device_status) */
+} ts_status;
+
+typedef enum {
+    TS_W_BF16 = 0,            /* data: bf16 [out][in] */
+    TS_W_INT4_AFFINE = 1      /* data: uint8 [out][in/2], element 2i in the low nibble of
+                                 byte i; scales, biases: fp16 [out][in/group];
+                                 weight = q * scale + bias, q in [0, 15] */
+} ts_wtype;
+
+/* A linear weight [out][in] in its storage format (real_forward.rs,
+ * RealForwardRunner doc: projections are INT4-affine quantised or dense). */
+typedef struct {
+    int32_t type;             /* ts_wtype */
+    int32_t group;            /* INT4: inputs per (scale, bias) group: 32, 64 or 128 */
+    const void *data;
+    const void *scales;       /* INT4 only, else NULL */
+    const void *biases;       /* INT4 only, else NULL */
+} ts_weight;
+
+/*
+ * Bytes of device workspace ts_hc_call / ts_hc_mixer need for M tokens
+ * (0 for invalid shapes). The workspace is caller-owned scratch: it need not
+ * be initialised, is overwritten by every call, and must not be shared by two
+ * calls that can run at the same time.
+ *
+ * After a successful call the workspace holds two fp32 intermediates of the
+ * last call, at the byte offsets ts_hc_workspace_layout() reports:
+ *   inv_rms [M][C]: 1/sqrt(mean_h raw[m][c*H+h]^2 + eps), per token and stream;
+ *   act     [M][L]: silu(input_mix_weight_down(normed) / C).
+ */
+size_t ts_hc_workspace_bytes(int M, int H, int C, int lowrank);
+ts_status ts_hc_workspace_layout(int M, int H, int C, int lowrank,
+                                 size_t *inv_rms_offset, size_t *act_offset);
+
+/*
+ * One hyper-connection call (attn_hc / mlp_hc) on M independent tokens
+ * (families/qwen4/mod.rs "## Hyper-connections"; families/qwen4/hc.rs
+ * encode_hyper_connection):
+ *
+ *   normed  = hc_norm(raw)                 grouped RMS, group = H, eps inside
+ *                                          the root, scale applied directly
+ *   act     = silu(down(normed) / C)       C*H -> L
+ *   w       = sigmoid(up(act))             L -> C*H, no division
+ *   mixed   = mean_c(w[c*H+h] * normed[c*H+h])
+ *   gate    = 2 * sigmoid(inject(normed) / C)
+ *
+ *   raw        bf16 [M][C*H], read only (the caller injects separately)
+ *   hc_norm_w  bf16 [C*H] (hc_norm.weight)
+ *   down       [L][C*H]   (input_mix_weight_down.weight)
+ *   up         [C*H][L]   (input_mix_weight_up.weight)
+ *   inject     [C][C*H]   (block_inject_weight.weight)
+ *   mixed      bf16 [M][H], written (rounded to nearest even)
+ *   inject_w   fp32; token t's C gates are written at inject_w + t*inject_stride
+ *              (inject_stride >= C; 2*C with a +C base offset for mlp_hc gives
+ *              the per-token row t*C*2 of a shared micro-batch gate buffer)
+ *   eps        RMS epsilon (the pages use 1e-6)
+ *   workspace  >= ts_hc_workspace_bytes(M, H, C, lowrank) bytes, 256-byte aligned
+ *
+ * M == 0 is a no-op. Returns TS_OK or an error status (nothing launched on
+ * argument errors).
+ */
+ts_status ts_hc_call(const void *raw, const void *hc_norm_w,
+                     const ts_weight *down, const ts_weight *up, const ts_weight *inject,
+                     void *mixed, float *inject_w, long inject_stride,
+                     int M, int H, int C, int lowrank, float eps,
+                     void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * The inject-add (families/qwen4/mod.rs decoder pseudocode and THE INJECTION
+ * TRAP): raw[m][c*H+h] += out[m][h] * inject_w[m*inject_stride + c], in place
+ * on the UN-normalized residual, computed in fp32 and rounded to bf16 (nearest
+ * even).
+ *
+ *   raw       bf16 [M][C*H], read and written
+ *   out       bf16 [M][H], the sublayer output
+ *   inject_w  fp32, token m's gates at inject_w + m*inject_stride (inject_stride >= C)
+ */
+ts_status ts_hc_inject_add(void *raw, const void *out, const float *inject_w,
+                           long inject_stride, int M, int H, int C, cudaStream_t stream);
+
+/*
+ * The final hyper_connection_mixer (families/qwen4/mod.rs, paragraph after the
+ * hyper-connection pseudocode; families/qwen4/hc.rs, has_inject_gate = false):
+ * ts_hc_call without block_inject_weight. Writes `mixed` bf16 [M][H] only.
+ */
+ts_status ts_hc_mixer(const void *raw, const void *hc_norm_w,
+                      const ts_weight *down, const ts_weight *up,
+                      void *mixed, int M, int H, int C, int lowrank, float eps,
+                      void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Entry replication (families/qwen4/mod.rs, decoder pseudocode, entry line:
+ * the embedding row is repeated C times, not padded):
+ * raw[m][c*H + h] = emb[m][h] for every stream c.
+ *
+ *   emb  bf16 [M][H], read
+ *   raw  bf16 [M][C*H], written
+ */
+ts_status ts_hc_replicate_entry(const void *emb, void *raw, int M, int H, int C, cudaStream_t stream);
+
+/* The last error message of the calling thread ("" if none). */
+const char *ts_hc_last_error(void);
+
+/*
+ * Reads the device-side status word of the current device (synchronising
+ * `stream`) into *status (TS_OK or TS_ERR_TIMEOUT) and clears it. Returns
+ * TS_ERR_CUDA if the read itself fails.
+ */
+ts_status ts_hc_device_status(cudaStream_t stream, int *status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TS_HC_H */

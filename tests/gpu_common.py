@@ -1,0 +1,74 @@
+"""Shared pieces of the GPU parity tests: tolerances and device helpers.
+
+Tolerances (the parity bar for this path):
+* bf16 outputs (mixed, the injected residual): |gpu - ref| <= 1e-2 * (1 + |ref|);
+* fp32 intermediates and the fp32 gates: |gpu - ref| <= 1e-3 * |ref| + 1e-5 * rms(ref),
+  i.e. 1e-3 relative, with an absolute floor of 1e-5 of the vector's RMS so
+  that elements that happen to sit near zero are not held to a relative bound
+  that no fp32 summation order can meet.
+"""
+import numpy as np
+import pytest
+import torch
+
+from hyper_connection_residual_call_gb300 import binding as B
+from hyper_connection_residual_call_gb300.build import build
+
+BF16_ATOL, BF16_RTOL = 1e-2, 1e-2
+FP32_RTOL, FP32_RMS_FLOOR = 1e-3, 1e-5
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    build()
+    B.library()
+
+
+def to_np(t) -> np.ndarray:
+    return t.detach().float().cpu().double().numpy()
+
+
+def check_bf16(gpu, ref, what: str) -> float:
+    g = to_np(gpu).reshape(np.shape(ref))
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite values"
+    lim = BF16_ATOL + BF16_RTOL * np.abs(ref)
+    ratio = np.abs(g - ref) / lim
+    worst = float(ratio.max()) if ratio.size else 0.0
+    assert worst <= 1.0, f"{what}: worst |err|/limit = {worst:.3g} at {np.unravel_index(ratio.argmax(), ratio.shape)}"
+    return worst
+
+
+def check_fp32(gpu, ref, what: str) -> float:
+    g = to_np(gpu).reshape(np.shape(ref))
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite values"
+    rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
+    lim = FP32_RTOL * np.abs(ref) + FP32_RMS_FLOOR * rms
+    ratio = np.abs(g - ref) / np.maximum(lim, 1e-300)
+    worst = float(ratio.max()) if ratio.size else 0.0
+    assert worst <= 1.0, f"{what}: worst |err|/limit = {worst:.3g} at {np.unravel_index(ratio.argmax(), ratio.shape)}"
+    return worst
+
+
+def guarded(shape, dtype, fill, device="cuda", guard=64):
+    """A buffer of `shape` followed by `guard` sentinel elements; returns (view, whole)."""
+    n = int(np.prod(shape))
+    whole = torch.full((n + guard,), fill, dtype=dtype, device=device)
+    return whole[:n].view(*shape), whole
+
+
+def guard_intact(whole, n, fill) -> bool:
+    tail = whole[n:]
+    if torch.is_floating_point(tail) and isinstance(fill, float) and np.isnan(fill):
+        return bool(torch.isnan(tail).all())
+    return bool((tail == fill).all())
+
+
+def workspace_intermediates(ws, M, H, C, L):
+    inv_off, act_off = B.ts_hc_workspace_layout(M, H, C, L)
+    f = ws.view(torch.uint8)
+    inv = f[inv_off: inv_off + 4 * M * C].view(torch.float32).view(M, C)
+    act = f[act_off: act_off + 4 * M * L].view(torch.float32).view(M, L)
+    return inv, act

@@ -1,0 +1,136 @@
+"""Host-side checks of the C ABI: the library loads, exports every entry point
+the header declares, and rejects bad arguments before launching anything.
+
+Every call here fails argument validation (or is an M = 0 no-op), so no CUDA
+call is made: these run on a machine without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from hyper_connection_residual_call_gb300 import binding as B
+from hyper_connection_residual_call_gb300.build import INCLUDE, build
+
+H, C, L = 2560, 4, 320
+FAKE = 0x10000  # an aligned address that is never dereferenced: validation fails first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return B.library()
+
+
+def declared_symbols():
+    text = open(os.path.join(INCLUDE, "ts_hc.h")).read()
+    return sorted(set(re.findall(r"\b(ts_hc_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert set(names) == set(B.EXPORTS), names
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+
+
+def test_workspace_size_and_layout(lib):
+    assert B.ts_hc_workspace_bytes(1, H, C, L) == 256 + 1280
+    assert B.ts_hc_workspace_bytes(128, H, C, L) == 2048 + 163840
+    assert B.ts_hc_workspace_bytes(0, H, C, L) == 0
+    assert B.ts_hc_workspace_bytes(-1, H, C, L) == 0
+    inv, act = B.ts_hc_workspace_layout(3, H, C, L)
+    assert inv == 0 and act == 256 and act % 256 == 0
+
+
+def _w(data=FAKE, typ=B.TS_W_BF16, group=0, scales=None, biases=None):
+    return B.TsWeight(typ, group, data, scales, biases)
+
+
+def _call(**kw):
+    a = dict(raw=FAKE, g=FAKE, down=_w(), up=_w(), inject=_w(), mixed=FAKE, inject_w=FAKE, stride=C,
+             M=1, H=H, C=C, L=L, eps=1e-6, ws=FAKE, ws_bytes=1 << 20, stream=None)
+    a.update(kw)
+    return B.ts_hc_call(a["raw"], a["g"], a["down"], a["up"], a["inject"], a["mixed"], a["inject_w"],
+                        a["stride"], a["M"], a["H"], a["C"], a["L"], a["eps"], a["ws"], a["ws_bytes"],
+                        a["stream"])
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(raw=None), B.TS_ERR_INVALID_ARG, "raw is NULL"),
+    (dict(raw=FAKE + 2), B.TS_ERR_INVALID_ARG, "raw is not 16-byte aligned"),
+    (dict(mixed=None), B.TS_ERR_INVALID_ARG, "mixed is NULL"),
+    (dict(g=FAKE + 8), B.TS_ERR_INVALID_ARG, "hc_norm_w"),
+    (dict(H=2561), B.TS_ERR_INVALID_ARG, "H = 2561"),
+    (dict(C=0), B.TS_ERR_INVALID_ARG, "C = 0"),
+    (dict(C=9), B.TS_ERR_INVALID_ARG, "C = 9"),
+    (dict(L=4), B.TS_ERR_INVALID_ARG, "lowrank = 4"),
+    (dict(M=-1), B.TS_ERR_INVALID_ARG, "M = -1"),
+    (dict(stride=C - 1), B.TS_ERR_INVALID_ARG, "inject_stride"),
+    (dict(inject=None), B.TS_ERR_INVALID_ARG, "ts_hc_mixer"),
+    (dict(inject_w=None), B.TS_ERR_INVALID_ARG, "inject_w is NULL"),
+    (dict(down=_w(data=None)), B.TS_ERR_INVALID_ARG, "down.data"),
+    (dict(up=_w(typ=7)), B.TS_ERR_INVALID_ARG, "up.type"),
+    (dict(down=_w(typ=B.TS_W_INT4_AFFINE, group=48, scales=FAKE, biases=FAKE)), B.TS_ERR_UNSUPPORTED, "group = 48"),
+    (dict(up=_w(typ=B.TS_W_INT4_AFFINE, group=64, scales=None, biases=FAKE)), B.TS_ERR_INVALID_ARG, "scales"),
+    (dict(inject=_w(typ=B.TS_W_INT4_AFFINE, group=64, scales=FAKE, biases=FAKE)), B.TS_ERR_UNSUPPORTED,
+     "same storage format"),
+    (dict(eps=-1.0), B.TS_ERR_INVALID_ARG, "eps"),
+    (dict(ws_bytes=16), B.TS_ERR_WORKSPACE, "workspace of 16 bytes"),
+    (dict(ws=None), B.TS_ERR_WORKSPACE, "workspace"),
+    (dict(ws=FAKE + 16), B.TS_ERR_INVALID_ARG, "256-byte aligned"),
+])
+def test_call_rejects(lib, kw, status, needle):
+    assert _call(**kw) == status
+    assert needle in B.ts_hc_last_error()
+
+
+def test_call_m0_is_noop(lib):
+    assert _call(M=0, ws=None, ws_bytes=0) == B.TS_OK
+    assert B.ts_hc_last_error() == ""
+
+
+def test_mixer_rejects(lib):
+    st = B.ts_hc_mixer(None, FAKE, _w(), _w(), FAKE, 1, H, C, L, 1e-6, FAKE, 1 << 20, None)
+    assert st == B.TS_ERR_INVALID_ARG and "raw is NULL" in B.ts_hc_last_error()
+    st = B.ts_hc_mixer(FAKE, FAKE, _w(), _w(), FAKE, 0, H, C, L, 1e-6, None, 0, None)
+    assert st == B.TS_OK
+
+
+@pytest.mark.parametrize("args,needle", [
+    ((None, FAKE, FAKE, C, 1, H, C), "raw is NULL"),
+    ((FAKE, FAKE + 4, FAKE, C, 1, H, C), "out is not 16-byte aligned"),
+    ((FAKE, FAKE, FAKE + 2, C, 1, H, C), "inject_w is not 4-byte aligned"),
+    ((FAKE, FAKE, FAKE, C - 1, 1, H, C), "inject_stride"),
+    ((FAKE, FAKE, FAKE, C, 1, 12, C), "H = 12"),
+])
+def test_inject_add_rejects(lib, args, needle):
+    assert B.ts_hc_inject_add(*args, None) == B.TS_ERR_INVALID_ARG
+    assert needle in B.ts_hc_last_error()
+
+
+def test_inject_add_m0_is_noop(lib):
+    assert B.ts_hc_inject_add(FAKE, FAKE, FAKE, C, 0, H, C, None) == B.TS_OK
+
+
+def test_replicate_entry_rejects(lib):
+    assert B.ts_hc_replicate_entry(None, FAKE, 1, H, C, None) == B.TS_ERR_INVALID_ARG
+    assert "emb is NULL" in B.ts_hc_last_error()
+    assert B.ts_hc_replicate_entry(FAKE, FAKE + 8, 1, H, C, None) == B.TS_ERR_INVALID_ARG
+    assert B.ts_hc_replicate_entry(FAKE, FAKE, 0, H, C, None) == B.TS_OK
+
+
+def test_device_status_rejects_null(lib):
+    assert lib.ts_hc_device_status(None, None) == B.TS_ERR_INVALID_ARG
+
+
+def test_torch_layer_requires_cuda_tensors(lib):
+    import torch
+    from hyper_connection_residual_call_gb300 import inputs
+    w = inputs.make_hc_weights(256, 4, 32, 0)
+    raw = inputs.make_residual(1, 256, 4, 0)
+    with pytest.raises(B.HCError, match="CUDA tensor"):
+        B.hc_call(raw, w, H=256, C=4)
+    with pytest.raises(B.HCError, match="CUDA tensor"):
+        B.hc_inject_add(raw, torch.zeros(1, 256, dtype=torch.bfloat16), torch.ones(1, 4), H=256, C=4)

@@ -1,0 +1,266 @@
+"""GPU parity: the CUDA library (called through the C ABI) against the fp64 oracle.
+
+Covers the five workloads (tiny call, full-shape decode call, the M=128
+chunked-prefill micro-batch with per-token gate rows, the 40-layer stack at
+M=1 and M=16, INT4-affine weights at M=1 and M=64), plus ragged token counts
+and shapes that exercise other cluster sizes, chunk widths and tile tails,
+the M=0 no-op, guard regions after every output, the read-only residual,
+run-to-run bit identity and the device status word.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hyper_connection_residual_call_gb300 import binding as B
+from hyper_connection_residual_call_gb300 import inputs
+from gpu_common import (check_bf16, check_fp32, guard_intact, guarded, require_gpu, to_np,
+                        workspace_intermediates)
+
+pytestmark = pytest.mark.gpu
+EPS = 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.get()
+
+
+def gpu_call(raw_d, w_d, H, C, gates=None, stride=None):
+    """One ts_hc_call with sentinel guards after mixed (and after gates when owned)."""
+    M = raw_d.shape[0]
+    L = w_d.down.rows
+    mixed, mwhole = guarded((M, H), torch.bfloat16, -77.0)
+    own = gates is None
+    if own:
+        gates, gwhole = guarded((M, C), torch.float32, float("nan"))
+        stride = C
+    ws = B.workspace(M, H, C, L)
+    B.hc_call(raw_d, w_d, H=H, C=C, mixed=mixed, inject_w=gates, inject_stride=stride, eps=EPS, ws=ws)
+    torch.cuda.synchronize()
+    assert guard_intact(mwhole, M * H, -77.0), "write past the end of mixed"
+    if own:
+        assert guard_intact(gwhole, M * C, float("nan")), "write past the end of inject_w"
+    inv, act = workspace_intermediates(ws, M, H, C, L)
+    return mixed, gates, inv, act
+
+
+def check_call(res, ref, tag):
+    mixed, gates, inv, act = res
+    check_bf16(mixed, ref["mixed"], f"{tag} mixed")
+    check_fp32(inv, ref["inv_rms"], f"{tag} inv_rms")
+    check_fp32(act, ref["a"], f"{tag} act")
+    if "gate" in ref and gates is not None:
+        check_fp32(gates, ref["gate"], f"{tag} gate")
+
+
+def call_and_inject(orc, shape, seed, kind="bf16", group=64, up_group=None):
+    H, C, L, M = shape.H, shape.C, shape.L, shape.M
+    w = inputs.make_hc_weights(H, C, L, seed, kind=kind, group=group, up_group=up_group)
+    raw = inputs.make_residual(M, H, C, seed)
+    out = inputs.make_sublayer_out(M, H, seed)
+    ref = orc.hc_call(raw, w.g, w.down, w.up, w.inject, H=H, C=C, L=L, eps=EPS)
+    ref_raw = orc.inject_add(raw, out, ref["gate"], H=H, C=C)
+    w_d, raw_d, out_d = w.to("cuda"), raw.cuda(), out.cuda()
+    raw_before = raw_d.clone()
+    res = gpu_call(raw_d, w_d, H, C)
+    assert torch.equal(raw_d, raw_before), "ts_hc_call wrote the residual"
+    check_call(res, ref, f"{kind} M={M} H={H} C={C} L={L}")
+    raw2, rwhole = guarded((M, C * H), torch.bfloat16, -5.0)
+    raw2.copy_(raw_d)
+    B.hc_inject_add(raw2, out_d, res[1], H=H, C=C)
+    torch.cuda.synchronize()
+    assert guard_intact(rwhole, M * C * H, -5.0)
+    check_bf16(raw2, ref_raw, "injected residual")
+    return res
+
+
+def test_tiny_call(orc):
+    call_and_inject(orc, inputs.TINY, inputs.SEEDS["tiny"])
+
+
+def test_full_decode_call(orc):
+    call_and_inject(orc, inputs.FULL_DECODE, inputs.SEEDS["full_decode"])
+
+
+def test_bit_identical_runs(orc):
+    s = inputs.FULL_DECODE
+    w = inputs.make_hc_weights(s.H, s.C, s.L, 1).to("cuda")
+    raw = inputs.make_residual(3, s.H, s.C, 1).cuda()
+    a = gpu_call(raw, w, s.H, s.C)
+    b = gpu_call(raw, w, s.H, s.C)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("M,H,C,L", [(3, 40, 3, 24), (5, 64, 1, 8), (9, 128, 8, 16), (17, 256, 4, 32),
+                                     (2, 2560, 4, 320), (1, 8, 2, 8), (11, 96, 5, 40), (33, 512, 2, 64)])
+def test_shapes_and_ragged_tokens(orc, M, H, C, L):
+    call_and_inject(orc, inputs.Shape(M=M, H=H, C=C, L=L), seed=100 + M)
+
+
+@pytest.mark.parametrize("M,H,C,L,group", [(3, 128, 2, 64, 32), (2, 256, 4, 64, 64), (5, 256, 1, 128, 128)])
+def test_int4_shapes(orc, M, H, C, L, group):
+    call_and_inject(orc, inputs.Shape(M=M, H=H, C=C, L=L), seed=200 + M, kind="int4", group=group)
+
+
+def test_int4_tiny_up_group_32(orc):
+    # the tiny shape's lowrank (32) is below the group of 64: the up weight uses groups of 32
+    call_and_inject(orc, inputs.TINY, inputs.SEEDS["int4"], kind="int4", group=64, up_group=32)
+
+
+@pytest.mark.parametrize("M", [1, 64])
+def test_int4_full_shape(orc, M):
+    s = inputs.FULL_DECODE
+    call_and_inject(orc, inputs.Shape(M=M, H=s.H, C=s.C, L=s.L), inputs.SEEDS["int4"], kind="int4",
+                    group=inputs.INT4_GROUP)
+
+
+def test_mixer(orc):
+    s = inputs.FULL_DECODE
+    M = 3
+    w = inputs.make_hc_weights(s.H, s.C, s.L, 7, with_inject=False)
+    raw = inputs.make_residual(M, s.H, s.C, 7)
+    ref = orc.mixer(raw, w.g, w.down, w.up, H=s.H, C=s.C, L=s.L, eps=EPS)
+    w_d, raw_d = w.to("cuda"), raw.cuda()
+    mixed, mwhole = guarded((M, s.H), torch.bfloat16, -77.0)
+    ws = B.workspace(M, s.H, s.C, s.L)
+    B.hc_mixer(raw_d, w_d, H=s.H, C=s.C, mixed=mixed, eps=EPS, ws=ws)
+    torch.cuda.synchronize()
+    assert guard_intact(mwhole, M * s.H, -77.0)
+    inv, act = workspace_intermediates(ws, M, s.H, s.C, s.L)
+    check_call((mixed, None, inv, act), ref, "mixer")
+
+
+def test_mixer_equals_call_mixed():
+    s = inputs.TINY
+    w = inputs.make_hc_weights(s.H, s.C, s.L, 9).to("cuda")
+    raw = inputs.make_residual(4, s.H, s.C, 9).cuda()
+    mixed_call = gpu_call(raw, w, s.H, s.C)[0]
+    mixed_mix = B.hc_mixer(raw, w, H=s.H, C=s.C, eps=EPS)
+    torch.cuda.synchronize()
+    assert torch.equal(mixed_call, mixed_mix)
+
+
+def test_prefill_microbatch(orc):
+    """attn_hc + inject, mlp_hc + inject on 128 tokens; token t's gates at
+    t*C*2 (attn) and t*C*2 + C (mlp) of one buffer, none overwritten."""
+    s = inputs.PREFILL
+    seed = inputs.SEEDS["prefill"]
+    M, H, C, L = s.M, s.H, s.C, s.L
+    attn = inputs.make_hc_weights(H, C, L, seed, 0)
+    mlp = inputs.make_hc_weights(H, C, L, seed, 1)
+    raw = inputs.make_residual(M, H, C, seed)
+    oa, om = inputs.make_sublayer_out(M, H, seed, 0), inputs.make_sublayer_out(M, H, seed, 1)
+    ref = orc.prefill_pair(raw, attn, oa, mlp, om, H=H, C=C, L=L, eps=EPS, round_residual=True)
+
+    attn_d, mlp_d = attn.to("cuda"), mlp.to("cuda")
+    raw_d, oa_d, om_d = raw.cuda(), oa.cuda(), om.cuda()
+    gates, gwhole = guarded((M * 2 * C,), torch.float32, float("nan"))
+    mixed_a, _, inv_a, act_a = gpu_call(raw_d, attn_d, H, C, gates=gates, stride=2 * C)
+    assert torch.isnan(gates.view(M, 2, C)[:, 1]).all(), "attn_hc wrote an mlp gate slot"
+    B.hc_inject_add(raw_d, oa_d, gates, H=H, C=C, inject_stride=2 * C)
+    raw_after_attn = raw_d.clone()
+    mixed_m, _, inv_m, act_m = gpu_call(raw_d, mlp_d, H, C, gates=gates[C:], stride=2 * C)
+    B.hc_inject_add(raw_d, om_d, gates[C:], H=H, C=C, inject_stride=2 * C)
+    torch.cuda.synchronize()
+    assert guard_intact(gwhole, M * 2 * C, float("nan")), "write past the gate buffer"
+    assert not torch.isnan(gates).any(), "a gate slot was never written"
+    check_fp32(gates.view(M, 2, C), ref["gates"], "gate slots")
+    check_bf16(mixed_a, ref["mixed_attn"], "attn mixed")
+    check_fp32(inv_a, ref["inv_rms_attn"], "attn inv_rms")
+    check_fp32(act_a, ref["a_attn"], "attn act")
+    check_bf16(raw_after_attn, ref["raw_after_attn"], "residual after attn inject")
+    check_bf16(mixed_m, ref["mixed_mlp"], "mlp mixed")
+    check_fp32(inv_m, ref["inv_rms_mlp"], "mlp inv_rms")
+    check_fp32(act_m, ref["a_mlp"], "mlp act")
+    check_bf16(raw_d, ref["raw_after_mlp"], "residual after mlp inject")
+
+    # The same micro-batch as 128 single-token calls, each at its own gate row.
+    raw_t = raw.cuda()
+    gates_t = torch.full((M * 2 * C,), float("nan"), device="cuda")
+    mixed_t = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    ws = B.workspace(1, H, C, L)
+    for t in range(M):
+        B.hc_call(raw_t[t:t + 1], attn_d, H=H, C=C, mixed=mixed_t[t:t + 1], inject_w=gates_t[t * 2 * C:],
+                  inject_stride=2 * C, ws=ws)
+        B.hc_inject_add(raw_t[t:t + 1], oa_d[t:t + 1], gates_t[t * 2 * C:], H=H, C=C, inject_stride=2 * C)
+    for t in range(M):
+        B.hc_call(raw_t[t:t + 1], mlp_d, H=H, C=C, mixed=mixed_t[t:t + 1],
+                  inject_w=gates_t[t * 2 * C + C:], inject_stride=2 * C, ws=ws)
+        B.hc_inject_add(raw_t[t:t + 1], om_d[t:t + 1], gates_t[t * 2 * C + C:], H=H, C=C, inject_stride=2 * C)
+    torch.cuda.synchronize()
+    check_fp32(gates_t.view(M, 2, C), ref["gates"], "per-token gate slots")
+    check_bf16(mixed_t, ref["mixed_mlp"], "per-token mlp mixed")
+    check_bf16(raw_t, ref["raw_after_mlp"], "per-token residual")
+
+
+def run_stack_gpu(st, H, C):
+    """entry replication, 40 x (attn_hc + inject, mlp_hc + inject), exit mixer."""
+    M = st.emb.shape[0]
+    L = st.final.down.rows
+    raw = B.hc_replicate_entry(st.emb.cuda(), C=C)
+    gates = torch.empty((M * 2 * C,), dtype=torch.float32, device="cuda")
+    mixed = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    ws = B.workspace(M, H, C, L)
+    for (attn, mlp), (oa, om) in zip(st.layers, st.outs):
+        B.hc_call(raw, attn, H=H, C=C, mixed=mixed, inject_w=gates, inject_stride=2 * C, ws=ws)
+        B.hc_inject_add(raw, oa, gates, H=H, C=C, inject_stride=2 * C)
+        B.hc_call(raw, mlp, H=H, C=C, mixed=mixed, inject_w=gates[C:], inject_stride=2 * C, ws=ws)
+        B.hc_inject_add(raw, om, gates[C:], H=H, C=C, inject_stride=2 * C)
+    out = B.hc_mixer(raw, st.final, H=H, C=C, ws=ws)
+    torch.cuda.synchronize()
+    return out, raw
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_full_depth_stack(orc, M):
+    s = inputs.FULL_DECODE
+    H, C, L = s.H, s.C, s.L
+    st = inputs.make_stack(M, H, C, L, inputs.STACK_LAYERS, inputs.SEEDS["stack"])
+    ref = orc.stack(st.emb, st.layers, st.outs, st.final, H=H, C=C, L=L, eps=EPS, round_residual=True)
+    dev = inputs.StackInputs(st.emb, [(a.to("cuda"), m.to("cuda")) for a, m in st.layers],
+                             [(a.cuda(), m.cuda()) for a, m in st.outs], st.final.to("cuda"))
+    mixed, raw = run_stack_gpu(dev, H, C)
+    check_bf16(raw, ref["raw"], f"stack residual M={M}")
+    check_bf16(mixed, ref["mixed"], f"stack mixer output M={M}")
+
+
+def test_replicate_entry():
+    emb = inputs.make_embedding(3, 256, 5).cuda()
+    raw, whole = guarded((3, 4 * 256), torch.bfloat16, -9.0)
+    B.hc_replicate_entry(emb, C=4, raw=raw)
+    torch.cuda.synchronize()
+    assert guard_intact(whole, 3 * 1024, -9.0)
+    assert torch.equal(raw, emb.repeat(1, 4))
+
+
+def test_m0_is_noop():
+    s = inputs.TINY
+    w = inputs.make_hc_weights(s.H, s.C, s.L, 0).to("cuda")
+    raw = torch.empty((0, s.W), dtype=torch.bfloat16, device="cuda")
+    mixed, gates = B.hc_call(raw, w, H=s.H, C=s.C)
+    assert mixed.shape == (0, s.H)
+    B.hc_inject_add(raw, torch.empty((0, s.H), dtype=torch.bfloat16, device="cuda"), gates, H=s.H, C=s.C)
+    torch.cuda.synchronize()
+
+
+def test_inject_add_strided_gates(orc):
+    M, H, C = 3, 64, 4
+    raw = inputs.make_residual(M, H, C, 31)
+    out = inputs.make_sublayer_out(M, H, 31)
+    gates = torch.rand(M * 7, dtype=torch.float32) * 2
+    ref = orc.inject_add(raw, out, gates.double().numpy(), H=H, C=C, gate_stride=7)
+    r = raw.cuda()
+    B.hc_inject_add(r, out.cuda(), gates.cuda(), H=H, C=C, inject_stride=7)
+    torch.cuda.synchronize()
+    check_bf16(r, ref, "strided inject-add")
+
+
+def test_device_status_clean():
+    assert B.device_status() == B.TS_OK
