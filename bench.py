@@ -144,6 +144,21 @@ def _dist():
     return ws, rank, local
 
 
+def aggregate_ranks(local_ms: float, calls_per_rank: int, device="cpu"):
+    """Whole-job throughput of independent replicas: the slowest rank's time
+    (max over ranks) and the calls of all ranks. Returns (max_ms, calls/s)."""
+    import torch
+    import torch.distributed as dist
+
+    world = dist.get_world_size() if dist.is_available() and dist.is_initialized() else 1
+    ms = float(local_ms)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, calls_per_rank * world / (ms / 1e3)
+
+
 def run_reference(args):
     """The fp64 CPU oracle on this host's cores, timed on a bounded sample per step."""
     ws, rank, _ = _dist()
@@ -301,11 +316,7 @@ def run_ours(args):
                 body()
             e1.record(stream)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1)
-        if ws > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms, _ = aggregate_ranks(e0.elapsed_time(e1), n_steps * CALLS_PER_STEP, device=dev)
         return ms
 
     with torch.cuda.stream(stream):

@@ -1,0 +1,580 @@
+// hc_tc.cu -- the batched (M >= 64 tokens) hyper-connection call on the
+// 5th-generation tensor cores: tcgen05.mma with TMEM accumulators, weights
+// streamed by tensor-map TMA in the 128-byte swizzled layout.
+//
+// At M tokens the projections are dense contractions (families/qwen4/hc.rs
+// runs them as GEMVs per token; real_forward.rs batches such GEMVs into M-row
+// GEMMs inside a prefill micro-batch). Three kernels, PDL-chained:
+//
+//  hc_tc_down_kernel   D[128 rows][N tokens] = W[rows][chunk] * X[chunk][tokens]
+//                      with X = raw * g built by producer warps as bf16 hi + lo
+//                      (x = hi + lo to ~16 significant bits; two MMAs per
+//                      K step), so the down projection keeps fp32-level
+//                      accuracy. A cluster of CS CTAs covers one stream; the
+//                      partial tiles meet in distributed shared memory and the
+//                      cluster writes the stream's partial z and the stream's
+//                      per-token sum of squares.
+//  hc_tc_reduce_kernel z = sum_c inv_rms[c] * part[c]; act = silu(z / C) (fp32 and
+//                      bf16 hi/lo for the up GEMM), gates = 2 sigmoid(z / C).
+//  hc_tc_up_kernel     D[C*HBt rows][N] = Wu[rows {c*H + h}][L] * act^T (hi + lo),
+//                      epilogue: w = sigmoid(D), mixed[h] = mean_c w * raw *
+//                      inv_rms * g, with the raw tile staged by TMA.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "hc_tc.h"
+#include "ptx.cuh"
+#include "umma.cuh"
+
+namespace tshc {
+
+namespace {
+
+constexpr int kThreads = 256;  // 8 warps
+constexpr int kTileRows = 128; // UMMA M
+constexpr int kKBlock = 64;    // bf16 elements per 128-byte swizzled row
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+__device__ __forceinline__ void record_timeout(unsigned *status)
+{
+    if (status)
+        atomicExch(status, kStatusTimeout);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+__host__ __device__ constexpr uint32_t tmem_cols(int n)
+{
+    return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : 256u;
+}
+
+struct TcSmem {
+    uint32_t stage_bytes, a_bytes, b_bytes;
+    uint32_t ring, extra, bars, total;
+};
+
+// Down kernel shared memory: ring of stages [A 16 KB | B_hi | B_lo], then the
+// per-token sums of squares, then barriers.
+__host__ __device__ inline TcSmem down_tc_layout(int NT, int ns)
+{
+    TcSmem s;
+    s.a_bytes = kTileRows * 128;
+    s.b_bytes = NT * 128;
+    s.stage_bytes = s.a_bytes + 2 * s.b_bytes;
+    s.ring = 0;
+    s.extra = s.ring + ns * s.stage_bytes;          // ssq_s: NT floats
+    s.bars = s.extra + ((NT * 4 + 127) / 128) * 128;
+    s.total = s.bars + 8 * (3 * ns + 2) + 16;
+    return s;
+}
+
+// Up kernel: ring, then raw tile [C][NT][HBt] bf16 and inv_rms tile [NT][C].
+__host__ __device__ inline TcSmem up_tc_layout(int NT, int ns, int C, int HBt)
+{
+    TcSmem s;
+    s.a_bytes = kTileRows * 128;
+    s.b_bytes = NT * 128;
+    s.stage_bytes = s.a_bytes + 2 * s.b_bytes;
+    s.ring = 0;
+    s.extra = s.ring + ns * s.stage_bytes;
+    const uint32_t raw_bytes = ((C * NT * HBt * 2 + 1023) / 1024) * 1024;
+    const uint32_t inv_bytes = ((NT * C * 4 + 127) / 128) * 128;
+    s.bars = s.extra + raw_bytes + inv_bytes;
+    s.total = s.bars + 8 * (3 * ns + 2) + 16;
+    return s;
+}
+
+// ---------------------------------------------------------------- down
+
+__global__ void __launch_bounds__(kThreads, 1)
+hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_d,
+                  const __grid_constant__ CUtensorMap map_i)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int NT = p.NT, NS = p.n_stages;
+    const TcSmem lay = down_tc_layout(NT, NS);
+    float *ssq_s = reinterpret_cast<float *>(smem + lay.extra);
+    uint64_t *full_a = reinterpret_cast<uint64_t *>(smem + lay.bars);
+    uint64_t *full_b = full_a + NS;
+    uint64_t *empty = full_b + NS;
+    uint64_t *done = empty + NS;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 2);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q = blockIdx.x;                 // chunk within the stream == cluster rank
+    const int c = blockIdx.y / p.RT;          // stream
+    const int rt = blockIdx.y % p.RT;         // row tile
+    const int tile = blockIdx.z;              // token tile
+    const int r0 = rt * kTileRows;
+    const int k0 = c * p.H + q * p.chunk;
+    const int KB = p.chunk / kKBlock;
+    const uint32_t ncols = tmem_cols(NT);
+
+    // Boxes of 32 rows making up this row tile: from W_down, from
+    // block_inject_weight (rows beyond its C are zero-filled), or skipped.
+    int nbox = 0;
+    for (int b = 0; b < 4; ++b) {
+        const int gr = r0 + 32 * b;
+        if (gr + 32 <= p.L || (gr == p.L && p.has_inject)) ++nbox;
+    }
+
+    pdl_launch_dependents();
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full_a[s], 1);
+            mbar_init(&full_b[s], 128);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, ncols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    bool timed_out = false;
+
+    if (warp == 0 && lane == 0) {
+        // TMA producer of the weight tiles (independent of the previous kernel).
+        tma_prefetch_map(&map_d);
+        if (p.has_inject) tma_prefetch_map(&map_i);
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % NS, u = kb / NS;
+            if (u > 0 && !mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
+            uint8_t *a = smem + lay.ring + s * lay.stage_bytes;
+            mbar_arrive_expect_tx(&full_a[s], nbox * 32 * 128);
+            for (int b = 0; b < 4; ++b) {
+                const int gr = r0 + 32 * b;
+                if (gr + 32 <= p.L)
+                    tma_load_2d(a + b * 32 * 128, &map_d, k0 + kb * kKBlock, gr, &full_a[s]);
+                else if (gr == p.L && p.has_inject)
+                    tma_load_2d(a + b * 32 * 128, &map_i, k0 + kb * kKBlock, 0, &full_a[s]);
+            }
+        }
+    }
+    pdl_wait();  // raw is produced by the previous kernel in the stream
+
+    if (warp >= 4) {
+        // Activation producers: thread n builds token n's row of X = raw * g
+        // as bf16 hi + lo in the swizzled K-major layout, and its sum of squares.
+        const int n = tid - 128;
+        const int m = tile * NT + n;
+        const bool live = n < NT && m < p.M;
+        float ssq = 0.f;
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % NS, u = kb / NS;
+            if (u > 0 && !mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
+            uint8_t *bhi = smem + lay.ring + s * lay.stage_bytes + lay.a_bytes;
+            uint8_t *blo = bhi + lay.b_bytes;
+            if (n < NT) {
+                const uint4 *rp = reinterpret_cast<const uint4 *>(p.raw + (size_t)(live ? m : 0) * p.W + k0 + kb * kKBlock);
+                const uint4 *gp = reinterpret_cast<const uint4 *>(p.g + k0 + kb * kKBlock);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
+                    if (live) {
+                        const uint4 rv = rp[j], gv = gp[j];
+                        const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                        uint32_t h[4], l[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float r_a = bf16_lo(rw[e]), r_b = bf16_hi(rw[e]);
+                            ssq = fmaf(r_a, r_a, ssq);
+                            ssq = fmaf(r_b, r_b, ssq);
+                            const float x_a = r_a * bf16_lo(gw[e]), x_b = r_b * bf16_hi(gw[e]);
+                            const float h_a = bf16_round(x_a), h_b = bf16_round(x_b);
+                            h[e] = pack_bf16x2(h_a, h_b);
+                            l[e] = pack_bf16x2(x_a - h_a, x_b - h_b);
+                        }
+                        hi = make_uint4(h[0], h[1], h[2], h[3]);
+                        lo = make_uint4(l[0], l[1], l[2], l[3]);
+                    }
+                    *reinterpret_cast<uint4 *>(bhi + sw128_offset(n, 8 * j)) = hi;
+                    *reinterpret_cast<uint4 *>(blo + sw128_offset(n, 8 * j)) = lo;
+                }
+            }
+            fence_async_shared();
+            mbar_arrive(&full_b[s]);
+        }
+        if (n < NT) ssq_s[n] = ssq;
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer.
+        const uint32_t idesc = umma_idesc_bf16(kTileRows, NT);
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % NS, u = kb / NS;
+            if (!mbar_wait_bounded(&full_a[s], u & 1)) timed_out = true;
+            if (!mbar_wait_bounded(&full_b[s], u & 1)) timed_out = true;
+            tc_fence_after();
+            const uint32_t a = smem_addr(smem + lay.ring + s * lay.stage_bytes);
+            const uint32_t bh = a + lay.a_bytes, bl = bh + lay.b_bytes;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(bh + 32 * k), idesc, (kb | k) != 0);
+                umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(bl + 32 * k), idesc, 1);
+            }
+            umma_commit(&empty[s]);
+        }
+        umma_commit(done);
+    }
+
+    // Epilogue: the 128 x NT fp32 partial tile, TMEM -> shared (over the ring).
+    // The barrier also reconverges the warps whose lane 0 had a producer role.
+    __syncthreads();
+    float *ptile = reinterpret_cast<float *>(smem + lay.ring);
+    const int pstride = NT + 4;
+    if (warp < 4) {
+        if (!mbar_wait_bounded(done, 0)) timed_out = true;
+        tc_fence_after();
+        const int row = warp * 32 + lane;
+        for (int c0 = 0; c0 < NT; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+                *reinterpret_cast<float4 *>(ptile + row * pstride + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+    }
+    if (timed_out) record_timeout(p.status);
+    tc_fence_before();
+    cluster_sync();  // every CTA of the stream has its partial tile and sums of squares in shared memory
+
+    // Rank q sums rows [q*RS, (q+1)*RS) over the cluster, in rank order.
+    const int RS = kTileRows / p.CS;
+    for (int i = tid; i < RS * NT; i += kThreads) {
+        const int r = q * RS + i / NT, n = i % NT;
+        const int gr = r0 + r, m = tile * NT + n;
+        float z = 0.f;
+        for (int pr = 0; pr < p.CS; ++pr)
+            z += dsmem_ld_f32(dsmem_addr(ptile + r * pstride + n, pr));
+        if (gr < p.R && m < p.M)
+            p.part[((size_t)c * p.R + gr) * p.M + m] = z;
+    }
+    if (q == 0 && rt == 0) {
+        for (int n = tid; n < NT; n += kThreads) {
+            const int m = tile * NT + n;
+            float s = 0.f;
+            for (int pr = 0; pr < p.CS; ++pr)
+                s += dsmem_ld_f32(dsmem_addr(ssq_s + n, pr));
+            if (m < p.M)
+                p.ssq[(size_t)c * p.M + m] = s;
+        }
+    }
+    cluster_sync();  // peers have finished reading this CTA's shared memory
+    tc_fence_after();
+    if (warp == 0)
+        tmem_dealloc(tmem, ncols);
+}
+
+// ---------------------------------------------------------------- reduce
+
+__global__ void __launch_bounds__(256) hc_tc_reduce_kernel(const TcReduceParams p)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const long total = (long)p.R * p.M;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+        const int r = (int)(i / p.M), m = (int)(i % p.M);
+        float z = 0.f;
+        for (int c = 0; c < p.C; ++c) {
+            const float inv = 1.0f / sqrtf(p.ssq[(size_t)c * p.M + m] / (float)p.H + p.eps);
+            z = fmaf(inv, p.part[((size_t)c * p.R + r) * p.M + m], z);
+            if (r == 0)
+                p.inv_rms[(size_t)m * p.C + c] = inv;
+        }
+        const float zc = z * p.inv_C;
+        if (r < p.L) {
+            const float a = zc * sigm(zc);
+            const float hi = bf16_round(a);
+            p.act[(size_t)m * p.L + r] = a;
+            p.act_hi[(size_t)m * p.L + r] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+            p.act_lo[(size_t)m * p.L + r] = __bfloat16_as_ushort(__float2bfloat16_rn(a - hi));
+        } else {
+            p.gate[(size_t)m * p.gate_stride + (r - p.L)] = 2.0f * sigm(zc);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- up
+
+__global__ void __launch_bounds__(kThreads, 1)
+hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
+                const __grid_constant__ CUtensorMap map_ahi, const __grid_constant__ CUtensorMap map_alo,
+                const __grid_constant__ CUtensorMap map_raw)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int NT = p.NT, NS = p.n_stages, C = p.C, HBt = p.HBt;
+    const TcSmem lay = up_tc_layout(NT, NS, C, HBt);
+    uint16_t *raw_s = reinterpret_cast<uint16_t *>(smem + lay.extra);  // [C][NT][HBt]
+    float *inv_s = reinterpret_cast<float *>(smem + lay.extra + ((C * NT * HBt * 2 + 1023) / 1024) * 1024);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
+    uint64_t *empty = full + NS;
+    uint64_t *done = empty + NS;
+    uint64_t *raw_bar = done + 1;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(raw_bar + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h0 = blockIdx.x * HBt;
+    const int tile = blockIdx.y;
+    const int KB = p.L / kKBlock;
+    const uint32_t ncols = tmem_cols(NT);
+
+    pdl_launch_dependents();
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        mbar_init(raw_bar, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, ncols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    bool timed_out = false;
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&map_u);
+        // Weights first (independent of the previous kernels) ...
+        const int npre = KB < NS ? KB : NS;
+        for (int kb = 0; kb < npre; ++kb) {
+            uint8_t *a = smem + lay.ring + kb * lay.stage_bytes;
+            mbar_arrive_expect_tx(&full[kb], C * HBt * 128 + 2 * NT * 128);
+            for (int cc = 0; cc < C; ++cc)
+                tma_load_2d(a + cc * HBt * 128, &map_u, kb * kKBlock, cc * p.H + h0, &full[kb]);
+        }
+        pdl_wait();  // ... then the activations and the residual tile
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % NS, u = kb / NS;
+            uint8_t *a = smem + lay.ring + s * lay.stage_bytes;
+            if (kb >= npre) {
+                if (!mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
+                mbar_arrive_expect_tx(&full[s], C * HBt * 128 + 2 * NT * 128);
+                for (int cc = 0; cc < C; ++cc)
+                    tma_load_2d(a + cc * HBt * 128, &map_u, kb * kKBlock, cc * p.H + h0, &full[s]);
+            }
+            tma_load_2d(a + lay.a_bytes, &map_ahi, kb * kKBlock, tile * NT, &full[s]);
+            tma_load_2d(a + lay.a_bytes + lay.b_bytes, &map_alo, kb * kKBlock, tile * NT, &full[s]);
+        }
+        mbar_arrive_expect_tx(raw_bar, C * NT * HBt * 2);
+        for (int cc = 0; cc < C; ++cc)
+            tma_load_2d(raw_s + cc * NT * HBt, &map_raw, cc * p.H + h0, tile * NT, raw_bar);
+    } else {
+        pdl_wait();
+    }
+
+    if (warp == 1 && lane == 0) {
+        const uint32_t idesc = umma_idesc_bf16(kTileRows, NT);
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % NS, u = kb / NS;
+            if (!mbar_wait_bounded(&full[s], u & 1)) timed_out = true;
+            tc_fence_after();
+            const uint32_t a = smem_addr(smem + lay.ring + s * lay.stage_bytes);
+            const uint32_t bh = a + lay.a_bytes, bl = bh + lay.b_bytes;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(bh + 32 * k), idesc, (kb | k) != 0);
+                umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(bl + 32 * k), idesc, 1);
+            }
+            umma_commit(&empty[s]);
+        }
+        umma_commit(done);
+    }
+    if (warp >= 4) {
+        for (int i = tid - 128; i < NT * C; i += 128) {
+            const int n = i / C, cc = i % C, m = tile * NT + n;
+            inv_s[i] = m < p.M ? p.inv_rms[(size_t)m * C + cc] : 0.f;
+        }
+    }
+    __syncthreads();
+
+    // Epilogue: warp w holds rows 32w..32w+31 = (stream, h) pairs.
+    float *mix_s = reinterpret_cast<float *>(smem + lay.ring);  // [C][NT][HBt], over the ring
+    if (warp < 4) {
+        if (!mbar_wait_bounded(done, 0)) timed_out = true;
+        if (!mbar_wait_bounded(raw_bar, 0)) timed_out = true;
+        tc_fence_after();
+        const int row = warp * 32 + lane;
+        const int cc = row / HBt, hl = row % HBt;
+        const bool live = cc < C && h0 + hl < p.H;
+        const float gv = live ? __bfloat162float(__ushort_as_bfloat16(p.g[cc * p.H + h0 + hl])) : 0.f;
+        for (int c0 = 0; c0 < NT; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+            if (live) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int n = c0 + j;
+                    const float rv = __bfloat162float(__ushort_as_bfloat16(raw_s[(cc * NT + n) * HBt + hl]));
+                    mix_s[(cc * NT + n) * HBt + hl] = sigm(v[j]) * (rv * inv_s[n * C + cc] * gv);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    for (int i = tid; i < NT * HBt; i += kThreads) {
+        const int n = i / HBt, hl = i % HBt;
+        const int m = tile * NT + n, h = h0 + hl;
+        if (m < p.M && h < p.H) {
+            float acc = 0.f;
+            for (int cc = 0; cc < C; ++cc)
+                acc += mix_s[(cc * NT + n) * HBt + hl];
+            p.mixed[(size_t)m * p.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(acc * p.inv_C));
+        }
+    }
+    if (timed_out) record_timeout(p.status);
+    tc_fence_after();
+    if (warp == 0)
+        tmem_dealloc(tmem, ncols);
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// A 2-D bf16 tensor map: `rows` x `cols` (row-major), box box_cols x box_rows.
+bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+              uint32_t box_rows, bool swizzle)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_tc(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                      int cluster_x, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    int n = 0;
+    if (cluster_x > 0) {
+        attrs[n].id = cudaLaunchAttributeClusterDimension;
+        attrs[n].val.clusterDim.x = cluster_x;
+        attrs[n].val.clusterDim.y = 1;
+        attrs[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename K>
+cudaError_t allow_smem_tc(K kernel)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    static std::mutex mu;
+    static std::set<std::pair<const void *, int>> done;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_pair(reinterpret_cast<const void *>(kernel), dev);
+    if (done.count(key))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemLimit);
+    if (e == cudaSuccess)
+        done.insert(key);
+    return e;
+}
+
+}  // namespace
+
+size_t tc_down_smem(int NT, int ns) { return down_tc_layout(NT, ns).total + 1024; }
+size_t tc_up_smem(int NT, int ns, int C, int HBt) { return up_tc_layout(NT, ns, C, HBt).total + 1024; }
+
+cudaError_t launch_tc_call(const TcCall &t, cudaStream_t stream)
+{
+    CUtensorMap map_d, map_i, map_u, map_ahi, map_alo, map_raw;
+    const TcDownParams &d = t.down;
+    const TcUpParams &u = t.up;
+    if (!make_map(&map_d, t.wd, d.L, d.W, kKBlock, 32, true) ||
+        !make_map(&map_i, d.has_inject ? t.wi : t.wd, d.has_inject ? d.C : d.L, d.W, kKBlock, 32, true) ||
+        !make_map(&map_u, t.wu, u.W, u.L, kKBlock, u.HBt, true) ||
+        !make_map(&map_ahi, t.red.act_hi, u.M, u.L, kKBlock, u.NT, true) ||
+        !make_map(&map_alo, t.red.act_lo, u.M, u.L, kKBlock, u.NT, true) ||
+        !make_map(&map_raw, u.raw, u.M, u.W, u.HBt, u.NT, false))
+        return cudaErrorInvalidValue;
+
+    cudaError_t e;
+    if ((e = allow_smem_tc(hc_tc_down_kernel)) != cudaSuccess) return e;
+    if ((e = allow_smem_tc(hc_tc_up_kernel)) != cudaSuccess) return e;
+    const int ntiles = (d.M + d.NT - 1) / d.NT;
+    e = launch_tc(hc_tc_down_kernel, dim3(d.CS, d.C * d.RT, ntiles), dim3(kThreads),
+                  tc_down_smem(d.NT, d.n_stages), stream, d.CS, d, map_d, map_i);
+    if (e != cudaSuccess)
+        return e;
+    const long total = (long)t.red.R * t.red.M;
+    const int rblocks = (int)std::max<long>(1, std::min<long>((total + 255) / 256, 4L * 152));
+    e = launch_tc(hc_tc_reduce_kernel, dim3(rblocks), dim3(256), 0, stream, 0, t.red);
+    if (e != cudaSuccess)
+        return e;
+    return launch_tc(hc_tc_up_kernel, dim3((u.H + u.HBt - 1) / u.HBt, ntiles), dim3(kThreads),
+                     tc_up_smem(u.NT, u.n_stages, u.C, u.HBt), stream, 0, u, map_u, map_ahi, map_alo, map_raw);
+}
+
+}  // namespace tshc

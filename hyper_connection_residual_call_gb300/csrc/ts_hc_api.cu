@@ -9,6 +9,7 @@
 #include <string>
 
 #include "hc_kernels.h"
+#include "hc_tc.h"
 #include "ts_hc.h"
 
 namespace {
@@ -137,6 +138,40 @@ tshc::WeightView view(const ts_weight *w)
     return v;
 }
 
+// The batched tensor-core path: M >= kTcMinTokens, lowrank a multiple of 64,
+// and a stream split into CS chunks that are multiples of 64 (largest CS <= 8).
+// Returns CS, or 0 when the shape does not qualify.
+int tc_cluster_size(int M, int H, int C, int L)
+{
+    if (M < tshc::kTcMinTokens || L % 64 != 0 || C > 8)
+        return 0;
+    for (int cs = 8; cs >= 1; cs /= 2)
+        if (H % (64 * cs) == 0)
+            return cs;
+    return 0;
+}
+
+struct WsLayout {
+    size_t inv_rms, act, part, ssq, act_hi, act_lo, total;
+};
+
+WsLayout ws_layout(int M, int H, int C, int L)
+{
+    WsLayout w{};
+    w.inv_rms = 0;
+    w.act = align256(sizeof(float) * (size_t)M * C);
+    w.total = w.act + align256(sizeof(float) * (size_t)M * L);
+    if (tc_cluster_size(M, H, C, L) > 0) {
+        const size_t R = (size_t)L + C;
+        w.part = w.total;
+        w.ssq = w.part + align256(sizeof(float) * (size_t)C * R * M);
+        w.act_hi = w.ssq + align256(sizeof(float) * (size_t)C * M);
+        w.act_lo = w.act_hi + align256(2 * (size_t)M * L);
+        w.total = w.act_lo + align256(2 * (size_t)M * L);
+    }
+    return w;
+}
+
 // Chunks per stream for the split-K down kernel: the largest sps with
 // C * sps <= 8 (one portable cluster) whose chunk H / sps is a multiple of
 // `align` elements.
@@ -191,10 +226,57 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
     if ((st = device_info(&dev)) != TS_OK)
         return st;
 
-    size_t inv_off = 0, act_off = 0;
-    ts_hc_workspace_layout(M, H, C, L, &inv_off, &act_off);
-    float *inv_rms = reinterpret_cast<float *>(static_cast<char *>(workspace) + inv_off);
-    float *act = reinterpret_cast<float *>(static_cast<char *>(workspace) + act_off);
+    const WsLayout wl = ws_layout(M, H, C, L);
+    char *wsb = static_cast<char *>(workspace);
+    float *inv_rms = reinterpret_cast<float *>(wsb + wl.inv_rms);
+    float *act = reinterpret_cast<float *>(wsb + wl.act);
+
+    const int cs = tc_cluster_size(M, H, C, L);
+    const bool all_bf16 = down->type == TS_W_BF16 && up->type == TS_W_BF16 && (!inject || inject->type == TS_W_BF16);
+    if (cs > 0 && all_bf16) {
+        tshc::TcCall t{};
+        const int R = L + (inject ? C : 0);
+        const int NT = M >= 128 ? 128 : (M + 15) / 16 * 16;
+        tshc::TcDownParams &td = t.down;
+        td.raw = static_cast<const uint16_t *>(raw);
+        td.g = static_cast<const uint16_t *>(hc_norm_w);
+        td.part = reinterpret_cast<float *>(wsb + wl.part);
+        td.ssq = reinterpret_cast<float *>(wsb + wl.ssq);
+        td.M = M; td.H = H; td.C = C; td.L = L; td.R = R; td.W = W;
+        td.has_inject = inject ? 1 : 0;
+        td.RT = (R + 127) / 128;
+        td.CS = cs; td.chunk = H / cs;
+        td.NT = NT;
+        td.n_stages = 4;
+        while (td.n_stages > 2 && tshc::tc_down_smem(NT, td.n_stages) > tshc::kTcSmemLimit)
+            --td.n_stages;
+        td.status = dev.status;
+        tshc::TcReduceParams &tr = t.red;
+        tr.part = td.part; tr.ssq = td.ssq; tr.act = act;
+        tr.act_hi = reinterpret_cast<uint16_t *>(wsb + wl.act_hi);
+        tr.act_lo = reinterpret_cast<uint16_t *>(wsb + wl.act_lo);
+        tr.inv_rms = inv_rms;
+        tr.gate = inject ? inject_w : nullptr;
+        tr.gate_stride = inject ? inject_stride : 0;
+        tr.M = M; tr.H = H; tr.C = C; tr.L = L; tr.R = R;
+        tr.eps = eps; tr.inv_C = 1.0f / (float)C;
+        tshc::TcUpParams &tu = t.up;
+        tu.raw = td.raw; tu.g = td.g; tu.inv_rms = inv_rms;
+        tu.mixed = static_cast<uint16_t *>(mixed);
+        tu.M = M; tu.H = H; tu.C = C; tu.L = L; tu.W = W;
+        tu.HBt = (128 / C) / 8 * 8;
+        tu.NT = NT;
+        tu.n_stages = 3;
+        tu.inv_C = tr.inv_C;
+        tu.status = dev.status;
+        t.wd = down->data;
+        t.wi = inject ? inject->data : nullptr;
+        t.wu = up->data;
+        const cudaError_t e = tshc::launch_tc_call(t, stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "launching the tensor-core path");
+        return TS_OK;
+    }
 
     tshc::DownParams d{};
     d.raw = static_cast<const uint16_t *>(raw);
@@ -258,7 +340,7 @@ size_t ts_hc_workspace_bytes(int M, int H, int C, int lowrank)
 {
     if (M < 0 || H < 1 || C < 1 || lowrank < 1)
         return 0;
-    return align256(sizeof(float) * (size_t)M * C) + align256(sizeof(float) * (size_t)M * lowrank);
+    return ws_layout(M, H, C, lowrank).total;
 }
 
 ts_status ts_hc_workspace_layout(int M, int H, int C, int lowrank, size_t *inv_rms_offset,
@@ -266,10 +348,11 @@ ts_status ts_hc_workspace_layout(int M, int H, int C, int lowrank, size_t *inv_r
 {
     if (M < 0 || H < 1 || C < 1 || lowrank < 1)
         return fail(TS_ERR_INVALID_ARG, "invalid shape");
+    const WsLayout w = ws_layout(M, H, C, lowrank);
     if (inv_rms_offset)
-        *inv_rms_offset = 0;
+        *inv_rms_offset = w.inv_rms;
     if (act_offset)
-        *act_offset = align256(sizeof(float) * (size_t)M * C);
+        *act_offset = w.act;
     return TS_OK;
 }
 

@@ -1,0 +1,135 @@
+// umma.cuh -- inline-PTX helpers for the 5th-generation tensor cores (tcgen05)
+// and tensor-map TMA loads on sm_103a: TMEM allocation, shared-memory matrix
+// descriptors, instruction descriptors, MMA issue/commit, TMEM loads.
+//
+// Operand layout used throughout: K-major tiles in the 128-byte swizzled
+// canonical form. A tile row holds 64 bf16 (128 bytes) of one K-block; rows
+// come in atoms of 8 (1024 bytes, 1024-byte aligned); inside an atom the
+// 16-byte chunk j of row r sits at chunk position j ^ (r % 8). This is what a
+// TMA load with CU_TENSOR_MAP_SWIZZLE_128B and a 64-element inner box writes.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace tshc {
+
+// Byte offset of element (row, k) of a 64-wide bf16 K-block tile in the
+// 128-byte swizzled layout (tile base 1024-byte aligned).
+__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t k)
+{
+    return row * 128u + ((((k >> 3) ^ (row & 7u)) & 7u) << 4) + (k & 7u) * 2u;
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms
+// 1024 bytes apart. `saddr` is the shared-window address of the first
+// element used (tile base + 32 bytes per 16-element K step).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);         // start address
+    d |= (uint64_t)1u << 16;                          // leading byte offset (unused for this layout)
+    d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset: next 8-row atom
+    d |= (uint64_t)1u << 46;                          // descriptor version for this architecture
+    d |= (uint64_t)2u << 61;                          // swizzle mode: 128-byte
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B (both K-major), fp32
+// accumulation, tile M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N)
+{
+    return (1u << 4)                        // D format: fp32
+         | (1u << 7)                        // A format: bf16
+         | (1u << 10)                       // B format: bf16
+         | ((uint32_t)(N >> 3) << 17)       // N / 8
+         | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
+// ---- TMEM ------------------------------------------------------------------
+
+// Allocates `ncols` (power of two >= 32) TMEM columns; the address lands in
+// *dst. Executed by one full warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_addr(dst)), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Makes generic-proxy shared-memory writes visible to the tensor cores / TMA.
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// ---- MMA -------------------------------------------------------------------
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one 128 x N x 16 step; single thread.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives once on `bar` when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_addr(bar)) : "memory");
+}
+
+// 32 lanes x 32 bits, 16 consecutive columns: lane i of the warp receives
+// row (lane base + i), columns col .. col+15.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+// ---- tensor-map TMA ----------------------------------------------------------
+
+// 2-D tiled load of box (x = inner coordinate, y = row) into shared memory,
+// completion counted on `bar`. x * 2 bytes must be a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+}  // namespace tshc

@@ -37,7 +37,13 @@ def test_exports_every_declared_symbol(lib):
 
 def test_workspace_size_and_layout(lib):
     assert B.ts_hc_workspace_bytes(1, H, C, L) == 256 + 1280
-    assert B.ts_hc_workspace_bytes(128, H, C, L) == 2048 + 163840
+    # from 64 tokens the tensor-core path adds per-stream partials [C][L+C][M] fp32,
+    # sums of squares [C][M] fp32 and the bf16 hi/lo activations [M][L] x 2
+    a256 = lambda n: (n + 255) // 256 * 256
+    M = 128
+    tc = a256(4 * C * (L + C) * M) + a256(4 * C * M) + 2 * a256(2 * M * L)
+    assert B.ts_hc_workspace_bytes(M, H, C, L) == a256(4 * M * C) + a256(4 * M * L) + tc
+    assert B.ts_hc_workspace_bytes(63, H, C, L) == a256(4 * 63 * C) + a256(4 * 63 * L)
     assert B.ts_hc_workspace_bytes(0, H, C, L) == 0
     assert B.ts_hc_workspace_bytes(-1, H, C, L) == 0
     inv, act = B.ts_hc_workspace_layout(3, H, C, L)

@@ -121,6 +121,25 @@ def test_int4_full_shape(orc, M):
                     group=inputs.INT4_GROUP)
 
 
+@pytest.mark.parametrize("M,H,C,L", [(64, 2560, 4, 320), (100, 2560, 4, 320), (130, 2560, 4, 320),
+                                     (256, 2560, 4, 320), (64, 512, 2, 64), (80, 1024, 8, 128),
+                                     (70, 320, 3, 64), (96, 256, 1, 128)])
+def test_tensor_core_path(orc, M, H, C, L):
+    # M >= 64 with bf16 weights runs on tcgen05 (tiles of up to 128 tokens)
+    call_and_inject(orc, inputs.Shape(M=M, H=H, C=C, L=L), seed=300 + M)
+
+
+def test_tensor_core_mixer(orc):
+    s = inputs.FULL_DECODE
+    M = 128
+    w = inputs.make_hc_weights(s.H, s.C, s.L, 8, with_inject=False)
+    raw = inputs.make_residual(M, s.H, s.C, 8)
+    ref = orc.mixer(raw, w.g, w.down, w.up, H=s.H, C=s.C, L=s.L, eps=EPS)
+    mixed = B.hc_mixer(raw.cuda(), w.to("cuda"), H=s.H, C=s.C, eps=EPS)
+    torch.cuda.synchronize()
+    check_bf16(mixed, ref["mixed"], "tensor-core mixer")
+
+
 def test_mixer(orc):
     s = inputs.FULL_DECODE
     M = 3
