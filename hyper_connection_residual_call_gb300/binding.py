@@ -27,7 +27,8 @@ TS_W_BF16, TS_W_INT4_AFFINE = 0, 1
 RMS_EPS = 1e-6  # families/qwen4/mod.rs, RMS_EPS
 
 EXPORTS = ("ts_hc_workspace_bytes", "ts_hc_workspace_layout", "ts_hc_call", "ts_hc_inject_add",
-           "ts_hc_mixer", "ts_hc_replicate_entry", "ts_hc_last_error", "ts_hc_device_status")
+           "ts_hc_mixer", "ts_hc_inject_call", "ts_hc_replicate_entry", "ts_hc_last_error",
+           "ts_hc_device_status")
 
 
 class HCError(RuntimeError):
@@ -72,6 +73,8 @@ def library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.ts_hc_mixer.restype = i
         lib.ts_hc_inject_add.argtypes = [vp, vp, vp, l, i, i, i, vp]
         lib.ts_hc_inject_add.restype = i
+        lib.ts_hc_inject_call.argtypes = [vp, vp, vp, l, vp, wp, wp, wp, vp, vp, l, i, i, i, i, f, vp, sz, vp]
+        lib.ts_hc_inject_call.restype = i
         lib.ts_hc_replicate_entry.argtypes = [vp, vp, i, i, i, vp]
         lib.ts_hc_replicate_entry.restype = i
         lib.ts_hc_last_error.argtypes = []
@@ -110,6 +113,14 @@ def ts_hc_mixer(raw, hc_norm_w, down, up, mixed, M, H, C, lowrank, eps, workspac
 
 def ts_hc_inject_add(raw, out, inject_w, inject_stride, M, H, C, stream) -> int:
     return library().ts_hc_inject_add(raw, out, inject_w, inject_stride, M, H, C, stream)
+
+
+def ts_hc_inject_call(raw, out, prev_inject_w, prev_inject_stride, hc_norm_w, down, up, inject, mixed,
+                      inject_w, inject_stride, M, H, C, lowrank, eps, workspace, workspace_bytes,
+                      stream) -> int:
+    return library().ts_hc_inject_call(raw, out, prev_inject_w, prev_inject_stride, hc_norm_w, _wref(down),
+                                       _wref(up), _wref(inject), mixed, inject_w, inject_stride, M, H, C,
+                                       lowrank, eps, workspace, workspace_bytes, stream)
 
 
 def ts_hc_replicate_entry(emb, raw, M, H, C, stream) -> int:
@@ -242,6 +253,41 @@ def hc_inject_add(raw, out, inject_w, *, H: int, C: int, inject_stride: Optional
                           C if inject_stride is None else inject_stride, M, H, C, _stream_handle(stream))
     _check(st)
     return raw
+
+
+def hc_inject_call(raw, out, prev_inject_w, weights, *, H: int, C: int, prev_inject_stride: Optional[int] = None,
+                   mixed=None, inject_w=None, inject_stride: Optional[int] = None, eps: float = RMS_EPS,
+                   ws=None, stream=None):
+    """The previous sublayer's inject-add fused into the next call: raw += out * prev gates
+    (in place), then attn_hc / mlp_hc on it -- or the exit mixer when weights.inject is None.
+    Returns (mixed, inject_w); inject_w is None for the mixer."""
+    torch = _torch()
+    M = raw.shape[0]
+    L = weights.down.rows
+    _need(raw, "raw", torch.bfloat16, (M, C * H))
+    _need(out, "out", torch.bfloat16, (M, H))
+    _need(weights.g, "hc_norm_w", torch.bfloat16, (C * H,))
+    if not prev_inject_w.is_cuda or prev_inject_w.dtype != torch.float32:
+        raise HCError(TS_ERR_INVALID_ARG, "prev_inject_w must be a CUDA float32 tensor")
+    if mixed is None:
+        mixed = torch.empty((M, H), dtype=torch.bfloat16, device=raw.device)
+    _need(mixed, "mixed", torch.bfloat16, (M, H))
+    has_inject = weights.inject is not None
+    if has_inject and inject_w is None:
+        inject_stride = C
+        inject_w = torch.empty((max(M, 1), C), dtype=torch.float32, device=raw.device)
+    if has_inject and inject_stride is None:
+        raise HCError(TS_ERR_INVALID_ARG, "inject_stride is required with a caller-given inject_w")
+    if ws is None:
+        ws = workspace(M, H, C, L, raw.device)
+    st = ts_hc_inject_call(raw.data_ptr(), out.data_ptr(), prev_inject_w.data_ptr(),
+                           C if prev_inject_stride is None else prev_inject_stride, weights.g.data_ptr(),
+                           weight_struct(weights.down), weight_struct(weights.up),
+                           weight_struct(weights.inject) if has_inject else None, mixed.data_ptr(),
+                           inject_w.data_ptr() if has_inject else None, inject_stride or 0, M, H, C, L, eps,
+                           ws.data_ptr(), ws.numel() * ws.element_size(), _stream_handle(stream))
+    _check(st)
+    return mixed, (inject_w if has_inject else None)
 
 
 def hc_replicate_entry(emb, *, C: int, raw=None, stream=None):

@@ -108,6 +108,17 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&f)[8])
     f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
 }
 
+// rf[e] <- bf16(out[e] * gate + rf[e]): the inject-add of the previous
+// sublayer, rounded exactly as the stand-alone inject-add kernel rounds it.
+__device__ __forceinline__ void inject_bf16x8(float (&rf)[8], const uint16_t *out, float gate)
+{
+    float of[8];
+    unpack_bf16x8(*reinterpret_cast<const uint4 *>(out), of);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        rf[e] = __bfloat162float(__float2bfloat16_rn(fmaf(of[e], gate, rf[e])));
+}
+
 __device__ __forceinline__ float half_bits_to_float(uint16_t b)
 {
     return __half2float(__ushort_as_half(b));
@@ -260,8 +271,12 @@ __global__ void __launch_bounds__(512) hc_down_kernel(const DownParams p)
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 float rf[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                if (t < mt)
+                if (t < mt) {
                     unpack_bf16x8(*reinterpret_cast<const uint4 *>(p.raw + (size_t)(t0 + t) * p.W + k0 + v * 8), rf);
+                    if (p.inj_out)
+                        inject_bf16x8(rf, p.inj_out + (size_t)(t0 + t) * p.H + k0 % p.H + v * 8,
+                                      p.inj_gate[(size_t)(t0 + t) * p.inj_stride + k0 / p.H]);
+                }
                 float q = 0.f;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) q = fmaf(rf[e], rf[e], q);
@@ -407,14 +422,20 @@ __global__ void __launch_bounds__(768) hc_up_kernel(const UpParams p)
             have_weights = true;
         }
 
-        for (int rr = warp * 4 + team; rr < p.C * hb; rr += nwarps * 4) {
-            const int c = rr / hb, hl = rr % hb;
+        // The loop bound is uniform across the warp (every lane reaches the
+        // full-warp shuffles below); teams past the last row compute nothing.
+        for (int base = warp * 4; base < p.C * hb; base += nwarps * 4) {
+            const int rr = base + team;
+            const bool row_ok = rr < p.C * hb;
+            const int c = row_ok ? rr / hb : 0, hl = row_ok ? rr % hb : 0;
             const int srow = c * HB + hl;
             const uint4 *wrow = reinterpret_cast<const uint4 *>(w_s + srow * row_bytes);
             float acc[MT];
 #pragma unroll
             for (int t = 0; t < MT; ++t) acc[t] = 0.f;
-            if constexpr (WT == 0) {
+            if (!row_ok) {
+                // no row for this team
+            } else if constexpr (WT == 0) {
                 for (int v = tl; v < L / 8; v += 8) {
                     float wf[8];
                     unpack_bf16x8(wrow[v], wf);
@@ -464,7 +485,7 @@ __global__ void __launch_bounds__(768) hc_up_kernel(const UpParams p)
                 v += __shfl_xor_sync(0xffffffffu, v, 4);
                 v += __shfl_xor_sync(0xffffffffu, v, 2);
                 v += __shfl_xor_sync(0xffffffffu, v, 1);
-                if (tl == 0) wv_s[(t * p.C + c) * HB + hl] = sigmoidf_(v);
+                if (tl == 0 && row_ok) wv_s[(t * p.C + c) * HB + hl] = sigmoidf_(v);
             }
         }
         __syncthreads();
@@ -476,7 +497,13 @@ __global__ void __launch_bounds__(768) hc_up_kernel(const UpParams p)
             float acc = 0.f;
             for (int c = 0; c < p.C; ++c) {
                 const int j = c * p.H + h;
-                const float rv = __bfloat162float(__ushort_as_bfloat16(p.raw[m * p.W + j]));
+                float rv = __bfloat162float(__ushort_as_bfloat16(p.raw[m * p.W + j]));
+                if (p.raw_out) {
+                    // fused inject-add: this thread owns element (m, j); write it back
+                    const float ov = __bfloat162float(__ushort_as_bfloat16(p.inj_out[m * p.H + h]));
+                    rv = __bfloat162float(__float2bfloat16_rn(fmaf(ov, p.inj_gate[m * p.inj_stride + c], rv)));
+                    p.raw_out[m * p.W + j] = __bfloat16_as_ushort(__float2bfloat16_rn(rv));
+                }
                 const float gv = __bfloat162float(__ushort_as_bfloat16(p.g[j]));
                 const float nv = rv * p.inv_rms[m * p.C + c] * gv;
                 acc = fmaf(wv_s[(t * p.C + c) * HB + hl], nv, acc);

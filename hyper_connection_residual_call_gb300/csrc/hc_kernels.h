@@ -35,6 +35,11 @@ struct DownParams {
     int mt;                   // tokens per tile (1, 2, 4 or 8)
     float eps, inv_C;
     unsigned *status;
+    // Optional fused inject-add of the previous sublayer: the call sees
+    // raw + out * prev_gate (rounded to bf16) in place of raw. Not written here.
+    const uint16_t *inj_out;  // bf16 [M][H], or nullptr
+    const float *inj_gate;    // token m's previous gates at inj_gate + m * inj_stride
+    long inj_stride;
 };
 
 // Up projection + sigmoid + mean mix: CTA b owns h in [b*HB, b*HB + HB) of
@@ -51,6 +56,12 @@ struct UpParams {
     int mt;                   // tokens per tile (1, 2, 4 or 8)
     float inv_C;
     unsigned *status;
+    // Optional fused inject-add (see DownParams): each CTA owns its h-block of
+    // every stream, recomputes raw + out * prev_gate there and writes it back.
+    uint16_t *raw_out;        // == raw when fused, else nullptr
+    const uint16_t *inj_out;
+    const float *inj_gate;
+    long inj_stride;
 };
 
 struct InjectParams {

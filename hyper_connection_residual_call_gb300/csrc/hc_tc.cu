@@ -148,6 +148,7 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
         mbar_fence_init();
     }
     if (warp == 0) {
+        __syncwarp();
         tmem_alloc(tslot, ncols);
         tmem_relinquish();
     }
@@ -183,6 +184,7 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
         const int n = tid - 128;
         const int m = tile * NT + n;
         const bool live = n < NT && m < p.M;
+        const float inj_g = (live && p.inj_out) ? p.inj_gate[(size_t)m * p.inj_stride + c] : 0.f;
         float ssq = 0.f;
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % NS, u = kb / NS;
@@ -199,10 +201,20 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
                         const uint4 rv = rp[j], gv = gp[j];
                         const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
                         const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                        uint32_t ow[4] = {0u, 0u, 0u, 0u};
+                        if (p.inj_out) {
+                            const uint4 ov = *reinterpret_cast<const uint4 *>(
+                                p.inj_out + (size_t)m * p.H + q * p.chunk + kb * kKBlock + 8 * j);
+                            ow[0] = ov.x; ow[1] = ov.y; ow[2] = ov.z; ow[3] = ov.w;
+                        }
                         uint32_t h[4], l[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float r_a = bf16_lo(rw[e]), r_b = bf16_hi(rw[e]);
+                            float r_a = bf16_lo(rw[e]), r_b = bf16_hi(rw[e]);
+                            if (p.inj_out) {  // fused inject-add, rounded as the inject-add kernel rounds
+                                r_a = bf16_round(fmaf(bf16_lo(ow[e]), inj_g, r_a));
+                                r_b = bf16_round(fmaf(bf16_hi(ow[e]), inj_g, r_b));
+                            }
                             ssq = fmaf(r_a, r_a, ssq);
                             ssq = fmaf(r_b, r_b, ssq);
                             const float x_a = r_a * bf16_lo(gw[e]), x_b = r_b * bf16_hi(gw[e]);
@@ -248,6 +260,7 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
     const int pstride = NT + 4;
     if (warp < 4) {
         if (!mbar_wait_bounded(done, 0)) timed_out = true;
+        __syncwarp();  // the TMEM loads below are .aligned
         tc_fence_after();
         const int row = warp * 32 + lane;
         for (int c0 = 0; c0 < NT; c0 += 16) {
@@ -354,6 +367,7 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         mbar_fence_init();
     }
     if (warp == 0) {
+        __syncwarp();
         tmem_alloc(tslot, ncols);
         tmem_relinquish();
     }
@@ -423,6 +437,7 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
     if (warp < 4) {
         if (!mbar_wait_bounded(done, 0)) timed_out = true;
         if (!mbar_wait_bounded(raw_bar, 0)) timed_out = true;
+        __syncwarp();  // the TMEM loads below are .aligned
         tc_fence_after();
         const int row = warp * 32 + lane;
         const int cc = row / HBt, hl = row % HBt;
@@ -435,7 +450,15 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int n = c0 + j;
-                    const float rv = __bfloat162float(__ushort_as_bfloat16(raw_s[(cc * NT + n) * HBt + hl]));
+                    const int m = tile * NT + n;
+                    float rv = __bfloat162float(__ushort_as_bfloat16(raw_s[(cc * NT + n) * HBt + hl]));
+                    if (p.raw_out && m < p.M) {
+                        // fused inject-add: this thread owns residual element (m, cc, h)
+                        const size_t h = (size_t)h0 + hl;
+                        const float ov = __bfloat162float(__ushort_as_bfloat16(p.inj_out[(size_t)m * p.H + h]));
+                        rv = bf16_round(fmaf(ov, p.inj_gate[(size_t)m * p.inj_stride + cc], rv));
+                        p.raw_out[(size_t)m * p.W + (size_t)cc * p.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(rv));
+                    }
                     mix_s[(cc * NT + n) * HBt + hl] = sigm(v[j]) * (rv * inv_s[n * C + cc] * gv);
                 }
             }
@@ -454,6 +477,7 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         }
     }
     if (timed_out) record_timeout(p.status);
+    __syncwarp();
     tc_fence_after();
     if (warp == 0)
         tmem_dealloc(tmem, ncols);

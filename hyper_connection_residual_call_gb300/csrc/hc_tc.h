@@ -20,6 +20,9 @@ struct TcDownParams {
     int CS, chunk;            // CTAs per stream (cluster size), chunk width (multiple of 64)
     int NT, n_stages;         // tokens per tile (multiple of 16, <= 128), pipeline depth
     unsigned *status;
+    const uint16_t *inj_out;  // fused inject-add of the previous sublayer, or nullptr
+    const float *inj_gate;
+    long inj_stride;
 };
 
 struct TcReduceParams {
@@ -45,6 +48,10 @@ struct TcUpParams {
     int NT, n_stages;
     float inv_C;
     unsigned *status;
+    uint16_t *raw_out;        // == raw when the inject-add is fused, else nullptr
+    const uint16_t *inj_out;
+    const float *inj_gate;
+    long inj_stride;
 };
 
 struct TcCall {

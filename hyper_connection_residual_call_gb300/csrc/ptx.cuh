@@ -112,9 +112,12 @@ __device__ __forceinline__ uint32_t cluster_rank()
     return r;
 }
 
-// Full cluster barrier with release/acquire ordering of shared memory.
+// Full cluster barrier with release/acquire ordering of shared memory. Called
+// by every thread; the warp is reconverged first because the barrier is
+// .aligned.
 __device__ __forceinline__ void cluster_sync()
 {
+    __syncwarp();
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

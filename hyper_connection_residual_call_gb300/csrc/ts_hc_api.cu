@@ -184,11 +184,19 @@ int choose_sps(int H, int C, int align)
     return best;
 }
 
-// The shared part of ts_hc_call and ts_hc_mixer.
+// The previous sublayer's inject-add, fused into a call (ts_hc_inject_call).
+struct FusedInject {
+    const uint16_t *out;
+    const float *gate;
+    long stride;
+    uint16_t *raw;  // the residual, written back by the up kernel
+};
+
+// The shared part of ts_hc_call, ts_hc_mixer and ts_hc_inject_call.
 ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *down,
                        const ts_weight *up, const ts_weight *inject, void *mixed, float *inject_w,
                        long inject_stride, int M, int H, int C, int L, float eps, void *workspace,
-                       size_t workspace_bytes, cudaStream_t stream)
+                       size_t workspace_bytes, cudaStream_t stream, const FusedInject *fi = nullptr)
 {
     ts_status st = check_shape(M, H, C, L);
     if (st != TS_OK)
@@ -251,6 +259,11 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         while (td.n_stages > 2 && tshc::tc_down_smem(NT, td.n_stages) > tshc::kTcSmemLimit)
             --td.n_stages;
         td.status = dev.status;
+        if (fi) {
+            td.inj_out = fi->out;
+            td.inj_gate = fi->gate;
+            td.inj_stride = fi->stride;
+        }
         tshc::TcReduceParams &tr = t.red;
         tr.part = td.part; tr.ssq = td.ssq; tr.act = act;
         tr.act_hi = reinterpret_cast<uint16_t *>(wsb + wl.act_hi);
@@ -269,6 +282,12 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         tu.n_stages = 3;
         tu.inv_C = tr.inv_C;
         tu.status = dev.status;
+        if (fi) {
+            tu.raw_out = fi->raw;
+            tu.inj_out = fi->out;
+            tu.inj_gate = fi->gate;
+            tu.inj_stride = fi->stride;
+        }
         t.wd = down->data;
         t.wi = inject ? inject->data : nullptr;
         t.wu = up->data;
@@ -293,6 +312,11 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
     d.eps = eps;
     d.inv_C = 1.0f / (float)C;
     d.status = dev.status;
+    if (fi) {
+        d.inj_out = fi->out;
+        d.inj_gate = fi->gate;
+        d.inj_stride = fi->stride;
+    }
     const int target_blocks = std::max(1, dev.sm_count / d.S);
     d.rows_per_block = (d.R + target_blocks - 1) / target_blocks;
     d.mt = tshc::gemv_token_tile(M);
@@ -314,6 +338,12 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
     u.HB = (H + dev.sm_count - 1) / dev.sm_count;
     u.inv_C = d.inv_C;
     u.status = dev.status;
+    if (fi) {
+        u.raw_out = fi->raw;
+        u.inj_out = fi->out;
+        u.inj_gate = fi->gate;
+        u.inj_stride = fi->stride;
+    }
     u.mt = tshc::gemv_token_tile(M);
     while (tshc::up_smem_bytes(u, u.mt) > tshc::kSmemBudget && u.mt > 1)
         u.mt /= 2;
@@ -375,6 +405,52 @@ ts_status ts_hc_mixer(const void *raw, const void *hc_norm_w, const ts_weight *d
     g_last_error.clear();
     return hc_call_impl(raw, hc_norm_w, down, up, nullptr, mixed, nullptr, 0, M, H, C, lowrank, eps,
                         workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Whether the strided gate sets {a + m*sa + c} and {b + m*sb + c} (m < M,
+// c < C, in floats) can share an element. Exact for equal strides (two slots
+// of one [M][2][C] buffer are disjoint), conservative otherwise.
+bool gates_overlap(const float *a, long sa, const float *b, long sb, int M, int C)
+{
+    const intptr_t diff = reinterpret_cast<intptr_t>(b) - reinterpret_cast<intptr_t>(a);
+    const long ea = (long)(M - 1) * sa + C, eb = (long)(M - 1) * sb + C;
+    if (diff >= (intptr_t)(4 * ea) || -diff >= (intptr_t)(4 * eb))
+        return false;  // disjoint address ranges
+    if (diff % 4 != 0 || sa != sb)
+        return true;
+    const long r = ((long)(diff / 4) % sa + sa) % sa;
+    return !(r >= C && r <= sa - C);
+}
+
+}  // namespace
+
+extern "C" {
+
+ts_status ts_hc_inject_call(void *raw, const void *out, const float *prev_inject_w, long prev_inject_stride,
+                            const void *hc_norm_w, const ts_weight *down, const ts_weight *up,
+                            const ts_weight *inject, void *mixed, float *inject_w, long inject_stride,
+                            int M, int H, int C, int lowrank, float eps,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    g_last_error.clear();
+    ts_status st = check_shape(M, H, C, lowrank);
+    if (st != TS_OK)
+        return st;
+    if ((st = check_ptr(out, "out", 16)) != TS_OK) return st;
+    if ((st = check_ptr(prev_inject_w, "prev_inject_w", 4)) != TS_OK) return st;
+    if (prev_inject_stride < C)
+        return fail(TS_ERR_INVALID_ARG, "prev_inject_stride = %ld must be >= C = %d", prev_inject_stride, C);
+    if (inject && inject_w && M > 0 && inject_stride >= C &&
+        gates_overlap(prev_inject_w, prev_inject_stride, inject_w, inject_stride, M, C))
+        return fail(TS_ERR_INVALID_ARG, "inject_w shares elements with prev_inject_w");
+    const FusedInject fi{static_cast<const uint16_t *>(out), prev_inject_w, prev_inject_stride,
+                         static_cast<uint16_t *>(raw)};
+    return hc_call_impl(raw, hc_norm_w, down, up, inject, mixed, inject_w, inject_stride, M, H, C, lowrank,
+                        eps, workspace, workspace_bytes, stream, &fi);
 }
 
 ts_status ts_hc_inject_add(void *raw, const void *out, const float *inject_w, long inject_stride,

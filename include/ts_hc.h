@@ -140,6 +140,30 @@ ts_status ts_hc_mixer(const void *raw, const void *hc_norm_w,
                       void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * The previous sublayer's inject-add fused into the next call
+ * (families/qwen4/mod.rs, decoder pseudocode: each `hidden = raw + out * inject_w`
+ * is immediately followed by the next attn_hc / mlp_hc, or by the exit mixer).
+ * Equivalent, bit for bit, to
+ *     ts_hc_inject_add(raw, out, prev_inject_w, prev_inject_stride, ...);
+ *     ts_hc_call(raw, ...)            (or ts_hc_mixer when inject == NULL)
+ * but with one kernel fewer on the dependency chain: the call reads
+ * raw + out * prev_gate directly and writes the updated residual back to raw.
+ *
+ *   raw            bf16 [M][C*H], read and written (in place)
+ *   out            bf16 [M][H], the sublayer output
+ *   prev_inject_w  fp32, token m's previous gates at prev_inject_w + m*prev_inject_stride
+ *   inject         may be NULL: then this is the exit mixer and inject_w is unused
+ *   inject_w       must not share an element with prev_inject_w (two slots of a
+ *                  [M][2][C] micro-batch buffer are fine); refused otherwise
+ * Other arguments as for ts_hc_call.
+ */
+ts_status ts_hc_inject_call(void *raw, const void *out, const float *prev_inject_w, long prev_inject_stride,
+                            const void *hc_norm_w, const ts_weight *down, const ts_weight *up,
+                            const ts_weight *inject, void *mixed, float *inject_w, long inject_stride,
+                            int M, int H, int C, int lowrank, float eps,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Entry replication (families/qwen4/mod.rs, decoder pseudocode, entry line:
  * the embedding row is repeated C times, not padded):
  * raw[m][c*H + h] = emb[m][h] for every stream c.

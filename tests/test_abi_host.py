@@ -127,6 +127,37 @@ def test_replicate_entry_rejects(lib):
     assert B.ts_hc_replicate_entry(FAKE, FAKE, 0, H, C, None) == B.TS_OK
 
 
+def _icall(**kw):
+    a = dict(raw=FAKE, out=FAKE, prev=FAKE, prev_stride=C, g=FAKE, down=_w(), up=_w(), inject=_w(),
+             mixed=FAKE, inject_w=FAKE + 4096, stride=C, M=1, H=H, C=C, L=L, eps=1e-6, ws=FAKE,
+             ws_bytes=1 << 20, stream=None)
+    a.update(kw)
+    return B.ts_hc_inject_call(a["raw"], a["out"], a["prev"], a["prev_stride"], a["g"], a["down"], a["up"],
+                               a["inject"], a["mixed"], a["inject_w"], a["stride"], a["M"], a["H"], a["C"],
+                               a["L"], a["eps"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(out=None), B.TS_ERR_INVALID_ARG, "out is NULL"),
+    (dict(out=FAKE + 8), B.TS_ERR_INVALID_ARG, "out is not 16-byte aligned"),
+    (dict(prev=None), B.TS_ERR_INVALID_ARG, "prev_inject_w is NULL"),
+    (dict(prev_stride=C - 1), B.TS_ERR_INVALID_ARG, "prev_inject_stride"),
+    (dict(inject_w=FAKE), B.TS_ERR_INVALID_ARG, "shares elements"),                      # same slot
+    (dict(inject_w=FAKE + 8, M=3), B.TS_ERR_INVALID_ARG, "shares elements"),             # partial overlap
+    (dict(inject_w=FAKE + 4 * C, prev_stride=2 * C, stride=2 * C, M=5, ws_bytes=16),     # two slots: fine,
+     B.TS_ERR_WORKSPACE, "workspace"),                                                   # fails later on ws
+    (dict(raw=None), B.TS_ERR_INVALID_ARG, "raw is NULL"),
+    (dict(ws_bytes=16), B.TS_ERR_WORKSPACE, "workspace"),
+])
+def test_inject_call_rejects(lib, kw, status, needle):
+    assert _icall(**kw) == status
+    assert needle in B.ts_hc_last_error()
+
+
+def test_inject_call_m0_is_noop(lib):
+    assert _icall(M=0, ws=None, ws_bytes=0) == B.TS_OK
+
+
 def test_device_status_rejects_null(lib):
     assert lib.ts_hc_device_status(None, None) == B.TS_ERR_INVALID_ARG
 

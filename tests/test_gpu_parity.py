@@ -237,6 +237,57 @@ def run_stack_gpu(st, H, C):
     return out, raw
 
 
+def run_stack_gpu_fused(st, H, C):
+    """The same stack with every inject-add fused into the call that follows it."""
+    M = st.emb.shape[0]
+    L = st.final.down.rows
+    raw = B.hc_replicate_entry(st.emb.cuda(), C=C)
+    gates = torch.empty((M * 2 * C,), dtype=torch.float32, device="cuda")
+    mixed = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    ws = B.workspace(M, H, C, L)
+    prev_out, prev_gate = None, None
+    for (attn, mlp), (oa, om) in zip(st.layers, st.outs):
+        for wts, out, slot in ((attn, oa, gates), (mlp, om, gates[C:])):
+            if prev_out is None:
+                B.hc_call(raw, wts, H=H, C=C, mixed=mixed, inject_w=slot, inject_stride=2 * C, ws=ws)
+            else:
+                B.hc_inject_call(raw, prev_out, prev_gate, wts, H=H, C=C, prev_inject_stride=2 * C, mixed=mixed,
+                                 inject_w=slot, inject_stride=2 * C, ws=ws)
+            prev_out, prev_gate = out, slot
+    out, _ = B.hc_inject_call(raw, prev_out, prev_gate, st.final, H=H, C=C, prev_inject_stride=2 * C, ws=ws)
+    torch.cuda.synchronize()
+    return out, raw
+
+
+@pytest.mark.parametrize("M", [1, 3, 128])
+def test_fused_inject_call_is_bit_identical(M):
+    s = inputs.FULL_DECODE
+    H, C, L = s.H, s.C, s.L
+    w1, w2 = inputs.make_hc_weights(H, C, L, 11, 0).to("cuda"), inputs.make_hc_weights(H, C, L, 11, 1).to("cuda")
+    wm = inputs.make_hc_weights(H, C, L, 11, 2, with_inject=False).to("cuda")
+    raw = inputs.make_residual(M, H, C, 11).cuda()
+    o1, o2 = inputs.make_sublayer_out(M, H, 11, 0).cuda(), inputs.make_sublayer_out(M, H, 11, 1).cuda()
+    ra, rb = raw.clone(), raw.clone()
+    ga = torch.full((M * 2 * C,), float("nan"), device="cuda")
+    gb = ga.clone()
+    # separate inject-add
+    B.hc_call(ra, w1, H=H, C=C, inject_w=ga, inject_stride=2 * C)
+    B.hc_inject_add(ra, o1, ga, H=H, C=C, inject_stride=2 * C)
+    ma, _ = B.hc_call(ra, w2, H=H, C=C, inject_w=ga[C:], inject_stride=2 * C)
+    B.hc_inject_add(ra, o2, ga[C:], H=H, C=C, inject_stride=2 * C)
+    xa = B.hc_mixer(ra, wm, H=H, C=C)
+    # fused into the following call
+    B.hc_call(rb, w1, H=H, C=C, inject_w=gb, inject_stride=2 * C)
+    mb, _ = B.hc_inject_call(rb, o1, gb, w2, H=H, C=C, prev_inject_stride=2 * C, inject_w=gb[C:],
+                             inject_stride=2 * C)
+    xb, none = B.hc_inject_call(rb, o2, gb[C:], wm, H=H, C=C, prev_inject_stride=2 * C)
+    torch.cuda.synchronize()
+    assert none is None
+    assert torch.equal(ma, mb) and torch.equal(xa, xb)
+    assert torch.equal(ra, rb)
+    assert torch.equal(ga, gb)
+
+
 @pytest.mark.parametrize("M", [1, 16])
 def test_full_depth_stack(orc, M):
     s = inputs.FULL_DECODE
@@ -248,6 +299,8 @@ def test_full_depth_stack(orc, M):
     mixed, raw = run_stack_gpu(dev, H, C)
     check_bf16(raw, ref["raw"], f"stack residual M={M}")
     check_bf16(mixed, ref["mixed"], f"stack mixer output M={M}")
+    mixed_f, raw_f = run_stack_gpu_fused(dev, H, C)
+    assert torch.equal(raw_f, raw) and torch.equal(mixed_f, mixed), "fused stack differs from the unfused one"
 
 
 def test_replicate_entry():
