@@ -201,6 +201,8 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
     ts_status st = check_shape(M, H, C, L);
     if (st != TS_OK)
         return st;
+    if (M == 0)  // nothing is read or written: pointers are not examined
+        return TS_OK;
     const int W = C * H;
     if ((st = check_ptr(raw, "raw", 16)) != TS_OK) return st;
     if ((st = check_ptr(hc_norm_w, "hc_norm_w", 16)) != TS_OK) return st;
@@ -440,6 +442,8 @@ ts_status ts_hc_inject_call(void *raw, const void *out, const float *prev_inject
     ts_status st = check_shape(M, H, C, lowrank);
     if (st != TS_OK)
         return st;
+    if (M == 0)  // nothing is read or written: pointers are not examined
+        return TS_OK;
     if ((st = check_ptr(out, "out", 16)) != TS_OK) return st;
     if ((st = check_ptr(prev_inject_w, "prev_inject_w", 4)) != TS_OK) return st;
     if (prev_inject_stride < C)
@@ -463,6 +467,8 @@ ts_status ts_hc_inject_add(void *raw, const void *out, const float *inject_w, lo
         return fail(TS_ERR_INVALID_ARG, "H = %d must be a multiple of 8 in [8, %d]", H, kMaxH);
     if (C < 1 || C > kMaxC)
         return fail(TS_ERR_INVALID_ARG, "C = %d must be in [1, %d]", C, kMaxC);
+    if (M == 0)  // nothing is read or written: pointers are not examined
+        return TS_OK;
     ts_status st;
     if ((st = check_ptr(raw, "raw", 16)) != TS_OK) return st;
     if ((st = check_ptr(out, "out", 16)) != TS_OK) return st;
@@ -495,6 +501,8 @@ ts_status ts_hc_replicate_entry(const void *emb, void *raw, int M, int H, int C,
         return fail(TS_ERR_INVALID_ARG, "H = %d must be a multiple of 8 in [8, %d]", H, kMaxH);
     if (C < 1 || C > kMaxC)
         return fail(TS_ERR_INVALID_ARG, "C = %d must be in [1, %d]", C, kMaxC);
+    if (M == 0)  // nothing is read or written: pointers are not examined
+        return TS_OK;
     ts_status st;
     if ((st = check_ptr(emb, "emb", 16)) != TS_OK) return st;
     if ((st = check_ptr(raw, "raw", 16)) != TS_OK) return st;

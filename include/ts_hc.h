@@ -22,6 +22,8 @@
  *     elements [c*H, (c+1)*H). Linear weights are [out][in] with no bias.
  *   - bf16 tensors are 16-byte aligned; H is a multiple of 8, hc_lowrank (L)
  *     a multiple of 8 (32 for INT4 weights); 1 <= C <= 8; 8 <= L <= 1024.
+ *   - M == 0 (no tokens) is a no-op for every entry point: once the shape
+ *     arguments are valid it returns TS_OK without examining any pointer.
  *   - Arguments are validated on the host before anything is launched; a bad
  *     argument returns an error status without launching, and
  *     ts_hc_last_error() names it. Launch failures return TS_ERR_CUDA.

@@ -307,15 +307,21 @@ class Oracle:
         ``round_residual``: the residual is a bf16 tensor between calls, so it
         is rounded to bf16 (ties to even) after every inject-add, as stored.
         Each call itself is exact in fp64.
+
+        Also returns ``peak``: per element, the largest |raw| the residual held
+        at entry or after any inject-add (a bf16 rounding decision taken at
+        that magnitude moves the element by one ulp of it).
         """
         raw = self.replicate_entry(emb, H=H, C=C)
+        peak = np.abs(raw)
         for (attn, mlp), (o_attn, o_mlp) in zip(layers, outs):
             r = self.prefill_pair(raw, attn, o_attn, mlp, o_mlp, H=H, C=C, L=L, eps=eps,
                                   round_residual=round_residual, threads=threads)
+            peak = np.maximum(peak, np.maximum(np.abs(r["raw_after_attn"]), np.abs(r["raw_after_mlp"])))
             raw = r["raw_after_mlp"]
         fin = self.mixer(raw, final.g, final.down, final.up, H=H, C=C, L=L, eps=eps,
                          threads=threads)
-        return {"mixed": fin["mixed"], "raw": raw}
+        return {"mixed": fin["mixed"], "raw": raw, "peak": peak}
 
 
 _lock = threading.Lock()
