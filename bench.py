@@ -1,16 +1,21 @@
 """Benchmark of the hyper-connection call on GB300.
 
 Workload (one GPU): the full-shape decode call, M=1 token, H=2560, C=4
-(wide 10240), hc_lowrank=320, bf16 weights: one attn_hc-style call
-(ts_hc_call) followed by its inject-add (ts_hc_inject_add), each call
-depending on the previous one through the residual, as in a decoder stack.
+(wide 10240), hc_lowrank=320, bf16 weights: one attn_hc-style call and its
+inject-add, each call depending on the previous one through the residual, as
+in a decoder stack.
 
 One step = one replay of a CUDA graph that holds CALLS_PER_STEP dependent
-(call + inject-add) pairs cycling through WEIGHT_SETS distinct seeded weight
-sets (634 MB per pass, far larger than the 129 MB L2, so every call streams
-its weights from HBM). Inputs are resident in HBM when the timed region
-starts; ``e2e`` repeats the measurement with the step's inputs copied from
-pinned host memory and its results read back inside the timed region.
+calls, each with its inject-add, cycling through WEIGHT_SETS distinct seeded
+weight sets (634 MB per pass, far larger than the 129 MB L2, so every call
+streams its weights from HBM). Two sequences of the same work are timed:
+  * fused (the headline): ts_hc_call, then ts_hc_inject_call for every later
+    call (the previous inject-add folded into the call), then one final
+    ts_hc_inject_add;
+  * separate: ts_hc_call + ts_hc_inject_add for every call.
+Inputs are resident in HBM when the timed region starts; ``e2e`` repeats the
+headline with the step's inputs copied from pinned host memory and its
+results read back inside the timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -45,7 +50,6 @@ CONFIG_SEED = 1  # the full-shape decode workload's seed
 BYTES_PER_CALL = (2 * L * C * H + 2 * C * H * L + 2 * C * C * H + 2 * C * H + 2 * M * C * H
                   + 2 * M * H + 4 * M * C) + (2 * 2 * M * C * H + 2 * M * H + 4 * M * C)
 assert BYTES_PER_CALL == 13_281_312
-KERNELS_PER_CALL = 3  # down, up (ts_hc_call) + inject-add
 
 
 def _peaks():
@@ -159,6 +163,17 @@ def aggregate_ranks(local_ms: float, calls_per_rank: int, device="cpu"):
     return ms, calls_per_rank * world / (ms / 1e3)
 
 
+def _config():
+    return {"workload": "full-shape decode hyper-connection call + inject-add: M=1, H=2560, C=4 "
+                        "(wide 10240), hc_lowrank=320, bf16 weights",
+            "M": M, "H": H, "C": C, "hc_lowrank": L, "calls_per_step": CALLS_PER_STEP,
+            "weight_sets": WEIGHT_SETS,
+            "sequence": "ts_hc_call, then ts_hc_inject_call (previous inject-add fused) for each later "
+                        "call, then a final ts_hc_inject_add",
+            "l2": "inputs larger than L2: 48 distinct weight sets, 634 MB per pass, cycled",
+            "parallelism": "replicas"}
+
+
 def run_reference(args):
     """The fp64 CPU oracle on this host's cores, timed on a bounded sample per step."""
     ws, rank, _ = _dist()
@@ -172,7 +187,6 @@ def run_reference(args):
     w = inputs.make_hc_weights(H, C, L, CONFIG_SEED)
     raw = inputs.make_residual(M, H, C, CONFIG_SEED)
     out = inputs.make_sublayer_out(M, H, CONFIG_SEED)
-    calls_per_step = 1
 
     def step(r):
         res = orc.hc_call(r, w.g, w.down, w.up, w.inject, H=H, C=C, L=L, threads=threads)
@@ -185,7 +199,7 @@ def run_reference(args):
     for _ in range(args.steps):
         r = step(r)
     dt = time.perf_counter() - t0
-    value = args.steps * calls_per_step / dt
+    value = args.steps / dt
     sample = f"{args.steps} x 1 full-shape call + inject-add (M=1, H=2560, C=4, L=320), fp64 oracle"
     line = {
         "metric": METRIC, "value": value, "unit": "calls/s", "impl": "reference", "n_gpus": ws,
@@ -197,15 +211,6 @@ def run_reference(args):
         "e2e": {"value": value, "unit": "calls/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
-
-
-def _config():
-    return {"workload": "full-shape decode hyper-connection call + inject-add: M=1, H=2560, C=4 "
-                        "(wide 10240), hc_lowrank=320, bf16 weights",
-            "M": M, "H": H, "C": C, "hc_lowrank": L, "calls_per_step": CALLS_PER_STEP,
-            "weight_sets": WEIGHT_SETS,
-            "l2": "inputs larger than L2: 48 distinct weight sets, 634 MB per pass, cycled",
-            "parallelism": "replicas"}
 
 
 def cpu_baseline(budget_s: float = 12.0):
@@ -229,7 +234,7 @@ def cpu_baseline(budget_s: float = 12.0):
                       f"fp64 oracle, OpenMP over output rows"}
 
 
-def parity_check(B, inputs, w0_d, w0, raw0, out0):
+def parity_check(B, w0_d, w0, raw0, out0):
     """The full-shape call on weight set 0 against the oracle, before timing."""
     import numpy as np
     import torch
@@ -251,8 +256,7 @@ def parity_check(B, inputs, w0_d, w0, raw0, out0):
     res = {"mixed": worst(mixed, ref["mixed"], 1e-2, 1e-2),
            "raw": worst(raw_d, ref_raw, 1e-2, 1e-2),
            "gate": worst(gates, ref["gate"], 1e-5 * rms, 1e-3)}
-    ok = all(v <= 1.0 for v in res.values())
-    if not ok:
+    if not all(v <= 1.0 for v in res.values()):
         raise SystemExit(f"parity check failed before timing: {res}")
     return {"checked": "full-shape call + inject-add vs fp64 oracle", "worst_err_over_limit": max(res.values())}
 
@@ -279,30 +283,46 @@ def run_ours(args):
     raw_h = inputs.make_residual(M, H, C, CONFIG_SEED)
     sets = [w.to(dev) for w in sets_h]
     outs = torch.stack([o.to(dev) for o in outs_h])          # [sets, M, H]
-    raw0 = raw_h.to(dev)
 
-    parity = parity_check(B, inputs, sets[0], sets_h[0], raw_h, outs_h[0]) if rank == 0 else None
+    parity = parity_check(B, sets[0], sets_h[0], raw_h, outs_h[0]) if rank == 0 else None
 
-    raw = raw0.clone()
+    raw = raw_h.to(dev)
     mixed = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
-    gates = torch.empty((M, C), dtype=torch.float32, device=dev)
+    gates = torch.empty((2, M, C), dtype=torch.float32, device=dev)  # two slots, alternating
     wsp = B.workspace(M, H, C, L, dev)
 
-    def one_step():
+    def separate_step():
         for i in range(CALLS_PER_STEP):
             k = i % WEIGHT_SETS
-            B.hc_call(raw, sets[k], H=H, C=C, mixed=mixed, inject_w=gates, inject_stride=C, ws=wsp)
-            B.hc_inject_add(raw, outs[k], gates, H=H, C=C)
+            B.hc_call(raw, sets[k], H=H, C=C, mixed=mixed, inject_w=gates[0], inject_stride=C, ws=wsp)
+            B.hc_inject_add(raw, outs[k], gates[0], H=H, C=C)
+
+    def fused_step():
+        for i in range(CALLS_PER_STEP):
+            k = i % WEIGHT_SETS
+            slot = gates[i % 2]
+            if i == 0:
+                B.hc_call(raw, sets[k], H=H, C=C, mixed=mixed, inject_w=slot, inject_stride=C, ws=wsp)
+            else:
+                kp = (i - 1) % WEIGHT_SETS
+                B.hc_inject_call(raw, outs[kp], gates[(i - 1) % 2], sets[k], H=H, C=C, prev_inject_stride=C,
+                                 mixed=mixed, inject_w=slot, inject_stride=C, ws=wsp)
+        last = CALLS_PER_STEP - 1
+        B.hc_inject_add(raw, outs[last % WEIGHT_SETS], gates[last % 2], H=H, C=C)
 
     stream = torch.cuda.Stream(device=dev)
+    graphs = {}
+    for name, body in (("fused", fused_step), ("separate", separate_step)):
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            body()  # eager warm-up (also initialises the library's per-device state)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            body()
+        graphs[name] = g
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        one_step()  # eager warm-up (also initialises the library's per-device state)
-    stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        one_step()
-    torch.cuda.synchronize()
+    launches_per_step = {"fused": 2 * CALLS_PER_STEP + 1, "separate": 3 * CALLS_PER_STEP}
 
     def timed(n_steps, body):
         if ws > 1:
@@ -319,15 +339,17 @@ def run_ours(args):
         ms, _ = aggregate_ranks(e0.elapsed_time(e1), n_steps * CALLS_PER_STEP, device=dev)
         return ms
 
-    with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 3)):
-            graph.replay()
+    for g in graphs.values():
+        with torch.cuda.stream(stream):
+            for _ in range(max(args.warmup, 3)):
+                g.replay()
     torch.cuda.synchronize()
 
+    ms_sep = timed(args.steps, graphs["separate"].replay)
     sampler = ClockSampler(local)
     sampler.start()
     t0 = time.time()
-    ms = timed(args.steps, graph.replay)
+    ms = timed(args.steps, graphs["fused"].replay)
     t1 = time.time()
     clocks = sampler.stop(t0, t1)
 
@@ -341,7 +363,7 @@ def run_ours(args):
     def e2e_step():
         raw.copy_(raw_pin, non_blocking=True)
         outs.copy_(outs_pin, non_blocking=True)
-        graph.replay()
+        graphs["fused"].replay()
         mixed_pin.copy_(mixed, non_blocking=True)
         res_pin.copy_(raw, non_blocking=True)
 
@@ -353,10 +375,10 @@ def run_ours(args):
     h2d = raw_pin.numel() * 2 + outs_pin.numel() * 2
     d2h = mixed_pin.numel() * 2 + res_pin.numel() * 2
 
-    calls = args.steps * CALLS_PER_STEP * ws
-    value = calls / (ms / 1e3)
-    per_call_s = (ms / 1e3) / (args.steps * CALLS_PER_STEP)
-    achieved = BYTES_PER_CALL / per_call_s / 1e9
+    n_calls = args.steps * CALLS_PER_STEP
+    value = n_calls * ws / (ms / 1e3)
+    achieved = BYTES_PER_CALL / ((ms / 1e3) / n_calls) / 1e9
+    achieved_sep = BYTES_PER_CALL / ((ms_sep / 1e3) / n_calls) / 1e9
     peak, peak_kind = _peaks()
     e2e_value = e2e_steps * CALLS_PER_STEP * ws / (ms_e2e / 1e3)
 
@@ -369,15 +391,20 @@ def run_ours(args):
             "config": _config(),
             "tokens_per_s": value * M,
             "hbm_gbs": achieved,
+            "us_per_call": 1e3 * ms / n_calls,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": _recorded_traffic(),
-                         "kernel": "one hyper-connection call (down + up kernels, PDL-overlapped) "
-                                   "+ its inject-add; 13,281,312 algorithmic bytes per call",
-                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                         "kernel": "one hyper-connection call with its inject-add (down + up kernels, "
+                                   "PDL-overlapped); 13,281,312 algorithmic bytes per call",
+                         "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s"},
+            "separate_inject": {"value": n_calls * ws / (ms_sep / 1e3), "unit": "calls/s",
+                                "us_per_call": 1e3 * ms_sep / n_calls, "hbm_gbs": achieved_sep,
+                                "frac": achieved_sep / peak,
+                                "sequence": "ts_hc_call + ts_hc_inject_add per call"},
             "e2e": {"value": e2e_value, "unit": "calls/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": KERNELS_PER_CALL * CALLS_PER_STEP * args.steps,
+            "gpu_launches": launches_per_step["fused"] * args.steps,
             "clocks": clocks,
             "cpu_baseline": base,
             "parity": parity,
