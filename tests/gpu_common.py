@@ -69,12 +69,20 @@ def check_bf16_carried(gpu, ref, peak, what: str) -> float:
     return worst
 
 
-def check_fp32(gpu, ref, what: str) -> float:
+# A call whose input residual came out of an earlier bf16-rounded inject-add
+# sees, on the two sides, residuals that differ by legitimate rounding flips
+# (one ulp in a few elements). Its fp32 intermediates then get a floor of
+# 1e-3 of the vector's RMS: perturbing the oracle's own gates by 2^-22
+# (163 flips in 1.3M elements) moves near-zero act values by up to 1.8e-4 RMS.
+CHAINED_RMS_FLOOR = 1e-3
+
+
+def check_fp32(gpu, ref, what: str, floor: float = FP32_RMS_FLOOR) -> float:
     g = to_np(gpu).reshape(np.shape(ref))
     ref = np.asarray(ref, dtype=np.float64)
     assert np.all(np.isfinite(g)), f"{what}: non-finite values"
     rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
-    lim = FP32_RTOL * np.abs(ref) + FP32_RMS_FLOOR * rms
+    lim = FP32_RTOL * np.abs(ref) + floor * rms
     ratio = np.abs(g - ref) / np.maximum(lim, 1e-300)
     worst = float(ratio.max()) if ratio.size else 0.0
     assert worst <= 1.0, f"{what}: worst |err|/limit = {worst:.3g} at {np.unravel_index(ratio.argmax(), ratio.shape)}"
