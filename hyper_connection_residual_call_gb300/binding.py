@@ -28,7 +28,8 @@ RMS_EPS = 1e-6  # families/qwen4/mod.rs, RMS_EPS
 
 EXPORTS = ("ts_hc_workspace_bytes", "ts_hc_workspace_layout", "ts_hc_call", "ts_hc_inject_add",
            "ts_hc_mixer", "ts_hc_inject_call", "ts_hc_replicate_entry", "ts_hc_last_error",
-           "ts_hc_device_status")
+           "ts_hc_device_status", "ts_hc_call_noalloc")
+TS_HC_STATIC_SCRATCH_BYTES = 4 * 1024 * 1024  # include/ts_hc.h
 
 
 class HCError(RuntimeError):
@@ -75,6 +76,8 @@ def library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.ts_hc_inject_add.restype = i
         lib.ts_hc_inject_call.argtypes = [vp, vp, vp, l, vp, wp, wp, wp, vp, vp, l, i, i, i, i, f, vp, sz, vp]
         lib.ts_hc_inject_call.restype = i
+        lib.ts_hc_call_noalloc.argtypes = [vp, vp, wp, wp, wp, vp, vp, l, i, i, i, i, f, vp]
+        lib.ts_hc_call_noalloc.restype = i
         lib.ts_hc_replicate_entry.argtypes = [vp, vp, i, i, i, vp]
         lib.ts_hc_replicate_entry.restype = i
         lib.ts_hc_last_error.argtypes = []
@@ -121,6 +124,14 @@ def ts_hc_inject_call(raw, out, prev_inject_w, prev_inject_stride, hc_norm_w, do
     return library().ts_hc_inject_call(raw, out, prev_inject_w, prev_inject_stride, hc_norm_w, _wref(down),
                                        _wref(up), _wref(inject), mixed, inject_w, inject_stride, M, H, C,
                                        lowrank, eps, workspace, workspace_bytes, stream)
+
+
+def ts_hc_call_noalloc(raw, hc_norm_w, down, up, inject, mixed, inject_w, inject_stride, M, H, C, lowrank,
+                       eps, stream) -> int:
+    """ts_hc_call with its scratch in the library's own device array (no workspace argument),
+    for callers that cannot allocate device memory."""
+    return library().ts_hc_call_noalloc(raw, hc_norm_w, _wref(down), _wref(up), _wref(inject), mixed,
+                                        inject_w, inject_stride, M, H, C, lowrank, eps, stream)
 
 
 def ts_hc_replicate_entry(emb, raw, M, H, C, stream) -> int:

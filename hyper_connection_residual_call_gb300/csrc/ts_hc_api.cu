@@ -538,3 +538,65 @@ ts_status ts_hc_device_status(cudaStream_t stream, int *status)
 }
 
 }  // extern "C"
+
+// ---- ts_hc_call_noalloc: the workspace in a file-scope device array ---------
+
+// Scratch for callers that cannot allocate. Host code only ever sees a
+// host-side stand-in for this name; the device address is looked up per
+// device with cudaGetSymbolAddress and passed to the kernels.
+static __device__ __align__(256) unsigned char g_hc_static_scratch[TS_HC_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_static_mutex;
+void *g_static_scratch[kMaxDevices];
+
+// Device address of the array on the current device, looked up on the first
+// call there (with that device current).
+ts_status static_scratch(void **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(TS_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (!g_static_scratch[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_hc_static_scratch);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        g_static_scratch[dev] = p;
+    }
+    *out = g_static_scratch[dev];
+    return TS_OK;
+}
+
+}  // namespace
+
+extern "C" ts_status ts_hc_call_noalloc(const void *raw, const void *hc_norm_w, const ts_weight *down,
+                                        const ts_weight *up, const ts_weight *inject, void *mixed,
+                                        float *inject_w, long inject_stride, int M, int H, int C,
+                                        int lowrank, float eps, cudaStream_t stream)
+{
+    g_last_error.clear();
+    if (!inject)
+        return fail(TS_ERR_INVALID_ARG, "inject is NULL (the no-allocation variant covers ts_hc_call)");
+    ts_status st = check_shape(M, H, C, lowrank);
+    if (st != TS_OK)
+        return st;
+    if (M == 0)
+        return TS_OK;
+    const size_t need = ts_hc_workspace_bytes(M, H, C, lowrank);
+    if (need > TS_HC_STATIC_SCRATCH_BYTES)
+        return fail(TS_ERR_WORKSPACE,
+                    "M = %d tokens need %zu bytes of scratch; the static scratch holds %u bytes "
+                    "(call ts_hc_call with a workspace, or split the tokens)",
+                    M, need, (unsigned)TS_HC_STATIC_SCRATCH_BYTES);
+    void *ws = nullptr;
+    if ((st = static_scratch(&ws)) != TS_OK)
+        return st;
+    return hc_call_impl(raw, hc_norm_w, down, up, inject, mixed, inject_w, inject_stride, M, H, C, lowrank,
+                        eps, ws, TS_HC_STATIC_SCRATCH_BYTES, stream);
+}

@@ -142,6 +142,38 @@ ts_status ts_hc_mixer(const void *raw, const void *hc_norm_w,
                       void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * ts_hc_call for callers that cannot allocate device memory. The pages have
+ * no counterpart to this entry point; it exists for this library's users.
+ *
+ * Some callers cannot call cudaMalloc (or any allocator) at the point where
+ * they run the call: code that runs while a stream is being captured with a
+ * capture mode that forbids allocation, real-time loops that must not hit the
+ * implicit synchronisation an allocation can cause, and hosts that hand this
+ * library a fixed memory budget and no allocator. They pass inputs and outputs
+ * as for ts_hc_call but no workspace: the scratch lives in a file-scope device
+ * array of TS_HC_STATIC_SCRATCH_BYTES that every GPU which loads this library
+ * holds until the process exits.
+ *
+ *   - Shapes whose ts_hc_workspace_bytes() exceeds TS_HC_STATIC_SCRATCH_BYTES
+ *     are refused with TS_ERR_WORKSPACE before anything is launched (at the
+ *     full shape H=2560, C=4, lowrank=320 that allows up to 539 tokens).
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind. Nothing in it needs to start at zero: each call writes every
+ *     scratch byte it reads. Calls that can overlap on the GPU (other streams,
+ *     other threads) race on it; serialise them.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *
+ * Arguments and results as for ts_hc_call, without workspace/workspace_bytes.
+ */
+#define TS_HC_STATIC_SCRATCH_BYTES (4u * 1024u * 1024u)
+ts_status ts_hc_call_noalloc(const void *raw, const void *hc_norm_w,
+                             const ts_weight *down, const ts_weight *up, const ts_weight *inject,
+                             void *mixed, float *inject_w, long inject_stride,
+                             int M, int H, int C, int lowrank, float eps, cudaStream_t stream);
+
+/*
  * The previous sublayer's inject-add fused into the next call
  * (families/qwen4/mod.rs, decoder pseudocode: each `hidden = raw + out * inject_w`
  * is immediately followed by the next attn_hc / mlp_hc, or by the exit mixer).
