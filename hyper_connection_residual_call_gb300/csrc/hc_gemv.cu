@@ -38,6 +38,8 @@ namespace tshc {
 
 namespace {
 
+constexpr int kMaxCluster = 8;  // CTAs per split-K cluster (portable maximum)
+
 // Elements per 16-byte vector of weight storage: 8 bf16 or 32 INT4 codes.
 template <int WT> struct Vec;
 template <> struct Vec<0> { static constexpr int kElems = 8; };
@@ -81,9 +83,12 @@ __host__ __device__ inline DownSmem down_layout(const DownParams &p, int mt)
 }
 
 struct UpSmem {
-    size_t bar, w, sb, act, wv, total;
+    size_t bar, w, sb, act, wv, rv, gv, inv, invq, total;
 };
 
+// Up kernel shared memory: weight rows, INT4 scales/biases, act tile, sigmoid
+// outputs, and the mix operands staged right after the dependency wait:
+// residual values rv [mt][C][HB], norm scale gv [C][HB], inv_rms [mt][C].
 __host__ __device__ inline UpSmem up_layout(const UpParams &p, int mt)
 {
     const size_t row = p.up.type == 0 ? (size_t)p.L * 2 : (size_t)p.L / 2;
@@ -94,7 +99,11 @@ __host__ __device__ inline UpSmem up_layout(const UpParams &p, int mt)
     s.sb = round_up_sz(s.w + row * p.C * p.HB, 128);
     s.act = round_up_sz(s.sb + sizeof(float) * 2 * (size_t)ng * p.C * p.HB, 128);
     s.wv = round_up_sz(s.act + sizeof(float) * (size_t)mt * p.L, 128);
-    s.total = round_up_sz(s.wv + sizeof(float) * (size_t)mt * p.C * p.HB, 128);
+    s.rv = round_up_sz(s.wv + sizeof(float) * (size_t)mt * p.C * p.HB, 128);
+    s.gv = round_up_sz(s.rv + sizeof(float) * (size_t)mt * p.C * p.HB, 128);
+    s.inv = round_up_sz(s.gv + sizeof(float) * (size_t)p.C * p.HB, 128);
+    s.invq = round_up_sz(s.inv + sizeof(float) * (size_t)mt * p.C, 128);
+    s.total = round_up_sz(s.invq + sizeof(float) * kMaxCluster, 128);
     return s;
 }
 
@@ -144,6 +153,12 @@ template <int MT>
 __device__ __forceinline__ void row_dot_bf16(const uint4 *wrow, int nvec, const float *x, int xstride,
                                              int lane, float (&acc)[MT])
 {
+    // Two accumulation chains per token (even / odd elements) halve the
+    // dependent-FMA depth; they are added once at the end.
+    float a0[MT], a1[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) { a0[t] = 0.f; a1[t] = 0.f; }
+#pragma unroll 2
     for (int v = lane; v < nvec; v += 32) {
         float wf[8];
         unpack_bf16x8(wrow[v], wf);
@@ -152,14 +167,14 @@ __device__ __forceinline__ void row_dot_bf16(const uint4 *wrow, int nvec, const 
         for (int t = 0; t < MT; ++t) {
             const float4 xa = *reinterpret_cast<const float4 *>(x + t * xstride + p0);
             const float4 xb = *reinterpret_cast<const float4 *>(x + t * xstride + p0 + 128);
-            float a = acc[t];
-            a = fmaf(wf[0], xa.x, a); a = fmaf(wf[1], xa.y, a);
-            a = fmaf(wf[2], xa.z, a); a = fmaf(wf[3], xa.w, a);
-            a = fmaf(wf[4], xb.x, a); a = fmaf(wf[5], xb.y, a);
-            a = fmaf(wf[6], xb.z, a); a = fmaf(wf[7], xb.w, a);
-            acc[t] = a;
+            a0[t] = fmaf(wf[0], xa.x, a0[t]); a1[t] = fmaf(wf[1], xa.y, a1[t]);
+            a0[t] = fmaf(wf[2], xa.z, a0[t]); a1[t] = fmaf(wf[3], xa.w, a1[t]);
+            a0[t] = fmaf(wf[4], xb.x, a0[t]); a1[t] = fmaf(wf[5], xb.y, a1[t]);
+            a0[t] = fmaf(wf[6], xb.z, a0[t]); a1[t] = fmaf(wf[7], xb.w, a1[t]);
         }
     }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) acc[t] += a0[t] + a1[t];
 }
 
 // INT4-affine: lane handles vectors of 32 codes (one group-aligned run of 32
@@ -168,6 +183,9 @@ template <int MT>
 __device__ __forceinline__ void row_dot_int4(const uint4 *wrow, int nvec, const float *sb, int group,
                                              const float *x, int xstride, int lane, float (&acc)[MT])
 {
+    float a0[MT], a1[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) { a0[t] = 0.f; a1[t] = 0.f; }
     for (int v = lane; v < nvec; v += 32) {
         const uint4 q = wrow[v];
         const int gi = (v * 32) / group;
@@ -185,15 +203,15 @@ __device__ __forceinline__ void row_dot_int4(const uint4 *wrow, int nvec, const 
                 // elements e = 8*wd .. 8*wd+7 sit in float4 groups e/4 = 2*wd, 2*wd+1
                 const float4 xa = *reinterpret_cast<const float4 *>(x + t * xstride + base + (2 * wd) * 128);
                 const float4 xb = *reinterpret_cast<const float4 *>(x + t * xstride + base + (2 * wd + 1) * 128);
-                float a = acc[t];
-                a = fmaf(wf[0], xa.x, a); a = fmaf(wf[1], xa.y, a);
-                a = fmaf(wf[2], xa.z, a); a = fmaf(wf[3], xa.w, a);
-                a = fmaf(wf[4], xb.x, a); a = fmaf(wf[5], xb.y, a);
-                a = fmaf(wf[6], xb.z, a); a = fmaf(wf[7], xb.w, a);
-                acc[t] = a;
+                a0[t] = fmaf(wf[0], xa.x, a0[t]); a1[t] = fmaf(wf[1], xa.y, a1[t]);
+                a0[t] = fmaf(wf[2], xa.z, a0[t]); a1[t] = fmaf(wf[3], xa.w, a1[t]);
+                a0[t] = fmaf(wf[4], xb.x, a0[t]); a1[t] = fmaf(wf[5], xb.y, a1[t]);
+                a0[t] = fmaf(wf[6], xb.z, a0[t]); a1[t] = fmaf(wf[7], xb.w, a1[t]);
             }
         }
     }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) acc[t] += a0[t] + a1[t];
 }
 
 template <int WT, int MT>
@@ -325,11 +343,18 @@ __global__ void __launch_bounds__(512) hc_down_kernel(const DownParams p)
 
         cluster_sync();  // every rank's partials and sums of squares are complete
 
+        // Remote (DSMEM) loads are all issued before any is used, so their
+        // latencies overlap; the sums then run in rank order.
         if (tid < mt) {
+            float ssr[kMaxCluster];
+#pragma unroll
+            for (int q = 0; q < kMaxCluster; ++q)
+                ssr[q] = q < p.S ? dsmem_ld_f32(dsmem_addr(ssq_s + tid, q)) : 0.f;
             for (int c = 0; c < p.C; ++c) {
                 float ss = 0.f;
-                for (int j = 0; j < p.sps; ++j)
-                    ss += dsmem_ld_f32(dsmem_addr(ssq_s + tid, c * p.sps + j));
+#pragma unroll
+                for (int q = 0; q < kMaxCluster; ++q)
+                    if (q / p.sps == c && q < p.S) ss += ssr[q];
                 invr_s[tid * p.C + c] = 1.0f / sqrtf(ss / (float)p.H + p.eps);
             }
         }
@@ -343,9 +368,14 @@ __global__ void __launch_bounds__(512) hc_down_kernel(const DownParams p)
         const int my_rows = s < nrows ? (nrows - s + p.S - 1) / p.S : 0;
         for (int i = tid; i < my_rows * mt; i += blockDim.x) {
             const int r = s + p.S * (i / mt), t = i % mt;
+            float pv[kMaxCluster];
+#pragma unroll
+            for (int q = 0; q < kMaxCluster; ++q)
+                pv[q] = q < p.S ? dsmem_ld_f32(dsmem_addr(part_s + t * RPB + r, q)) : 0.f;
             float z = 0.f;
-            for (int q = 0; q < p.S; ++q)
-                z = fmaf(invr_s[t * p.C + q / p.sps], dsmem_ld_f32(dsmem_addr(part_s + t * RPB + r, q)), z);
+#pragma unroll
+            for (int q = 0; q < kMaxCluster; ++q)
+                if (q < p.S) z = fmaf(invr_s[t * p.C + q / p.sps], pv[q], z);
             const int gr = r0 + r;
             const int m = t0 + t;
             const float zc = z * p.inv_C;
@@ -403,16 +433,82 @@ __global__ void __launch_bounds__(768) hc_up_kernel(const UpParams p)
         }
     }
 
+    const int team = lane >> 3, tl = lane & 7;  // 8 lanes per up row
+    bool have_weights = false, timed_out = false;
+    float *rv_s = reinterpret_cast<float *>(smem + lay.rv);
+    float *gv_s = reinterpret_cast<float *>(smem + lay.gv);
+    float *inv_s = reinterpret_cast<float *>(smem + lay.inv);
+    // g is a weight: staged before the dependency wait.
+    for (int i = tid; i < p.C * HB; i += blockDim.x) {
+        const int c = i / HB, hl = i % HB;
+        gv_s[i] = hl < hb ? __bfloat162float(__ushort_as_bfloat16(p.g[c * p.H + h0 + hl])) : 0.f;
+    }
+
     // act and inv_rms come from the down kernel; raw from the kernel before it.
     pdl_wait();
 
-    const int team = lane >> 3, tl = lane & 7;  // 8 lanes per up row
-    bool have_weights = false, timed_out = false;
     for (int t0 = 0; t0 < p.M; t0 += MT) {
         const int mt = min(MT, p.M - t0);
-        for (int i = tid; i < MT * L; i += blockDim.x) {
-            const int t = i / L, k = i % L;
-            act_s[i] = t < mt ? p.act[(size_t)(t0 + t) * L + k] : 0.f;
+        // Everything the tile needs is loaded in one round: act, inv_rms and
+        // the residual of this CTA's h-block (with a fused inject-add applied
+        // and written back here -- this CTA owns these elements).
+        if (p.part1) {
+            // One token: finish the down projection from the per-chunk partials.
+            // Thread k issues its partial loads first; threads c < C form the
+            // stream's inv_rms (chunk order) into shared memory; one barrier.
+            const int k = tid;  // the host launches at least R threads on this path
+            float pv[kMaxCluster];
+#pragma unroll
+            for (int q = 0; q < kMaxCluster; ++q)
+                pv[q] = (k < p.R && q < p.S) ? p.part1[(size_t)q * p.R + k] : 0.f;
+            float *invq_s = reinterpret_cast<float *>(smem + lay.invq);  // inv_rms of chunk q's stream
+            if (tid < p.C) {
+                float t = 0.f;
+                for (int j = 0; j < p.sps; ++j)
+                    t += p.ssq1[tid * p.sps + j];
+                const float iv = 1.0f / sqrtf(t / (float)p.H + p.eps);
+                inv_s[tid] = iv;
+                for (int j = 0; j < p.sps; ++j)
+                    invq_s[tid * p.sps + j] = iv;
+                if (blockIdx.x == 0) p.inv_out[tid] = iv;
+            }
+            __syncthreads();
+            if (k < p.R) {
+                float z = 0.f;
+#pragma unroll
+                for (int q = 0; q < kMaxCluster; ++q)
+                    if (q < p.S) z = fmaf(invq_s[q], pv[q], z);
+                const float zc = z * p.inv_C;
+                if (k < L) {
+                    const float a = zc * sigmoidf_(zc);
+                    act_s[k] = a;
+                    if (blockIdx.x == 0) p.act_out[k] = a;
+                } else if (blockIdx.x == 0) {
+                    p.gate[k - L] = 2.0f * sigmoidf_(zc);
+                }
+            }
+        } else {
+            for (int i = tid; i < MT * L; i += blockDim.x) {
+                const int t = i / L, k = i % L;
+                act_s[i] = t < mt ? p.act[(size_t)(t0 + t) * L + k] : 0.f;
+            }
+            for (int i = tid; i < MT * p.C; i += blockDim.x)
+                inv_s[i] = i / p.C < mt ? p.inv_rms[(size_t)t0 * p.C + i] : 0.f;
+        }
+        for (int i = tid; i < MT * p.C * HB; i += blockDim.x) {
+            const int t = i / (p.C * HB), c = (i / HB) % p.C, hl = i % HB;
+            float rv = 0.f;
+            if (t < mt && hl < hb) {
+                const size_t m = (size_t)(t0 + t);
+                const int h = h0 + hl, j = c * p.H + h;
+                rv = __bfloat162float(__ushort_as_bfloat16(p.raw[m * p.W + j]));
+                if (p.raw_out) {
+                    const float ov = __bfloat162float(__ushort_as_bfloat16(p.inj_out[m * p.H + h]));
+                    rv = __bfloat162float(__float2bfloat16_rn(fmaf(ov, p.inj_gate[m * p.inj_stride + c], rv)));
+                    p.raw_out[m * p.W + j] = __bfloat16_as_ushort(__float2bfloat16_rn(rv));
+                }
+            }
+            rv_s[i] = rv;
         }
         __syncthreads();
         if (!have_weights) {
@@ -436,6 +532,10 @@ __global__ void __launch_bounds__(768) hc_up_kernel(const UpParams p)
             if (!row_ok) {
                 // no row for this team
             } else if constexpr (WT == 0) {
+                float a1[MT];  // second chain (odd elements), added at the end
+#pragma unroll
+                for (int t = 0; t < MT; ++t) a1[t] = 0.f;
+#pragma unroll 2
                 for (int v = tl; v < L / 8; v += 8) {
                     float wf[8];
                     unpack_bf16x8(wrow[v], wf);
@@ -443,14 +543,14 @@ __global__ void __launch_bounds__(768) hc_up_kernel(const UpParams p)
                     for (int t = 0; t < MT; ++t) {
                         const float4 xa = *reinterpret_cast<const float4 *>(act_s + t * L + v * 8);
                         const float4 xb = *reinterpret_cast<const float4 *>(act_s + t * L + v * 8 + 4);
-                        float a = acc[t];
-                        a = fmaf(wf[0], xa.x, a); a = fmaf(wf[1], xa.y, a);
-                        a = fmaf(wf[2], xa.z, a); a = fmaf(wf[3], xa.w, a);
-                        a = fmaf(wf[4], xb.x, a); a = fmaf(wf[5], xb.y, a);
-                        a = fmaf(wf[6], xb.z, a); a = fmaf(wf[7], xb.w, a);
-                        acc[t] = a;
+                        acc[t] = fmaf(wf[0], xa.x, acc[t]); a1[t] = fmaf(wf[1], xa.y, a1[t]);
+                        acc[t] = fmaf(wf[2], xa.z, acc[t]); a1[t] = fmaf(wf[3], xa.w, a1[t]);
+                        acc[t] = fmaf(wf[4], xb.x, acc[t]); a1[t] = fmaf(wf[5], xb.y, a1[t]);
+                        acc[t] = fmaf(wf[6], xb.z, acc[t]); a1[t] = fmaf(wf[7], xb.w, a1[t]);
                     }
                 }
+#pragma unroll
+                for (int t = 0; t < MT; ++t) acc[t] += a1[t];
             } else {
                 const float *sb = sb_s + 2 * srow * ng;
                 for (int v = tl; v < L / 32; v += 8) {
@@ -496,21 +596,167 @@ __global__ void __launch_bounds__(768) hc_up_kernel(const UpParams p)
             const size_t m = (size_t)(t0 + t);
             float acc = 0.f;
             for (int c = 0; c < p.C; ++c) {
-                const int j = c * p.H + h;
-                float rv = __bfloat162float(__ushort_as_bfloat16(p.raw[m * p.W + j]));
-                if (p.raw_out) {
-                    // fused inject-add: this thread owns element (m, j); write it back
-                    const float ov = __bfloat162float(__ushort_as_bfloat16(p.inj_out[m * p.H + h]));
-                    rv = __bfloat162float(__float2bfloat16_rn(fmaf(ov, p.inj_gate[m * p.inj_stride + c], rv)));
-                    p.raw_out[m * p.W + j] = __bfloat16_as_ushort(__float2bfloat16_rn(rv));
-                }
-                const float gv = __bfloat162float(__ushort_as_bfloat16(p.g[j]));
-                const float nv = rv * p.inv_rms[m * p.C + c] * gv;
+                const float nv = rv_s[(t * p.C + c) * HB + hl] * inv_s[t * p.C + c] * gv_s[c * HB + hl];
                 acc = fmaf(wv_s[(t * p.C + c) * HB + hl], nv, acc);
             }
             p.mixed[m * p.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(acc * p.inv_C));
         }
         __syncthreads();
+    }
+    if (timed_out)  // do not leave with a copy into this CTA's shared memory in flight
+        mbar_wait_bounded(bar, 0);
+}
+
+// ---- one token: split-K down kernel without a cluster ------------------------
+//
+// Grid (S, row blocks): CTA (s, rb) owns rows [rb*RPB, ...) over input chunk s,
+// which lies inside stream s / sps. Before the dependency wait it streams its
+// weight row segments and its chunk of g (one bulk copy per lane of warp 0).
+// After it: one read of its residual chunk (applying a fused inject-add),
+// x = raw * g and the chunk's sum of squares, then each row's partial dot.
+// Partials go to part1[s][r] and the chunk's sum of squares (row block 0) to
+// ssq1[s]; the up kernel finishes the norm, silu and the gates. No cluster
+// barrier and no cross-CTA exchange on this kernel's critical path.
+
+struct PartSmem {
+    size_t bar, w, sb, g, x, red, total;
+};
+
+__host__ __device__ inline PartSmem part_layout(const DownParams &p)
+{
+    const int VW = p.down.type == 0 ? 8 : 32;
+    const int kcp = round_up(p.KC, 32 * VW);
+    const size_t seg = p.down.type == 0 ? (size_t)p.KC * 2 : (size_t)p.KC / 2;
+    const int ng = p.down.type == 0 ? 0 : p.KC / p.down.group;
+    PartSmem s;
+    s.bar = 0;
+    s.w = 128;
+    s.sb = round_up_sz(s.w + seg * p.rows_per_block, 128);
+    s.g = round_up_sz(s.sb + sizeof(float) * 2 * (size_t)ng * p.rows_per_block, 128);
+    s.x = round_up_sz(s.g + (size_t)p.KC * 2, 128);
+    s.red = round_up_sz(s.x + sizeof(float) * (size_t)kcp, 128);
+    s.total = round_up_sz(s.red + sizeof(float) * 32, 128);
+    return s;
+}
+
+template <int WT>
+__global__ void __launch_bounds__(1024) hc_down_part_kernel(const DownParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int VW = Vec<WT>::kElems;
+    const PartSmem lay = part_layout(p);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + lay.bar);
+    unsigned char *w_s = smem + lay.w;
+    float *sb_s = reinterpret_cast<float *>(smem + lay.sb);
+    const uint16_t *g_s = reinterpret_cast<const uint16_t *>(smem + lay.g);
+    float *x_s = reinterpret_cast<float *>(smem + lay.x);
+    float *red_s = reinterpret_cast<float *>(smem + lay.red);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    const int s = blockIdx.x;
+    const int RPB = p.rows_per_block;
+    const int r0 = blockIdx.y * RPB;
+    const int nrows = min(RPB, p.R - r0);
+    const int KC = p.KC, k0 = s * KC;
+    const int kcp = round_up(KC, 32 * VW);
+    const size_t seg = WT == 0 ? (size_t)KC * 2 : (size_t)KC / 2;
+
+    pdl_launch_dependents();
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0)
+            mbar_arrive_expect_tx(bar, (uint32_t)(seg * nrows + (size_t)KC * 2));
+        __syncwarp();
+        for (int j = lane; j <= nrows; j += 32) {
+            if (j == nrows) {
+                bulk_copy_g2s(smem + lay.g, p.g + k0, (uint32_t)KC * 2, bar);
+            } else {
+                const int gr = r0 + j;
+                const WeightView &wv = gr < p.L ? p.down : p.inject;
+                const int row = gr < p.L ? gr : gr - p.L;
+                const unsigned char *src = static_cast<const unsigned char *>(wv.data)
+                    + (WT == 0 ? ((size_t)row * p.W + k0) * 2 : ((size_t)row * p.W + k0) / 2);
+                bulk_copy_g2s(w_s + j * seg, src, (uint32_t)seg, bar);
+            }
+        }
+    }
+    if constexpr (WT == 1) {
+        const int ng = KC / p.down.group;
+        for (int i = tid; i < nrows * ng; i += blockDim.x) {
+            const int r = i / ng, gi = i % ng;
+            const int gr = r0 + r;
+            const WeightView &wv = gr < p.L ? p.down : p.inject;
+            const int row = gr < p.L ? gr : gr - p.L;
+            const size_t off = (size_t)row * (p.W / wv.group) + k0 / wv.group + gi;
+            sb_s[2 * i] = half_bits_to_float(wv.scales[off]);
+            sb_s[2 * i + 1] = half_bits_to_float(wv.biases[off]);
+        }
+    }
+
+    pdl_wait();  // the residual and the previous gates come from earlier kernels
+
+    // One vector of 8 residual elements per thread (the host launches at least
+    // KC/8 threads); loads are issued before waiting for the weights.
+    const int v = tid;
+    const bool has_v = v < KC / 8;
+    uint4 rvv = make_uint4(0, 0, 0, 0), ovv = make_uint4(0, 0, 0, 0);
+    float gt = 0.f;
+    if (has_v) {
+        rvv = *reinterpret_cast<const uint4 *>(p.raw + k0 + v * 8);
+        if (p.inj_out) {
+            ovv = *reinterpret_cast<const uint4 *>(p.inj_out + k0 % p.H + v * 8);
+            gt = p.inj_gate[k0 / p.H];
+        }
+    }
+    const bool timed_out = !mbar_wait_bounded(bar, 0);
+    if (timed_out)
+        record_timeout(p.status);
+
+    float q = 0.f;
+    if (has_v) {
+        float rf[8], gf[8];
+        unpack_bf16x8(rvv, rf);
+        if (p.inj_out) {
+            float of[8];
+            unpack_bf16x8(ovv, of);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                rf[e] = __bfloat162float(__float2bfloat16_rn(fmaf(of[e], gt, rf[e])));
+        }
+        unpack_bf16x8(*reinterpret_cast<const uint4 *>(g_s + v * 8), gf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            q = fmaf(rf[e], rf[e], q);
+        *reinterpret_cast<float4 *>(x_s + xpos<VW>(v * 8)) =
+            make_float4(rf[0] * gf[0], rf[1] * gf[1], rf[2] * gf[2], rf[3] * gf[3]);
+        *reinterpret_cast<float4 *>(x_s + xpos<VW>(v * 8 + 4)) =
+            make_float4(rf[4] * gf[4], rf[5] * gf[5], rf[6] * gf[6], rf[7] * gf[7]);
+    }
+    q = warp_sum(q);
+    if (lane == 0)
+        red_s[warp] = q;
+    __syncthreads();
+    if (blockIdx.y == 0 && tid == 0) {
+        float t = 0.f;
+        for (int w = 0; w < nwarps; ++w)
+            t += red_s[w];
+        p.ssq1[s] = t;
+    }
+
+    for (int r = warp; r < nrows; r += nwarps) {
+        float acc[1] = {0.f};
+        const uint4 *wrow = reinterpret_cast<const uint4 *>(w_s + r * seg);
+        if constexpr (WT == 0)
+            row_dot_bf16<1>(wrow, KC / VW, x_s, kcp, lane, acc);
+        else
+            row_dot_int4<1>(wrow, KC / VW, sb_s + 2 * r * (KC / p.down.group), p.down.group, x_s, kcp, lane, acc);
+        const float d = warp_sum(acc[0]);
+        if (lane == 0)
+            p.part1[(size_t)s * p.R + r0 + r] = d;
     }
     if (timed_out)  // do not leave with a copy into this CTA's shared memory in flight
         mbar_wait_bounded(bar, 0);
@@ -680,7 +926,9 @@ int down_threads(const DownParams &p)
 
 int up_threads(const UpParams &p)
 {
-    const int warps = std::min(24, std::max(2, (p.C * p.HB + 3) / 4));
+    int warps = std::min(24, std::max(2, (p.C * p.HB + 3) / 4));
+    if (p.part1)  // one thread per down row in the one-token prologue
+        warps = std::max(warps, (p.R + 31) / 32);
     return 32 * warps;
 }
 
@@ -688,6 +936,25 @@ cudaError_t launch_down(const DownParams &p, const LaunchCfg &cfg, cudaStream_t 
 {
     return p.down.type == 0 ? launch_down_wt<0>(p, cfg, stream) : launch_down_wt<1>(p, cfg, stream);
 }
+
+size_t down_part_smem_bytes(const DownParams &p) { return part_layout(p).total; }
+
+cudaError_t launch_down_part(const DownParams &p, const LaunchCfg &cfg, cudaStream_t stream)
+{
+    const size_t smem = part_layout(p).total;
+    // One warp per row of the block, and at least one thread per 8-element
+    // vector of the chunk.
+    const int threads = std::max(32 * std::min(p.rows_per_block, 32), (p.KC / 8 + 31) / 32 * 32);
+    if (threads > 1024)
+        return cudaErrorInvalidConfiguration;
+    void (*k)(DownParams) = p.down.type == 0 ? hc_down_part_kernel<0> : hc_down_part_kernel<1>;
+    cudaError_t e = allow_smem(k, smem);
+    if (e != cudaSuccess)
+        return e;
+    const dim3 grid(p.S, (p.R + p.rows_per_block - 1) / p.rows_per_block, 1);
+    return launch_ex(k, grid, dim3(threads), smem, stream, 0, cfg.pdl, p);
+}
+
 
 cudaError_t launch_up(const UpParams &p, const LaunchCfg &cfg, cudaStream_t stream)
 {

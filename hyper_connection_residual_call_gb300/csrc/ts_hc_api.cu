@@ -152,8 +152,12 @@ int tc_cluster_size(int M, int H, int C, int L)
 }
 
 struct WsLayout {
-    size_t inv_rms, act, part, ssq, act_hi, act_lo, total;
+    size_t inv_rms, act, part, ssq, act_hi, act_lo, part1, ssq1, total;
 };
+
+// Per-chunk partial dots and sums of squares of the one-token path: at most
+// 8 chunks (C * sps <= 8) of L + C rows.
+constexpr int kPart1Chunks = 8;
 
 WsLayout ws_layout(int M, int H, int C, int L)
 {
@@ -161,6 +165,11 @@ WsLayout ws_layout(int M, int H, int C, int L)
     w.inv_rms = 0;
     w.act = align256(sizeof(float) * (size_t)M * C);
     w.total = w.act + align256(sizeof(float) * (size_t)M * L);
+    if (M == 1) {  // one token: the down kernel leaves partials, the up kernel reduces them
+        w.part1 = w.total;
+        w.ssq1 = w.part1 + align256(sizeof(float) * kPart1Chunks * ((size_t)L + C));
+        w.total = w.ssq1 + align256(sizeof(float) * kPart1Chunks);
+    }
     if (tc_cluster_size(M, H, C, L) > 0) {
         const size_t R = (size_t)L + C;
         w.part = w.total;
@@ -355,7 +364,27 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         return fail(TS_ERR_UNSUPPORTED, "shape C = %d, lowrank = %d exceeds the shared-memory budget", C, L);
 
     const tshc::LaunchCfg cfg{dev.sm_count, true};
-    cudaError_t e = tshc::launch_down(d, cfg, stream);
+    cudaError_t e;
+    // One token: the down kernel leaves per-chunk partials and the up kernel
+    // reduces them, so neither kernel waits on another CTA.
+    const bool one_token = M == 1 && d.KC / 8 <= 1024 && d.S <= kPart1Chunks && d.R <= 768 &&
+                           tshc::down_part_smem_bytes(d) <= tshc::kSmemBudget;
+    if (one_token) {
+        d.part1 = reinterpret_cast<float *>(wsb + wl.part1);
+        d.ssq1 = reinterpret_cast<float *>(wsb + wl.ssq1);
+        u.part1 = d.part1;
+        u.ssq1 = d.ssq1;
+        u.S = d.S;
+        u.sps = d.sps;
+        u.R = d.R;
+        u.eps = eps;
+        u.act_out = act;
+        u.inv_out = inv_rms;
+        u.gate = inject ? inject_w : nullptr;
+        e = tshc::launch_down_part(d, cfg, stream);
+    } else {
+        e = tshc::launch_down(d, cfg, stream);
+    }
     if (e != cudaSuccess)
         return cuda_fail(e, "launching the down kernel");
     e = tshc::launch_up(u, cfg, stream);
