@@ -83,7 +83,7 @@ __host__ __device__ inline DownSmem down_layout(const DownParams &p, int mt)
 }
 
 struct UpSmem {
-    size_t bar, w, sb, act, wv, rv, gv, inv, invq, total;
+    size_t bar, w, sb, act, wv, rv, gv, inv, total;
 };
 
 // Up kernel shared memory: weight rows, INT4 scales/biases, act tile, sigmoid
@@ -102,8 +102,7 @@ __host__ __device__ inline UpSmem up_layout(const UpParams &p, int mt)
     s.rv = round_up_sz(s.wv + sizeof(float) * (size_t)mt * p.C * p.HB, 128);
     s.gv = round_up_sz(s.rv + sizeof(float) * (size_t)mt * p.C * p.HB, 128);
     s.inv = round_up_sz(s.gv + sizeof(float) * (size_t)p.C * p.HB, 128);
-    s.invq = round_up_sz(s.inv + sizeof(float) * (size_t)mt * p.C, 128);
-    s.total = round_up_sz(s.invq + sizeof(float) * kMaxCluster, 128);
+    s.total = round_up_sz(s.inv + sizeof(float) * (size_t)mt * p.C, 128);
     return s;
 }
 
@@ -392,7 +391,7 @@ __global__ void __launch_bounds__(512) hc_down_kernel(const DownParams p)
 }
 
 template <int WT, int MT>
-__global__ void __launch_bounds__(768) hc_up_kernel(const UpParams p)
+__global__ void __launch_bounds__(768, 1) hc_up_kernel(const UpParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     const UpSmem lay = up_layout(p, MT);
@@ -452,49 +451,12 @@ __global__ void __launch_bounds__(768) hc_up_kernel(const UpParams p)
         // Everything the tile needs is loaded in one round: act, inv_rms and
         // the residual of this CTA's h-block (with a fused inject-add applied
         // and written back here -- this CTA owns these elements).
-        if (p.part1) {
-            // One token: finish the down projection from the per-chunk partials.
-            // Thread k issues its partial loads first; threads c < C form the
-            // stream's inv_rms (chunk order) into shared memory; one barrier.
-            const int k = tid;  // the host launches at least R threads on this path
-            float pv[kMaxCluster];
-#pragma unroll
-            for (int q = 0; q < kMaxCluster; ++q)
-                pv[q] = (k < p.R && q < p.S) ? p.part1[(size_t)q * p.R + k] : 0.f;
-            float *invq_s = reinterpret_cast<float *>(smem + lay.invq);  // inv_rms of chunk q's stream
-            if (tid < p.C) {
-                float t = 0.f;
-                for (int j = 0; j < p.sps; ++j)
-                    t += p.ssq1[tid * p.sps + j];
-                const float iv = 1.0f / sqrtf(t / (float)p.H + p.eps);
-                inv_s[tid] = iv;
-                for (int j = 0; j < p.sps; ++j)
-                    invq_s[tid * p.sps + j] = iv;
-                if (blockIdx.x == 0) p.inv_out[tid] = iv;
-            }
-            __syncthreads();
-            if (k < p.R) {
-                float z = 0.f;
-#pragma unroll
-                for (int q = 0; q < kMaxCluster; ++q)
-                    if (q < p.S) z = fmaf(invq_s[q], pv[q], z);
-                const float zc = z * p.inv_C;
-                if (k < L) {
-                    const float a = zc * sigmoidf_(zc);
-                    act_s[k] = a;
-                    if (blockIdx.x == 0) p.act_out[k] = a;
-                } else if (blockIdx.x == 0) {
-                    p.gate[k - L] = 2.0f * sigmoidf_(zc);
-                }
-            }
-        } else {
-            for (int i = tid; i < MT * L; i += blockDim.x) {
-                const int t = i / L, k = i % L;
-                act_s[i] = t < mt ? p.act[(size_t)(t0 + t) * L + k] : 0.f;
-            }
-            for (int i = tid; i < MT * p.C; i += blockDim.x)
-                inv_s[i] = i / p.C < mt ? p.inv_rms[(size_t)t0 * p.C + i] : 0.f;
+        for (int i = tid; i < MT * L; i += blockDim.x) {
+            const int t = i / L, k = i % L;
+            act_s[i] = t < mt ? p.act[(size_t)(t0 + t) * L + k] : 0.f;
         }
+        for (int i = tid; i < MT * p.C; i += blockDim.x)
+            inv_s[i] = i / p.C < mt ? p.inv_rms[(size_t)t0 * p.C + i] : 0.f;
         for (int i = tid; i < MT * p.C * HB; i += blockDim.x) {
             const int t = i / (p.C * HB), c = (i / HB) % p.C, hl = i % HB;
             float rv = 0.f;
@@ -607,59 +569,106 @@ __global__ void __launch_bounds__(768) hc_up_kernel(const UpParams p)
         mbar_wait_bounded(bar, 0);
 }
 
-// ---- one token: split-K down kernel without a cluster ------------------------
+// ---- one token (M == 1): two kernels, no cluster, no cross-CTA wait ---------
 //
-// Grid (S, row blocks): CTA (s, rb) owns rows [rb*RPB, ...) over input chunk s,
-// which lies inside stream s / sps. Before the dependency wait it streams its
-// weight row segments and its chunk of g (one bulk copy per lane of warp 0).
-// After it: one read of its residual chunk (applying a fused inject-add),
-// x = raw * g and the chunk's sum of squares, then each row's partial dot.
-// Partials go to part1[s][r] and the chunk's sum of squares (row block 0) to
-// ssq1[s]; the up kernel finishes the norm, silu and the gates. No cluster
-// barrier and no cross-CTA exchange on this kernel's critical path.
+// hc_down1_kernel  Grid (S, row blocks): CTA (s, rb) owns rows [rb*RPB, ...)
+//                  over input chunk s (which lies inside stream s / sps).
+//                  Before the dependency wait, warp 0 streams the block's
+//                  weight row segments and the chunk of g into shared memory
+//                  (one bulk copy per lane). Thread v of a group owns the
+//                  chunk's inputs [8v, 8v + 8): after the wait it reads them
+//                  once (applying a fused inject-add), keeps x = raw * g in
+//                  registers and forms their dot with each of its group's rows
+//                  (the block's rows are split evenly over G groups of
+//                  threads). Partial sums leave the warp by a transposed
+//                  butterfly and meet across warps in shared memory; the
+//                  block writes part1[s][r] and (row block 0) the chunk's sum
+//                  of squares ssq1[s].
+// hc_up1_kernel    Every CTA forms inv_rms, z = sum_s inv_rms[stream(s)] * P_s
+//                  and silu(z / C) for all rows from the partials in a fixed
+//                  order (CTA 0 also writes act, inv_rms and the gates out).
+//                  Warp w owns h = h0 + w: lane l owns act inputs [8v, 8v + 8)
+//                  for v = l, l + 32, ... and dots them with the C up rows
+//                  {c*H + h}; after the transposed butterfly, lane 4c holds
+//                  row c, applies the sigmoid and its term of the mean mix,
+//                  and lane 0 writes mixed[h]. With a fused inject-add, lane 4c
+//                  also writes the updated residual element back.
 
-struct PartSmem {
-    size_t bar, w, sb, g, x, red, total;
+// Sums v[0..7] over the 32 lanes of a warp. On return lane l holds the total
+// of v[(l >> 2) & 7]. Every lane must take part; the order is fixed.
+__device__ __forceinline__ float warp_transpose_sum8(float (&v)[8], int lane)
+{
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // v[i] -> value 4*b4 + i
+        const float send = b4 ? v[i] : v[i + 4];
+        const float keep = b4 ? v[i + 4] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {  // v[i] -> value 4*b4 + 2*b3 + i
+        const float send = b3 ? v[i] : v[i + 2];
+        const float keep = b3 ? v[i + 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    const float send = b2 ? v[0] : v[1];
+    const float keep = b2 ? v[1] : v[0];
+    float r = keep + __shfl_xor_sync(0xffffffffu, send, 4);  // value 4*b4 + 2*b3 + b2
+    r += __shfl_xor_sync(0xffffffffu, r, 2);
+    r += __shfl_xor_sync(0xffffffffu, r, 1);
+    return r;
+}
+
+constexpr int kRowsPerGroup = 8;  // rows one thread of hc_down1_kernel dots
+
+struct Down1Smem {
+    size_t bar, w, sb, g, red, total;
 };
 
-__host__ __device__ inline PartSmem part_layout(const DownParams &p)
+__host__ __device__ inline Down1Smem down1_layout(const DownParams &p)
 {
-    const int VW = p.down.type == 0 ? 8 : 32;
-    const int kcp = round_up(p.KC, 32 * VW);
     const size_t seg = p.down.type == 0 ? (size_t)p.KC * 2 : (size_t)p.KC / 2;
     const int ng = p.down.type == 0 ? 0 : p.KC / p.down.group;
-    PartSmem s;
+    Down1Smem s;
     s.bar = 0;
     s.w = 128;
     s.sb = round_up_sz(s.w + seg * p.rows_per_block, 128);
     s.g = round_up_sz(s.sb + sizeof(float) * 2 * (size_t)ng * p.rows_per_block, 128);
-    s.x = round_up_sz(s.g + (size_t)p.KC * 2, 128);
-    s.red = round_up_sz(s.x + sizeof(float) * (size_t)kcp, 128);
-    s.total = round_up_sz(s.red + sizeof(float) * 32, 128);
+    s.red = round_up_sz(s.g + (size_t)p.KC * 2, 128);
+    s.total = round_up_sz(s.red + sizeof(float) * 32 * (kRowsPerGroup + 1), 128);
     return s;
 }
 
+// Threads of one group of hc_down1_kernel: one per 8 inputs of the chunk.
+__host__ __device__ inline int down1_group_threads(const DownParams &p) { return round_up(p.KC / 8, 32); }
+// Groups (the block's rows split evenly, at most kRowsPerGroup each).
+__host__ __device__ inline int down1_groups(const DownParams &p)
+{
+    return (p.rows_per_block + kRowsPerGroup - 1) / kRowsPerGroup;
+}
+
 template <int WT>
-__global__ void __launch_bounds__(1024) hc_down_part_kernel(const DownParams p)
+__global__ void __launch_bounds__(1024, 1) hc_down1_kernel(const DownParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int VW = Vec<WT>::kElems;
-    const PartSmem lay = part_layout(p);
+    const Down1Smem lay = down1_layout(p);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + lay.bar);
-    unsigned char *w_s = smem + lay.w;
+    const unsigned char *w_s = smem + lay.w;
     float *sb_s = reinterpret_cast<float *>(smem + lay.sb);
     const uint16_t *g_s = reinterpret_cast<const uint16_t *>(smem + lay.g);
-    float *x_s = reinterpret_cast<float *>(smem + lay.x);
     float *red_s = reinterpret_cast<float *>(smem + lay.red);
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int s = blockIdx.x;
-    const int RPB = p.rows_per_block;
-    const int r0 = blockIdx.y * RPB;
-    const int nrows = min(RPB, p.R - r0);
-    const int KC = p.KC, k0 = s * KC;
-    const int kcp = round_up(KC, 32 * VW);
+    const int r0 = blockIdx.y * p.rows_per_block;
+    const int nrows = min(p.rows_per_block, p.R - r0);
+    const int KC = p.KC, k0 = s * KC, nv = KC / 8;
     const size_t seg = WT == 0 ? (size_t)KC * 2 : (size_t)KC / 2;
+    const int tpg = down1_group_threads(p), wpg = tpg / 32;
+    const int ngroups = blockDim.x / tpg;
+    const int rpg = (nrows + ngroups - 1) / ngroups;  // rows per group (<= kRowsPerGroup)
+    const int grp = tid / tpg, v = tid % tpg;
+    const int gr0 = grp * rpg, gnr = max(0, min(rpg, nrows - gr0));
 
     pdl_launch_dependents();
     if (tid == 0) {
@@ -680,12 +689,12 @@ __global__ void __launch_bounds__(1024) hc_down_part_kernel(const DownParams p)
                 const int row = gr < p.L ? gr : gr - p.L;
                 const unsigned char *src = static_cast<const unsigned char *>(wv.data)
                     + (WT == 0 ? ((size_t)row * p.W + k0) * 2 : ((size_t)row * p.W + k0) / 2);
-                bulk_copy_g2s(w_s + j * seg, src, (uint32_t)seg, bar);
+                bulk_copy_g2s(smem + lay.w + j * seg, src, (uint32_t)seg, bar);
             }
         }
     }
+    const int ng = WT == 0 ? 1 : KC / p.down.group;
     if constexpr (WT == 1) {
-        const int ng = KC / p.down.group;
         for (int i = tid; i < nrows * ng; i += blockDim.x) {
             const int r = i / ng, gi = i % ng;
             const int gr = r0 + r;
@@ -695,14 +704,12 @@ __global__ void __launch_bounds__(1024) hc_down_part_kernel(const DownParams p)
             sb_s[2 * i] = half_bits_to_float(wv.scales[off]);
             sb_s[2 * i + 1] = half_bits_to_float(wv.biases[off]);
         }
+        __syncthreads();  // other warps read these scales (no later barrier precedes the dots)
     }
 
     pdl_wait();  // the residual and the previous gates come from earlier kernels
 
-    // One vector of 8 residual elements per thread (the host launches at least
-    // KC/8 threads); loads are issued before waiting for the weights.
-    const int v = tid;
-    const bool has_v = v < KC / 8;
+    const bool has_v = v < nv;
     uint4 rvv = make_uint4(0, 0, 0, 0), ovv = make_uint4(0, 0, 0, 0);
     float gt = 0.f;
     if (has_v) {
@@ -716,8 +723,8 @@ __global__ void __launch_bounds__(1024) hc_down_part_kernel(const DownParams p)
     if (timed_out)
         record_timeout(p.status);
 
-    float q = 0.f;
-    if (has_v) {
+    float x[8], q = 0.f;
+    {
         float rf[8], gf[8];
         unpack_bf16x8(rvv, rf);
         if (p.inj_out) {
@@ -727,36 +734,231 @@ __global__ void __launch_bounds__(1024) hc_down_part_kernel(const DownParams p)
             for (int e = 0; e < 8; ++e)
                 rf[e] = __bfloat162float(__float2bfloat16_rn(fmaf(of[e], gt, rf[e])));
         }
-        unpack_bf16x8(*reinterpret_cast<const uint4 *>(g_s + v * 8), gf);
+        unpack_bf16x8(has_v ? *reinterpret_cast<const uint4 *>(g_s + v * 8) : make_uint4(0, 0, 0, 0), gf);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
+        for (int e = 0; e < 8; ++e) {
             q = fmaf(rf[e], rf[e], q);
-        *reinterpret_cast<float4 *>(x_s + xpos<VW>(v * 8)) =
-            make_float4(rf[0] * gf[0], rf[1] * gf[1], rf[2] * gf[2], rf[3] * gf[3]);
-        *reinterpret_cast<float4 *>(x_s + xpos<VW>(v * 8 + 4)) =
-            make_float4(rf[4] * gf[4], rf[5] * gf[5], rf[6] * gf[6], rf[7] * gf[7]);
-    }
-    q = warp_sum(q);
-    if (lane == 0)
-        red_s[warp] = q;
-    __syncthreads();
-    if (blockIdx.y == 0 && tid == 0) {
-        float t = 0.f;
-        for (int w = 0; w < nwarps; ++w)
-            t += red_s[w];
-        p.ssq1[s] = t;
+            x[e] = rf[e] * gf[e];
+        }
     }
 
-    for (int r = warp; r < nrows; r += nwarps) {
-        float acc[1] = {0.f};
-        const uint4 *wrow = reinterpret_cast<const uint4 *>(w_s + r * seg);
-        if constexpr (WT == 0)
-            row_dot_bf16<1>(wrow, KC / VW, x_s, kcp, lane, acc);
-        else
-            row_dot_int4<1>(wrow, KC / VW, sb_s + 2 * r * (KC / p.down.group), p.down.group, x_s, kcp, lane, acc);
-        const float d = warp_sum(acc[0]);
+    float acc[kRowsPerGroup];
+#pragma unroll
+    for (int j = 0; j < kRowsPerGroup; ++j) {
+        acc[j] = 0.f;
+        if (has_v && j < gnr) {
+            const unsigned char *wr = w_s + (size_t)(gr0 + j) * seg;
+            float wf[8];
+            if constexpr (WT == 0) {
+                unpack_bf16x8(*reinterpret_cast<const uint4 *>(wr + v * 16), wf);
+            } else {
+                const uint32_t codes = *reinterpret_cast<const uint32_t *>(wr + v * 4);
+                const float *sb = sb_s + 2 * ((gr0 + j) * ng + (v * 8) / p.down.group);
+                const float sc = sb[0], bi = sb[1];
+#pragma unroll
+                for (int n = 0; n < 8; ++n)
+                    wf[n] = fmaf((float)((codes >> (4 * n)) & 0xFu), sc, bi);
+            }
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                a0 = fmaf(wf[e], x[e], a0);
+                a1 = fmaf(wf[e + 1], x[e + 1], a1);
+            }
+            acc[j] = a0 + a1;
+        }
+    }
+    const float rsum = warp_transpose_sum8(acc, lane);
+    if ((lane & 3) == 0)
+        red_s[warp * (kRowsPerGroup + 1) + (lane >> 2)] = rsum;
+    q = warp_sum(q);
+    if (lane == 0)
+        red_s[warp * (kRowsPerGroup + 1) + kRowsPerGroup] = q;
+    __syncthreads();
+
+    if (tid < nrows) {  // row tid of the block, in group tid / rpg
+        const int g = tid / rpg, j = tid % rpg;
+        float t = 0.f;
+        for (int w = 0; w < wpg; ++w)
+            t += red_s[(g * wpg + w) * (kRowsPerGroup + 1) + j];
+        p.part1[(size_t)s * p.R + r0 + tid] = t;
+    }
+    if (blockIdx.y == 0 && tid == blockDim.x - 1) {  // every group saw the same inputs: use group 0
+        float t = 0.f;
+        for (int w = 0; w < wpg; ++w)
+            t += red_s[w * (kRowsPerGroup + 1) + kRowsPerGroup];
+        p.ssq1[s] = t;
+    }
+    if (timed_out)  // do not leave with a copy into this CTA's shared memory in flight
+        mbar_wait_bounded(bar, 0);
+}
+
+struct Up1Smem {
+    size_t bar, w, sb, act, invq, inv, total;
+};
+
+__host__ __device__ inline Up1Smem up1_layout(const UpParams &p)
+{
+    const size_t row = p.up.type == 0 ? (size_t)p.L * 2 : (size_t)p.L / 2;
+    const int ng = p.up.type == 0 ? 0 : p.L / p.up.group;
+    Up1Smem s;
+    s.bar = 0;
+    s.w = 128;
+    s.sb = round_up_sz(s.w + row * p.C * p.HB, 128);
+    s.act = round_up_sz(s.sb + sizeof(float) * 2 * (size_t)ng * p.C * p.HB, 128);
+    s.invq = round_up_sz(s.act + sizeof(float) * (size_t)p.L, 128);
+    s.inv = round_up_sz(s.invq + sizeof(float) * kMaxCluster, 16);
+    s.total = round_up_sz(s.inv + sizeof(float) * kMaxCluster, 128);
+    return s;
+}
+
+template <int WT>
+__global__ void __launch_bounds__(1024) hc_up1_kernel(const UpParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const Up1Smem lay = up1_layout(p);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + lay.bar);
+    const unsigned char *w_s = smem + lay.w;
+    float *sb_s = reinterpret_cast<float *>(smem + lay.sb);
+    float *act_s = reinterpret_cast<float *>(smem + lay.act);
+    float *invq_s = reinterpret_cast<float *>(smem + lay.invq);  // inv_rms of chunk q's stream
+    float *inv_s = reinterpret_cast<float *>(smem + lay.inv);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int HB = p.HB, h0 = blockIdx.x * HB;
+    const int hb = min(HB, p.H - h0);
+    const int L = p.L;
+    const size_t row_bytes = WT == 0 ? (size_t)L * 2 : (size_t)L / 2;
+    const int ng = WT == 0 ? 1 : L / p.up.group;
+
+    pdl_launch_dependents();
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar, (uint32_t)(row_bytes * hb * p.C));
+        for (int c = 0; c < p.C; ++c)
+            bulk_copy_g2s(smem + lay.w + (size_t)c * HB * row_bytes,
+                          static_cast<const unsigned char *>(p.up.data) + ((size_t)c * p.H + h0) * row_bytes,
+                          (uint32_t)(row_bytes * hb), bar);
+    }
+    if constexpr (WT == 1) {
+        for (int i = tid; i < p.C * hb * ng; i += blockDim.x) {
+            const int c = i / (hb * ng), rem = i % (hb * ng), hl = rem / ng, gi = rem % ng;
+            const size_t off = ((size_t)c * p.H + h0 + hl) * ng + gi;
+            const int srow = c * HB + hl;
+            sb_s[2 * (srow * ng + gi)] = half_bits_to_float(p.up.scales[off]);
+            sb_s[2 * (srow * ng + gi) + 1] = half_bits_to_float(p.up.biases[off]);
+        }
+    }
+
+    // Warp w owns h = h0 + w (the host launches at least hb warps); lane 4c
+    // holds stream c's up row after the butterfly.
+    const int hl = warp, h = h0 + hl;
+    const bool h_ok = hl < hb;
+    const int hc = lane >> 2;
+    const bool holder = h_ok && (lane & 3) == 0 && hc < p.C;
+    float gval = 0.f;  // g is a weight: read before the dependency wait
+    if (holder)
+        gval = __bfloat162float(__ushort_as_bfloat16(p.g[hc * p.H + h]));
+
+    pdl_wait();  // partials from the down kernel; the residual from before it
+
+    // One round of loads: partials (thread k owns down row k), sums of
+    // squares, and this lane's residual element with the previous gate.
+    const int k = tid;  // the host launches at least R threads
+    float pv[kMaxCluster];
+#pragma unroll
+    for (int q = 0; q < kMaxCluster; ++q)
+        pv[q] = (k < p.R && q < p.S) ? p.part1[(size_t)q * p.R + k] : 0.f;
+    float rv = 0.f, ov = 0.f, gp = 0.f;
+    if (holder) {
+        rv = __bfloat162float(__ushort_as_bfloat16(p.raw[hc * p.H + h]));
+        if (p.raw_out) {
+            ov = __bfloat162float(__ushort_as_bfloat16(p.inj_out[h]));
+            gp = p.inj_gate[hc];
+        }
+    }
+    if (tid < p.C) {
+        float t = 0.f;
+        for (int j = 0; j < p.sps; ++j)
+            t += p.ssq1[tid * p.sps + j];
+        const float iv = 1.0f / sqrtf(t / (float)p.H + p.eps);
+        inv_s[tid] = iv;
+        for (int j = 0; j < p.sps; ++j)
+            invq_s[tid * p.sps + j] = iv;
+        if (blockIdx.x == 0)
+            p.inv_out[tid] = iv;
+    }
+    __syncthreads();
+    if (k < p.R) {
+        float z = 0.f;
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; ++q)
+            if (q < p.S) z = fmaf(invq_s[q], pv[q], z);
+        const float zc = z * p.inv_C;
+        if (k < L) {
+            const float a = zc * sigmoidf_(zc);
+            act_s[k] = a;
+            if (blockIdx.x == 0)
+                p.act_out[k] = a;
+        } else if (blockIdx.x == 0 && p.gate) {
+            p.gate[k - L] = 2.0f * sigmoidf_(zc);
+        }
+    }
+    const bool timed_out = !mbar_wait_bounded(bar, 0);
+    if (timed_out)
+        record_timeout(p.status);
+    __syncthreads();
+
+    if (h_ok) {  // warp-uniform
+        float acc[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[c] = 0.f;
+        for (int v = lane; v < L / 8; v += 32) {
+            const float4 xa = *reinterpret_cast<const float4 *>(act_s + v * 8);
+            const float4 xb = *reinterpret_cast<const float4 *>(act_s + v * 8 + 4);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                if (c < p.C) {
+                    const int srow = c * HB + hl;
+                    const unsigned char *wr = w_s + (size_t)srow * row_bytes;
+                    float wf[8];
+                    if constexpr (WT == 0) {
+                        unpack_bf16x8(*reinterpret_cast<const uint4 *>(wr + v * 16), wf);
+                    } else {
+                        const uint32_t codes = *reinterpret_cast<const uint32_t *>(wr + v * 4);
+                        const float *sb = sb_s + 2 * (srow * ng + (v * 8) / p.up.group);
+                        const float sc = sb[0], bi = sb[1];
+#pragma unroll
+                        for (int n = 0; n < 8; ++n)
+                            wf[n] = fmaf((float)((codes >> (4 * n)) & 0xFu), sc, bi);
+                    }
+                    float a0 = acc[c], a1 = 0.f;
+                    a0 = fmaf(wf[0], xa.x, a0); a1 = fmaf(wf[1], xa.y, a1);
+                    a0 = fmaf(wf[2], xa.z, a0); a1 = fmaf(wf[3], xa.w, a1);
+                    a0 = fmaf(wf[4], xb.x, a0); a1 = fmaf(wf[5], xb.y, a1);
+                    a0 = fmaf(wf[6], xb.z, a0); a1 = fmaf(wf[7], xb.w, a1);
+                    acc[c] = a0 + a1;
+                }
+            }
+        }
+        const float d = warp_transpose_sum8(acc, lane);
+        float term = 0.f;
+        if (holder) {
+            if (p.raw_out) {
+                rv = __bfloat162float(__float2bfloat16_rn(fmaf(ov, gp, rv)));
+                p.raw_out[hc * p.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(rv));
+            }
+            term = sigmoidf_(d) * (rv * inv_s[hc] * gval);
+        }
+        term += __shfl_xor_sync(0xffffffffu, term, 4);
+        term += __shfl_xor_sync(0xffffffffu, term, 8);
+        term += __shfl_xor_sync(0xffffffffu, term, 16);
         if (lane == 0)
-            p.part1[(size_t)s * p.R + r0 + r] = d;
+            p.mixed[h] = __bfloat16_as_ushort(__float2bfloat16_rn(term * p.inv_C));
     }
     if (timed_out)  // do not leave with a copy into this CTA's shared memory in flight
         mbar_wait_bounded(bar, 0);
@@ -834,13 +1036,15 @@ cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// Raises a kernel's dynamic shared-memory limit once per device (to the
-// budget, which covers every launch the host logic allows).
+// Once per kernel and device: raises the dynamic shared-memory limit to the
+// budget (which covers every launch the host logic allows) and asks for the
+// largest shared-memory carveout. Consecutive kernels of a call share SMs
+// (a dependent launch is resident while its predecessor runs); an SM can only
+// hold CTAs of kernels whose carveouts agree and fit, so every kernel here
+// asks for the same, largest one.
 template <typename K>
 cudaError_t allow_smem(K kernel, size_t smem)
 {
-    if (smem <= 48 * 1024)
-        return cudaSuccess;
     if (smem > kSmemBudget)
         return cudaErrorInvalidValue;
     int dev = 0;
@@ -854,6 +1058,9 @@ cudaError_t allow_smem(K kernel, size_t smem)
     if (done.count(key))
         return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess)
         done.insert(key);
     return e;
@@ -906,6 +1113,9 @@ cudaError_t launch_replicate(const ReplicateParams &p, const LaunchCfg &cfg, cud
     const long nvec = (long)p.M * p.C * p.H / 8;
     const int threads = 128;
     long blocks = std::max<long>(1, std::min<long>((nvec + threads - 1) / threads, (long)cfg.sm_count * 8));
+    const cudaError_t e = allow_smem(hc_replicate_kernel, 0);
+    if (e != cudaSuccess)
+        return e;
     return launch_ex(hc_replicate_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, 0, cfg.pdl, p);
 }
 
@@ -926,9 +1136,7 @@ int down_threads(const DownParams &p)
 
 int up_threads(const UpParams &p)
 {
-    int warps = std::min(24, std::max(2, (p.C * p.HB + 3) / 4));
-    if (p.part1)  // one thread per down row in the one-token prologue
-        warps = std::max(warps, (p.R + 31) / 32);
+    const int warps = std::min(24, std::max(2, (p.C * p.HB + 3) / 4));
     return 32 * warps;
 }
 
@@ -937,24 +1145,35 @@ cudaError_t launch_down(const DownParams &p, const LaunchCfg &cfg, cudaStream_t 
     return p.down.type == 0 ? launch_down_wt<0>(p, cfg, stream) : launch_down_wt<1>(p, cfg, stream);
 }
 
-size_t down_part_smem_bytes(const DownParams &p) { return part_layout(p).total; }
+int up1_threads(const UpParams &u) { return 32 * std::max(u.HB, (u.R + 31) / 32); }
 
-cudaError_t launch_down_part(const DownParams &p, const LaunchCfg &cfg, cudaStream_t stream)
+bool one_token_ok(const DownParams &d, const UpParams &u)
 {
-    const size_t smem = part_layout(p).total;
-    // One warp per row of the block, and at least one thread per 8-element
-    // vector of the chunk.
-    const int threads = std::max(32 * std::min(p.rows_per_block, 32), (p.KC / 8 + 31) / 32 * 32);
-    if (threads > 1024)
-        return cudaErrorInvalidConfiguration;
-    void (*k)(DownParams) = p.down.type == 0 ? hc_down_part_kernel<0> : hc_down_part_kernel<1>;
-    cudaError_t e = allow_smem(k, smem);
-    if (e != cudaSuccess)
-        return e;
-    const dim3 grid(p.S, (p.R + p.rows_per_block - 1) / p.rows_per_block, 1);
-    return launch_ex(k, grid, dim3(threads), smem, stream, 0, cfg.pdl, p);
+    if (d.M != 1 || d.S > kMaxCluster || d.C > 8 || u.HB > 32 || u.R > 1024)
+        return false;
+    if (down1_groups(d) * down1_group_threads(d) > 1024 || up1_threads(u) > 1024)
+        return false;
+    return down1_layout(d).total <= kSmemBudget && up1_layout(u).total <= kSmemBudget;
 }
 
+cudaError_t launch_one_token(const DownParams &d, const UpParams &u, const LaunchCfg &cfg, cudaStream_t stream)
+{
+    if (!one_token_ok(d, u))
+        return cudaErrorInvalidConfiguration;
+    void (*kd)(DownParams) = d.down.type == 0 ? hc_down1_kernel<0> : hc_down1_kernel<1>;
+    void (*ku)(UpParams) = u.up.type == 0 ? hc_up1_kernel<0> : hc_up1_kernel<1>;
+    const size_t sd = down1_layout(d).total, su = up1_layout(u).total;
+    cudaError_t e = allow_smem(kd, sd);
+    if (e == cudaSuccess)
+        e = allow_smem(ku, su);
+    if (e != cudaSuccess)
+        return e;
+    const dim3 dgrid(d.S, (d.R + d.rows_per_block - 1) / d.rows_per_block, 1);
+    e = launch_ex(kd, dgrid, dim3(down1_groups(d) * down1_group_threads(d)), sd, stream, 0, cfg.pdl, d);
+    if (e != cudaSuccess)
+        return e;
+    return launch_ex(ku, dim3((u.H + u.HB - 1) / u.HB), dim3(up1_threads(u)), su, stream, 0, cfg.pdl, u);
+}
 
 cudaError_t launch_up(const UpParams &p, const LaunchCfg &cfg, cudaStream_t stream)
 {
@@ -968,6 +1187,9 @@ cudaError_t launch_inject(const InjectParams &p, const LaunchCfg &cfg, cudaStrea
     long blocks = (nvec + threads - 1) / threads;
     blocks = std::min<long>(blocks, (long)cfg.sm_count * 8);
     blocks = std::max<long>(blocks, 1);
+    const cudaError_t e = allow_smem(hc_inject_kernel, 0);
+    if (e != cudaSuccess)
+        return e;
     return launch_ex(hc_inject_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, 0, cfg.pdl, p);
 }
 

@@ -40,7 +40,7 @@ struct DownParams {
     const uint16_t *inj_out;  // bf16 [M][H], or nullptr
     const float *inj_gate;    // token m's previous gates at inj_gate + m * inj_stride
     long inj_stride;
-    // One-token path (launch_down_part): per-chunk partial dots [S][R] and
+    // One-token path (launch_one_token): per-chunk partial dots [S][R] and
     // per-chunk sums of squares [S], left in the workspace for the up kernel.
     float *part1;
     float *ssq1;
@@ -66,7 +66,7 @@ struct UpParams {
     const uint16_t *inj_out;
     const float *inj_gate;
     long inj_stride;
-    // One-token path: when part1 is set, every CTA forms inv_rms, act and the
+    // One-token path (launch_one_token): every CTA forms inv_rms, act and the
     // gates itself from the down kernel's per-chunk partials (fixed order);
     // CTA 0 also writes them out (act / inv_rms to the workspace, gates).
     const float *part1;       // [S][R]
@@ -107,10 +107,11 @@ int down_threads(const DownParams &p);
 int up_threads(const UpParams &p);
 
 cudaError_t launch_down(const DownParams &p, const LaunchCfg &cfg, cudaStream_t stream);
-// One token (M == 1): the split-K down kernel without a cluster; it writes
-// per-chunk partials (p.part1, p.ssq1) that the up kernel reduces.
-size_t down_part_smem_bytes(const DownParams &p);
-cudaError_t launch_down_part(const DownParams &p, const LaunchCfg &cfg, cudaStream_t stream);
+// One token (M == 1): hc_down1_kernel leaves per-chunk partials in d.part1 /
+// d.ssq1 and hc_up1_kernel reduces them (u.part1 / u.ssq1 point at the same
+// buffers). one_token_ok says whether a shape fits these kernels' limits.
+bool one_token_ok(const DownParams &d, const UpParams &u);
+cudaError_t launch_one_token(const DownParams &d, const UpParams &u, const LaunchCfg &cfg, cudaStream_t stream);
 
 cudaError_t launch_up(const UpParams &p, const LaunchCfg &cfg, cudaStream_t stream);
 cudaError_t launch_inject(const InjectParams &p, const LaunchCfg &cfg, cudaStream_t stream);

@@ -561,6 +561,9 @@ cudaError_t allow_smem_tc(K kernel)
     if (done.count(key))
         return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemLimit);
+    if (e == cudaSuccess)  // same carveout as every other kernel of the library (co-residency)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess)
         done.insert(key);
     return e;
@@ -587,6 +590,7 @@ cudaError_t launch_tc_call(const TcCall &t, cudaStream_t stream)
     cudaError_t e;
     if ((e = allow_smem_tc(hc_tc_down_kernel)) != cudaSuccess) return e;
     if ((e = allow_smem_tc(hc_tc_up_kernel)) != cudaSuccess) return e;
+    if ((e = allow_smem_tc(hc_tc_reduce_kernel)) != cudaSuccess) return e;
     const int ntiles = (d.M + d.NT - 1) / d.NT;
     e = launch_tc(hc_tc_down_kernel, dim3(d.CS, d.C * d.RT, ntiles), dim3(kThreads),
                   tc_down_smem(d.NT, d.n_stages), stream, d.CS, d, map_d, map_i);

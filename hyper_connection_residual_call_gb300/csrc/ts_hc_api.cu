@@ -365,11 +365,9 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
 
     const tshc::LaunchCfg cfg{dev.sm_count, true};
     cudaError_t e;
-    // One token: the down kernel leaves per-chunk partials and the up kernel
-    // reduces them, so neither kernel waits on another CTA.
-    const bool one_token = M == 1 && d.KC / 8 <= 1024 && d.S <= kPart1Chunks && d.R <= 768 &&
-                           tshc::down_part_smem_bytes(d) <= tshc::kSmemBudget;
-    if (one_token) {
+    if (M == 1) {
+        // One token: the down kernel leaves per-chunk partials and the up
+        // kernel reduces them, so neither kernel waits on another CTA.
         d.part1 = reinterpret_cast<float *>(wsb + wl.part1);
         d.ssq1 = reinterpret_cast<float *>(wsb + wl.ssq1);
         u.part1 = d.part1;
@@ -381,10 +379,14 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         u.act_out = act;
         u.inv_out = inv_rms;
         u.gate = inject ? inject_w : nullptr;
-        e = tshc::launch_down_part(d, cfg, stream);
-    } else {
-        e = tshc::launch_down(d, cfg, stream);
+        if (d.S <= kPart1Chunks && tshc::one_token_ok(d, u)) {
+            e = tshc::launch_one_token(d, u, cfg, stream);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "launching the one-token kernels");
+            return TS_OK;
+        }
     }
+    e = tshc::launch_down(d, cfg, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "launching the down kernel");
     e = tshc::launch_up(u, cfg, stream);
