@@ -140,6 +140,39 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+// ---- packed fp32x2 arithmetic (two IEEE fp32 FMAs in one instruction) ----
+
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+// A bf16 pair (element 2i in the low half of the word) as an fp32 pair.
+__device__ __forceinline__ uint64_t bf16x2_as_f32x2(uint32_t w)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w << 16), "r"(w & 0xffff0000u));
+    return r;
+}
+
+// d = a * b + c, lane-wise, round to nearest.
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// Sum of the two lanes: low + high.
+__device__ __forceinline__ float f32x2_sum(uint64_t v)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo + hi;
+}
+
 __device__ __forceinline__ void record_timeout(unsigned *status)
 {
     if (status)
@@ -670,7 +703,6 @@ __global__ void __launch_bounds__(1024, 1) hc_down1_kernel(const DownParams p)
     const int grp = tid / tpg, v = tid % tpg;
     const int gr0 = grp * rpg, gnr = max(0, min(rpg, nrows - gr0));
 
-    pdl_launch_dependents();
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_fence_init();
@@ -719,6 +751,12 @@ __global__ void __launch_bounds__(1024, 1) hc_down1_kernel(const DownParams p)
             gt = p.inj_gate[k0 / p.H];
         }
     }
+    // Only now let the up kernel launch: (1) it reads the residual and the
+    // previous gates before its own dependency wait, which is safe once every
+    // CTA of this kernel has passed its wait (everything earlier in the
+    // stream has completed); (2) its weight stream, which starts about a
+    // microsecond later, then no longer competes with these residual loads.
+    pdl_launch_dependents();
     const bool timed_out = !mbar_wait_bounded(bar, 0);
     if (timed_out)
         record_timeout(p.status);
@@ -742,30 +780,36 @@ __global__ void __launch_bounds__(1024, 1) hc_down1_kernel(const DownParams p)
         }
     }
 
+    // Even and odd inputs accumulate in the two lanes of a packed fp32 pair.
+    uint64_t xp[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        xp[e] = f32x2(x[2 * e], x[2 * e + 1]);
     float acc[kRowsPerGroup];
 #pragma unroll
     for (int j = 0; j < kRowsPerGroup; ++j) {
         acc[j] = 0.f;
         if (has_v && j < gnr) {
             const unsigned char *wr = w_s + (size_t)(gr0 + j) * seg;
-            float wf[8];
+            uint64_t a = 0;
             if constexpr (WT == 0) {
-                unpack_bf16x8(*reinterpret_cast<const uint4 *>(wr + v * 16), wf);
+                const uint4 wq = *reinterpret_cast<const uint4 *>(wr + v * 16);
+                a = ffma2(bf16x2_as_f32x2(wq.x), xp[0], a);
+                a = ffma2(bf16x2_as_f32x2(wq.y), xp[1], a);
+                a = ffma2(bf16x2_as_f32x2(wq.z), xp[2], a);
+                a = ffma2(bf16x2_as_f32x2(wq.w), xp[3], a);
             } else {
                 const uint32_t codes = *reinterpret_cast<const uint32_t *>(wr + v * 4);
                 const float *sb = sb_s + 2 * ((gr0 + j) * ng + (v * 8) / p.down.group);
-                const float sc = sb[0], bi = sb[1];
+                const uint64_t sc = f32x2(sb[0], sb[0]), bi = f32x2(sb[1], sb[1]);
 #pragma unroll
-                for (int n = 0; n < 8; ++n)
-                    wf[n] = fmaf((float)((codes >> (4 * n)) & 0xFu), sc, bi);
+                for (int e = 0; e < 4; ++e) {
+                    const uint64_t q = f32x2((float)((codes >> (8 * e)) & 0xFu),
+                                             (float)((codes >> (8 * e + 4)) & 0xFu));
+                    a = ffma2(ffma2(q, sc, bi), xp[e], a);
+                }
             }
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                a0 = fmaf(wf[e], x[e], a0);
-                a1 = fmaf(wf[e + 1], x[e + 1], a1);
-            }
-            acc[j] = a0 + a1;
+            acc[j] = f32x2_sum(a);
         }
     }
     const float rsum = warp_transpose_sum8(acc, lane);
@@ -794,7 +838,7 @@ __global__ void __launch_bounds__(1024, 1) hc_down1_kernel(const DownParams p)
 }
 
 struct Up1Smem {
-    size_t bar, w, sb, act, invq, inv, total;
+    size_t bar, w, sb, act, ssq, invq, inv, total;
 };
 
 __host__ __device__ inline Up1Smem up1_layout(const UpParams &p)
@@ -806,14 +850,16 @@ __host__ __device__ inline Up1Smem up1_layout(const UpParams &p)
     s.w = 128;
     s.sb = round_up_sz(s.w + row * p.C * p.HB, 128);
     s.act = round_up_sz(s.sb + sizeof(float) * 2 * (size_t)ng * p.C * p.HB, 128);
-    s.invq = round_up_sz(s.act + sizeof(float) * (size_t)p.L, 128);
+    s.ssq = round_up_sz(s.act + sizeof(float) * (size_t)p.L, 128);
+    s.invq = round_up_sz(s.ssq + sizeof(float) * kMaxCluster, 16);
     s.inv = round_up_sz(s.invq + sizeof(float) * kMaxCluster, 16);
     s.total = round_up_sz(s.inv + sizeof(float) * kMaxCluster, 128);
     return s;
 }
 
-template <int WT>
-__global__ void __launch_bounds__(1024) hc_up1_kernel(const UpParams p)
+// CC: the stream count when it is a compile-time constant (4), else 0.
+template <int WT, int CC>
+__global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     const Up1Smem lay = up1_layout(p);
@@ -821,6 +867,7 @@ __global__ void __launch_bounds__(1024) hc_up1_kernel(const UpParams p)
     const unsigned char *w_s = smem + lay.w;
     float *sb_s = reinterpret_cast<float *>(smem + lay.sb);
     float *act_s = reinterpret_cast<float *>(smem + lay.act);
+    float *ssq_s = reinterpret_cast<float *>(smem + lay.ssq);    // sum of squares of chunk q
     float *invq_s = reinterpret_cast<float *>(smem + lay.invq);  // inv_rms of chunk q's stream
     float *inv_s = reinterpret_cast<float *>(smem + lay.inv);
 
@@ -831,13 +878,12 @@ __global__ void __launch_bounds__(1024) hc_up1_kernel(const UpParams p)
     const size_t row_bytes = WT == 0 ? (size_t)L * 2 : (size_t)L / 2;
     const int ng = WT == 0 ? 1 : L / p.up.group;
 
-    pdl_launch_dependents();
+    // Thread 0 initialises the barrier and issues the weight copies at once;
+    // no other thread touches the barrier before the first block-wide
+    // barrier below.
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_fence_init();
-    }
-    __syncthreads();
-    if (tid == 0) {
         mbar_arrive_expect_tx(bar, (uint32_t)(row_bytes * hb * p.C));
         for (int c = 0; c < p.C; ++c)
             bulk_copy_g2s(smem + lay.w + (size_t)c * HB * row_bytes,
@@ -860,37 +906,49 @@ __global__ void __launch_bounds__(1024) hc_up1_kernel(const UpParams p)
     const bool h_ok = hl < hb;
     const int hc = lane >> 2;
     const bool holder = h_ok && (lane & 3) == 0 && hc < p.C;
-    float gval = 0.f;  // g is a weight: read before the dependency wait
-    if (holder)
+    // Read before the dependency wait: g (a weight), and this lane's residual
+    // element with the previous gate -- the down kernel lets this kernel
+    // launch only after all its CTAs passed their own wait, so these are
+    // final; they are read from L2 (.cg). The residual is written back only
+    // after the wait, when the down kernel has finished reading it.
+    float gval = 0.f, rv = 0.f, ov = 0.f, gp = 0.f;
+    if (holder) {
         gval = __bfloat162float(__ushort_as_bfloat16(p.g[hc * p.H + h]));
+        rv = __bfloat162float(__ushort_as_bfloat16(__ldcg(p.raw + hc * p.H + h)));
+        if (p.raw_out) {
+            ov = __bfloat162float(__ushort_as_bfloat16(__ldcg(p.inj_out + h)));
+            gp = __ldcg(p.inj_gate + hc);
+        }
+    }
 
-    pdl_wait();  // partials from the down kernel; the residual from before it
+    pdl_wait();  // the partials come from the down kernel
 
-    // One round of loads: partials (thread k owns down row k), sums of
-    // squares, and this lane's residual element with the previous gate.
+    // One round of loads: partials (thread k owns down row k) and the chunks'
+    // sums of squares (thread q < S owns chunk q).
     const int k = tid;  // the host launches at least R threads
     float pv[kMaxCluster];
 #pragma unroll
     for (int q = 0; q < kMaxCluster; ++q)
         pv[q] = (k < p.R && q < p.S) ? p.part1[(size_t)q * p.R + k] : 0.f;
-    float rv = 0.f, ov = 0.f, gp = 0.f;
-    if (holder) {
-        rv = __bfloat162float(__ushort_as_bfloat16(p.raw[hc * p.H + h]));
-        if (p.raw_out) {
-            ov = __bfloat162float(__ushort_as_bfloat16(p.inj_out[h]));
-            gp = p.inj_gate[hc];
-        }
-    }
-    if (tid < p.C) {
+    const float sq = tid < p.S ? p.ssq1[tid] : 0.f;
+    // The next kernel's weight stream starts about a microsecond after this
+    // trigger, once these loads are on their way.
+    pdl_launch_dependents();
+    if (tid < p.S)
+        ssq_s[tid] = sq;
+    __syncthreads();
+    if (tid < p.S) {  // chunk q = tid: inv_rms of its stream (the stream's chunks in order)
+        const int c = tid / p.sps;
         float t = 0.f;
         for (int j = 0; j < p.sps; ++j)
-            t += p.ssq1[tid * p.sps + j];
+            t += ssq_s[c * p.sps + j];
         const float iv = 1.0f / sqrtf(t / (float)p.H + p.eps);
-        inv_s[tid] = iv;
-        for (int j = 0; j < p.sps; ++j)
-            invq_s[tid * p.sps + j] = iv;
-        if (blockIdx.x == 0)
-            p.inv_out[tid] = iv;
+        invq_s[tid] = iv;
+        if (tid % p.sps == 0) {
+            inv_s[c] = iv;
+            if (blockIdx.x == 0)
+                p.inv_out[c] = iv;
+        }
     }
     __syncthreads();
     if (k < p.R) {
@@ -917,31 +975,48 @@ __global__ void __launch_bounds__(1024) hc_up1_kernel(const UpParams p)
         float acc[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) acc[c] = 0.f;
-        for (int v = lane; v < L / 8; v += 32) {
-            const float4 xa = *reinterpret_cast<const float4 *>(act_s + v * 8);
-            const float4 xb = *reinterpret_cast<const float4 *>(act_s + v * 8 + 4);
+        if constexpr (WT == 0) {
+            // Lane owns the bf16 pairs j = lane + 32 i of each of the C rows (the
+            // lanes stay balanced for any L); the act pair is read once per j.
+            constexpr int NC = CC > 0 ? CC : 8;
+            uint64_t a2[NC];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                if (c < p.C) {
-                    const int srow = c * HB + hl;
-                    const unsigned char *wr = w_s + (size_t)srow * row_bytes;
-                    float wf[8];
-                    if constexpr (WT == 0) {
-                        unpack_bf16x8(*reinterpret_cast<const uint4 *>(wr + v * 16), wf);
-                    } else {
-                        const uint32_t codes = *reinterpret_cast<const uint32_t *>(wr + v * 4);
+            for (int c = 0; c < NC; ++c) a2[c] = 0;
+            const uint32_t *wr = reinterpret_cast<const uint32_t *>(w_s) + (size_t)hl * (L / 2);
+            const size_t cstride = (size_t)HB * (L / 2);  // words between streams' rows
+#pragma unroll 2
+            for (int j = lane; j < L / 2; j += 32) {
+                const uint64_t xpair = *reinterpret_cast<const uint64_t *>(act_s + 2 * j);
+#pragma unroll
+                for (int c = 0; c < NC; ++c)
+                    if (CC > 0 || c < p.C)
+                        a2[c] = ffma2(bf16x2_as_f32x2(wr[c * cstride + j]), xpair, a2[c]);
+            }
+#pragma unroll
+            for (int c = 0; c < NC; ++c) acc[c] = f32x2_sum(a2[c]);
+        } else {
+            for (int v = lane; v < L / 8; v += 32) {
+                const float4 xa = *reinterpret_cast<const float4 *>(act_s + v * 8);
+                const float4 xb = *reinterpret_cast<const float4 *>(act_s + v * 8 + 4);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    if (c < p.C) {
+                        const int srow = c * HB + hl;
+                        const uint32_t codes =
+                            *reinterpret_cast<const uint32_t *>(w_s + (size_t)srow * row_bytes + v * 4);
                         const float *sb = sb_s + 2 * (srow * ng + (v * 8) / p.up.group);
                         const float sc = sb[0], bi = sb[1];
+                        float wf[8];
 #pragma unroll
                         for (int n = 0; n < 8; ++n)
                             wf[n] = fmaf((float)((codes >> (4 * n)) & 0xFu), sc, bi);
+                        float a0 = acc[c], a1 = 0.f;
+                        a0 = fmaf(wf[0], xa.x, a0); a1 = fmaf(wf[1], xa.y, a1);
+                        a0 = fmaf(wf[2], xa.z, a0); a1 = fmaf(wf[3], xa.w, a1);
+                        a0 = fmaf(wf[4], xb.x, a0); a1 = fmaf(wf[5], xb.y, a1);
+                        a0 = fmaf(wf[6], xb.z, a0); a1 = fmaf(wf[7], xb.w, a1);
+                        acc[c] = a0 + a1;
                     }
-                    float a0 = acc[c], a1 = 0.f;
-                    a0 = fmaf(wf[0], xa.x, a0); a1 = fmaf(wf[1], xa.y, a1);
-                    a0 = fmaf(wf[2], xa.z, a0); a1 = fmaf(wf[3], xa.w, a1);
-                    a0 = fmaf(wf[4], xb.x, a0); a1 = fmaf(wf[5], xb.y, a1);
-                    a0 = fmaf(wf[6], xb.z, a0); a1 = fmaf(wf[7], xb.w, a1);
-                    acc[c] = a0 + a1;
                 }
             }
         }
@@ -1161,7 +1236,9 @@ cudaError_t launch_one_token(const DownParams &d, const UpParams &u, const Launc
     if (!one_token_ok(d, u))
         return cudaErrorInvalidConfiguration;
     void (*kd)(DownParams) = d.down.type == 0 ? hc_down1_kernel<0> : hc_down1_kernel<1>;
-    void (*ku)(UpParams) = u.up.type == 0 ? hc_up1_kernel<0> : hc_up1_kernel<1>;
+    void (*ku)(UpParams) = u.up.type != 0 ? hc_up1_kernel<1, 0>
+                           : u.C == 4     ? hc_up1_kernel<0, 4>
+                                          : hc_up1_kernel<0, 0>;
     const size_t sd = down1_layout(d).total, su = up1_layout(u).total;
     cudaError_t e = allow_smem(kd, sd);
     if (e == cudaSuccess)
