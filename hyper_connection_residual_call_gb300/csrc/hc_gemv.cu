@@ -825,13 +825,17 @@ __global__ void __launch_bounds__(1024, 1) hc_down1_kernel(const DownParams p)
         float t = 0.f;
         for (int w = 0; w < wpg; ++w)
             t += red_s[(g * wpg + w) * (kRowsPerGroup + 1) + j];
-        p.part1[(size_t)s * p.R + r0 + tid] = t;
+#pragma unroll
+        for (int c = 0; c < kPartCopies; ++c)
+            p.part1[c * p.part1_stride + (size_t)s * p.R + r0 + tid] = t;
     }
     if (blockIdx.y == 0 && tid == blockDim.x - 1) {  // every group saw the same inputs: use group 0
         float t = 0.f;
         for (int w = 0; w < wpg; ++w)
             t += red_s[w * (kRowsPerGroup + 1) + kRowsPerGroup];
-        p.ssq1[s] = t;
+#pragma unroll
+        for (int c = 0; c < kPartCopies; ++c)
+            p.ssq1[c * kSsqStride + s] = t;
     }
     if (timed_out)  // do not leave with a copy into this CTA's shared memory in flight
         mbar_wait_bounded(bar, 0);
@@ -926,11 +930,14 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
     // One round of loads: partials (thread k owns down row k) and the chunks'
     // sums of squares (thread q < S owns chunk q).
     const int k = tid;  // the host launches at least R threads
+    const int copy = blockIdx.x % kPartCopies;
+    const float *part = p.part1 + copy * p.part1_stride;
+    const float *ssq = p.ssq1 + copy * kSsqStride;
     float pv[kMaxCluster];
 #pragma unroll
     for (int q = 0; q < kMaxCluster; ++q)
-        pv[q] = (k < p.R && q < p.S) ? p.part1[(size_t)q * p.R + k] : 0.f;
-    const float sq = tid < p.S ? p.ssq1[tid] : 0.f;
+        pv[q] = (k < p.R && q < p.S) ? part[(size_t)q * p.R + k] : 0.f;
+    const float sq = tid < p.S ? ssq[tid] : 0.f;
     // The next kernel's weight stream starts about a microsecond after this
     // trigger, once these loads are on their way.
     pdl_launch_dependents();

@@ -41,10 +41,17 @@ struct DownParams {
     const float *inj_gate;    // token m's previous gates at inj_gate + m * inj_stride
     long inj_stride;
     // One-token path (launch_one_token): per-chunk partial dots [S][R] and
-    // per-chunk sums of squares [S], left in the workspace for the up kernel.
+    // per-chunk sums of squares [S], left in the workspace for the up kernel,
+    // written kPartCopies times (copy c at part1 + c * part1_stride and at
+    // ssq1 + c * kSsqStride) so that fewer up CTAs read each L2 line.
     float *part1;
     float *ssq1;
+    long part1_stride;
 };
+
+// Copies of the one-token partials; up CTA b reads copy b % kPartCopies.
+constexpr int kPartCopies = 8;
+constexpr long kSsqStride = 64;  // floats between the copies of the sums of squares
 
 // Up projection + sigmoid + mean mix: CTA b owns h in [b*HB, b*HB + HB) of
 // every stream, i.e. up rows {c*H + h}.
@@ -69,8 +76,9 @@ struct UpParams {
     // One-token path (launch_one_token): every CTA forms inv_rms, act and the
     // gates itself from the down kernel's per-chunk partials (fixed order);
     // CTA 0 also writes them out (act / inv_rms to the workspace, gates).
-    const float *part1;       // [S][R]
-    const float *ssq1;        // [S]
+    const float *part1;       // [S][R], kPartCopies copies part1_stride apart
+    const float *ssq1;        // [S], kPartCopies copies kSsqStride apart
+    long part1_stride;
     int S, sps, R;
     float eps;
     float *act_out;           // [L]

@@ -167,8 +167,8 @@ WsLayout ws_layout(int M, int H, int C, int L)
     w.total = w.act + align256(sizeof(float) * (size_t)M * L);
     if (M == 1) {  // one token: the down kernel leaves partials, the up kernel reduces them
         w.part1 = w.total;
-        w.ssq1 = w.part1 + align256(sizeof(float) * kPart1Chunks * ((size_t)L + C));
-        w.total = w.ssq1 + align256(sizeof(float) * kPart1Chunks);
+        w.ssq1 = w.part1 + tshc::kPartCopies * align256(sizeof(float) * kPart1Chunks * ((size_t)L + C));
+        w.total = w.ssq1 + tshc::kPartCopies * sizeof(float) * tshc::kSsqStride;
     }
     if (tc_cluster_size(M, H, C, L) > 0) {
         const size_t R = (size_t)L + C;
@@ -370,8 +370,10 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         // kernel reduces them, so neither kernel waits on another CTA.
         d.part1 = reinterpret_cast<float *>(wsb + wl.part1);
         d.ssq1 = reinterpret_cast<float *>(wsb + wl.ssq1);
+        d.part1_stride = (long)(align256(sizeof(float) * kPart1Chunks * ((size_t)L + C)) / sizeof(float));
         u.part1 = d.part1;
         u.ssq1 = d.ssq1;
+        u.part1_stride = d.part1_stride;
         u.S = d.S;
         u.sps = d.sps;
         u.R = d.R;

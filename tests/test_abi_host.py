@@ -37,8 +37,9 @@ def test_exports_every_declared_symbol(lib):
 
 def test_workspace_size_and_layout(lib):
     a256 = lambda n: (n + 255) // 256 * 256
-    # one token: inv_rms, act, and up to 8 chunks of per-row partials and sums of squares
-    assert B.ts_hc_workspace_bytes(1, H, C, L) == 256 + 1280 + a256(4 * 8 * (L + C)) + a256(4 * 8)
+    # one token: inv_rms, act, and 8 copies of up to 8 chunks of per-row partials and of
+    # the chunks' sums of squares (64-float stride)
+    assert B.ts_hc_workspace_bytes(1, H, C, L) == 256 + 1280 + 8 * a256(4 * 8 * (L + C)) + 8 * 4 * 64
     # from 64 tokens the tensor-core path adds per-stream partials [C][L+C][M] fp32,
     # sums of squares [C][M] fp32 and the bf16 hi/lo activations [M][L] x 2
     a256 = lambda n: (n + 255) // 256 * 256
