@@ -107,6 +107,10 @@ __host__ __device__ inline UpSmem up_layout(const UpParams &p, int mt)
 }
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+// Shorter-latency sigmoid for the one-token kernels' dependency chain: the
+// fast exponential and reciprocal intrinsics (relative error ~1e-6, far
+// inside the 1e-3 bar on fp32 intermediates).
+__device__ __forceinline__ float sigmoid_fast(float x) { return __frcp_rn(1.0f + __expf(-x)); }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&f)[8])
 {
@@ -949,7 +953,7 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
         float t = 0.f;
         for (int j = 0; j < p.sps; ++j)
             t += ssq_s[c * p.sps + j];
-        const float iv = 1.0f / sqrtf(t / (float)p.H + p.eps);
+        const float iv = rsqrtf(fmaf(t, p.inv_H, p.eps));
         invq_s[tid] = iv;
         if (tid % p.sps == 0) {
             inv_s[c] = iv;
@@ -965,18 +969,29 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
             if (q < p.S) z = fmaf(invq_s[q], pv[q], z);
         const float zc = z * p.inv_C;
         if (k < L) {
-            const float a = zc * sigmoidf_(zc);
+            const float a = zc * sigmoid_fast(zc);
             act_s[k] = a;
             if (blockIdx.x == 0)
                 p.act_out[k] = a;
         } else if (blockIdx.x == 0 && p.gate) {
-            p.gate[k - L] = 2.0f * sigmoidf_(zc);
+            p.gate[k - L] = 2.0f * sigmoid_fast(zc);
         }
     }
     const bool timed_out = !mbar_wait_bounded(bar, 0);
     if (timed_out)
         record_timeout(p.status);
     __syncthreads();
+
+    // This lane's residual element (with the fused inject-add written back)
+    // and its normed value, ready before the dots.
+    float nvh = 0.f;
+    if (holder) {
+        if (p.raw_out) {
+            rv = __bfloat162float(__float2bfloat16_rn(fmaf(ov, gp, rv)));
+            p.raw_out[hc * p.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(rv));
+        }
+        nvh = rv * inv_s[hc] * gval;
+    }
 
     if (h_ok) {  // warp-uniform
         float acc[8];
@@ -1028,14 +1043,7 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
             }
         }
         const float d = warp_transpose_sum8(acc, lane);
-        float term = 0.f;
-        if (holder) {
-            if (p.raw_out) {
-                rv = __bfloat162float(__float2bfloat16_rn(fmaf(ov, gp, rv)));
-                p.raw_out[hc * p.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(rv));
-            }
-            term = sigmoidf_(d) * (rv * inv_s[hc] * gval);
-        }
+        float term = holder ? sigmoid_fast(d) * nvh : 0.f;
         term += __shfl_xor_sync(0xffffffffu, term, 4);
         term += __shfl_xor_sync(0xffffffffu, term, 8);
         term += __shfl_xor_sync(0xffffffffu, term, 16);

@@ -80,7 +80,7 @@ struct UpParams {
     const float *ssq1;        // [S], kPartCopies copies kSsqStride apart
     long part1_stride;
     int S, sps, R;
-    float eps;
+    float eps, inv_H;
     float *act_out;           // [L]
     float *inv_out;           // [C]
     float *gate;              // gates (R > L), or nullptr

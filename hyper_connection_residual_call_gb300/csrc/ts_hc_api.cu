@@ -378,6 +378,7 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         u.sps = d.sps;
         u.R = d.R;
         u.eps = eps;
+        u.inv_H = 1.0f / (float)H;
         u.act_out = act;
         u.inv_out = inv_rms;
         u.gate = inject ? inject_w : nullptr;
