@@ -17,6 +17,12 @@ Inputs are resident in HBM when the timed region starts; ``e2e`` repeats the
 headline with the step's inputs copied from pinned host memory and its
 results read back inside the timed region.
 
+``other_configs`` (skipped with --no-configs) times the rest of the workload
+family the same way, each over distinct weight sets: the M=128 prefill
+micro-batch (attn_hc + mlp_hc per batch, tensor-core path), the INT4-affine
+full shape at M=1 and M=64, and the 40-layer stack (entry replication, 80
+fused calls, exit mixer) at M=1 and M=16.
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints one JSON line (rank 0). Under torchrun each rank runs an independent
@@ -261,6 +267,127 @@ def parity_check(B, w0_d, w0, raw0, out0):
     return {"checked": "full-shape call + inject-add vs fp64 oracle", "worst_err_over_limit": max(res.values())}
 
 
+def bytes_per_call(M: int, weight_bytes: int, inject: bool = True) -> int:
+    """Algorithmic bytes of one call (+ its inject-add) on M tokens: weights once,
+    raw read, mixed written, gates written; inject-add: raw read + written, the
+    sublayer output read, the gates read."""
+    b = weight_bytes + 2 * M * C * H + 2 * M * H
+    if inject:
+        b += 4 * M * C + (2 * 2 * M * C * H + 2 * M * H + 4 * M * C)
+    return b
+
+
+def measure_other_configs(B, inputs, torch, dev, stream, sets_bf16, peak):
+    """The workload family's other configurations, each a CUDA graph over
+    distinct weight sets (every pass is larger than the 129 MB L2), timed with
+    CUDA events after three warm-up replays: the M=128 prefill micro-batch
+    (tensor-core path), the INT4-affine full shape at M=1 and M=64, and the
+    40-layer stack (entry replication, 80 fused calls, exit mixer) at M=1 and
+    M=16."""
+    out = {}
+
+    def graph_ms(body, reps):
+        with torch.cuda.stream(stream):
+            body()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            body()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def chain(raw, outs, gates, sets, n_calls, mixed, ws, slots):
+        """n_calls fused calls; call i writes its gates to slot i % 2 of `gates`."""
+        def body():
+            for i in range(n_calls):
+                w = sets[i % len(sets)]
+                sl, st = slots[i % 2]
+                if i == 0:
+                    B.hc_call(raw, w, H=H, C=C, mixed=mixed, inject_w=sl, inject_stride=st, ws=ws)
+                else:
+                    psl, pst = slots[(i - 1) % 2]
+                    B.hc_inject_call(raw, outs[(i - 1) % len(outs)], psl, w, H=H, C=C, prev_inject_stride=pst,
+                                     mixed=mixed, inject_w=sl, inject_stride=st, ws=ws)
+            psl, pst = slots[(n_calls - 1) % 2]
+            B.hc_inject_add(raw, outs[(n_calls - 1) % len(outs)], psl, H=H, C=C, inject_stride=pst)
+        return body
+
+    def record(name, Mx, ms, n_calls, bytes_call, extra=None):
+        gbs = bytes_call * n_calls / (ms / 1e3) / 1e9
+        out[name] = {"M": Mx, "calls_per_s": n_calls / (ms / 1e3), "tokens_per_s": Mx * n_calls / (ms / 1e3),
+                     "us_per_call": 1e3 * ms / n_calls, "bytes_per_call": bytes_call, "hbm_gbs": gbs,
+                     "frac": gbs / peak, **(extra or {})}
+
+    # Prefill micro-batch: M = 128, attn_hc + inject then mlp_hc + inject per batch,
+    # token t's gates at t*2C (attn) and t*2C + C (mlp).
+    Mp = 128
+    raw = inputs.make_residual(Mp, H, C, 2).to(dev)
+    outs = [inputs.make_sublayer_out(Mp, H, 2, i).to(dev) for i in range(4)]
+    gates = torch.zeros((Mp, 2 * C), dtype=torch.float32, device=dev)
+    slots = [(gates[:, :C], 2 * C), (gates[:, C:], 2 * C)]
+    mixed = torch.empty((Mp, H), dtype=torch.bfloat16, device=dev)
+    ws = B.workspace(Mp, H, C, L, dev)
+    n = 2 * len(sets_bf16)
+    ms = graph_ms(chain(raw, outs, gates, sets_bf16, n, mixed, ws, slots), 5)
+    record("prefill_m128_bf16", Mp, ms, n, bytes_per_call(Mp, sets_bf16[0].nbytes),
+           {"path": "tensor-core (tcgen05) kernels", "sequence": "attn_hc + mlp_hc per batch, fused inject"})
+    del raw, outs, ws, mixed
+
+    # INT4-affine (group 64), full shape, M = 1 and M = 64.
+    sets_q = [inputs.make_hc_weights(H, C, L, 4, i, kind="int4").to(dev) for i in range(len(sets_bf16))]
+    for Mq in (1, 64):
+        raw = inputs.make_residual(Mq, H, C, 4).to(dev)
+        outs = [inputs.make_sublayer_out(Mq, H, 4, i).to(dev) for i in range(4)]
+        gates = torch.zeros((2, Mq, C), dtype=torch.float32, device=dev)
+        slots = [(gates[0], C), (gates[1], C)]
+        mixed = torch.empty((Mq, H), dtype=torch.bfloat16, device=dev)
+        ws = B.workspace(Mq, H, C, L, dev)
+        n = 4 * len(sets_q) if Mq == 1 else 2 * len(sets_q)
+        ms = graph_ms(chain(raw, outs, gates, sets_q, n, mixed, ws, slots), 5)
+        record(f"int4_m{Mq}", Mq, ms, n, bytes_per_call(Mq, sets_q[0].nbytes),
+               {"path": "CUDA-core one-token kernels" if Mq == 1 else "CUDA-core cluster split-K kernels"})
+    del sets_q
+
+    # Full-depth stack: entry replication, 40 x (attn_hc + inject, mlp_hc + inject), exit mixer.
+    n_layers = 40
+    mixer_w = inputs.HCWeights(sets_bf16[0].g, sets_bf16[0].down, sets_bf16[0].up, None)
+    for Ms in (1, 16):
+        emb = inputs.make_embedding(Ms, H, 3).to(dev)
+        raw = torch.empty((Ms, C * H), dtype=torch.bfloat16, device=dev)
+        outs = [inputs.make_sublayer_out(Ms, H, 3, i).to(dev) for i in range(8)]
+        gates = torch.zeros((Ms, 2 * C), dtype=torch.float32, device=dev)
+        slots = [(gates[:, :C], 2 * C), (gates[:, C:], 2 * C)]
+        mixed = torch.empty((Ms, H), dtype=torch.bfloat16, device=dev)
+        final = torch.empty((Ms, H), dtype=torch.bfloat16, device=dev)
+        ws = B.workspace(Ms, H, C, L, dev)
+        calls = chain(raw, outs, gates, sets_bf16, 2 * n_layers, mixed, ws, slots)
+
+        def stack():
+            B.hc_replicate_entry(emb, C=C, raw=raw)
+            calls()
+            B.hc_mixer(raw, mixer_w, H=H, C=C, mixed=final, ws=ws)
+
+        ms = graph_ms(stack, 5)
+        wb = sets_bf16[0].nbytes
+        total = (2 * n_layers * bytes_per_call(Ms, wb) + bytes_per_call(Ms, mixer_w.nbytes, inject=False)
+                 + 2 * Ms * H + 2 * Ms * C * H)
+        gbs = total / (ms / 1e3) / 1e9
+        out[f"stack40_m{Ms}"] = {"M": Ms, "tokens_per_s": Ms / (ms / 1e3), "us_per_token_step": 1e3 * ms,
+                                 "bytes_per_step": total, "hbm_gbs": gbs, "frac": gbs / peak,
+                                 "calls_per_step": 2 * n_layers + 1}
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -285,7 +412,7 @@ def run_ours(args):
     outs = torch.stack([o.to(dev) for o in outs_h])          # [sets, M, H]
 
     parity = None
-    if rank == 0 and not args.profile_calls:
+    if rank == 0 and not (args.profile_calls or args.profile_prefill):
         parity = parity_check(B, sets[0], sets_h[0], raw_h, outs_h[0])
 
     raw = raw_h.to(dev)
@@ -313,6 +440,22 @@ def run_ours(args):
         B.hc_inject_add(raw, outs[last % WEIGHT_SETS], gates[last % 2], H=H, C=C)
 
     stream = torch.cuda.Stream(device=dev)
+    if args.profile_prefill:
+        # A short eager run of M-token calls (M=128 by default: the tensor-core
+        # path; --profile-int4 for INT4-affine weights) for a profiler.
+        Mp = args.profile_tokens
+        psets = sets if not args.profile_int4 else [
+            inputs.make_hc_weights(H, C, L, 4, i, kind="int4").to(dev) for i in range(8)]
+        rawp = inputs.make_residual(Mp, H, C, 2).to(dev)
+        mixedp = torch.empty((Mp, H), dtype=torch.bfloat16, device=dev)
+        wsp2 = B.workspace(Mp, H, C, L, dev)
+        with torch.cuda.stream(stream):
+            for i in range(args.profile_prefill):
+                B.hc_call(rawp, psets[i % len(psets)], H=H, C=C, mixed=mixedp, ws=wsp2)
+        stream.synchronize()
+        if rank == 0:
+            print(f"ran {args.profile_prefill} M={Mp} calls (profiling run)")
+        return
     if args.profile_calls:
         # A short eager chain of the fused call for a profiler that captures
         # single launches: no graphs, no timing, no JSON line.
@@ -393,6 +536,10 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     e2e_value = e2e_steps * CALLS_PER_STEP * ws / (ms_e2e / 1e3)
 
+    others = None
+    if rank == 0 and not args.no_configs:
+        others = measure_other_configs(B, inputs, torch, dev, stream, sets, peak)
+
     if rank == 0:
         base = cpu_baseline() if ws == 1 else None
         line = {
@@ -418,6 +565,7 @@ def run_ours(args):
             "gpu_launches": launches_per_step["fused"] * args.steps,
             "clocks": clocks,
             "cpu_baseline": base,
+            "other_configs": others,
             "parity": parity,
         }
         print(json.dumps(line), flush=True)
@@ -432,6 +580,12 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the timing of the other workload configurations")
+    ap.add_argument("--profile-prefill", type=int, default=0,
+                    help="run this many eager M-token calls and exit (for ncu captures)")
+    ap.add_argument("--profile-tokens", type=int, default=128, help="M for --profile-prefill")
+    ap.add_argument("--profile-int4", action="store_true", help="INT4-affine weights for --profile-prefill")
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="run this many eager fused calls of the workload and exit (for ncu captures)")
     args = ap.parse_args()

@@ -46,6 +46,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 }
 
 __device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
+// Sigmoid from the fast exponential and reciprocal intrinsics (relative error
+// ~1e-6, far inside the 1e-3 bar), for the per-element epilogues.
+__device__ __forceinline__ float sigm_fast(float x) { return __frcp_rn(1.0f + __expf(-x)); }
+
+__device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+    return v;
+}
 
 __device__ __forceinline__ void record_timeout(unsigned *status)
 {
@@ -72,7 +83,9 @@ struct TcSmem {
 };
 
 // Down kernel shared memory: ring of stages [A 16 KB | B_hi | B_lo], then the
-// per-token sums of squares, then barriers.
+// per-token sums of squares, then this CTA's chunk of g (bf16, at most
+// kMaxChunk elements), then barriers.
+constexpr int kMaxChunk = 2048;
 __host__ __device__ inline TcSmem down_tc_layout(int NT, int ns)
 {
     TcSmem s;
@@ -80,13 +93,22 @@ __host__ __device__ inline TcSmem down_tc_layout(int NT, int ns)
     s.b_bytes = NT * 128;
     s.stage_bytes = s.a_bytes + 2 * s.b_bytes;
     s.ring = 0;
-    s.extra = s.ring + ns * s.stage_bytes;          // ssq_s: NT floats
-    s.bars = s.extra + ((NT * 4 + 127) / 128) * 128;
+    s.extra = s.ring + ns * s.stage_bytes;          // ssq_s: NT floats, then g_s
+    s.bars = s.extra + ((NT * 4 + 127) / 128) * 128 + kMaxChunk * 2;
     s.total = s.bars + 8 * (3 * ns + 2) + 16;
     return s;
 }
 
-// Up kernel: ring, then raw tile [C][NT][HBt] bf16 and inv_rms tile [NT][C].
+// Up kernel: ring, then raw tile [C][NT][HBt] bf16, inv_rms tile [NT][C], and
+// for a fused inject-add the sublayer-output tile [NT][HBt] bf16 and the
+// previous gates [NT][C].
+__host__ __device__ inline uint32_t up_tc_raw_bytes(int NT, int C, int HBt)
+{
+    return ((C * NT * HBt * 2 + 1023) / 1024) * 1024;
+}
+__host__ __device__ inline uint32_t up_tc_small_bytes(int NT, int C) { return ((NT * C * 4 + 127) / 128) * 128; }
+__host__ __device__ inline uint32_t up_tc_out_bytes(int NT, int HBt) { return ((NT * HBt * 2 + 127) / 128) * 128; }
+
 __host__ __device__ inline TcSmem up_tc_layout(int NT, int ns, int C, int HBt)
 {
     TcSmem s;
@@ -95,9 +117,7 @@ __host__ __device__ inline TcSmem up_tc_layout(int NT, int ns, int C, int HBt)
     s.stage_bytes = s.a_bytes + 2 * s.b_bytes;
     s.ring = 0;
     s.extra = s.ring + ns * s.stage_bytes;
-    const uint32_t raw_bytes = ((C * NT * HBt * 2 + 1023) / 1024) * 1024;
-    const uint32_t inv_bytes = ((NT * C * 4 + 127) / 128) * 128;
-    s.bars = s.extra + raw_bytes + inv_bytes;
+    s.bars = s.extra + up_tc_raw_bytes(NT, C, HBt) + 2 * up_tc_small_bytes(NT, C) + up_tc_out_bytes(NT, HBt);
     s.total = s.bars + 8 * (3 * ns + 2) + 16;
     return s;
 }
@@ -113,6 +133,7 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
     const int NT = p.NT, NS = p.n_stages;
     const TcSmem lay = down_tc_layout(NT, NS);
     float *ssq_s = reinterpret_cast<float *>(smem + lay.extra);
+    uint16_t *g_s = reinterpret_cast<uint16_t *>(smem + lay.extra + ((NT * 4 + 127) / 128) * 128);
     uint64_t *full_a = reinterpret_cast<uint64_t *>(smem + lay.bars);
     uint64_t *full_b = full_a + NS;
     uint64_t *empty = full_b + NS;
@@ -152,6 +173,11 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
         tmem_alloc(tslot, ncols);
         tmem_relinquish();
     }
+    // g is a weight: this CTA's chunk goes to shared memory before the wait
+    // (read by the producers after this barrier; the TMA producer below runs
+    // ahead without any further block barrier).
+    for (int i = tid; i < p.chunk / 8; i += kThreads)
+        reinterpret_cast<uint4 *>(g_s)[i] = reinterpret_cast<const uint4 *>(p.g + k0)[i];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -186,27 +212,44 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
         const bool live = n < NT && m < p.M;
         const float inj_g = (live && p.inj_out) ? p.inj_gate[(size_t)m * p.inj_stride + c] : 0.f;
         float ssq = 0.f;
+        // This token's 64 residual (and sublayer-output) elements of K block
+        // kb + 1 are loaded while block kb is converted.
+        uint4 rnext[8], onext[8];
+        auto fetch = [&](int kb) {
+            const uint4 *rp = reinterpret_cast<const uint4 *>(p.raw + (size_t)(live ? m : 0) * p.W + k0 + kb * kKBlock);
+            const uint4 *op = p.inj_out ? reinterpret_cast<const uint4 *>(
+                p.inj_out + (size_t)(live ? m : 0) * p.H + q * p.chunk + kb * kKBlock) : nullptr;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                rnext[j] = live ? rp[j] : make_uint4(0, 0, 0, 0);
+                onext[j] = (live && p.inj_out) ? op[j] : make_uint4(0, 0, 0, 0);
+            }
+        };
+        if (n < NT)
+            fetch(0);
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % NS, u = kb / NS;
+            uint4 rcur[8], ocur[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                rcur[j] = rnext[j];
+                ocur[j] = onext[j];
+            }
+            if (n < NT && kb + 1 < KB)
+                fetch(kb + 1);
             if (u > 0 && !mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
             uint8_t *bhi = smem + lay.ring + s * lay.stage_bytes + lay.a_bytes;
             uint8_t *blo = bhi + lay.b_bytes;
             if (n < NT) {
-                const uint4 *rp = reinterpret_cast<const uint4 *>(p.raw + (size_t)(live ? m : 0) * p.W + k0 + kb * kKBlock);
-                const uint4 *gp = reinterpret_cast<const uint4 *>(p.g + k0 + kb * kKBlock);
+                const uint4 *gp = reinterpret_cast<const uint4 *>(g_s + kb * kKBlock);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
                     if (live) {
-                        const uint4 rv = rp[j], gv = gp[j];
+                        const uint4 rv = rcur[j], gv = gp[j];
                         const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
                         const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-                        uint32_t ow[4] = {0u, 0u, 0u, 0u};
-                        if (p.inj_out) {
-                            const uint4 ov = *reinterpret_cast<const uint4 *>(
-                                p.inj_out + (size_t)m * p.H + q * p.chunk + kb * kKBlock + 8 * j);
-                            ow[0] = ov.x; ow[1] = ov.y; ow[2] = ov.z; ow[3] = ov.w;
-                        }
+                        const uint32_t ow[4] = {ocur[j].x, ocur[j].y, ocur[j].z, ocur[j].w};
                         uint32_t h[4], l[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -275,16 +318,34 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
     tc_fence_before();
     cluster_sync();  // every CTA of the stream has its partial tile and sums of squares in shared memory
 
-    // Rank q sums rows [q*RS, (q+1)*RS) over the cluster, in rank order.
+    // Rank q sums rows [q*RS, (q+1)*RS) over the cluster, in rank order, four
+    // tokens at a time; the remote loads of a group are all issued before any
+    // is used, so their latencies overlap.
     const int RS = kTileRows / p.CS;
-    for (int i = tid; i < RS * NT; i += kThreads) {
-        const int r = q * RS + i / NT, n = i % NT;
-        const int gr = r0 + r, m = tile * NT + n;
-        float z = 0.f;
-        for (int pr = 0; pr < p.CS; ++pr)
-            z += dsmem_ld_f32(dsmem_addr(ptile + r * pstride + n, pr));
-        if (gr < p.R && m < p.M)
-            p.part[((size_t)c * p.R + gr) * p.M + m] = z;
+    const int NT4 = NT / 4;  // NT is a multiple of 16
+    for (int i = tid; i < RS * NT4; i += kThreads) {
+        const int r = q * RS + i / NT4, n = (i % NT4) * 4;
+        const int gr = r0 + r;
+        float4 v[8];
+#pragma unroll
+        for (int pr = 0; pr < 8; ++pr)
+            v[pr] = pr < p.CS ? dsmem_ld_f32x4(dsmem_addr(ptile + r * pstride + n, pr)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 z = v[0];
+#pragma unroll
+        for (int pr = 1; pr < 8; ++pr) {
+            if (pr < p.CS) {
+                z.x += v[pr].x; z.y += v[pr].y; z.z += v[pr].z; z.w += v[pr].w;
+            }
+        }
+        if (gr < p.R) {
+            const float zz[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = tile * NT + n + e;
+                if (m < p.M)
+                    p.part[((size_t)c * p.R + gr) * p.M + m] = zz[e];
+            }
+        }
     }
     if (q == 0 && rt == 0) {
         for (int n = tid; n < NT; n += kThreads) {
@@ -343,7 +404,9 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
     const int NT = p.NT, NS = p.n_stages, C = p.C, HBt = p.HBt;
     const TcSmem lay = up_tc_layout(NT, NS, C, HBt);
     uint16_t *raw_s = reinterpret_cast<uint16_t *>(smem + lay.extra);  // [C][NT][HBt]
-    float *inv_s = reinterpret_cast<float *>(smem + lay.extra + ((C * NT * HBt * 2 + 1023) / 1024) * 1024);
+    float *inv_s = reinterpret_cast<float *>(smem + lay.extra + up_tc_raw_bytes(NT, C, HBt));  // [NT][C]
+    float *pgate_s = inv_s + up_tc_small_bytes(NT, C) / 4;                                       // [NT][C]
+    uint16_t *out_s = reinterpret_cast<uint16_t *>(pgate_s + up_tc_small_bytes(NT, C) / 4);     // [NT][HBt]
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
     uint64_t *empty = full + NS;
     uint64_t *done = empty + NS;
@@ -425,27 +488,53 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         umma_commit(done);
     }
     if (warp >= 4) {
-        for (int i = tid - 128; i < NT * C; i += 128) {
+        // While the MMAs run: inv_rms and, for a fused inject-add, the previous
+        // gates and the sublayer-output tile of this CTA's h-block.
+        // Every load of a thread is issued before any is stored (one round trip).
+        constexpr int kPer = 16;  // NT * C <= 128 * 8 and NT * HBt / 8 <= 128 * 16
+        float iv[kPer], gv2[kPer];
+        uint4 ov[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int i = tid - 128 + 128 * j;
             const int n = i / C, cc = i % C, m = tile * NT + n;
-            inv_s[i] = m < p.M ? p.inv_rms[(size_t)m * C + cc] : 0.f;
+            const bool ok = i < NT * C && m < p.M;
+            iv[j] = ok ? p.inv_rms[(size_t)m * C + cc] : 0.f;
+            gv2[j] = (ok && p.raw_out) ? p.inj_gate[(size_t)m * p.inj_stride + cc] : 0.f;
+            const int v = i, nv = v / (HBt / 8), hv = (v % (HBt / 8)) * 8, mv = tile * NT + nv;
+            const bool okv = p.raw_out && v < NT * HBt / 8 && mv < p.M && h0 + hv + 8 <= p.H;
+            ov[j] = okv ? *reinterpret_cast<const uint4 *>(p.inj_out + (size_t)mv * p.H + h0 + hv)
+                        : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int i = tid - 128 + 128 * j;
+            if (i < NT * C) {
+                inv_s[i] = iv[j];
+                pgate_s[i] = gv2[j];
+            }
+            if (i < NT * HBt / 8)
+                reinterpret_cast<uint4 *>(out_s)[i] = ov[j];
         }
     }
     __syncthreads();
 
-    // Epilogue: warp w holds rows 32w..32w+31 = (stream, h) pairs.
+    // Epilogue on all 8 warps: warp w reads TMEM lanes 32*(w%4).. (rows = (stream,
+    // h) pairs) for the 16-column chunks of parity w/4.
     float *mix_s = reinterpret_cast<float *>(smem + lay.ring);  // [C][NT][HBt], over the ring
-    if (warp < 4) {
+    {
         if (!mbar_wait_bounded(done, 0)) timed_out = true;
         if (!mbar_wait_bounded(raw_bar, 0)) timed_out = true;
         __syncwarp();  // the TMEM loads below are .aligned
         tc_fence_after();
-        const int row = warp * 32 + lane;
+        const int quad = warp & 3, half = warp >> 2;
+        const int row = quad * 32 + lane;
         const int cc = row / HBt, hl = row % HBt;
         const bool live = cc < C && h0 + hl < p.H;
         const float gv = live ? __bfloat162float(__ushort_as_bfloat16(p.g[cc * p.H + h0 + hl])) : 0.f;
-        for (int c0 = 0; c0 < NT; c0 += 16) {
+        for (int c0 = 16 * half; c0 < NT; c0 += 32) {
             float v[16];
-            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+            tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + c0, v);
             if (live) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
@@ -455,25 +544,32 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
                     if (p.raw_out && m < p.M) {
                         // fused inject-add: this thread owns residual element (m, cc, h)
                         const size_t h = (size_t)h0 + hl;
-                        const float ov = __bfloat162float(__ushort_as_bfloat16(p.inj_out[(size_t)m * p.H + h]));
-                        rv = bf16_round(fmaf(ov, p.inj_gate[(size_t)m * p.inj_stride + cc], rv));
+                        const float ov = __bfloat162float(__ushort_as_bfloat16(out_s[n * HBt + hl]));
+                        rv = bf16_round(fmaf(ov, pgate_s[n * C + cc], rv));
                         p.raw_out[(size_t)m * p.W + (size_t)cc * p.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(rv));
                     }
-                    mix_s[(cc * NT + n) * HBt + hl] = sigm(v[j]) * (rv * inv_s[n * C + cc] * gv);
+                    mix_s[(cc * NT + n) * HBt + hl] = sigm_fast(v[j]) * (rv * inv_s[n * C + cc] * gv);
                 }
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    for (int i = tid; i < NT * HBt; i += kThreads) {
-        const int n = i / HBt, hl = i % HBt;
-        const int m = tile * NT + n, h = h0 + hl;
-        if (m < p.M && h < p.H) {
-            float acc = 0.f;
-            for (int cc = 0; cc < C; ++cc)
-                acc += mix_s[(cc * NT + n) * HBt + hl];
-            p.mixed[(size_t)m * p.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(acc * p.inv_C));
+    // Mean over the streams, 8 consecutive h of one token per item (stream order).
+    for (int i = tid; i < NT * (HBt / 8); i += kThreads) {
+        const int n = i / (HBt / 8), hv = (i % (HBt / 8)) * 8;
+        const int m = tile * NT + n, h = h0 + hv;
+        if (m < p.M && h + 8 <= p.H) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int cc = 0; cc < C; ++cc) {
+                const float4 a = *reinterpret_cast<const float4 *>(mix_s + (cc * NT + n) * HBt + hv);
+                const float4 b = *reinterpret_cast<const float4 *>(mix_s + (cc * NT + n) * HBt + hv + 4);
+                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+                acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+            }
+            *reinterpret_cast<uint4 *>(p.mixed + (size_t)m * p.H + h) =
+                make_uint4(pack_bf16x2(acc[0] * p.inv_C, acc[1] * p.inv_C), pack_bf16x2(acc[2] * p.inv_C, acc[3] * p.inv_C),
+                           pack_bf16x2(acc[4] * p.inv_C, acc[5] * p.inv_C), pack_bf16x2(acc[6] * p.inv_C, acc[7] * p.inv_C));
         }
     }
     if (timed_out) record_timeout(p.status);

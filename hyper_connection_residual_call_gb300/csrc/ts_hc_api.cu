@@ -147,7 +147,7 @@ int tc_cluster_size(int M, int H, int C, int L)
         return 0;
     for (int cs = 8; cs >= 1; cs /= 2)
         if (H % (64 * cs) == 0)
-            return cs;
+            return H / cs <= 2048 ? cs : 0;  // a CTA stages its chunk of g (<= 2048 elements)
     return 0;
 }
 
@@ -291,6 +291,8 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         tu.HBt = (128 / C) / 8 * 8;
         tu.NT = NT;
         tu.n_stages = 3;
+        while (tu.n_stages > 2 && tshc::tc_up_smem(NT, tu.n_stages, C, tu.HBt) > tshc::kTcSmemLimit)
+            --tu.n_stages;
         tu.inv_C = tr.inv_C;
         tu.status = dev.status;
         if (fi) {
