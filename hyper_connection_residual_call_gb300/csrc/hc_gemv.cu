@@ -108,9 +108,9 @@ __host__ __device__ inline UpSmem up_layout(const UpParams &p, int mt)
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 // Shorter-latency sigmoid for the one-token kernels' dependency chain: the
-// fast exponential and reciprocal intrinsics (relative error ~1e-6, far
+// fast exponential and division intrinsics (relative error ~1e-6, far
 // inside the 1e-3 bar on fp32 intermediates).
-__device__ __forceinline__ float sigmoid_fast(float x) { return __frcp_rn(1.0f + __expf(-x)); }
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&f)[8])
 {

@@ -39,6 +39,7 @@ namespace {
 constexpr int kThreads = 256;  // 8 warps
 constexpr int kTileRows = 128; // UMMA M
 constexpr int kKBlock = 64;    // bf16 elements per 128-byte swizzled row
+constexpr int kProducers = 192; // warps 2-7 build the down kernel's activation tiles
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
@@ -46,9 +47,9 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 }
 
 __device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
-// Sigmoid from the fast exponential and reciprocal intrinsics (relative error
+// Sigmoid from the fast exponential and division intrinsics (relative error
 // ~1e-6, far inside the 1e-3 bar), for the per-element epilogues.
-__device__ __forceinline__ float sigm_fast(float x) { return __frcp_rn(1.0f + __expf(-x)); }
+__device__ __forceinline__ float sigm_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr)
 {
@@ -162,7 +163,7 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full_a[s], 1);
-            mbar_init(&full_b[s], 128);
+            mbar_init(&full_b[s], kProducers);
             mbar_init(&empty[s], 1);
         }
         mbar_init(done, 1);
@@ -204,78 +205,103 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
     }
     pdl_wait();  // raw is produced by the previous kernel in the stream
 
-    if (warp >= 4) {
-        // Activation producers: thread n builds token n's row of X = raw * g
-        // as bf16 hi + lo in the swizzled K-major layout, and its sum of squares.
-        const int n = tid - 128;
-        const int m = tile * NT + n;
-        const bool live = n < NT && m < p.M;
-        const float inj_g = (live && p.inj_out) ? p.inj_gate[(size_t)m * p.inj_stride + c] : 0.f;
-        float ssq = 0.f;
-        // This token's 64 residual (and sublayer-output) elements of K block
-        // kb + 1 are loaded while block kb is converted.
-        uint4 rnext[8], onext[8];
-        auto fetch = [&](int kb) {
-            const uint4 *rp = reinterpret_cast<const uint4 *>(p.raw + (size_t)(live ? m : 0) * p.W + k0 + kb * kKBlock);
-            const uint4 *op = p.inj_out ? reinterpret_cast<const uint4 *>(
-                p.inj_out + (size_t)(live ? m : 0) * p.H + q * p.chunk + kb * kKBlock) : nullptr;
+    if (warp >= 2) {
+        // Activation producers (warps 2-7): per K block, X = raw * g as bf16
+        // hi + lo in the swizzled K-major layout. Thread t handles the 16-byte
+        // chunks i = t + kProducers j of the NT x 64 block: token i / 8, chunk
+        // i % 8, so eight consecutive lanes read one token's 128 contiguous
+        // bytes (coalesced), and accumulate that token's sum of squares.
+        const int t = tid - 64;
+        const int ck = t & 7;                  // 16-byte chunk within the 64-element K block
+        constexpr int kItems = (kTileRows * 8 + kProducers - 1) / kProducers;
+        float ssq[kItems], inj_g[kItems];
+        const uint4 *rrow[kItems];
+        const uint4 *orow[kItems];
+        bool live[kItems];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                rnext[j] = live ? rp[j] : make_uint4(0, 0, 0, 0);
-                onext[j] = (live && p.inj_out) ? op[j] : make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < kItems; ++j) {
+            const int n = (t + kProducers * j) >> 3;   // token of chunk t + kProducers j
+            const int m = tile * NT + n;
+            live[j] = n < NT && m < p.M;
+            ssq[j] = 0.f;
+            inj_g[j] = (live[j] && p.inj_out) ? p.inj_gate[(size_t)m * p.inj_stride + c] : 0.f;
+            rrow[j] = reinterpret_cast<const uint4 *>(p.raw + (size_t)(live[j] ? m : 0) * p.W + k0) + ck;
+            orow[j] = p.inj_out ? reinterpret_cast<const uint4 *>(p.inj_out + (size_t)(live[j] ? m : 0) * p.H
+                                                                  + q * p.chunk) + ck
+                                : nullptr;
+        }
+        // The next K block's chunks are loaded while the current one is converted.
+        uint4 rnext[kItems], onext[kItems];
+        auto fetch = [&](int kb) {
+#pragma unroll
+            for (int j = 0; j < kItems; ++j) {
+                rnext[j] = live[j] ? rrow[j][kb * (kKBlock / 8)] : make_uint4(0, 0, 0, 0);
+                onext[j] = (live[j] && p.inj_out) ? orow[j][kb * (kKBlock / 8)] : make_uint4(0, 0, 0, 0);
             }
         };
-        if (n < NT)
-            fetch(0);
+        fetch(0);
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % NS, u = kb / NS;
-            uint4 rcur[8], ocur[8];
+            uint4 rcur[kItems], ocur[kItems];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < kItems; ++j) {
                 rcur[j] = rnext[j];
                 ocur[j] = onext[j];
             }
-            if (n < NT && kb + 1 < KB)
+            if (kb + 1 < KB)
                 fetch(kb + 1);
             if (u > 0 && !mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
             uint8_t *bhi = smem + lay.ring + s * lay.stage_bytes + lay.a_bytes;
             uint8_t *blo = bhi + lay.b_bytes;
-            if (n < NT) {
-                const uint4 *gp = reinterpret_cast<const uint4 *>(g_s + kb * kKBlock);
+            const uint4 gv = reinterpret_cast<const uint4 *>(g_s + kb * kKBlock)[ck];
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
-                    if (live) {
-                        const uint4 rv = rcur[j], gv = gp[j];
-                        const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
-                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-                        const uint32_t ow[4] = {ocur[j].x, ocur[j].y, ocur[j].z, ocur[j].w};
-                        uint32_t h[4], l[4];
+            for (int j = 0; j < kItems; ++j) {
+                const int n = (t + kProducers * j) >> 3;
+                if (n >= NT)
+                    continue;
+                uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
+                if (live[j]) {
+                    const uint32_t rw[4] = {rcur[j].x, rcur[j].y, rcur[j].z, rcur[j].w};
+                    const uint32_t ow[4] = {ocur[j].x, ocur[j].y, ocur[j].z, ocur[j].w};
+                    uint32_t h[4], l[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            float r_a = bf16_lo(rw[e]), r_b = bf16_hi(rw[e]);
-                            if (p.inj_out) {  // fused inject-add, rounded as the inject-add kernel rounds
-                                r_a = bf16_round(fmaf(bf16_lo(ow[e]), inj_g, r_a));
-                                r_b = bf16_round(fmaf(bf16_hi(ow[e]), inj_g, r_b));
-                            }
-                            ssq = fmaf(r_a, r_a, ssq);
-                            ssq = fmaf(r_b, r_b, ssq);
-                            const float x_a = r_a * bf16_lo(gw[e]), x_b = r_b * bf16_hi(gw[e]);
-                            const float h_a = bf16_round(x_a), h_b = bf16_round(x_b);
-                            h[e] = pack_bf16x2(h_a, h_b);
-                            l[e] = pack_bf16x2(x_a - h_a, x_b - h_b);
+                    for (int e = 0; e < 4; ++e) {
+                        // Packed conversions: one bf16x2 rounding per pair.
+                        float r_a = bf16_lo(rw[e]), r_b = bf16_hi(rw[e]);
+                        if (p.inj_out) {  // fused inject-add, rounded as the inject-add kernel rounds
+                            const uint32_t rr = pack_bf16x2(fmaf(bf16_lo(ow[e]), inj_g[j], r_a),
+                                                            fmaf(bf16_hi(ow[e]), inj_g[j], r_b));
+                            r_a = bf16_lo(rr);
+                            r_b = bf16_hi(rr);
                         }
-                        hi = make_uint4(h[0], h[1], h[2], h[3]);
-                        lo = make_uint4(l[0], l[1], l[2], l[3]);
+                        ssq[j] = fmaf(r_a, r_a, ssq[j]);
+                        ssq[j] = fmaf(r_b, r_b, ssq[j]);
+                        const float x_a = r_a * bf16_lo(gw[e]), x_b = r_b * bf16_hi(gw[e]);
+                        const uint32_t hh = pack_bf16x2(x_a, x_b);
+                        h[e] = hh;
+                        l[e] = pack_bf16x2(x_a - bf16_lo(hh), x_b - bf16_hi(hh));
                     }
-                    *reinterpret_cast<uint4 *>(bhi + sw128_offset(n, 8 * j)) = hi;
-                    *reinterpret_cast<uint4 *>(blo + sw128_offset(n, 8 * j)) = lo;
+                    hi = make_uint4(h[0], h[1], h[2], h[3]);
+                    lo = make_uint4(l[0], l[1], l[2], l[3]);
                 }
+                *reinterpret_cast<uint4 *>(bhi + sw128_offset(n, 8 * ck)) = hi;
+                *reinterpret_cast<uint4 *>(blo + sw128_offset(n, 8 * ck)) = lo;
             }
             fence_async_shared();
             mbar_arrive(&full_b[s]);
         }
-        if (n < NT) ssq_s[n] = ssq;
+        // A token's sum of squares: its 8 lanes (one octet of the warp), fixed order.
+#pragma unroll
+        for (int j = 0; j < kItems; ++j) {
+            float v = ssq[j];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            const int n = (t + kProducers * j) >> 3;
+            if (ck == 0 && n < NT)
+                ssq_s[n] = v;
+        }
     } else if (warp == 1 && lane == 0) {
         // MMA issuer.
         const uint32_t idesc = umma_idesc_bf16(kTileRows, NT);
@@ -365,30 +391,52 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
 
 // ---------------------------------------------------------------- reduce
 
-__global__ void __launch_bounds__(256) hc_tc_reduce_kernel(const TcReduceParams p)
+// Grid (ceil(M / 32), ceil(R / 32)); 1024 threads, one element each. The
+// partials are read along tokens and act is written along rows, through a
+// shared-memory transpose, so both sides are coalesced.
+__global__ void __launch_bounds__(1024) hc_tc_reduce_kernel(const TcReduceParams p)
 {
+    __shared__ float zt[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int m0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
     pdl_launch_dependents();
     pdl_wait();
-    const long total = (long)p.R * p.M;
-    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
-        const int r = (int)(i / p.M), m = (int)(i % p.M);
+    {
+        // z of row r0 + ty, token m0 + tx: every load first, then the sum in stream order.
+        const int m = m0 + tx, r = r0 + ty;
+        const bool ok = m < p.M && r < p.R;
+        float sq[8], pt[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            sq[c] = (c < p.C && ok) ? p.ssq[(size_t)c * p.M + m] : 0.f;
+            pt[c] = (c < p.C && ok) ? p.part[((size_t)c * p.R + r) * p.M + m] : 0.f;
+        }
         float z = 0.f;
-        for (int c = 0; c < p.C; ++c) {
-            const float inv = 1.0f / sqrtf(p.ssq[(size_t)c * p.M + m] / (float)p.H + p.eps);
-            z = fmaf(inv, p.part[((size_t)c * p.R + r) * p.M + m], z);
-            if (r == 0)
-                p.inv_rms[(size_t)m * p.C + c] = inv;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            if (c < p.C && ok) {
+                const float inv = 1.0f / sqrtf(sq[c] / (float)p.H + p.eps);
+                z = fmaf(inv, pt[c], z);
+                if (r == 0)
+                    p.inv_rms[(size_t)m * p.C + c] = inv;
+            }
         }
-        const float zc = z * p.inv_C;
-        if (r < p.L) {
-            const float a = zc * sigm(zc);
-            const float hi = bf16_round(a);
-            p.act[(size_t)m * p.L + r] = a;
-            p.act_hi[(size_t)m * p.L + r] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-            p.act_lo[(size_t)m * p.L + r] = __bfloat16_as_ushort(__float2bfloat16_rn(a - hi));
-        } else {
-            p.gate[(size_t)m * p.gate_stride + (r - p.L)] = 2.0f * sigm(zc);
-        }
+        zt[ty][tx] = z;
+    }
+    __syncthreads();
+    // Row r0 + tx of token m0 + ty.
+    const int r = r0 + tx, mm = m0 + ty;
+    if (r >= p.R || mm >= p.M)
+        return;
+    const float zc = zt[tx][ty] * p.inv_C;
+    if (r < p.L) {
+        const float a = zc * sigm_fast(zc);
+        const float hi = bf16_round(a);
+        p.act[(size_t)mm * p.L + r] = a;
+        p.act_hi[(size_t)mm * p.L + r] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+        p.act_lo[(size_t)mm * p.L + r] = __bfloat16_as_ushort(__float2bfloat16_rn(a - hi));
+    } else {
+        p.gate[(size_t)mm * p.gate_stride + (r - p.L)] = 2.0f * sigm_fast(zc);
     }
 }
 
@@ -532,12 +580,22 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         const int cc = row / HBt, hl = row % HBt;
         const bool live = cc < C && h0 + hl < p.H;
         const float gv = live ? __bfloat162float(__ushort_as_bfloat16(p.g[cc * p.H + h0 + hl])) : 0.f;
-        for (int c0 = 16 * half; c0 < NT; c0 += 32) {
-            float v[16];
-            tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + c0, v);
-            if (live) {
+        // All of this warp's TMEM chunks (NT <= 128: at most 4) are loaded
+        // before one wait.
+        constexpr int kChunks = 4;
+        uint32_t vr[kChunks][16];
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k)
+            if (16 * half + 32 * k < NT)  // warp-uniform
+                tmem_ld16_async(tmem + ((uint32_t)(quad * 32) << 16) + 16 * half + 32 * k, vr[k]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k) {
+            const int c0 = 16 * half + 32 * k;
+            if (c0 < NT && live) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
+                    const float vj = __uint_as_float(vr[k][j]);
                     const int n = c0 + j;
                     const int m = tile * NT + n;
                     float rv = __bfloat162float(__ushort_as_bfloat16(raw_s[(cc * NT + n) * HBt + hl]));
@@ -548,7 +606,7 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
                         rv = bf16_round(fmaf(ov, pgate_s[n * C + cc], rv));
                         p.raw_out[(size_t)m * p.W + (size_t)cc * p.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(rv));
                     }
-                    mix_s[(cc * NT + n) * HBt + hl] = sigm_fast(v[j]) * (rv * inv_s[n * C + cc] * gv);
+                    mix_s[(cc * NT + n) * HBt + hl] = sigm_fast(vj) * (rv * inv_s[n * C + cc] * gv);
                 }
             }
         }
@@ -643,8 +701,10 @@ cudaError_t launch_tc(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Once per kernel and device: the dynamic shared-memory limit (when
+// `dynamic` is set) and the largest carveout.
 template <typename K>
-cudaError_t allow_smem_tc(K kernel)
+cudaError_t allow_smem_tc(K kernel, bool dynamic = true)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -656,7 +716,8 @@ cudaError_t allow_smem_tc(K kernel)
     const auto key = std::make_pair(reinterpret_cast<const void *>(kernel), dev);
     if (done.count(key))
         return cudaSuccess;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemLimit);
+    e = dynamic ? cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemLimit)
+                : cudaSuccess;
     if (e == cudaSuccess)  // same carveout as every other kernel of the library (co-residency)
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
@@ -686,15 +747,14 @@ cudaError_t launch_tc_call(const TcCall &t, cudaStream_t stream)
     cudaError_t e;
     if ((e = allow_smem_tc(hc_tc_down_kernel)) != cudaSuccess) return e;
     if ((e = allow_smem_tc(hc_tc_up_kernel)) != cudaSuccess) return e;
-    if ((e = allow_smem_tc(hc_tc_reduce_kernel)) != cudaSuccess) return e;
+    if ((e = allow_smem_tc(hc_tc_reduce_kernel, false)) != cudaSuccess) return e;
     const int ntiles = (d.M + d.NT - 1) / d.NT;
     e = launch_tc(hc_tc_down_kernel, dim3(d.CS, d.C * d.RT, ntiles), dim3(kThreads),
                   tc_down_smem(d.NT, d.n_stages), stream, d.CS, d, map_d, map_i);
     if (e != cudaSuccess)
         return e;
-    const long total = (long)t.red.R * t.red.M;
-    const int rblocks = (int)std::max<long>(1, std::min<long>((total + 255) / 256, 4L * 152));
-    e = launch_tc(hc_tc_reduce_kernel, dim3(rblocks), dim3(256), 0, stream, 0, t.red);
+    e = launch_tc(hc_tc_reduce_kernel, dim3((t.red.M + 31) / 32, (t.red.R + 31) / 32), dim3(1024), 0, stream, 0,
+                  t.red);
     if (e != cudaSuccess)
         return e;
     return launch_tc(hc_tc_up_kernel, dim3((u.H + u.HBt - 1) / u.HBt, ntiles), dim3(kThreads),
