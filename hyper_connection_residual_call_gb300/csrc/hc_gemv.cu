@@ -551,30 +551,30 @@ __global__ void __launch_bounds__(768, 1) hc_up_kernel(const UpParams p)
 #pragma unroll
                 for (int t = 0; t < MT; ++t) acc[t] += a1[t];
             } else {
+                // Lane tl of the team owns the 4-byte words (8 codes) w = tl + 8 i
+                // of the row: the team reads 32 contiguous bytes of codes and act
+                // rows 32 bytes apart per lane (no 128-byte-stride bank conflicts).
                 const float *sb = sb_s + 2 * srow * ng;
-                for (int v = tl; v < L / 32; v += 8) {
-                    const uint4 q = wrow[v];
-                    const int gi = (v * 32) / p.up.group;
+                const uint32_t *wrow32 = reinterpret_cast<const uint32_t *>(wrow);
+                for (int w = tl; w < L / 8; w += 8) {
+                    const uint32_t codes = wrow32[w];
+                    const int gi = (w * 8) / p.up.group;
                     const float sc = sb[2 * gi], bi = sb[2 * gi + 1];
-                    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+                    float wf[8];
 #pragma unroll
-                    for (int wd = 0; wd < 4; ++wd) {
-                        float wf[8];
+                    for (int n = 0; n < 8; ++n)
+                        wf[n] = fmaf((float)((codes >> (4 * n)) & 0xFu), sc, bi);
 #pragma unroll
-                        for (int n = 0; n < 8; ++n)
-                            wf[n] = fmaf((float)((words[wd] >> (4 * n)) & 0xFu), sc, bi);
-#pragma unroll
-                        for (int t = 0; t < MT; ++t) {
-                            const float *xr = act_s + t * L + v * 32 + wd * 8;
-                            const float4 xa = *reinterpret_cast<const float4 *>(xr);
-                            const float4 xb = *reinterpret_cast<const float4 *>(xr + 4);
-                            float a = acc[t];
-                            a = fmaf(wf[0], xa.x, a); a = fmaf(wf[1], xa.y, a);
-                            a = fmaf(wf[2], xa.z, a); a = fmaf(wf[3], xa.w, a);
-                            a = fmaf(wf[4], xb.x, a); a = fmaf(wf[5], xb.y, a);
-                            a = fmaf(wf[6], xb.z, a); a = fmaf(wf[7], xb.w, a);
-                            acc[t] = a;
-                        }
+                    for (int t = 0; t < MT; ++t) {
+                        const float *xr = act_s + t * L + w * 8;
+                        const float4 xa = *reinterpret_cast<const float4 *>(xr);
+                        const float4 xb = *reinterpret_cast<const float4 *>(xr + 4);
+                        float a = acc[t];
+                        a = fmaf(wf[0], xa.x, a); a = fmaf(wf[1], xa.y, a);
+                        a = fmaf(wf[2], xa.z, a); a = fmaf(wf[3], xa.w, a);
+                        a = fmaf(wf[4], xb.x, a); a = fmaf(wf[5], xb.y, a);
+                        a = fmaf(wf[6], xb.z, a); a = fmaf(wf[7], xb.w, a);
+                        acc[t] = a;
                     }
                 }
             }

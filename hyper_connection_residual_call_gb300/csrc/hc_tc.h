@@ -6,7 +6,7 @@
 
 namespace tshc {
 
-constexpr int kTcMinTokens = 64;          // the batched path starts at this many tokens
+constexpr int kTcMinTokens = 16;          // the batched path starts at this many tokens
 constexpr size_t kTcSmemLimit = 232448;   // 227 KB opt-in shared memory per CTA
 
 struct TcDownParams {

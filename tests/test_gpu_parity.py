@@ -121,11 +121,12 @@ def test_int4_full_shape(orc, M):
                     group=inputs.INT4_GROUP)
 
 
-@pytest.mark.parametrize("M,H,C,L", [(64, 2560, 4, 320), (100, 2560, 4, 320), (130, 2560, 4, 320),
+@pytest.mark.parametrize("M,H,C,L", [(16, 2560, 4, 320), (40, 2560, 4, 320),
+                                     (64, 2560, 4, 320), (100, 2560, 4, 320), (130, 2560, 4, 320),
                                      (256, 2560, 4, 320), (64, 512, 2, 64), (80, 1024, 8, 128),
                                      (70, 320, 3, 64), (96, 256, 1, 128)])
 def test_tensor_core_path(orc, M, H, C, L):
-    # M >= 64 with bf16 weights runs on tcgen05 (tiles of up to 128 tokens)
+    # M >= 16 with bf16 weights runs on tcgen05 (tiles of up to 128 tokens)
     call_and_inject(orc, inputs.Shape(M=M, H=H, C=C, L=L), seed=300 + M)
 
 
