@@ -230,7 +230,7 @@ def cpu_baseline(budget_s: float = 12.0):
     out = inputs.make_sublayer_out(M, H, CONFIG_SEED)
     n = 0
     t0 = time.perf_counter()
-    while time.perf_counter() - t0 < budget_s and n < 2000:
+    while time.perf_counter() - t0 < budget_s and n < 20000:
         res = orc.hc_call(raw, w.g, w.down, w.up, w.inject, H=H, C=C, L=L, threads=threads)
         raw = orc.inject_add(raw, out, res["gate"], H=H, C=C)
         n += 1
