@@ -87,17 +87,37 @@ struct TcSmem {
 // per-token sums of squares, then this CTA's chunk of g (bf16, at most
 // kMaxChunk elements), then barriers.
 constexpr int kMaxChunk = 2048;
-__host__ __device__ inline TcSmem down_tc_layout(int NT, int ns)
+// A stage is [A_hi | A_lo (INT4 weights only) | B_hi | B_lo].
+__host__ __device__ inline TcSmem down_tc_layout(int NT, int ns, int wt)
 {
     TcSmem s;
     s.a_bytes = kTileRows * 128;
     s.b_bytes = NT * 128;
-    s.stage_bytes = s.a_bytes + 2 * s.b_bytes;
+    s.stage_bytes = s.a_bytes * (1 + wt) + 2 * s.b_bytes;
     s.ring = 0;
     s.extra = s.ring + ns * s.stage_bytes;          // ssq_s: NT floats, then g_s
     s.bars = s.extra + ((NT * 4 + 127) / 128) * 128 + kMaxChunk * 2;
     s.total = s.bars + 8 * (3 * ns + 2) + 16;
     return s;
+}
+
+// Dequantises 8 INT4-affine codes (element e in nibble e of `codes`) with one
+// scale and bias (fp16 bits) and splits them into bf16 hi and lo parts:
+// w = q * s + b in fp32, hi = bf16(w), lo = bf16(w - hi).
+__device__ __forceinline__ void int4x8_hilo(uint32_t codes, uint16_t sb, uint16_t bb, uint4 &hi, uint4 &lo)
+{
+    const float sc = __half2float(__ushort_as_half(sb)), bi = __half2float(__ushort_as_half(bb));
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float wa = fmaf((float)((codes >> (8 * e)) & 0xFu), sc, bi);
+        const float wb = fmaf((float)((codes >> (8 * e + 4)) & 0xFu), sc, bi);
+        const uint32_t hh = pack_bf16x2(wa, wb);
+        h[e] = hh;
+        l[e] = pack_bf16x2(wa - bf16_lo(hh), wb - bf16_hi(hh));
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 // Up kernel: ring, then raw tile [C][NT][HBt] bf16, inv_rms tile [NT][C], and
@@ -110,21 +130,22 @@ __host__ __device__ inline uint32_t up_tc_raw_bytes(int NT, int C, int HBt)
 __host__ __device__ inline uint32_t up_tc_small_bytes(int NT, int C) { return ((NT * C * 4 + 127) / 128) * 128; }
 __host__ __device__ inline uint32_t up_tc_out_bytes(int NT, int HBt) { return ((NT * HBt * 2 + 127) / 128) * 128; }
 
-__host__ __device__ inline TcSmem up_tc_layout(int NT, int ns, int C, int HBt)
+__host__ __device__ inline TcSmem up_tc_layout(int NT, int ns, int C, int HBt, int wt)
 {
     TcSmem s;
     s.a_bytes = kTileRows * 128;
     s.b_bytes = NT * 128;
-    s.stage_bytes = s.a_bytes + 2 * s.b_bytes;
+    s.stage_bytes = s.a_bytes * (1 + wt) + 2 * s.b_bytes;
     s.ring = 0;
     s.extra = s.ring + ns * s.stage_bytes;
     s.bars = s.extra + up_tc_raw_bytes(NT, C, HBt) + 2 * up_tc_small_bytes(NT, C) + up_tc_out_bytes(NT, HBt);
-    s.total = s.bars + 8 * (3 * ns + 2) + 16;
+    s.total = s.bars + 8 * (4 * ns + 2) + 16;
     return s;
 }
 
 // ---------------------------------------------------------------- down
 
+template <int WT>
 __global__ void __launch_bounds__(kThreads, 1)
 hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_d,
                   const __grid_constant__ CUtensorMap map_i)
@@ -132,7 +153,8 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int NT = p.NT, NS = p.n_stages;
-    const TcSmem lay = down_tc_layout(NT, NS);
+    const TcSmem lay = down_tc_layout(NT, NS, WT);
+    const uint32_t b_off = lay.a_bytes * (1 + WT);  // B_hi within a stage
     float *ssq_s = reinterpret_cast<float *>(smem + lay.extra);
     uint16_t *g_s = reinterpret_cast<uint16_t *>(smem + lay.extra + ((NT * 4 + 127) / 128) * 128);
     uint64_t *full_a = reinterpret_cast<uint64_t *>(smem + lay.bars);
@@ -185,7 +207,7 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
     const uint32_t tmem = *tslot;
     bool timed_out = false;
 
-    if (warp == 0 && lane == 0) {
+    if (WT == 0 && warp == 0 && lane == 0) {
         // TMA producer of the weight tiles (independent of the previous kernel).
         tma_prefetch_map(&map_d);
         if (p.has_inject) tma_prefetch_map(&map_i);
@@ -203,7 +225,8 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
             }
         }
     }
-    pdl_wait();  // raw is produced by the previous kernel in the stream
+    if (warp < 2)
+        pdl_wait();  // raw is produced by the previous kernel in the stream
 
     if (warp >= 2) {
         // Activation producers (warps 2-7): per K block, X = raw * g as bf16
@@ -230,29 +253,81 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
                                                                   + q * p.chunk) + ck
                                 : nullptr;
         }
+        // INT4 weights: item j is also row (t + kProducers j) / 8 of the A tile,
+        // chunk ck: 8 codes (4 bytes) and the group's scale and bias.
+        const uint8_t *wq[kItems];
+        const uint16_t *wsc[kItems];
+        const uint16_t *wbi[kItems];
+        if constexpr (WT == 1) {
+#pragma unroll
+            for (int j = 0; j < kItems; ++j) {
+                const int rr = (t + kProducers * j) >> 3, gr = r0 + rr;
+                const WeightView *v = gr < p.L ? &p.dw : (p.has_inject && gr < p.L + p.C) ? &p.iw : nullptr;
+                const int row = gr < p.L ? gr : gr - p.L;
+                wq[j] = (v && rr < kTileRows) ? static_cast<const uint8_t *>(v->data) + ((size_t)row * p.W + k0) / 2 : nullptr;
+                wsc[j] = wq[j] ? v->scales + (size_t)row * (p.W / v->group) : nullptr;
+                wbi[j] = wq[j] ? v->biases + (size_t)row * (p.W / v->group) : nullptr;
+            }
+        }
         // The next K block's chunks are loaded while the current one is converted.
         uint4 rnext[kItems], onext[kItems];
+        uint32_t qnext[kItems];
+        uint16_t snext[kItems], bnext[kItems];
+        auto fetch_w = [&](int kb) {
+            if constexpr (WT == 1) {
+                const int col = kb * kKBlock + 8 * ck;  // within the chunk
+#pragma unroll
+                for (int j = 0; j < kItems; ++j) {
+                    qnext[j] = wq[j] ? *reinterpret_cast<const uint32_t *>(wq[j] + col / 2) : 0u;
+                    snext[j] = wq[j] ? wsc[j][(k0 + col) / p.dw.group] : (uint16_t)0;
+                    bnext[j] = wq[j] ? wbi[j][(k0 + col) / p.dw.group] : (uint16_t)0;
+                }
+            }
+        };
         auto fetch = [&](int kb) {
 #pragma unroll
             for (int j = 0; j < kItems; ++j) {
                 rnext[j] = live[j] ? rrow[j][kb * (kKBlock / 8)] : make_uint4(0, 0, 0, 0);
                 onext[j] = (live[j] && p.inj_out) ? orow[j][kb * (kKBlock / 8)] : make_uint4(0, 0, 0, 0);
             }
+            fetch_w(kb);
         };
+        fetch_w(0);  // weights do not depend on the previous kernel
+        pdl_wait();  // raw is produced by the previous kernel in the stream
         fetch(0);
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % NS, u = kb / NS;
             uint4 rcur[kItems], ocur[kItems];
+            uint32_t qcur[kItems];
+            uint16_t scur[kItems], bcur[kItems];
 #pragma unroll
             for (int j = 0; j < kItems; ++j) {
                 rcur[j] = rnext[j];
                 ocur[j] = onext[j];
+                qcur[j] = qnext[j];
+                scur[j] = snext[j];
+                bcur[j] = bnext[j];
             }
             if (kb + 1 < KB)
                 fetch(kb + 1);
             if (u > 0 && !mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
-            uint8_t *bhi = smem + lay.ring + s * lay.stage_bytes + lay.a_bytes;
+            uint8_t *ahi = smem + lay.ring + s * lay.stage_bytes;
+            uint8_t *bhi = ahi + b_off;
             uint8_t *blo = bhi + lay.b_bytes;
+            if constexpr (WT == 1) {
+                uint8_t *alo = ahi + lay.a_bytes;
+#pragma unroll
+                for (int j = 0; j < kItems; ++j) {
+                    const int rr = (t + kProducers * j) >> 3;
+                    if (rr >= kTileRows)
+                        continue;
+                    uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
+                    if (wq[j])
+                        int4x8_hilo(qcur[j], scur[j], bcur[j], hi, lo);
+                    *reinterpret_cast<uint4 *>(ahi + sw128_offset(rr, 8 * ck)) = hi;
+                    *reinterpret_cast<uint4 *>(alo + sw128_offset(rr, 8 * ck)) = lo;
+                }
+            }
             const uint4 gv = reinterpret_cast<const uint4 *>(g_s + kb * kKBlock)[ck];
             const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
@@ -307,15 +382,18 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
         const uint32_t idesc = umma_idesc_bf16(kTileRows, NT);
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % NS, u = kb / NS;
-            if (!mbar_wait_bounded(&full_a[s], u & 1)) timed_out = true;
+            if (WT == 0 && !mbar_wait_bounded(&full_a[s], u & 1)) timed_out = true;
             if (!mbar_wait_bounded(&full_b[s], u & 1)) timed_out = true;
             tc_fence_after();
             const uint32_t a = smem_addr(smem + lay.ring + s * lay.stage_bytes);
-            const uint32_t bh = a + lay.a_bytes, bl = bh + lay.b_bytes;
+            const uint32_t al = a + lay.a_bytes;  // A_lo (INT4 weights)
+            const uint32_t bh = a + b_off, bl = bh + lay.b_bytes;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(bh + 32 * k), idesc, (kb | k) != 0);
                 umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(bl + 32 * k), idesc, 1);
+                if (WT == 1)  // the weight's lo part against the activation's hi part
+                    umma_bf16(tmem, umma_desc_sw128(al + 32 * k), umma_desc_sw128(bh + 32 * k), idesc, 1);
             }
             umma_commit(&empty[s]);
         }
@@ -442,6 +520,7 @@ __global__ void __launch_bounds__(1024) hc_tc_reduce_kernel(const TcReduceParams
 
 // ---------------------------------------------------------------- up
 
+template <int WT>
 __global__ void __launch_bounds__(kThreads, 1)
 hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
                 const __grid_constant__ CUtensorMap map_ahi, const __grid_constant__ CUtensorMap map_alo,
@@ -450,14 +529,16 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int NT = p.NT, NS = p.n_stages, C = p.C, HBt = p.HBt;
-    const TcSmem lay = up_tc_layout(NT, NS, C, HBt);
+    const TcSmem lay = up_tc_layout(NT, NS, C, HBt, WT);
+    const uint32_t b_off = lay.a_bytes * (1 + WT);  // B_hi within a stage
     uint16_t *raw_s = reinterpret_cast<uint16_t *>(smem + lay.extra);  // [C][NT][HBt]
     float *inv_s = reinterpret_cast<float *>(smem + lay.extra + up_tc_raw_bytes(NT, C, HBt));  // [NT][C]
     float *pgate_s = inv_s + up_tc_small_bytes(NT, C) / 4;                                       // [NT][C]
     uint16_t *out_s = reinterpret_cast<uint16_t *>(pgate_s + up_tc_small_bytes(NT, C) / 4);     // [NT][HBt]
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
     uint64_t *empty = full + NS;
-    uint64_t *done = empty + NS;
+    uint64_t *fullp = empty + NS;  // INT4: the producers' A tiles of a stage are written
+    uint64_t *done = fullp + NS;
     uint64_t *raw_bar = done + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(raw_bar + 1);
 
@@ -472,6 +553,7 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&fullp[s], kProducers);
         }
         mbar_init(done, 1);
         mbar_init(raw_bar, 1);
@@ -489,9 +571,10 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
     bool timed_out = false;
 
     if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&map_u);
-        // Weights first (independent of the previous kernels) ...
-        const int npre = KB < NS ? KB : NS;
+        // Weights first (bf16: TMA; independent of the previous kernels) ...
+        const int npre = WT == 0 ? (KB < NS ? KB : NS) : 0;
+        if (WT == 0)
+            tma_prefetch_map(&map_u);
         for (int kb = 0; kb < npre; ++kb) {
             uint8_t *a = smem + lay.ring + kb * lay.stage_bytes;
             mbar_arrive_expect_tx(&full[kb], C * HBt * 128 + 2 * NT * 128);
@@ -502,18 +585,75 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % NS, u = kb / NS;
             uint8_t *a = smem + lay.ring + s * lay.stage_bytes;
-            if (kb >= npre) {
+            if (WT == 0 && kb >= npre) {
                 if (!mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
                 mbar_arrive_expect_tx(&full[s], C * HBt * 128 + 2 * NT * 128);
                 for (int cc = 0; cc < C; ++cc)
                     tma_load_2d(a + cc * HBt * 128, &map_u, kb * kKBlock, cc * p.H + h0, &full[s]);
+            } else if (WT == 1) {
+                if (u > 0 && !mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
+                mbar_arrive_expect_tx(&full[s], 2 * NT * 128);
             }
-            tma_load_2d(a + lay.a_bytes, &map_ahi, kb * kKBlock, tile * NT, &full[s]);
-            tma_load_2d(a + lay.a_bytes + lay.b_bytes, &map_alo, kb * kKBlock, tile * NT, &full[s]);
+            tma_load_2d(a + b_off, &map_ahi, kb * kKBlock, tile * NT, &full[s]);
+            tma_load_2d(a + b_off + lay.b_bytes, &map_alo, kb * kKBlock, tile * NT, &full[s]);
         }
         mbar_arrive_expect_tx(raw_bar, C * NT * HBt * 2);
         for (int cc = 0; cc < C; ++cc)
             tma_load_2d(raw_s + cc * NT * HBt, &map_raw, cc * p.H + h0, tile * NT, raw_bar);
+    } else if (WT == 1 && warp >= 2) {
+        // INT4 weights: warps 2-7 dequantise the A tiles (rows (stream, h) of
+        // this CTA, 64 columns per stage) to bf16 hi + lo. Thread t handles the
+        // 16-byte chunks t + kProducers j: row / 8, chunk t % 8. The stages
+        // before the ring wraps are written before the dependency wait.
+        const int t = tid - 64;
+        const int ck = t & 7;
+        constexpr int kItems = (kTileRows * 8 + kProducers - 1) / kProducers;
+        const uint8_t *wq[kItems];
+        const uint16_t *wsc[kItems];
+        const uint16_t *wbi[kItems];
+        const int ngr = p.L / p.uw.group;
+#pragma unroll
+        for (int j = 0; j < kItems; ++j) {
+            const int rr = (t + kProducers * j) >> 3;
+            const int cc = rr / HBt, hl = rr % HBt;
+            const bool ok = rr < kTileRows && cc < C && h0 + hl < p.H;
+            const size_t row = (size_t)cc * p.H + h0 + hl;
+            wq[j] = ok ? static_cast<const uint8_t *>(p.uw.data) + row * (p.L / 2) : nullptr;
+            wsc[j] = ok ? p.uw.scales + row * ngr : nullptr;
+            wbi[j] = ok ? p.uw.biases + row * ngr : nullptr;
+        }
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % NS, u = kb / NS;
+            if (kb == NS)
+                pdl_wait();
+            const int col = kb * kKBlock + 8 * ck;
+            uint32_t q[kItems];
+            uint16_t sc[kItems], bi[kItems];
+#pragma unroll
+            for (int j = 0; j < kItems; ++j) {
+                q[j] = wq[j] ? *reinterpret_cast<const uint32_t *>(wq[j] + col / 2) : 0u;
+                sc[j] = wq[j] ? wsc[j][col / p.uw.group] : (uint16_t)0;
+                bi[j] = wq[j] ? wbi[j][col / p.uw.group] : (uint16_t)0;
+            }
+            if (u > 0 && !mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
+            uint8_t *ahi = smem + lay.ring + s * lay.stage_bytes;
+            uint8_t *alo = ahi + lay.a_bytes;
+#pragma unroll
+            for (int j = 0; j < kItems; ++j) {
+                const int rr = (t + kProducers * j) >> 3;
+                if (rr >= kTileRows)
+                    continue;
+                uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
+                if (wq[j])
+                    int4x8_hilo(q[j], sc[j], bi[j], hi, lo);
+                *reinterpret_cast<uint4 *>(ahi + sw128_offset(rr, 8 * ck)) = hi;
+                *reinterpret_cast<uint4 *>(alo + sw128_offset(rr, 8 * ck)) = lo;
+            }
+            fence_async_shared();
+            mbar_arrive(&fullp[s]);
+        }
+        if (KB <= NS)
+            pdl_wait();
     } else {
         pdl_wait();
     }
@@ -523,13 +663,17 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % NS, u = kb / NS;
             if (!mbar_wait_bounded(&full[s], u & 1)) timed_out = true;
+            if (WT == 1 && !mbar_wait_bounded(&fullp[s], u & 1)) timed_out = true;
             tc_fence_after();
             const uint32_t a = smem_addr(smem + lay.ring + s * lay.stage_bytes);
-            const uint32_t bh = a + lay.a_bytes, bl = bh + lay.b_bytes;
+            const uint32_t al = a + lay.a_bytes;  // A_lo (INT4 weights)
+            const uint32_t bh = a + b_off, bl = bh + lay.b_bytes;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(bh + 32 * k), idesc, (kb | k) != 0);
                 umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(bl + 32 * k), idesc, 1);
+                if (WT == 1)  // the weight's lo part against the activation's hi part
+                    umma_bf16(tmem, umma_desc_sw128(al + 32 * k), umma_desc_sw128(bh + 32 * k), idesc, 1);
             }
             umma_commit(&empty[s]);
         }
@@ -728,37 +872,43 @@ cudaError_t allow_smem_tc(K kernel, bool dynamic = true)
 
 }  // namespace
 
-size_t tc_down_smem(int NT, int ns) { return down_tc_layout(NT, ns).total + 1024; }
-size_t tc_up_smem(int NT, int ns, int C, int HBt) { return up_tc_layout(NT, ns, C, HBt).total + 1024; }
+size_t tc_down_smem(int NT, int ns, int wt) { return down_tc_layout(NT, ns, wt).total + 1024; }
+size_t tc_up_smem(int NT, int ns, int C, int HBt, int wt) { return up_tc_layout(NT, ns, C, HBt, wt).total + 1024; }
 
 cudaError_t launch_tc_call(const TcCall &t, cudaStream_t stream)
 {
     CUtensorMap map_d, map_i, map_u, map_ahi, map_alo, map_raw;
     const TcDownParams &d = t.down;
     const TcUpParams &u = t.up;
-    if (!make_map(&map_d, t.wd, d.L, d.W, kKBlock, 32, true) ||
-        !make_map(&map_i, d.has_inject ? t.wi : t.wd, d.has_inject ? d.C : d.L, d.W, kKBlock, 32, true) ||
-        !make_map(&map_u, t.wu, u.W, u.L, kKBlock, u.HBt, true) ||
+    // INT4 weights are dequantised by producer warps; their (unused) weight
+    // maps are encoded over the residual, a valid bf16 tensor.
+    const bool q = d.wt == 1;
+    if (!make_map(&map_d, q ? d.raw : t.wd, q ? d.M : d.L, d.W, kKBlock, 32, true) ||
+        !make_map(&map_i, q ? d.raw : d.has_inject ? t.wi : t.wd, q ? d.M : d.has_inject ? d.C : d.L, d.W, kKBlock,
+                  32, true) ||
+        !make_map(&map_u, q ? u.raw : t.wu, q ? u.M : u.W, q ? u.W : u.L, kKBlock, u.HBt, true) ||
         !make_map(&map_ahi, t.red.act_hi, u.M, u.L, kKBlock, u.NT, true) ||
         !make_map(&map_alo, t.red.act_lo, u.M, u.L, kKBlock, u.NT, true) ||
         !make_map(&map_raw, u.raw, u.M, u.W, u.HBt, u.NT, false))
         return cudaErrorInvalidValue;
 
+    auto kd = q ? hc_tc_down_kernel<1> : hc_tc_down_kernel<0>;
+    auto ku = u.wt == 1 ? hc_tc_up_kernel<1> : hc_tc_up_kernel<0>;
     cudaError_t e;
-    if ((e = allow_smem_tc(hc_tc_down_kernel)) != cudaSuccess) return e;
-    if ((e = allow_smem_tc(hc_tc_up_kernel)) != cudaSuccess) return e;
+    if ((e = allow_smem_tc(kd)) != cudaSuccess) return e;
+    if ((e = allow_smem_tc(ku)) != cudaSuccess) return e;
     if ((e = allow_smem_tc(hc_tc_reduce_kernel, false)) != cudaSuccess) return e;
     const int ntiles = (d.M + d.NT - 1) / d.NT;
-    e = launch_tc(hc_tc_down_kernel, dim3(d.CS, d.C * d.RT, ntiles), dim3(kThreads),
-                  tc_down_smem(d.NT, d.n_stages), stream, d.CS, d, map_d, map_i);
+    e = launch_tc(kd, dim3(d.CS, d.C * d.RT, ntiles), dim3(kThreads),
+                  tc_down_smem(d.NT, d.n_stages, d.wt), stream, d.CS, d, map_d, map_i);
     if (e != cudaSuccess)
         return e;
     e = launch_tc(hc_tc_reduce_kernel, dim3((t.red.M + 31) / 32, (t.red.R + 31) / 32), dim3(1024), 0, stream, 0,
                   t.red);
     if (e != cudaSuccess)
         return e;
-    return launch_tc(hc_tc_up_kernel, dim3((u.H + u.HBt - 1) / u.HBt, ntiles), dim3(kThreads),
-                     tc_up_smem(u.NT, u.n_stages, u.C, u.HBt), stream, 0, u, map_u, map_ahi, map_alo, map_raw);
+    return launch_tc(ku, dim3((u.H + u.HBt - 1) / u.HBt, ntiles), dim3(kThreads),
+                     tc_up_smem(u.NT, u.n_stages, u.C, u.HBt, u.wt), stream, 0, u, map_u, map_ahi, map_alo, map_raw);
 }
 
 }  // namespace tshc

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "hc_kernels.h"
+
 namespace tshc {
 
 constexpr int kTcMinTokens = 16;          // the batched path starts at this many tokens
@@ -23,6 +25,10 @@ struct TcDownParams {
     const uint16_t *inj_out;  // fused inject-add of the previous sublayer, or nullptr
     const float *inj_gate;
     long inj_stride;
+    // INT4-affine weights (wt == 1): the producers dequantise the weight tiles
+    // to bf16 hi + lo in place of the TMA loads of bf16 tiles (wt == 0).
+    int wt;
+    WeightView dw, iw;        // input_mix_weight_down, block_inject_weight
 };
 
 struct TcReduceParams {
@@ -52,6 +58,8 @@ struct TcUpParams {
     const uint16_t *inj_out;
     const float *inj_gate;
     long inj_stride;
+    int wt;                   // 1: INT4-affine up weights, dequantised by producer warps
+    WeightView uw;
 };
 
 struct TcCall {
@@ -61,8 +69,8 @@ struct TcCall {
     const void *wd, *wi, *wu;  // bf16 weights
 };
 
-size_t tc_down_smem(int NT, int ns);
-size_t tc_up_smem(int NT, int ns, int C, int HBt);
+size_t tc_down_smem(int NT, int ns, int wt);
+size_t tc_up_smem(int NT, int ns, int C, int HBt, int wt);
 cudaError_t launch_tc_call(const TcCall &t, cudaStream_t stream);
 
 }  // namespace tshc

@@ -252,7 +252,11 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
 
     const int cs = tc_cluster_size(M, H, C, L);
     const bool all_bf16 = down->type == TS_W_BF16 && up->type == TS_W_BF16 && (!inject || inject->type == TS_W_BF16);
-    if (cs > 0 && all_bf16) {
+    // INT4-affine weights on the tensor cores: dequantised per tile to bf16 hi + lo.
+    const bool all_int4 = down->type == TS_W_INT4_AFFINE && up->type == TS_W_INT4_AFFINE &&
+                          (!inject || inject->type == TS_W_INT4_AFFINE) && down->group % 8 == 0 &&
+                          up->group % 8 == 0;
+    if (cs > 0 && (all_bf16 || all_int4)) {
         tshc::TcCall t{};
         const int R = L + (inject ? C : 0);
         const int NT = M >= 128 ? 128 : (M + 15) / 16 * 16;
@@ -266,8 +270,11 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         td.RT = (R + 127) / 128;
         td.CS = cs; td.chunk = H / cs;
         td.NT = NT;
+        td.wt = all_int4 ? 1 : 0;
+        td.dw = view(down);
+        td.iw = view(inject);
         td.n_stages = 4;
-        while (td.n_stages > 2 && tshc::tc_down_smem(NT, td.n_stages) > tshc::kTcSmemLimit)
+        while (td.n_stages > 2 && tshc::tc_down_smem(NT, td.n_stages, td.wt) > tshc::kTcSmemLimit)
             --td.n_stages;
         td.status = dev.status;
         if (fi) {
@@ -290,8 +297,10 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         tu.M = M; tu.H = H; tu.C = C; tu.L = L; tu.W = W;
         tu.HBt = (128 / C) / 8 * 8;
         tu.NT = NT;
+        tu.wt = td.wt;
+        tu.uw = view(up);
         tu.n_stages = 3;
-        while (tu.n_stages > 2 && tshc::tc_up_smem(NT, tu.n_stages, C, tu.HBt) > tshc::kTcSmemLimit)
+        while (tu.n_stages > 2 && tshc::tc_up_smem(NT, tu.n_stages, C, tu.HBt, tu.wt) > tshc::kTcSmemLimit)
             --tu.n_stages;
         tu.inv_C = tr.inv_C;
         tu.status = dev.status;

@@ -114,6 +114,15 @@ def test_int4_tiny_up_group_32(orc):
     call_and_inject(orc, inputs.TINY, inputs.SEEDS["int4"], kind="int4", group=64, up_group=32)
 
 
+@pytest.mark.parametrize("M,H,C,L,group,up_group", [(16, 2560, 4, 320, 64, None), (40, 512, 2, 64, 32, None),
+                                                      (128, 1024, 8, 128, 64, 32)])
+def test_int4_tensor_core_path(orc, M, H, C, L, group, up_group):
+    # INT4-affine weights from 16 tokens run on tcgen05: each weight tile is dequantised
+    # to bf16 hi + lo and multiplied against the activation's hi + lo (three MMAs)
+    call_and_inject(orc, inputs.Shape(M=M, H=H, C=C, L=L), seed=400 + M, kind="int4", group=group,
+                    up_group=up_group)
+
+
 @pytest.mark.parametrize("M", [1, 64])
 def test_int4_full_shape(orc, M):
     s = inputs.FULL_DECODE
