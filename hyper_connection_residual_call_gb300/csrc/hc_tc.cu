@@ -724,35 +724,46 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         const int cc = row / HBt, hl = row % HBt;
         const bool live = cc < C && h0 + hl < p.H;
         const float gv = live ? __bfloat162float(__ushort_as_bfloat16(p.g[cc * p.H + h0 + hl])) : 0.f;
-        // All of this warp's TMEM chunks (NT <= 128: at most 4) are loaded
-        // before one wait.
-        constexpr int kChunks = 4;
-        uint32_t vr[kChunks][16];
+        // The warp's 16-column chunks c0 = 16*half + 32k: chunk k+1 is loaded from
+        // TMEM while chunk k is processed (two register buffers; the loop body
+        // stays small, which keeps the epilogue's code in the instruction cache).
+        auto process = [&](int c0, const uint32_t (&vr)[16]) {
+            if (!live)
+                return;
 #pragma unroll
-        for (int k = 0; k < kChunks; ++k)
-            if (16 * half + 32 * k < NT)  // warp-uniform
-                tmem_ld16_async(tmem + ((uint32_t)(quad * 32) << 16) + 16 * half + 32 * k, vr[k]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < kChunks; ++k) {
-            const int c0 = 16 * half + 32 * k;
-            if (c0 < NT && live) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float vj = __uint_as_float(vr[k][j]);
-                    const int n = c0 + j;
-                    const int m = tile * NT + n;
-                    float rv = __bfloat162float(__ushort_as_bfloat16(raw_s[(cc * NT + n) * HBt + hl]));
-                    if (p.raw_out && m < p.M) {
-                        // fused inject-add: this thread owns residual element (m, cc, h)
-                        const size_t h = (size_t)h0 + hl;
-                        const float ov = __bfloat162float(__ushort_as_bfloat16(out_s[n * HBt + hl]));
-                        rv = bf16_round(fmaf(ov, pgate_s[n * C + cc], rv));
-                        p.raw_out[(size_t)m * p.W + (size_t)cc * p.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(rv));
-                    }
-                    mix_s[(cc * NT + n) * HBt + hl] = sigm_fast(vj) * (rv * inv_s[n * C + cc] * gv);
+            for (int j = 0; j < 16; ++j) {
+                const float vj = __uint_as_float(vr[j]);
+                const int n = c0 + j;
+                const int m = tile * NT + n;
+                float rv = __bfloat162float(__ushort_as_bfloat16(raw_s[(cc * NT + n) * HBt + hl]));
+                if (p.raw_out && m < p.M) {
+                    // fused inject-add: this thread owns residual element (m, cc, h)
+                    const size_t h = (size_t)h0 + hl;
+                    const float ov = __bfloat162float(__ushort_as_bfloat16(out_s[n * HBt + hl]));
+                    rv = bf16_round(fmaf(ov, pgate_s[n * C + cc], rv));
+                    p.raw_out[(size_t)m * p.W + (size_t)cc * p.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(rv));
                 }
+                mix_s[(cc * NT + n) * HBt + hl] = sigm_fast(vj) * (rv * inv_s[n * C + cc] * gv);
             }
+        };
+        const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16);
+        uint32_t va[16], vb[16];
+        int c0 = 16 * half;
+        if (c0 < NT)  // warp-uniform
+            tmem_ld16_async(tbase + c0, va);
+        tmem_wait_ld(va);
+#pragma unroll 1
+        for (; c0 < NT; c0 += 64) {
+            if (c0 + 32 < NT)
+                tmem_ld16_async(tbase + c0 + 32, vb);
+            process(c0, va);
+            tmem_wait_ld(vb);
+            if (c0 + 32 >= NT)
+                break;
+            if (c0 + 64 < NT)
+                tmem_ld16_async(tbase + c0 + 64, va);
+            process(c0 + 32, vb);
+            tmem_wait_ld(va);
         }
     }
     tc_fence_before();
