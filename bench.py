@@ -360,27 +360,26 @@ def measure_other_configs(B, inputs, torch, dev, stream, sets_bf16, peak):
         n = 4 * len(sets_q) if Mq == 1 else 2 * len(sets_q)
         ms = graph_ms(chain(raw, outs, gates, sets_q, n, mixed, ws, slots), 5)
         record(f"int4_m{Mq}", Mq, ms, n, bytes_per_call(Mq, sets_q[0].nbytes),
-               {"path": "CUDA-core one-token kernels" if Mq == 1 else "CUDA-core cluster split-K kernels"})
+               {"path": "CUDA-core one-token kernels" if Mq == 1
+                else "tensor-core (tcgen05) kernels, INT4 dequantised to bf16 hi + lo per tile"})
     del sets_q
 
-    # Full-depth stack: entry replication, 40 x (attn_hc + inject, mlp_hc + inject), exit mixer.
+    # Full-depth stack through the native driver (ts_hc_stack): entry replication,
+    # 40 x (attn_hc + inject, mlp_hc + inject), exit mixer fused with the last inject-add.
+    # The sublayer callback hands back stored outputs (the sublayers are not part of this path).
     n_layers = 40
     mixer_w = inputs.HCWeights(sets_bf16[0].g, sets_bf16[0].down, sets_bf16[0].up, None)
+    layers = [(sets_bf16[(2 * l) % len(sets_bf16)], sets_bf16[(2 * l + 1) % len(sets_bf16)])
+              for l in range(n_layers)]
     for Ms in (1, 16):
         emb = inputs.make_embedding(Ms, H, 3).to(dev)
-        raw = torch.empty((Ms, C * H), dtype=torch.bfloat16, device=dev)
         outs = [inputs.make_sublayer_out(Ms, H, 3, i).to(dev) for i in range(8)]
-        gates = torch.zeros((Ms, 2 * C), dtype=torch.float32, device=dev)
-        slots = [(gates[:, :C], 2 * C), (gates[:, C:], 2 * C)]
-        mixed = torch.empty((Ms, H), dtype=torch.bfloat16, device=dev)
         final = torch.empty((Ms, H), dtype=torch.bfloat16, device=dev)
-        ws = B.workspace(Ms, H, C, L, dev)
-        calls = chain(raw, outs, gates, sets_bf16, 2 * n_layers, mixed, ws, slots)
+        sws = B.stack_workspace(Ms, H, C, L, dev)
 
         def stack():
-            B.hc_replicate_entry(emb, C=C, raw=raw)
-            calls()
-            B.hc_mixer(raw, mixer_w, H=H, C=C, mixed=final, ws=ws)
+            B.hc_stack(emb, layers, mixer_w, lambda l, w, t0, mixed: outs[(2 * l + w) % len(outs)], C=C,
+                       max_chunk=Ms, mixed_out=final, ws=sws)
 
         ms = graph_ms(stack, 5)
         wb = sets_bf16[0].nbytes
@@ -389,7 +388,7 @@ def measure_other_configs(B, inputs, torch, dev, stream, sets_bf16, peak):
         gbs = total / (ms / 1e3) / 1e9
         out[f"stack40_m{Ms}"] = {"M": Ms, "tokens_per_s": Ms / (ms / 1e3), "us_per_token_step": 1e3 * ms,
                                  "bytes_per_step": total, "hbm_gbs": gbs, "frac": gbs / peak,
-                                 "calls_per_step": 2 * n_layers + 1}
+                                 "calls_per_step": 2 * n_layers + 1, "driver": "ts_hc_stack"}
     return out
 
 

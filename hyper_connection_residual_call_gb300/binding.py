@@ -28,7 +28,7 @@ RMS_EPS = 1e-6  # families/qwen4/mod.rs, RMS_EPS
 
 EXPORTS = ("ts_hc_workspace_bytes", "ts_hc_workspace_layout", "ts_hc_call", "ts_hc_inject_add",
            "ts_hc_mixer", "ts_hc_inject_call", "ts_hc_replicate_entry", "ts_hc_last_error",
-           "ts_hc_device_status", "ts_hc_call_noalloc")
+           "ts_hc_device_status", "ts_hc_call_noalloc", "ts_hc_stack_workspace_bytes", "ts_hc_stack")
 TS_HC_STATIC_SCRATCH_BYTES = 4 * 1024 * 1024  # include/ts_hc.h
 
 
@@ -47,6 +47,20 @@ class TsWeight(ctypes.Structure):
         ("biases", ctypes.c_void_p),
     ]
 
+
+class TsHcModule(ctypes.Structure):
+    """``ts_hc_module``: one hyper-connection module's hc_norm weight and linears."""
+    _fields_ = [
+        ("hc_norm_w", ctypes.c_void_p),
+        ("down", TsWeight),
+        ("up", TsWeight),
+        ("inject", TsWeight),
+    ]
+
+
+# ts_hc_sublayer_fn: (user, layer, which, t0, M, mixed, &out, stream) -> ts_status
+SUBLAYER_FN = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p)
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -80,6 +94,11 @@ def library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.ts_hc_call_noalloc.restype = i
         lib.ts_hc_replicate_entry.argtypes = [vp, vp, i, i, i, vp]
         lib.ts_hc_replicate_entry.restype = i
+        mp = ctypes.POINTER(TsHcModule)
+        lib.ts_hc_stack_workspace_bytes.argtypes = [i, i, i, i]
+        lib.ts_hc_stack_workspace_bytes.restype = sz
+        lib.ts_hc_stack.argtypes = [vp, i, mp, mp, i, mp, SUBLAYER_FN, vp, vp, i, i, i, i, f, vp, sz, vp]
+        lib.ts_hc_stack.restype = i
         lib.ts_hc_last_error.argtypes = []
         lib.ts_hc_last_error.restype = ctypes.c_char_p
         lib.ts_hc_device_status.argtypes = [vp, ctypes.POINTER(i)]
@@ -136,6 +155,19 @@ def ts_hc_call_noalloc(raw, hc_norm_w, down, up, inject, mixed, inject_w, inject
 
 def ts_hc_replicate_entry(emb, raw, M, H, C, stream) -> int:
     return library().ts_hc_replicate_entry(emb, raw, M, H, C, stream)
+
+
+def ts_hc_stack_workspace_bytes(max_chunk: int, H: int, C: int, lowrank: int) -> int:
+    return library().ts_hc_stack_workspace_bytes(max_chunk, H, C, lowrank)
+
+
+def ts_hc_stack(emb, T, attn, mlp, n_layers, final_mixer, sublayer, user, mixed_out, max_chunk, H, C, lowrank,
+                eps, workspace, workspace_bytes, stream) -> int:
+    """``attn`` / ``mlp``: ctypes arrays of ``TsHcModule`` (or None); ``final_mixer``: a
+    ``TsHcModule`` (or None); ``sublayer``: a ``SUBLAYER_FN`` (or None)."""
+    return library().ts_hc_stack(emb, T, attn, mlp, n_layers, _wref(final_mixer),
+                                 sublayer if sublayer is not None else SUBLAYER_FN(), user, mixed_out,
+                                 max_chunk, H, C, lowrank, eps, workspace, workspace_bytes, stream)
 
 
 def ts_hc_last_error() -> str:
@@ -317,3 +349,73 @@ def device_status(stream=None) -> int:
     st, v = ts_hc_device_status(_stream_handle(stream))
     _check(st)
     return v
+
+
+def module_struct(w) -> TsHcModule:
+    """A ``TsHcModule`` for weights with attributes g, down, up, inject (inject may be None)."""
+    m = TsHcModule()
+    m.hc_norm_w = w.g.data_ptr()
+    m.down, m.up = weight_struct(w.down), weight_struct(w.up)
+    if w.inject is not None:
+        m.inject = weight_struct(w.inject)
+    return m
+
+
+def stack_workspace(max_chunk: int, H: int, C: int, L: int, device=None):
+    torch = _torch()
+    n = max(ts_hc_stack_workspace_bytes(max_chunk, H, C, L), 256)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def hc_stack(emb, layers, final, sublayer, *, C: int, max_chunk: Optional[int] = None, mixed_out=None,
+             eps: float = RMS_EPS, ws=None, stream=None):
+    """The decoder stack's hyper-connection path on T tokens through ``ts_hc_stack``.
+
+    ``emb`` [T, H] bf16; ``layers``: a sequence of (attn, mlp) weights (g, down, up,
+    inject); ``final``: the exit mixer's weights. ``sublayer(layer, which, t0, mixed)``
+    gets the call's output ``mixed`` ([M, H] bf16, a view into the workspace) and
+    returns the sublayer output, a CUDA bf16 tensor [M, H] that it may compute on the
+    current stream; the driver injects it with the call's gates. Returns
+    (mixed_out [T, H], the last chunk's residual [M, C*H] -- a view into ``ws``).
+    """
+    torch = _torch()
+    T, H = emb.shape
+    L = final.down.rows
+    _need(emb, "emb", torch.bfloat16, (T, H))
+    max_chunk = max(T, 1) if max_chunk is None else max_chunk
+    if mixed_out is None:
+        mixed_out = torch.empty((T, H), dtype=torch.bfloat16, device=emb.device)
+    _need(mixed_out, "mixed_out", torch.bfloat16, (T, H))
+    if ws is None:
+        ws = stack_workspace(max_chunk, H, C, L, emb.device)
+    n = len(layers)
+    attn = (TsHcModule * max(n, 1))(*[module_struct(a) for a, _ in layers])
+    mlp = (TsHcModule * max(n, 1))(*[module_struct(m) for _, m in layers])
+    fin = module_struct(final)
+    keep, errors = [], []
+    base = ws.data_ptr()
+
+    def trampoline(user, layer, which, t0, M, mixed_ptr, out_pp, stream_h):
+        try:
+            off = mixed_ptr - base
+            mixed = ws[off:off + 2 * M * H].view(torch.bfloat16).view(M, H)
+            out = sublayer(layer, which, t0, mixed)
+            _need(out, "sublayer output", torch.bfloat16, (M, H))
+            if stream is not None:  # the caching allocator must not hand it out before the driver's stream used it
+                out.record_stream(stream)
+            keep.append(out)
+            out_pp[0] = out.data_ptr()
+            return TS_OK
+        except Exception as e:  # reported after the C call returns
+            errors.append(e)
+            return TS_ERR_INVALID_ARG
+
+    fn = SUBLAYER_FN(trampoline)
+    st = ts_hc_stack(emb.data_ptr(), T, attn, mlp, n, fin, fn, None, mixed_out.data_ptr(), max_chunk, H, C,
+                     L, eps, base, ws.numel() * ws.element_size(), _stream_handle(stream))
+    if errors:
+        raise errors[0]
+    _check(st)
+    M_last = T - (max(T, 1) - 1) // max_chunk * max_chunk if T else 0
+    raw_last = ws[:2 * M_last * C * H].view(torch.bfloat16).view(M_last, C * H)
+    return mixed_out, raw_last

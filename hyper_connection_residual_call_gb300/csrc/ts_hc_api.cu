@@ -11,6 +11,7 @@
 #include "hc_kernels.h"
 #include "hc_tc.h"
 #include "ts_hc.h"
+#include "ts_hc_internal.h"
 
 namespace {
 
@@ -137,6 +138,59 @@ tshc::WeightView view(const ts_weight *w)
     v.biases = static_cast<const uint16_t *>(w->biases);
     return v;
 }
+
+}  // namespace
+
+namespace tshc {
+
+void clear_error() { g_last_error.clear(); }
+
+ts_status api_error(ts_status st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+ts_status check_shape_api(int M, int H, int C, int lowrank) { return check_shape(M, H, C, lowrank); }
+
+ts_status check_ptr_api(const void *p, const char *name, size_t align) { return check_ptr(p, name, align); }
+
+ts_status check_module(const ts_hc_module *m, bool with_inject, int H, int C, int lowrank, const char *name)
+{
+    if (!m)
+        return fail(TS_ERR_INVALID_ARG, "%s is NULL", name);
+    const int W = C * H;
+    char what[128];
+    snprintf(what, sizeof what, "%s.hc_norm_w", name);
+    ts_status st = check_ptr(m->hc_norm_w, what, 16);
+    if (st != TS_OK)
+        return st;
+    snprintf(what, sizeof what, "%s.down", name);
+    if ((st = check_weight(&m->down, what, lowrank, W)) != TS_OK)
+        return st;
+    snprintf(what, sizeof what, "%s.up", name);
+    if ((st = check_weight(&m->up, what, W, lowrank)) != TS_OK)
+        return st;
+    if (with_inject) {
+        snprintf(what, sizeof what, "%s.inject", name);
+        if ((st = check_weight(&m->inject, what, C, W)) != TS_OK)
+            return st;
+        if (m->inject.type != m->down.type ||
+            (m->down.type == TS_W_INT4_AFFINE && m->inject.group != m->down.group))
+            return fail(TS_ERR_UNSUPPORTED, "%s: inject must have the same storage format and group as down",
+                        name);
+    }
+    return TS_OK;
+}
+
+}  // namespace tshc
+
+namespace {
 
 // The batched tensor-core path: M >= kTcMinTokens, lowrank a multiple of 64,
 // and a stream split into CS chunks that are multiples of 64 (largest CS <= 8).

@@ -1,0 +1,167 @@
+// ts_hc_stack.cu -- the decoder stack's hyper-connection path over a prompt,
+// chunk by chunk (ts_hc_stack in include/ts_hc.h). Host code only: it
+// sequences the library's own entry points on one stream and allocates
+// nothing.
+//
+// families/qwen4/mod.rs, decoder-layer pseudocode: the residual enters as the
+// embedding row repeated C times, each layer reads it through attn_hc and
+// mlp_hc and adds the sublayer outputs back with the inject gates, and the
+// exit hyper_connection_mixer collapses it to H. real_forward.rs describes the
+// chunked-prefill driver that runs a prompt through the layers one
+// micro-batch of rows at a time; in this path tokens do not interact, so the
+// chunks are independent and run one after the other.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+
+#include "ts_hc.h"
+#include "ts_hc_internal.h"
+
+namespace {
+
+size_t a256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Workspace of the driver: the chunk's residual, the calls' mixed output, the
+// chunk's [M][2][C] gate buffer, then the calls' own workspace (the largest
+// any chunk size up to max_chunk needs).
+struct StackWs {
+    size_t raw, mixed, gates, call, call_bytes, total;
+};
+
+StackWs stack_ws(int max_chunk, int H, int C, int L)
+{
+    StackWs w{};
+    const size_t M = (size_t)max_chunk, W = (size_t)C * H;
+    w.raw = 0;
+    w.mixed = a256(2 * M * W);
+    w.gates = w.mixed + a256(2 * M * H);
+    w.call = w.gates + a256(4 * M * 2 * C);
+    size_t need = 0;
+    for (int m = 1; m <= max_chunk; ++m)
+        need = std::max(need, ts_hc_workspace_bytes(m, H, C, L));
+    w.call_bytes = a256(need);
+    w.total = w.call + w.call_bytes;
+    return w;
+}
+
+const char *sublayer_name(int which) { return which == 0 ? "attention" : "MoE"; }
+
+}  // namespace
+
+extern "C" {
+
+size_t ts_hc_stack_workspace_bytes(int max_chunk, int H, int C, int lowrank)
+{
+    if (max_chunk < 1 || tshc::check_shape_api(max_chunk, H, C, lowrank) != TS_OK) {
+        tshc::clear_error();
+        return 0;
+    }
+    return stack_ws(max_chunk, H, C, lowrank).total;
+}
+
+ts_status ts_hc_stack(const void *emb, int T, const ts_hc_module *attn, const ts_hc_module *mlp,
+                      int n_layers, const ts_hc_module *final_mixer, ts_hc_sublayer_fn sublayer,
+                      void *user, void *mixed_out, int max_chunk, int H, int C, int lowrank,
+                      float eps, void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    using tshc::api_error;
+    tshc::clear_error();
+    if (T < 0)
+        return api_error(TS_ERR_INVALID_ARG, "T = %d must be >= 0", T);
+    if (n_layers < 0)
+        return api_error(TS_ERR_INVALID_ARG, "n_layers = %d must be >= 0", n_layers);
+    if (max_chunk < 1)
+        return api_error(TS_ERR_INVALID_ARG, "max_chunk = %d must be >= 1", max_chunk);
+    ts_status st = tshc::check_shape_api(max_chunk, H, C, lowrank);
+    if (st != TS_OK)
+        return st;
+    if (T == 0)  // nothing is read or written: pointers are not examined
+        return TS_OK;
+
+    // Everything is validated before the first launch.
+    if ((st = tshc::check_ptr_api(emb, "emb", 16)) != TS_OK) return st;
+    if ((st = tshc::check_ptr_api(mixed_out, "mixed_out", 16)) != TS_OK) return st;
+    if (!(eps >= 0.0f) || eps > 1.0f)
+        return api_error(TS_ERR_INVALID_ARG, "eps = %g must be in [0, 1]", (double)eps);
+    if (n_layers > 0) {
+        if (!attn || !mlp)
+            return api_error(TS_ERR_INVALID_ARG, "%s is NULL with n_layers = %d", attn ? "mlp" : "attn", n_layers);
+        if (!sublayer)
+            return api_error(TS_ERR_INVALID_ARG, "sublayer is NULL with n_layers = %d", n_layers);
+        char name[64];
+        for (int l = 0; l < n_layers; ++l) {
+            snprintf(name, sizeof name, "attn[%d]", l);
+            if ((st = tshc::check_module(attn + l, true, H, C, lowrank, name)) != TS_OK) return st;
+            snprintf(name, sizeof name, "mlp[%d]", l);
+            if ((st = tshc::check_module(mlp + l, true, H, C, lowrank, name)) != TS_OK) return st;
+        }
+    }
+    if ((st = tshc::check_module(final_mixer, false, H, C, lowrank, "final_mixer")) != TS_OK)
+        return st;
+    const StackWs lay = stack_ws(max_chunk, H, C, lowrank);
+    if (!workspace || workspace_bytes < lay.total)
+        return api_error(TS_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace_bytes, lay.total);
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+        return api_error(TS_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+
+    char *ws = static_cast<char *>(workspace);
+    void *raw = ws + lay.raw;
+    void *mixed = ws + lay.mixed;
+    float *gates = reinterpret_cast<float *>(ws + lay.gates);
+    void *cws = ws + lay.call;
+    const long gstride = 2L * C;  // token t's slots at t*C*2 (attn_hc) and t*C*2 + C (mlp_hc)
+
+    for (int t0 = 0; t0 < T; t0 += max_chunk) {
+        const int M = std::min(max_chunk, T - t0);
+        st = ts_hc_replicate_entry(static_cast<const char *>(emb) + 2 * (size_t)t0 * H, raw, M, H, C, stream);
+        if (st != TS_OK)
+            return st;
+        const void *prev_out = nullptr;  // the last sublayer output, not yet injected
+        const float *prev_gate = nullptr;
+        for (int l = 0; l < n_layers; ++l) {
+            for (int which = 0; which < 2; ++which) {
+                const ts_hc_module &m = which == 0 ? attn[l] : mlp[l];
+                float *slot = gates + which * C;
+                st = prev_out == nullptr
+                         ? ts_hc_call(raw, m.hc_norm_w, &m.down, &m.up, &m.inject, mixed, slot, gstride, M, H,
+                                      C, lowrank, eps, cws, lay.call_bytes, stream)
+                         : ts_hc_inject_call(raw, prev_out, prev_gate, gstride, m.hc_norm_w, &m.down, &m.up,
+                                             &m.inject, mixed, slot, gstride, M, H, C, lowrank, eps, cws,
+                                             lay.call_bytes, stream);
+                if (st != TS_OK)
+                    return st;
+                const void *out = nullptr;
+                st = sublayer(user, l, which, t0, M, mixed, &out, stream);
+                if (st != TS_OK)
+                    return api_error(st, "the %s sublayer callback of layer %d (tokens %d..%d) returned status %d",
+                                     sublayer_name(which), l, t0, t0 + M - 1, (int)st);
+                if (!out || reinterpret_cast<uintptr_t>(out) % 16 != 0)
+                    return api_error(TS_ERR_INVALID_ARG,
+                                     "the %s sublayer callback of layer %d gave %s output pointer",
+                                     sublayer_name(which), l, out ? "a misaligned" : "a NULL");
+                // The next call overwrites the workspace (mixed included) while it reads out.
+                const char *o = static_cast<const char *>(out);
+                if (o < ws + lay.total && o + 2 * (size_t)M * H > ws)
+                    return api_error(TS_ERR_INVALID_ARG,
+                                     "the %s sublayer callback of layer %d gave an output inside the workspace",
+                                     sublayer_name(which), l);
+                prev_out = out;
+                prev_gate = slot;
+            }
+        }
+        void *mo = static_cast<char *>(mixed_out) + 2 * (size_t)t0 * H;
+        const ts_hc_module &f = *final_mixer;
+        st = prev_out == nullptr
+                 ? ts_hc_mixer(raw, f.hc_norm_w, &f.down, &f.up, mo, M, H, C, lowrank, eps, cws, lay.call_bytes,
+                               stream)
+                 : ts_hc_inject_call(raw, prev_out, prev_gate, gstride, f.hc_norm_w, &f.down, &f.up, nullptr,
+                                     mo, nullptr, 0, M, H, C, lowrank, eps, cws, lay.call_bytes, stream);
+        if (st != TS_OK)
+            return st;
+    }
+    return TS_OK;
+}
+
+}  // extern "C"

@@ -207,6 +207,65 @@ ts_status ts_hc_inject_call(void *raw, const void *out, const float *prev_inject
  */
 ts_status ts_hc_replicate_entry(const void *emb, void *raw, int M, int H, int C, cudaStream_t stream);
 
+/*
+ * The decoder stack's hyper-connection path, driven over a prompt in chunks
+ * (families/qwen4/mod.rs, decoder-layer pseudocode: entry replication, per
+ * layer attn_hc -> sublayer -> inject-add -> mlp_hc -> sublayer -> inject-add,
+ * exit hyper_connection_mixer; real_forward.rs, the chunked-prefill driver that
+ * runs a prompt through the layers a micro-batch of rows at a time).
+ *
+ * Tokens do not interact in this path, so the T tokens are processed in
+ * chunks of at most max_chunk tokens, one after the other. For each chunk of
+ * M tokens starting at token t0:
+ *   raw = repeat(emb[t0 .. t0+M), C)                        ts_hc_replicate_entry
+ *   for layer l: attn_hc(attn[l]) -> sublayer(l, 0) -> mlp_hc(mlp[l]) -> sublayer(l, 1),
+ *                each inject-add fused into the call after it   ts_hc_inject_call
+ *   mixed_out[t0 .. t0+M) = hyper_connection_mixer(final)   (fused with the last inject-add)
+ * attn_hc writes token t's gates to slot 0 and mlp_hc to slot 1 of a
+ * [M][2][C] gate buffer, i.e. at element t*C*2 and t*C*2 + C (hc.rs,
+ * inject_row_offset).
+ *
+ * The sublayers (GDN / QSA attention, MoE) are the caller's: after every
+ * hyper-connection call the driver calls
+ *     sublayer(user, layer, which, t0, M, mixed, &out, stream)
+ * with `mixed` the call's output (bf16 [M][H], device, valid in stream order
+ * until the driver's next launch) and which = 0 after attn_hc, 1 after mlp_hc.
+ * The callback may enqueue work on `stream`; it sets `out` to a 16-byte aligned
+ * device buffer bf16 [M][H] holding the sublayer output, outside the workspace,
+ * which must stay valid until the next hyper-connection call has read it (in
+ * stream order). A status other than TS_OK, or a NULL, misaligned or
+ * workspace-overlapping `out`, stops the driver, which returns an error; work
+ * launched before that point stays queued.
+ *
+ *   emb        bf16 [T][H], the embedding rows
+ *   attn, mlp  n_layers modules each; their inject weights are required
+ *   final      the exit mixer's module; its inject is not read
+ *   mixed_out  bf16 [T][H], written
+ *   max_chunk  >= 1 tokens per chunk
+ *   workspace  >= ts_hc_stack_workspace_bytes(max_chunk, H, C, lowrank) bytes,
+ *              256-byte aligned; on return it begins with the last chunk's
+ *              residual bf16 [M][C*H] after its last inject-add
+ * Every module's tensors are validated before anything is launched. The driver
+ * allocates nothing and never synchronises, so a caller may capture the whole
+ * pass into a CUDA graph when its callback's work is capturable. T == 0 is a
+ * no-op.
+ */
+typedef struct {
+    const void *hc_norm_w;    /* bf16 [C*H] */
+    ts_weight down;           /* [lowrank][C*H] */
+    ts_weight up;             /* [C*H][lowrank] */
+    ts_weight inject;         /* [C][C*H]; not read for the exit mixer */
+} ts_hc_module;
+
+typedef ts_status (*ts_hc_sublayer_fn)(void *user, int layer, int which, int t0, int M,
+                                       const void *mixed, const void **out, cudaStream_t stream);
+
+size_t ts_hc_stack_workspace_bytes(int max_chunk, int H, int C, int lowrank);
+ts_status ts_hc_stack(const void *emb, int T, const ts_hc_module *attn, const ts_hc_module *mlp,
+                      int n_layers, const ts_hc_module *final_mixer, ts_hc_sublayer_fn sublayer,
+                      void *user, void *mixed_out, int max_chunk, int H, int C, int lowrank,
+                      float eps, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* The last error message of the calling thread ("" if none). */
 const char *ts_hc_last_error(void);
 

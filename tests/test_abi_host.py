@@ -174,3 +174,62 @@ def test_torch_layer_requires_cuda_tensors(lib):
         B.hc_call(raw, w, H=256, C=4)
     with pytest.raises(B.HCError, match="CUDA tensor"):
         B.hc_inject_add(raw, torch.zeros(1, 256, dtype=torch.bfloat16), torch.ones(1, 4), H=256, C=4)
+
+
+def _module(**kw):
+    m = B.TsHcModule()
+    m.hc_norm_w = kw.get("g", FAKE)
+    m.down, m.up = kw.get("down", _w()), kw.get("up", _w())
+    m.inject = kw.get("inject", _w())
+    return m
+
+
+def _stack(**kw):
+    n = kw.get("n_layers", 2)
+    attn = kw.get("attn", (B.TsHcModule * max(n, 1))(*[_module() for _ in range(n)]))
+    mlp = kw.get("mlp", (B.TsHcModule * max(n, 1))(*[_module() for _ in range(n)]))
+    final = kw.get("final", _module(inject=_w(data=None)))
+    fn = kw.get("fn", B.SUBLAYER_FN(lambda *a: B.TS_OK))
+    return B.ts_hc_stack(kw.get("emb", FAKE), kw.get("T", 5), attn, mlp, n, final, fn, None,
+                         kw.get("mixed_out", FAKE), kw.get("max_chunk", 4), H, C, L, kw.get("eps", 1e-6),
+                         kw.get("ws", FAKE), kw.get("ws_bytes", 1 << 30), None)
+
+
+def test_stack_workspace_bytes(lib):
+    a256 = lambda n: (n + 255) // 256 * 256
+    for chunk in (1, 7, 16, 40):
+        calls = max(B.ts_hc_workspace_bytes(m, H, C, L) for m in range(1, chunk + 1))
+        want = a256(2 * chunk * C * H) + a256(2 * chunk * H) + a256(4 * chunk * 2 * C) + a256(calls)
+        assert B.ts_hc_stack_workspace_bytes(chunk, H, C, L) == want
+    assert B.ts_hc_stack_workspace_bytes(0, H, C, L) == 0
+    assert B.ts_hc_stack_workspace_bytes(4, H, 0, L) == 0
+
+
+def test_stack_t0_is_noop(lib):
+    assert _stack(T=0, emb=None, mixed_out=None, ws=None, ws_bytes=0) == B.TS_OK
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(T=-1), B.TS_ERR_INVALID_ARG, "T = -1"),
+    (dict(max_chunk=0), B.TS_ERR_INVALID_ARG, "max_chunk"),
+    (dict(emb=None), B.TS_ERR_INVALID_ARG, "emb is NULL"),
+    (dict(mixed_out=FAKE + 2), B.TS_ERR_INVALID_ARG, "mixed_out is not 16-byte aligned"),
+    (dict(fn=None), B.TS_ERR_INVALID_ARG, "sublayer is NULL"),
+    (dict(attn=None), B.TS_ERR_INVALID_ARG, "attn is NULL"),
+    (dict(mlp=(B.TsHcModule * 2)(_module(), _module(down=_w(data=FAKE + 8)))), B.TS_ERR_INVALID_ARG,
+     "mlp[1].down.data"),
+    (dict(attn=(B.TsHcModule * 2)(_module(), _module(inject=_w(data=None)))), B.TS_ERR_INVALID_ARG,
+     "attn[1].inject.data"),
+    (dict(attn=(B.TsHcModule * 2)(_module(g=None), _module())), B.TS_ERR_INVALID_ARG, "attn[0].hc_norm_w is NULL"),
+    (dict(final=None), B.TS_ERR_INVALID_ARG, "final_mixer is NULL"),
+    (dict(final=_module(up=_w(typ=7))), B.TS_ERR_INVALID_ARG, "final_mixer.up.type"),
+    (dict(ws_bytes=1024), B.TS_ERR_WORKSPACE, "workspace"),
+    (dict(ws=FAKE + 16), B.TS_ERR_INVALID_ARG, "256-byte aligned"),
+    (dict(eps=-1.0), B.TS_ERR_INVALID_ARG, "eps"),
+])
+def test_stack_rejects(lib, kw, status, needle):
+    calls = []
+    kw.setdefault("fn", B.SUBLAYER_FN(lambda *a: calls.append(a) or B.TS_OK))
+    assert _stack(**kw) == status
+    assert needle in B.ts_hc_last_error()
+    assert not calls, "the sublayer callback ran before validation finished"

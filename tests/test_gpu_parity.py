@@ -312,6 +312,92 @@ def test_full_depth_stack(orc, M):
     check_bf16_carried(raw, ref["raw"], ref["peak"], f"stack residual M={M}")
     mixed_f, raw_f = run_stack_gpu_fused(dev, H, C)
     assert torch.equal(raw_f, raw) and torch.equal(mixed_f, mixed), "fused stack differs from the unfused one"
+    # The native driver (ts_hc_stack): one chunk of all M tokens runs the same
+    # calls in the same order as the fused loop above, so it is bit-identical.
+    mixed_d, raw_d = run_stack_driver(dev, H, C, max_chunk=M)
+    assert torch.equal(raw_d, raw) and torch.equal(mixed_d, mixed), "driver differs from the fused loop"
+    if M > 1:
+        # Ragged chunks (5, 5, 5, 1 tokens) take other kernel paths per chunk;
+        # every token's output still matches the oracle.
+        mixed_c, raw_c = run_stack_driver(dev, H, C, max_chunk=5)
+        check_bf16(mixed_c, ref["mixed"], f"chunked driver mixer output M={M}")
+        check_bf16_carried(raw_c, ref["raw"][-raw_c.shape[0]:], ref["peak"][-raw_c.shape[0]:],
+                           f"chunked driver residual (last chunk) M={M}")
+
+
+def run_stack_driver(st, H, C, max_chunk):
+    """The stack through ts_hc_stack; the sublayer callback hands back the stored outputs."""
+    M = st.emb.shape[0]
+    seen = []
+
+    def sublayer(layer, which, t0, mixed):
+        seen.append((layer, which, t0, mixed.shape[0]))
+        return st.outs[layer][which][t0:t0 + mixed.shape[0]]
+
+    mixed, raw = B.hc_stack(st.emb.cuda(), st.layers, st.final, sublayer, C=C, max_chunk=max_chunk)
+    torch.cuda.synchronize()
+    n = len(st.layers)
+    want = [(l, w, t0, min(max_chunk, M - t0)) for t0 in range(0, M, max_chunk) for l in range(n) for w in (0, 1)]
+    assert seen == want, "sublayer callbacks out of order"
+    return mixed, raw.clone()
+
+
+@pytest.mark.parametrize("max_chunk", [3, 4])
+def test_stack_driver_feeds_mixed_to_the_sublayer(max_chunk):
+    """A sublayer that reads mixed (out = bf16(0.5 * mixed + the stored output)):
+    the driver equals the same library calls issued one by one, bit for bit."""
+    s = inputs.TINY
+    H, C, L, M, n = s.H, s.C, s.L, 7, 3
+    st = inputs.make_stack(M, H, C, L, n, 21)
+    dev = inputs.StackInputs(st.emb, [(a.to("cuda"), m.to("cuda")) for a, m in st.layers],
+                             [(a.cuda(), m.cuda()) for a, m in st.outs], st.final.to("cuda"))
+
+    def rule(layer, which, t0, mixed):
+        stored = dev.outs[layer][which][t0:t0 + mixed.shape[0]]
+        return (0.5 * mixed.float() + stored.float()).to(torch.bfloat16)
+
+    mixed_d, raw_last = B.hc_stack(dev.emb.cuda(), dev.layers, dev.final, rule, C=C, max_chunk=max_chunk)
+    torch.cuda.synchronize()
+    # the same calls by hand, chunk by chunk
+    ws = torch.empty(max(B.ts_hc_workspace_bytes(m, H, C, L) for m in range(1, max_chunk + 1)),
+                     dtype=torch.uint8, device="cuda")
+    want = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    for t0 in range(0, M, max_chunk):
+        m = min(max_chunk, M - t0)
+        raw = B.hc_replicate_entry(dev.emb[t0:t0 + m].cuda(), C=C)
+        gates = torch.empty((m * 2 * C,), dtype=torch.float32, device="cuda")
+        mixed = torch.empty((m, H), dtype=torch.bfloat16, device="cuda")
+        prev = None
+        for layer, (attn, mlp) in enumerate(dev.layers):
+            for which, (wts, slot) in enumerate(((attn, gates), (mlp, gates[C:]))):
+                if prev is None:
+                    B.hc_call(raw, wts, H=H, C=C, mixed=mixed, inject_w=slot, inject_stride=2 * C, ws=ws)
+                else:
+                    B.hc_inject_call(raw, prev[0], prev[1], wts, H=H, C=C, prev_inject_stride=2 * C, mixed=mixed,
+                                     inject_w=slot, inject_stride=2 * C, ws=ws)
+                prev = (rule(layer, which, t0, mixed), slot)
+        B.hc_inject_call(raw, prev[0], prev[1], dev.final, H=H, C=C, prev_inject_stride=2 * C,
+                         mixed=want[t0:t0 + m], ws=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(mixed_d, want), "driver differs from the calls issued by hand"
+    assert torch.equal(raw_last, raw), "driver's last-chunk residual differs"
+
+
+def test_stack_driver_rejects_bad_sublayer_outputs():
+    s = inputs.TINY
+    H, C, L, M = s.H, s.C, s.L, 2
+    st = inputs.make_stack(M, H, C, L, 1, 22)
+    layers = [(a.to("cuda"), m.to("cuda")) for a, m in st.layers]
+    final = st.final.to("cuda")
+    emb = st.emb.cuda()
+    with pytest.raises(B.HCError, match="inside the workspace"):
+        B.hc_stack(emb, layers, final, lambda l, w, t0, mixed: mixed, C=C)   # aliases the driver's buffer
+    with pytest.raises(ValueError, match="refused"):
+        def boom(l, w, t0, mixed):
+            raise ValueError("refused by the sublayer")
+        B.hc_stack(emb, layers, final, boom, C=C)
+    torch.cuda.synchronize()
+    assert B.device_status() == B.TS_OK
 
 
 def test_replicate_entry():
