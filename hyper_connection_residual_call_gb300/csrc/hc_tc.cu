@@ -46,7 +46,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-__device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
 // Sigmoid from the fast exponential and division intrinsics (relative error
 // ~1e-6, far inside the 1e-3 bar), for the per-element epilogues.
 __device__ __forceinline__ float sigm_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
@@ -247,7 +246,6 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
             const int m = tile * NT + n;
             live[j] = n < NT && m < p.M;
             ssq[j] = 0.f;
-            inj_g[j] = (live[j] && p.inj_out) ? p.inj_gate[(size_t)m * p.inj_stride + c] : 0.f;
             rrow[j] = reinterpret_cast<const uint4 *>(p.raw + (size_t)(live[j] ? m : 0) * p.W + k0) + ck;
             orow[j] = p.inj_out ? reinterpret_cast<const uint4 *>(p.inj_out + (size_t)(live[j] ? m : 0) * p.H
                                                                   + q * p.chunk) + ck
@@ -295,6 +293,13 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
         fetch_w(0);  // weights do not depend on the previous kernel
         pdl_wait();  // raw is produced by the previous kernel in the stream
         fetch(0);
+        // The previous gates come from the previous call's reduce kernel, which
+        // can still be running when this kernel starts: read only after the wait.
+#pragma unroll
+        for (int j = 0; j < kItems; ++j) {
+            const int m = tile * NT + ((t + kProducers * j) >> 3);
+            inj_g[j] = (live[j] && p.inj_out) ? p.inj_gate[(size_t)m * p.inj_stride + c] : 0.f;
+        }
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % NS, u = kb / NS;
             uint4 rcur[kItems], ocur[kItems];
@@ -727,24 +732,37 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         // The warp's 16-column chunks c0 = 16*half + 32k: chunk k+1 is loaded from
         // TMEM while chunk k is processed (two register buffers; the loop body
         // stays small, which keeps the epilogue's code in the instruction cache).
+        // Every shared-memory load of a chunk is issued before its first store:
+        // the compiler cannot tell the global residual from the shared tiles,
+        // so a load placed after a store would wait for it.
+        const bool fused = p.raw_out != nullptr;
+        uint16_t *rout = fused ? p.raw_out + (size_t)cc * p.H + h0 + hl : nullptr;
         auto process = [&](int c0, const uint32_t (&vr)[16]) {
             if (!live)
                 return;
+            float rv[16], sc[16], ov[16], pg[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const float vj = __uint_as_float(vr[j]);
                 const int n = c0 + j;
-                const int m = tile * NT + n;
-                float rv = __bfloat162float(__ushort_as_bfloat16(raw_s[(cc * NT + n) * HBt + hl]));
-                if (p.raw_out && m < p.M) {
-                    // fused inject-add: this thread owns residual element (m, cc, h)
-                    const size_t h = (size_t)h0 + hl;
-                    const float ov = __bfloat162float(__ushort_as_bfloat16(out_s[n * HBt + hl]));
-                    rv = bf16_round(fmaf(ov, pgate_s[n * C + cc], rv));
-                    p.raw_out[(size_t)m * p.W + (size_t)cc * p.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(rv));
+                rv[j] = __bfloat162float(__ushort_as_bfloat16(raw_s[(cc * NT + n) * HBt + hl]));
+                sc[j] = inv_s[n * C + cc] * gv;
+                if (fused) {
+                    ov[j] = __bfloat162float(__ushort_as_bfloat16(out_s[n * HBt + hl]));
+                    pg[j] = pgate_s[n * C + cc];
                 }
-                mix_s[(cc * NT + n) * HBt + hl] = sigm_fast(vj) * (rv * inv_s[n * C + cc] * gv);
             }
+            if (fused) {  // the inject-add: this thread owns residual elements (m, cc, h)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    rv[j] = bf16_round(fmaf(ov[j], pg[j], rv[j]));
+                    const int m = tile * NT + c0 + j;
+                    if (m < p.M)
+                        rout[(size_t)m * p.W] = __bfloat16_as_ushort(__float2bfloat16_rn(rv[j]));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                mix_s[(cc * NT + c0 + j) * HBt + hl] = sigm_fast(__uint_as_float(vr[j])) * (rv[j] * sc[j]);
         };
         const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16);
         uint32_t va[16], vb[16];

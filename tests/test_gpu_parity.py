@@ -299,6 +299,37 @@ def test_fused_inject_call_is_bit_identical(M):
     assert torch.equal(ga, gb)
 
 
+@pytest.mark.parametrize("M", [1, 3, 16, 40])
+def test_fused_inject_reads_the_previous_gates_after_they_are_written(M):
+    """A fused call starts before the previous call has finished (programmatic
+    dependent launch) but must read that call's gates only once written: with
+    the gate buffer refilled with NaN before every pair, each pair must equal,
+    bit for bit, the same pair with a host synchronisation between the calls."""
+    s = inputs.FULL_DECODE
+    H, C, L = s.H, s.C, s.L
+    w1, w2 = inputs.make_hc_weights(H, C, L, 12, 0).to("cuda"), inputs.make_hc_weights(H, C, L, 12, 1).to("cuda")
+    raw0 = inputs.make_residual(M, H, C, 12).cuda()
+    out = inputs.make_sublayer_out(M, H, 12, 0).cuda()
+    ws = B.workspace(M, H, C, L)
+
+    def pair(sync):
+        raw = raw0.clone()
+        gates = torch.full((M * 2 * C,), float("nan"), device="cuda")
+        B.hc_call(raw, w1, H=H, C=C, inject_w=gates, inject_stride=2 * C, ws=ws)
+        if sync:
+            torch.cuda.synchronize()
+        mixed, _ = B.hc_inject_call(raw, out, gates, w2, H=H, C=C, prev_inject_stride=2 * C,
+                                    inject_w=gates[C:], inject_stride=2 * C, ws=ws)
+        torch.cuda.synchronize()
+        return mixed, raw, gates
+
+    want = pair(True)
+    assert all(bool(torch.isfinite(t).all()) for t in want)
+    for _ in range(25):
+        got = pair(False)
+        assert all(torch.equal(a, b) for a, b in zip(got, want)), "a fused call read stale gates"
+
+
 @pytest.mark.parametrize("M", [1, 16])
 def test_full_depth_stack(orc, M):
     s = inputs.FULL_DECODE
