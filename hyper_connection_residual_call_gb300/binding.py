@@ -29,7 +29,7 @@ RMS_EPS = 1e-6  # families/qwen4/mod.rs, RMS_EPS
 EXPORTS = ("ts_hc_workspace_bytes", "ts_hc_workspace_layout", "ts_hc_call", "ts_hc_inject_add",
            "ts_hc_mixer", "ts_hc_inject_call", "ts_hc_replicate_entry", "ts_hc_last_error",
            "ts_hc_device_status", "ts_hc_call_noalloc", "ts_hc_stack_workspace_bytes", "ts_hc_stack")
-TS_HC_STATIC_SCRATCH_BYTES = 4 * 1024 * 1024  # include/ts_hc.h
+TS_HC_STATIC_SCRATCH_BYTES = 64 * 1024 * 1024  # include/ts_hc.h
 
 
 class HCError(RuntimeError):

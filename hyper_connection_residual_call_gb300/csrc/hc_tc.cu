@@ -1,24 +1,24 @@
 // hc_tc.cu -- the batched (M >= 16 tokens) hyper-connection call on the
-// 5th-generation tensor cores: tcgen05.mma with TMEM accumulators, weights
-// streamed by tensor-map TMA in the 128-byte swizzled layout.
+// 5th-generation tensor cores: tcgen05.mma with TMEM accumulators, operands
+// staged by tensor-map TMA in the 128-byte swizzled layout.
 //
 // At M tokens the projections are dense contractions (families/qwen4/hc.rs
 // runs them as GEMVs per token; real_forward.rs batches such GEMVs into M-row
-// GEMMs inside a prefill micro-batch). Three kernels, PDL-chained:
+// GEMMs inside a prefill micro-batch). Four kernels, PDL-chained:
 //
-//  hc_tc_down_kernel   D[128 rows][N tokens] = W[rows][chunk] * X[chunk][tokens]
-//                      with X = raw * g built by producer warps as bf16 hi + lo
-//                      (x = hi + lo to ~16 significant bits; two MMAs per
-//                      K step), so the down projection keeps fp32-level
-//                      accuracy. A cluster of CS CTAs covers one stream; the
-//                      partial tiles meet in distributed shared memory and the
-//                      cluster writes the stream's partial z and the stream's
-//                      per-token sum of squares.
-//  hc_tc_reduce_kernel z = sum_c inv_rms[c] * part[c]; act = silu(z / C) (fp32 and
-//                      bf16 hi/lo for the up GEMM), gates = 2 sigmoid(z / C).
+//  hc_tc_prep_kernel   per (token, stream): the fused inject-add (written back
+//                      to the residual), inv_rms, and normed = raw * g * inv_rms
+//                      stored as bf16 hi + lo (normed = hi + lo to ~16
+//                      significant bits), so that the GEMMs keep fp32-level
+//                      accuracy with bf16 operands.
+//  hc_tc_down_kernel   D[128 rows][N tokens] = W[rows][K chunk] * normed^T, two
+//                      MMAs per K step (hi, lo); CTA (chunk, row tile, token
+//                      tile) writes its fp32 partial tile to part[chunk][token][row].
+//  hc_tc_reduce_kernel z = sum over chunks (fixed order); act = silu(z / C)
+//                      (fp32 and bf16 hi/lo for the up GEMM), gates = 2 sigmoid(z / C).
 //  hc_tc_up_kernel     D[C*HBt rows][N] = Wu[rows {c*H + h}][L] * act^T (hi + lo),
-//                      epilogue: w = sigmoid(D), mixed[h] = mean_c w * raw *
-//                      inv_rms * g, with the raw tile staged by TMA.
+//                      epilogue: w = sigmoid(D), mixed[h] = mean_c w * normed,
+//                      with the normed tile staged by TMA.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -50,14 +50,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 // ~1e-6, far inside the 1e-3 bar), for the per-element epilogues.
 __device__ __forceinline__ float sigm_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
-__device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr)
-{
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ void record_timeout(unsigned *status)
 {
     if (status)
@@ -82,24 +74,6 @@ struct TcSmem {
     uint32_t ring, extra, bars, total;
 };
 
-// Down kernel shared memory: ring of stages [A 16 KB | B_hi | B_lo], then the
-// per-token sums of squares, then this CTA's chunk of g (bf16, at most
-// kMaxChunk elements), then barriers.
-constexpr int kMaxChunk = 2048;
-// A stage is [A_hi | A_lo (INT4 weights only) | B_hi | B_lo].
-__host__ __device__ inline TcSmem down_tc_layout(int NT, int ns, int wt)
-{
-    TcSmem s;
-    s.a_bytes = kTileRows * 128;
-    s.b_bytes = NT * 128;
-    s.stage_bytes = s.a_bytes * (1 + wt) + 2 * s.b_bytes;
-    s.ring = 0;
-    s.extra = s.ring + ns * s.stage_bytes;          // ssq_s: NT floats, then g_s
-    s.bars = s.extra + ((NT * 4 + 127) / 128) * 128 + kMaxChunk * 2;
-    s.total = s.bars + 8 * (3 * ns + 2) + 16;
-    return s;
-}
-
 // Dequantises 8 INT4-affine codes (element e in nibble e of `codes`) with one
 // scale and bias (fp16 bits) and splits them into bf16 hi and lo parts:
 // w = q * s + b in fp32, hi = bf16(w), lo = bf16(w - hi).
@@ -119,17 +93,102 @@ __device__ __forceinline__ void int4x8_hilo(uint32_t codes, uint16_t sb, uint16_
     lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// Up kernel: ring, then raw tile [C][NT][HBt] bf16, inv_rms tile [NT][C], and
-// for a fused inject-add the sublayer-output tile [NT][HBt] bf16 and the
-// previous gates [NT][C].
-__host__ __device__ inline uint32_t up_tc_raw_bytes(int NT, int C, int HBt)
-{
-    return ((C * NT * HBt * 2 + 1023) / 1024) * 1024;
-}
-__host__ __device__ inline uint32_t up_tc_small_bytes(int NT, int C) { return ((NT * C * 4 + 127) / 128) * 128; }
-__host__ __device__ inline uint32_t up_tc_out_bytes(int NT, int HBt) { return ((NT * HBt * 2 + 127) / 128) * 128; }
 
-__host__ __device__ inline TcSmem up_tc_layout(int NT, int ns, int C, int HBt, int wt)
+// ---------------------------------------------------------------- prep
+
+constexpr int kPrepThreads = 512;
+constexpr int kPrepVec = 4;  // 8-element vectors per thread: H <= 8 * kPrepThreads * kPrepVec = 16384
+
+__device__ __forceinline__ float warp_sum_f(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Grid (M, C): CTA (m, c) owns stream c of token m, one 8-element vector per
+// thread and round.
+__global__ void __launch_bounds__(kPrepThreads) hc_tc_prep_kernel(const TcPrepParams p)
+{
+    __shared__ float red_s[kPrepThreads / 32];
+    const int m = blockIdx.x, c = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    const int nv = p.H / 8;
+    const size_t base = (size_t)m * p.W + (size_t)c * p.H;
+    const bool fused = p.raw_out != nullptr;
+    pdl_launch_dependents();
+    pdl_wait();  // the residual, the sublayer output and the previous gates come from earlier kernels
+
+    // Every load first (the residual is written back below).
+    uint4 rv[kPrepVec], ov[kPrepVec];
+#pragma unroll
+    for (int k = 0; k < kPrepVec; ++k) {
+        const int v = tid + k * blockDim.x;
+        rv[k] = v < nv ? reinterpret_cast<const uint4 *>(p.raw + base)[v] : make_uint4(0, 0, 0, 0);
+        ov[k] = (fused && v < nv) ? reinterpret_cast<const uint4 *>(p.inj_out + (size_t)m * p.H)[v]
+                                  : make_uint4(0, 0, 0, 0);
+    }
+    const float gate = fused ? p.inj_gate[(size_t)m * p.inj_stride + c] : 0.f;
+    float q = 0.f;
+#pragma unroll
+    for (int k = 0; k < kPrepVec; ++k) {
+        const int v = tid + k * blockDim.x;
+        if (v >= nv)
+            continue;
+        uint32_t w[4] = {rv[k].x, rv[k].y, rv[k].z, rv[k].w};
+        if (fused) {  // raw + out * gate, rounded as the inject-add kernel rounds
+            const uint32_t o[4] = {ov[k].x, ov[k].y, ov[k].z, ov[k].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                w[e] = pack_bf16x2(fmaf(bf16_lo(o[e]), gate, bf16_lo(w[e])), fmaf(bf16_hi(o[e]), gate, bf16_hi(w[e])));
+            rv[k] = make_uint4(w[0], w[1], w[2], w[3]);
+            reinterpret_cast<uint4 *>(p.raw_out + base)[v] = rv[k];
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float a = bf16_lo(w[e]), b = bf16_hi(w[e]);
+            q = fmaf(a, a, q);
+            q = fmaf(b, b, q);
+        }
+    }
+    // The stream's sum of squares: warps, then the warp totals in warp order.
+    q = warp_sum_f(q);
+    if (lane == 0)
+        red_s[warp] = q;
+    __syncthreads();
+    float t = 0.f;
+    for (int w = 0; w < nwarps; ++w)
+        t += red_s[w];
+    const float inv = rsqrtf(fmaf(t, p.inv_H, p.eps));
+    if (tid == 0)
+        p.inv_rms[(size_t)m * p.C + c] = inv;
+#pragma unroll
+    for (int k = 0; k < kPrepVec; ++k) {
+        const int v = tid + k * blockDim.x;
+        if (v >= nv)
+            continue;
+        const uint4 gq = reinterpret_cast<const uint4 *>(p.g + (size_t)c * p.H)[v];
+        const uint32_t w[4] = {rv[k].x, rv[k].y, rv[k].z, rv[k].w};
+        const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float xa = bf16_lo(w[e]) * bf16_lo(gw[e]) * inv, xb = bf16_hi(w[e]) * bf16_hi(gw[e]) * inv;
+            const uint32_t hh = pack_bf16x2(xa, xb);
+            h[e] = hh;
+            l[e] = pack_bf16x2(xa - bf16_lo(hh), xb - bf16_hi(hh));
+        }
+        reinterpret_cast<uint4 *>(p.x_hi + base)[v] = make_uint4(h[0], h[1], h[2], h[3]);
+        reinterpret_cast<uint4 *>(p.x_lo + base)[v] = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+}
+
+// ---------------------------------------------------------------- down
+
+// Shared memory of the down kernel: a ring of stages [A_hi | A_lo (INT4
+// weights only) | B_hi | B_lo], then the barriers.
+__host__ __device__ inline TcSmem down_tc_layout(int NT, int ns, int wt)
 {
     TcSmem s;
     s.a_bytes = kTileRows * 128;
@@ -137,39 +196,38 @@ __host__ __device__ inline TcSmem up_tc_layout(int NT, int ns, int C, int HBt, i
     s.stage_bytes = s.a_bytes * (1 + wt) + 2 * s.b_bytes;
     s.ring = 0;
     s.extra = s.ring + ns * s.stage_bytes;
-    s.bars = s.extra + up_tc_raw_bytes(NT, C, HBt) + 2 * up_tc_small_bytes(NT, C) + up_tc_out_bytes(NT, HBt);
-    s.total = s.bars + 8 * (4 * ns + 2) + 16;
+    s.bars = s.extra;
+    s.total = s.bars + 8 * (3 * ns + 1) + 16;
     return s;
 }
 
-// ---------------------------------------------------------------- down
-
+// Grid (nchunk, row tiles, token tiles). Warp 0 lane 0 streams the weight
+// tiles (before the dependency wait) and the normed hi/lo tiles by TMA; with
+// INT4 weights, warps 2-7 dequantise the weight tiles instead. Warp 1 lane 0
+// issues the MMAs. All eight warps then move the fp32 tile from TMEM to
+// part[chunk][row][token].
 template <int WT>
 __global__ void __launch_bounds__(kThreads, 1)
 hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_d,
-                  const __grid_constant__ CUtensorMap map_i)
+                  const __grid_constant__ CUtensorMap map_i, const __grid_constant__ CUtensorMap map_xhi,
+                  const __grid_constant__ CUtensorMap map_xlo)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int NT = p.NT, NS = p.n_stages;
     const TcSmem lay = down_tc_layout(NT, NS, WT);
     const uint32_t b_off = lay.a_bytes * (1 + WT);  // B_hi within a stage
-    float *ssq_s = reinterpret_cast<float *>(smem + lay.extra);
-    uint16_t *g_s = reinterpret_cast<uint16_t *>(smem + lay.extra + ((NT * 4 + 127) / 128) * 128);
-    uint64_t *full_a = reinterpret_cast<uint64_t *>(smem + lay.bars);
-    uint64_t *full_b = full_a + NS;
-    uint64_t *empty = full_b + NS;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);  // TMA bytes of a stage
+    uint64_t *fullp = full + NS;                                      // INT4: producers' A tiles written
+    uint64_t *empty = fullp + NS;
     uint64_t *done = empty + NS;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 2);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q = blockIdx.x;                 // chunk within the stream == cluster rank
-    const int c = blockIdx.y / p.RT;          // stream
-    const int rt = blockIdx.y % p.RT;         // row tile
-    const int tile = blockIdx.z;              // token tile
+    const int kc = blockIdx.x, rt = blockIdx.y, tile = blockIdx.z;
     const int r0 = rt * kTileRows;
-    const int k0 = c * p.H + q * p.chunk;
-    const int KB = p.chunk / kKBlock;
+    const int KBT = p.W / kKBlock, kb0 = kc * p.KBc;
+    const int KB = min(p.KBc, KBT - kb0);
     const uint32_t ncols = tmem_cols(NT);
 
     // Boxes of 32 rows making up this row tile: from W_down, from
@@ -183,8 +241,8 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
     pdl_launch_dependents();
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(&full_a[s], 1);
-            mbar_init(&full_b[s], kProducers);
+            mbar_init(&full[s], 1);
+            mbar_init(&fullp[s], kProducers);
             mbar_init(&empty[s], 1);
         }
         mbar_init(done, 1);
@@ -195,200 +253,122 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
         tmem_alloc(tslot, ncols);
         tmem_relinquish();
     }
-    // g is a weight: this CTA's chunk goes to shared memory before the wait
-    // (read by the producers after this barrier; the TMA producer below runs
-    // ahead without any further block barrier).
-    for (int i = tid; i < p.chunk / 8; i += kThreads)
-        reinterpret_cast<uint4 *>(g_s)[i] = reinterpret_cast<const uint4 *>(p.g + k0)[i];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
     bool timed_out = false;
 
-    if (WT == 0 && warp == 0 && lane == 0) {
-        // TMA producer of the weight tiles (independent of the previous kernel).
-        tma_prefetch_map(&map_d);
-        if (p.has_inject) tma_prefetch_map(&map_i);
-        for (int kb = 0; kb < KB; ++kb) {
-            const int s = kb % NS, u = kb / NS;
-            if (u > 0 && !mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
+    if (warp == 0 && lane == 0) {
+        const uint32_t a_tx = WT == 0 ? (uint32_t)nbox * 32 * 128 : 0u;
+        const uint32_t b_tx = 2u * NT * 128;
+        auto load_a = [&](int kb, int s) {
             uint8_t *a = smem + lay.ring + s * lay.stage_bytes;
-            mbar_arrive_expect_tx(&full_a[s], nbox * 32 * 128);
+            const int col = (kb0 + kb) * kKBlock;
             for (int b = 0; b < 4; ++b) {
                 const int gr = r0 + 32 * b;
                 if (gr + 32 <= p.L)
-                    tma_load_2d(a + b * 32 * 128, &map_d, k0 + kb * kKBlock, gr, &full_a[s]);
+                    tma_load_2d(a + b * 32 * 128, &map_d, col, gr, &full[s]);
                 else if (gr == p.L && p.has_inject)
-                    tma_load_2d(a + b * 32 * 128, &map_i, k0 + kb * kKBlock, 0, &full_a[s]);
+                    tma_load_2d(a + b * 32 * 128, &map_i, col, 0, &full[s]);
             }
+        };
+        auto load_b = [&](int kb, int s) {
+            uint8_t *bh = smem + lay.ring + s * lay.stage_bytes + b_off;
+            const int col = (kb0 + kb) * kKBlock;
+            tma_load_2d(bh, &map_xhi, col, tile * NT, &full[s]);
+            tma_load_2d(bh + lay.b_bytes, &map_xlo, col, tile * NT, &full[s]);
+        };
+        if (WT == 0) {
+            tma_prefetch_map(&map_d);
+            if (p.has_inject) tma_prefetch_map(&map_i);
         }
-    }
-    if (warp < 2)
-        pdl_wait();  // raw is produced by the previous kernel in the stream
-
-    if (warp >= 2) {
-        // Activation producers (warps 2-7): per K block, X = raw * g as bf16
-        // hi + lo in the swizzled K-major layout. Thread t handles the 16-byte
-        // chunks i = t + kProducers j of the NT x 64 block: token i / 8, chunk
-        // i % 8, so eight consecutive lanes read one token's 128 contiguous
-        // bytes (coalesced), and accumulate that token's sum of squares.
+        // The stages before the ring wraps: weights first (independent of the
+        // previous kernels), then the activations once they exist.
+        const int npre = KB < NS ? KB : NS;
+        for (int kb = 0; kb < npre; ++kb) {
+            mbar_arrive_expect_tx(&full[kb], a_tx + b_tx);
+            if (WT == 0)
+                load_a(kb, kb);
+        }
+        pdl_wait();  // normed comes from the prep kernel
+        for (int kb = 0; kb < npre; ++kb)
+            load_b(kb, kb);
+        for (int kb = npre; kb < KB; ++kb) {
+            const int s = kb % NS, u = kb / NS;
+            if (!mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
+            mbar_arrive_expect_tx(&full[s], a_tx + b_tx);
+            if (WT == 0)
+                load_a(kb, s);
+            load_b(kb, s);
+        }
+    } else if (WT == 1 && warp >= 2) {
+        // INT4 weights: warps 2-7 dequantise the A tiles (weights only, so no
+        // dependency wait). Thread t handles the 16-byte chunks t + kProducers j
+        // of the 128 x 64 tile: row / 8, chunk t % 8 (8 codes, one scale and bias).
         const int t = tid - 64;
-        const int ck = t & 7;                  // 16-byte chunk within the 64-element K block
+        const int ck = t & 7;
         constexpr int kItems = (kTileRows * 8 + kProducers - 1) / kProducers;
-        float ssq[kItems], inj_g[kItems];
-        const uint4 *rrow[kItems];
-        const uint4 *orow[kItems];
-        bool live[kItems];
-#pragma unroll
-        for (int j = 0; j < kItems; ++j) {
-            const int n = (t + kProducers * j) >> 3;   // token of chunk t + kProducers j
-            const int m = tile * NT + n;
-            live[j] = n < NT && m < p.M;
-            ssq[j] = 0.f;
-            rrow[j] = reinterpret_cast<const uint4 *>(p.raw + (size_t)(live[j] ? m : 0) * p.W + k0) + ck;
-            orow[j] = p.inj_out ? reinterpret_cast<const uint4 *>(p.inj_out + (size_t)(live[j] ? m : 0) * p.H
-                                                                  + q * p.chunk) + ck
-                                : nullptr;
-        }
-        // INT4 weights: item j is also row (t + kProducers j) / 8 of the A tile,
-        // chunk ck: 8 codes (4 bytes) and the group's scale and bias.
         const uint8_t *wq[kItems];
         const uint16_t *wsc[kItems];
         const uint16_t *wbi[kItems];
-        if constexpr (WT == 1) {
-#pragma unroll
-            for (int j = 0; j < kItems; ++j) {
-                const int rr = (t + kProducers * j) >> 3, gr = r0 + rr;
-                const WeightView *v = gr < p.L ? &p.dw : (p.has_inject && gr < p.L + p.C) ? &p.iw : nullptr;
-                const int row = gr < p.L ? gr : gr - p.L;
-                wq[j] = (v && rr < kTileRows) ? static_cast<const uint8_t *>(v->data) + ((size_t)row * p.W + k0) / 2 : nullptr;
-                wsc[j] = wq[j] ? v->scales + (size_t)row * (p.W / v->group) : nullptr;
-                wbi[j] = wq[j] ? v->biases + (size_t)row * (p.W / v->group) : nullptr;
-            }
-        }
-        // The next K block's chunks are loaded while the current one is converted.
-        uint4 rnext[kItems], onext[kItems];
-        uint32_t qnext[kItems];
-        uint16_t snext[kItems], bnext[kItems];
-        auto fetch_w = [&](int kb) {
-            if constexpr (WT == 1) {
-                const int col = kb * kKBlock + 8 * ck;  // within the chunk
-#pragma unroll
-                for (int j = 0; j < kItems; ++j) {
-                    qnext[j] = wq[j] ? *reinterpret_cast<const uint32_t *>(wq[j] + col / 2) : 0u;
-                    snext[j] = wq[j] ? wsc[j][(k0 + col) / p.dw.group] : (uint16_t)0;
-                    bnext[j] = wq[j] ? wbi[j][(k0 + col) / p.dw.group] : (uint16_t)0;
-                }
-            }
-        };
-        auto fetch = [&](int kb) {
-#pragma unroll
-            for (int j = 0; j < kItems; ++j) {
-                rnext[j] = live[j] ? rrow[j][kb * (kKBlock / 8)] : make_uint4(0, 0, 0, 0);
-                onext[j] = (live[j] && p.inj_out) ? orow[j][kb * (kKBlock / 8)] : make_uint4(0, 0, 0, 0);
-            }
-            fetch_w(kb);
-        };
-        fetch_w(0);  // weights do not depend on the previous kernel
-        pdl_wait();  // raw is produced by the previous kernel in the stream
-        fetch(0);
-        // The previous gates come from the previous call's reduce kernel, which
-        // can still be running when this kernel starts: read only after the wait.
 #pragma unroll
         for (int j = 0; j < kItems; ++j) {
-            const int m = tile * NT + ((t + kProducers * j) >> 3);
-            inj_g[j] = (live[j] && p.inj_out) ? p.inj_gate[(size_t)m * p.inj_stride + c] : 0.f;
+            const int rr = (t + kProducers * j) >> 3, gr = r0 + rr;
+            const WeightView *v = gr < p.L ? &p.dw : (p.has_inject && gr < p.L + p.C) ? &p.iw : nullptr;
+            const int row = gr < p.L ? gr : gr - p.L;
+            wq[j] = (v && rr < kTileRows) ? static_cast<const uint8_t *>(v->data) + (size_t)row * (p.W / 2) : nullptr;
+            wsc[j] = wq[j] ? v->scales + (size_t)row * (p.W / v->group) : nullptr;
+            wbi[j] = wq[j] ? v->biases + (size_t)row * (p.W / v->group) : nullptr;
         }
-        for (int kb = 0; kb < KB; ++kb) {
-            const int s = kb % NS, u = kb / NS;
-            uint4 rcur[kItems], ocur[kItems];
-            uint32_t qcur[kItems];
-            uint16_t scur[kItems], bcur[kItems];
+        uint32_t qn[kItems];
+        uint16_t sn[kItems], bn[kItems];
+        auto fetch = [&](int kb) {
+            const int col = (kb0 + kb) * kKBlock + 8 * ck;
 #pragma unroll
             for (int j = 0; j < kItems; ++j) {
-                rcur[j] = rnext[j];
-                ocur[j] = onext[j];
-                qcur[j] = qnext[j];
-                scur[j] = snext[j];
-                bcur[j] = bnext[j];
+                qn[j] = wq[j] ? *reinterpret_cast<const uint32_t *>(wq[j] + col / 2) : 0u;
+                sn[j] = wq[j] ? wsc[j][col / p.dw.group] : (uint16_t)0;
+                bn[j] = wq[j] ? wbi[j][col / p.dw.group] : (uint16_t)0;
+            }
+        };
+        fetch(0);
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % NS, u = kb / NS;
+            uint32_t qc[kItems];
+            uint16_t sc[kItems], bc[kItems];
+#pragma unroll
+            for (int j = 0; j < kItems; ++j) {
+                qc[j] = qn[j];
+                sc[j] = sn[j];
+                bc[j] = bn[j];
             }
             if (kb + 1 < KB)
                 fetch(kb + 1);
             if (u > 0 && !mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
             uint8_t *ahi = smem + lay.ring + s * lay.stage_bytes;
-            uint8_t *bhi = ahi + b_off;
-            uint8_t *blo = bhi + lay.b_bytes;
-            if constexpr (WT == 1) {
-                uint8_t *alo = ahi + lay.a_bytes;
-#pragma unroll
-                for (int j = 0; j < kItems; ++j) {
-                    const int rr = (t + kProducers * j) >> 3;
-                    if (rr >= kTileRows)
-                        continue;
-                    uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
-                    if (wq[j])
-                        int4x8_hilo(qcur[j], scur[j], bcur[j], hi, lo);
-                    *reinterpret_cast<uint4 *>(ahi + sw128_offset(rr, 8 * ck)) = hi;
-                    *reinterpret_cast<uint4 *>(alo + sw128_offset(rr, 8 * ck)) = lo;
-                }
-            }
-            const uint4 gv = reinterpret_cast<const uint4 *>(g_s + kb * kKBlock)[ck];
-            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+            uint8_t *alo = ahi + lay.a_bytes;
 #pragma unroll
             for (int j = 0; j < kItems; ++j) {
-                const int n = (t + kProducers * j) >> 3;
-                if (n >= NT)
+                const int rr = (t + kProducers * j) >> 3;
+                if (rr >= kTileRows)
                     continue;
                 uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
-                if (live[j]) {
-                    const uint32_t rw[4] = {rcur[j].x, rcur[j].y, rcur[j].z, rcur[j].w};
-                    const uint32_t ow[4] = {ocur[j].x, ocur[j].y, ocur[j].z, ocur[j].w};
-                    uint32_t h[4], l[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        // Packed conversions: one bf16x2 rounding per pair.
-                        float r_a = bf16_lo(rw[e]), r_b = bf16_hi(rw[e]);
-                        if (p.inj_out) {  // fused inject-add, rounded as the inject-add kernel rounds
-                            const uint32_t rr = pack_bf16x2(fmaf(bf16_lo(ow[e]), inj_g[j], r_a),
-                                                            fmaf(bf16_hi(ow[e]), inj_g[j], r_b));
-                            r_a = bf16_lo(rr);
-                            r_b = bf16_hi(rr);
-                        }
-                        ssq[j] = fmaf(r_a, r_a, ssq[j]);
-                        ssq[j] = fmaf(r_b, r_b, ssq[j]);
-                        const float x_a = r_a * bf16_lo(gw[e]), x_b = r_b * bf16_hi(gw[e]);
-                        const uint32_t hh = pack_bf16x2(x_a, x_b);
-                        h[e] = hh;
-                        l[e] = pack_bf16x2(x_a - bf16_lo(hh), x_b - bf16_hi(hh));
-                    }
-                    hi = make_uint4(h[0], h[1], h[2], h[3]);
-                    lo = make_uint4(l[0], l[1], l[2], l[3]);
-                }
-                *reinterpret_cast<uint4 *>(bhi + sw128_offset(n, 8 * ck)) = hi;
-                *reinterpret_cast<uint4 *>(blo + sw128_offset(n, 8 * ck)) = lo;
+                if (wq[j])
+                    int4x8_hilo(qc[j], sc[j], bc[j], hi, lo);
+                *reinterpret_cast<uint4 *>(ahi + sw128_offset(rr, 8 * ck)) = hi;
+                *reinterpret_cast<uint4 *>(alo + sw128_offset(rr, 8 * ck)) = lo;
             }
             fence_async_shared();
-            mbar_arrive(&full_b[s]);
-        }
-        // A token's sum of squares: its 8 lanes (one octet of the warp), fixed order.
-#pragma unroll
-        for (int j = 0; j < kItems; ++j) {
-            float v = ssq[j];
-            v += __shfl_xor_sync(0xffffffffu, v, 1);
-            v += __shfl_xor_sync(0xffffffffu, v, 2);
-            v += __shfl_xor_sync(0xffffffffu, v, 4);
-            const int n = (t + kProducers * j) >> 3;
-            if (ck == 0 && n < NT)
-                ssq_s[n] = v;
+            mbar_arrive(&fullp[s]);
         }
     } else if (warp == 1 && lane == 0) {
         // MMA issuer.
         const uint32_t idesc = umma_idesc_bf16(kTileRows, NT);
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % NS, u = kb / NS;
-            if (WT == 0 && !mbar_wait_bounded(&full_a[s], u & 1)) timed_out = true;
-            if (!mbar_wait_bounded(&full_b[s], u & 1)) timed_out = true;
+            if (!mbar_wait_bounded(&full[s], u & 1)) timed_out = true;
+            if (WT == 1 && !mbar_wait_bounded(&fullp[s], u & 1)) timed_out = true;
             tc_fence_after();
             const uint32_t a = smem_addr(smem + lay.ring + s * lay.stage_bytes);
             const uint32_t al = a + lay.a_bytes;  // A_lo (INT4 weights)
@@ -405,68 +385,43 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
         umma_commit(done);
     }
 
-    // Epilogue: the 128 x NT fp32 partial tile, TMEM -> shared (over the ring).
-    // The barrier also reconverges the warps whose lane 0 had a producer role.
+    // Epilogue on all 8 warps: warp w reads TMEM lanes 32*(w%4).. (the tile's
+    // rows) for the 16-column chunks 16*(w/4) + 32k -- all of them before the
+    // one wait -- and stores them to part[chunk][token][row]: the 32 lanes of a
+    // store write 32 consecutive rows of one token (coalesced). The barrier
+    // reconverges the single-thread roles.
     __syncthreads();
-    float *ptile = reinterpret_cast<float *>(smem + lay.ring);
-    const int pstride = NT + 4;
-    if (warp < 4) {
-        if (!mbar_wait_bounded(done, 0)) timed_out = true;
-        __syncwarp();  // the TMEM loads below are .aligned
-        tc_fence_after();
-        const int row = warp * 32 + lane;
-        for (int c0 = 0; c0 < NT; c0 += 16) {
-            float v[16];
-            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+    if (!mbar_wait_bounded(done, 0)) timed_out = true;
+    __syncwarp();  // the TMEM loads below are .aligned
+    tc_fence_after();
+    {
+        const int quad = warp & 3, half = warp >> 2;
+        const int gr = r0 + quad * 32 + lane;
+        const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16);
+        uint32_t v[4][16];  // NT <= 128: at most four chunks per warp
 #pragma unroll
-            for (int j = 0; j < 16; j += 4)
-                *reinterpret_cast<float4 *>(ptile + row * pstride + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        for (int k = 0; k < 4; ++k)
+            if (16 * half + 32 * k < NT)  // warp-uniform
+                tmem_ld16_async(tbase + 16 * half + 32 * k, v[k]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            tmem_wait_ld(v[k]);
+        if (gr < p.R) {
+            float *dst = p.part + ((size_t)kc * p.Mp + (size_t)tile * NT) * p.R + gr;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int c0 = 16 * half + 32 * k;
+                if (c0 < NT) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        dst[(size_t)(c0 + j) * p.R] = __uint_as_float(v[k][j]);
+                }
+            }
         }
     }
     if (timed_out) record_timeout(p.status);
     tc_fence_before();
-    cluster_sync();  // every CTA of the stream has its partial tile and sums of squares in shared memory
-
-    // Rank q sums rows [q*RS, (q+1)*RS) over the cluster, in rank order, four
-    // tokens at a time; the remote loads of a group are all issued before any
-    // is used, so their latencies overlap.
-    const int RS = kTileRows / p.CS;
-    const int NT4 = NT / 4;  // NT is a multiple of 16
-    for (int i = tid; i < RS * NT4; i += kThreads) {
-        const int r = q * RS + i / NT4, n = (i % NT4) * 4;
-        const int gr = r0 + r;
-        float4 v[8];
-#pragma unroll
-        for (int pr = 0; pr < 8; ++pr)
-            v[pr] = pr < p.CS ? dsmem_ld_f32x4(dsmem_addr(ptile + r * pstride + n, pr)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 z = v[0];
-#pragma unroll
-        for (int pr = 1; pr < 8; ++pr) {
-            if (pr < p.CS) {
-                z.x += v[pr].x; z.y += v[pr].y; z.z += v[pr].z; z.w += v[pr].w;
-            }
-        }
-        if (gr < p.R) {
-            const float zz[4] = {z.x, z.y, z.z, z.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int m = tile * NT + n + e;
-                if (m < p.M)
-                    p.part[((size_t)c * p.R + gr) * p.M + m] = zz[e];
-            }
-        }
-    }
-    if (q == 0 && rt == 0) {
-        for (int n = tid; n < NT; n += kThreads) {
-            const int m = tile * NT + n;
-            float s = 0.f;
-            for (int pr = 0; pr < p.CS; ++pr)
-                s += dsmem_ld_f32(dsmem_addr(ssq_s + n, pr));
-            if (m < p.M)
-                p.ssq[(size_t)c * p.M + m] = s;
-        }
-    }
-    cluster_sync();  // peers have finished reading this CTA's shared memory
+    __syncthreads();
     tc_fence_after();
     if (warp == 0)
         tmem_dealloc(tmem, ncols);
@@ -474,78 +429,85 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
 
 // ---------------------------------------------------------------- reduce
 
-// Grid (ceil(M / 32), ceil(R / 32)); 1024 threads, one element each. The
-// partials are read along tokens and act is written along rows, through a
-// shared-memory transpose, so both sides are coalesced.
-__global__ void __launch_bounds__(1024) hc_tc_reduce_kernel(const TcReduceParams p)
+// One thread per (token, row): element i = m * R + r of every chunk's partial
+// tile, so the loads of a warp are contiguous; the chunks are summed in order,
+// every load of a thread in flight at once.
+constexpr int kReduceThreads = 256;
+constexpr int kReduceBatch = 20;
+
+__global__ void __launch_bounds__(kReduceThreads) hc_tc_reduce_kernel(const TcReduceParams p)
 {
-    __shared__ float zt[32][33];
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int m0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
     pdl_launch_dependents();
     pdl_wait();
-    {
-        // z of row r0 + ty, token m0 + tx: every load first, then the sum in stream order.
-        const int m = m0 + tx, r = r0 + ty;
-        const bool ok = m < p.M && r < p.R;
-        float sq[8], pt[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            sq[c] = (c < p.C && ok) ? p.ssq[(size_t)c * p.M + m] : 0.f;
-            pt[c] = (c < p.C && ok) ? p.part[((size_t)c * p.R + r) * p.M + m] : 0.f;
-        }
-        float z = 0.f;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            if (c < p.C && ok) {
-                const float inv = 1.0f / sqrtf(sq[c] / (float)p.H + p.eps);
-                z = fmaf(inv, pt[c], z);
-                if (r == 0)
-                    p.inv_rms[(size_t)m * p.C + c] = inv;
-            }
-        }
-        zt[ty][tx] = z;
-    }
-    __syncthreads();
-    // Row r0 + tx of token m0 + ty.
-    const int r = r0 + tx, mm = m0 + ty;
-    if (r >= p.R || mm >= p.M)
+    const long i = (long)blockIdx.x * kReduceThreads + threadIdx.x;
+    if (i >= (long)p.M * p.R)
         return;
-    const float zc = zt[tx][ty] * p.inv_C;
+    const float *src = p.part + i;
+    const size_t cstride = (size_t)p.Mp * p.R;
+    float z = 0.f;
+    for (int kc = 0; kc < p.nchunk; kc += kReduceBatch) {
+        float v[kReduceBatch];
+#pragma unroll
+        for (int j = 0; j < kReduceBatch; ++j)
+            v[j] = kc + j < p.nchunk ? src[(size_t)(kc + j) * cstride] : 0.f;
+#pragma unroll
+        for (int j = 0; j < kReduceBatch; ++j)
+            z += v[j];
+    }
+    const int m = (int)(i / p.R), r = (int)(i % p.R);
+    const float zc = z * p.inv_C;
     if (r < p.L) {
         const float a = zc * sigm_fast(zc);
         const float hi = bf16_round(a);
-        p.act[(size_t)mm * p.L + r] = a;
-        p.act_hi[(size_t)mm * p.L + r] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-        p.act_lo[(size_t)mm * p.L + r] = __bfloat16_as_ushort(__float2bfloat16_rn(a - hi));
+        p.act[(size_t)m * p.L + r] = a;
+        p.act_hi[(size_t)m * p.L + r] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+        p.act_lo[(size_t)m * p.L + r] = __bfloat16_as_ushort(__float2bfloat16_rn(a - hi));
     } else {
-        p.gate[(size_t)mm * p.gate_stride + (r - p.L)] = 2.0f * sigm_fast(zc);
+        p.gate[(size_t)m * p.gate_stride + (r - p.L)] = 2.0f * sigm_fast(zc);
     }
 }
 
 // ---------------------------------------------------------------- up
 
+// Up kernel shared memory: the ring, then the normed hi and lo tiles
+// [C][NT][HBt] bf16, then the barriers.
+__host__ __device__ inline uint32_t up_tc_tile_bytes(int NT, int C, int HBt)
+{
+    return ((C * NT * HBt * 2 + 1023) / 1024) * 1024;
+}
+
+__host__ __device__ inline TcSmem up_tc_layout(int NT, int ns, int C, int HBt, int wt)
+{
+    TcSmem s;
+    s.a_bytes = kTileRows * 128;
+    s.b_bytes = NT * 128;
+    s.stage_bytes = s.a_bytes * (1 + wt) + 2 * s.b_bytes;
+    s.ring = 0;
+    s.extra = s.ring + ns * s.stage_bytes;
+    s.bars = s.extra + 2 * up_tc_tile_bytes(NT, C, HBt);
+    s.total = s.bars + 8 * (3 * ns + 2) + 16;
+    return s;
+}
+
 template <int WT>
 __global__ void __launch_bounds__(kThreads, 1)
 hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
                 const __grid_constant__ CUtensorMap map_ahi, const __grid_constant__ CUtensorMap map_alo,
-                const __grid_constant__ CUtensorMap map_raw)
+                const __grid_constant__ CUtensorMap map_nhi, const __grid_constant__ CUtensorMap map_nlo)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int NT = p.NT, NS = p.n_stages, C = p.C, HBt = p.HBt;
     const TcSmem lay = up_tc_layout(NT, NS, C, HBt, WT);
     const uint32_t b_off = lay.a_bytes * (1 + WT);  // B_hi within a stage
-    uint16_t *raw_s = reinterpret_cast<uint16_t *>(smem + lay.extra);  // [C][NT][HBt]
-    float *inv_s = reinterpret_cast<float *>(smem + lay.extra + up_tc_raw_bytes(NT, C, HBt));  // [NT][C]
-    float *pgate_s = inv_s + up_tc_small_bytes(NT, C) / 4;                                       // [NT][C]
-    uint16_t *out_s = reinterpret_cast<uint16_t *>(pgate_s + up_tc_small_bytes(NT, C) / 4);     // [NT][HBt]
+    const uint16_t *nhi_s = reinterpret_cast<const uint16_t *>(smem + lay.extra);  // [C][NT][HBt]
+    const uint16_t *nlo_s = nhi_s + up_tc_tile_bytes(NT, C, HBt) / 2;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
     uint64_t *empty = full + NS;
     uint64_t *fullp = empty + NS;  // INT4: the producers' A tiles of a stage are written
     uint64_t *done = fullp + NS;
-    uint64_t *raw_bar = done + 1;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(raw_bar + 1);
+    uint64_t *nbar = done + 1;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(nbar + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h0 = blockIdx.x * HBt;
@@ -561,7 +523,7 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
             mbar_init(&fullp[s], kProducers);
         }
         mbar_init(done, 1);
-        mbar_init(raw_bar, 1);
+        mbar_init(nbar, 1);
         mbar_fence_init();
     }
     if (warp == 0) {
@@ -586,7 +548,7 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
             for (int cc = 0; cc < C; ++cc)
                 tma_load_2d(a + cc * HBt * 128, &map_u, kb * kKBlock, cc * p.H + h0, &full[kb]);
         }
-        pdl_wait();  // ... then the activations and the residual tile
+        pdl_wait();  // ... then the activations and the normed tiles
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % NS, u = kb / NS;
             uint8_t *a = smem + lay.ring + s * lay.stage_bytes;
@@ -602,14 +564,16 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
             tma_load_2d(a + b_off, &map_ahi, kb * kKBlock, tile * NT, &full[s]);
             tma_load_2d(a + b_off + lay.b_bytes, &map_alo, kb * kKBlock, tile * NT, &full[s]);
         }
-        mbar_arrive_expect_tx(raw_bar, C * NT * HBt * 2);
-        for (int cc = 0; cc < C; ++cc)
-            tma_load_2d(raw_s + cc * NT * HBt, &map_raw, cc * p.H + h0, tile * NT, raw_bar);
+        mbar_arrive_expect_tx(nbar, 2 * C * NT * HBt * 2);
+        for (int cc = 0; cc < C; ++cc) {
+            tma_load_2d(const_cast<uint16_t *>(nhi_s) + cc * NT * HBt, &map_nhi, cc * p.H + h0, tile * NT, nbar);
+            tma_load_2d(const_cast<uint16_t *>(nlo_s) + cc * NT * HBt, &map_nlo, cc * p.H + h0, tile * NT, nbar);
+        }
     } else if (WT == 1 && warp >= 2) {
         // INT4 weights: warps 2-7 dequantise the A tiles (rows (stream, h) of
         // this CTA, 64 columns per stage) to bf16 hi + lo. Thread t handles the
-        // 16-byte chunks t + kProducers j: row / 8, chunk t % 8. The stages
-        // before the ring wraps are written before the dependency wait.
+        // 16-byte chunks t + kProducers j: row / 8, chunk t % 8. Weights only:
+        // no dependency wait.
         const int t = tid - 64;
         const int ck = t & 7;
         constexpr int kItems = (kTileRows * 8 + kProducers - 1) / kProducers;
@@ -629,8 +593,6 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         }
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % NS, u = kb / NS;
-            if (kb == NS)
-                pdl_wait();
             const int col = kb * kKBlock + 8 * ck;
             uint32_t q[kItems];
             uint16_t sc[kItems], bi[kItems];
@@ -657,10 +619,6 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
             fence_async_shared();
             mbar_arrive(&fullp[s]);
         }
-        if (KB <= NS)
-            pdl_wait();
-    } else {
-        pdl_wait();
     }
 
     if (warp == 1 && lane == 0) {
@@ -684,85 +642,35 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         }
         umma_commit(done);
     }
-    if (warp >= 4) {
-        // While the MMAs run: inv_rms and, for a fused inject-add, the previous
-        // gates and the sublayer-output tile of this CTA's h-block.
-        // Every load of a thread is issued before any is stored (one round trip).
-        constexpr int kPer = 16;  // NT * C <= 128 * 8 and NT * HBt / 8 <= 128 * 16
-        float iv[kPer], gv2[kPer];
-        uint4 ov[kPer];
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int i = tid - 128 + 128 * j;
-            const int n = i / C, cc = i % C, m = tile * NT + n;
-            const bool ok = i < NT * C && m < p.M;
-            iv[j] = ok ? p.inv_rms[(size_t)m * C + cc] : 0.f;
-            gv2[j] = (ok && p.raw_out) ? p.inj_gate[(size_t)m * p.inj_stride + cc] : 0.f;
-            const int v = i, nv = v / (HBt / 8), hv = (v % (HBt / 8)) * 8, mv = tile * NT + nv;
-            const bool okv = p.raw_out && v < NT * HBt / 8 && mv < p.M && h0 + hv + 8 <= p.H;
-            ov[j] = okv ? *reinterpret_cast<const uint4 *>(p.inj_out + (size_t)mv * p.H + h0 + hv)
-                        : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int i = tid - 128 + 128 * j;
-            if (i < NT * C) {
-                inv_s[i] = iv[j];
-                pgate_s[i] = gv2[j];
-            }
-            if (i < NT * HBt / 8)
-                reinterpret_cast<uint4 *>(out_s)[i] = ov[j];
-        }
-    }
-    __syncthreads();
+    __syncthreads();  // reconverges the single-thread roles
 
     // Epilogue on all 8 warps: warp w reads TMEM lanes 32*(w%4).. (rows = (stream,
     // h) pairs) for the 16-column chunks of parity w/4.
     float *mix_s = reinterpret_cast<float *>(smem + lay.ring);  // [C][NT][HBt], over the ring
     {
         if (!mbar_wait_bounded(done, 0)) timed_out = true;
-        if (!mbar_wait_bounded(raw_bar, 0)) timed_out = true;
+        if (!mbar_wait_bounded(nbar, 0)) timed_out = true;
         __syncwarp();  // the TMEM loads below are .aligned
         tc_fence_after();
         const int quad = warp & 3, half = warp >> 2;
         const int row = quad * 32 + lane;
         const int cc = row / HBt, hl = row % HBt;
         const bool live = cc < C && h0 + hl < p.H;
-        const float gv = live ? __bfloat162float(__ushort_as_bfloat16(p.g[cc * p.H + h0 + hl])) : 0.f;
         // The warp's 16-column chunks c0 = 16*half + 32k: chunk k+1 is loaded from
-        // TMEM while chunk k is processed (two register buffers; the loop body
-        // stays small, which keeps the epilogue's code in the instruction cache).
-        // Every shared-memory load of a chunk is issued before its first store:
-        // the compiler cannot tell the global residual from the shared tiles,
-        // so a load placed after a store would wait for it.
-        const bool fused = p.raw_out != nullptr;
-        uint16_t *rout = fused ? p.raw_out + (size_t)cc * p.H + h0 + hl : nullptr;
+        // TMEM while chunk k is processed (two register buffers). A chunk's
+        // shared-memory loads are all issued before its stores.
         auto process = [&](int c0, const uint32_t (&vr)[16]) {
             if (!live)
                 return;
-            float rv[16], sc[16], ov[16], pg[16];
+            float x[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const int n = c0 + j;
-                rv[j] = __bfloat162float(__ushort_as_bfloat16(raw_s[(cc * NT + n) * HBt + hl]));
-                sc[j] = inv_s[n * C + cc] * gv;
-                if (fused) {
-                    ov[j] = __bfloat162float(__ushort_as_bfloat16(out_s[n * HBt + hl]));
-                    pg[j] = pgate_s[n * C + cc];
-                }
-            }
-            if (fused) {  // the inject-add: this thread owns residual elements (m, cc, h)
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    rv[j] = bf16_round(fmaf(ov[j], pg[j], rv[j]));
-                    const int m = tile * NT + c0 + j;
-                    if (m < p.M)
-                        rout[(size_t)m * p.W] = __bfloat16_as_ushort(__float2bfloat16_rn(rv[j]));
-                }
+                const int o = (cc * NT + c0 + j) * HBt + hl;
+                x[j] = __bfloat162float(__ushort_as_bfloat16(nhi_s[o])) + __bfloat162float(__ushort_as_bfloat16(nlo_s[o]));
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                mix_s[(cc * NT + c0 + j) * HBt + hl] = sigm_fast(__uint_as_float(vr[j])) * (rv[j] * sc[j]);
+                mix_s[(cc * NT + c0 + j) * HBt + hl] = sigm_fast(__uint_as_float(vr[j])) * x[j];
         };
         const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16);
         uint32_t va[16], vb[16];
@@ -906,38 +814,51 @@ size_t tc_up_smem(int NT, int ns, int C, int HBt, int wt) { return up_tc_layout(
 
 cudaError_t launch_tc_call(const TcCall &t, cudaStream_t stream)
 {
-    CUtensorMap map_d, map_i, map_u, map_ahi, map_alo, map_raw;
+    CUtensorMap map_d, map_i, map_u, map_xhi, map_xlo, map_ahi, map_alo, map_nhi, map_nlo;
+    const TcPrepParams &pp = t.prep;
     const TcDownParams &d = t.down;
     const TcUpParams &u = t.up;
     // INT4 weights are dequantised by producer warps; their (unused) weight
-    // maps are encoded over the residual, a valid bf16 tensor.
-    const bool q = d.wt == 1;
-    if (!make_map(&map_d, q ? d.raw : t.wd, q ? d.M : d.L, d.W, kKBlock, 32, true) ||
-        !make_map(&map_i, q ? d.raw : d.has_inject ? t.wi : t.wd, q ? d.M : d.has_inject ? d.C : d.L, d.W, kKBlock,
+    // maps are encoded over the normed buffer, a valid bf16 tensor.
+    const bool qd = d.wt == 1, qu = u.wt == 1;
+    const int M = pp.M, W = pp.W;
+    if (!make_map(&map_d, qd ? pp.x_hi : t.wd, qd ? M : d.L, W, kKBlock, 32, true) ||
+        !make_map(&map_i, qd ? pp.x_hi : d.has_inject ? t.wi : t.wd, qd ? M : d.has_inject ? d.C : d.L, W, kKBlock,
                   32, true) ||
-        !make_map(&map_u, q ? u.raw : t.wu, q ? u.M : u.W, q ? u.W : u.L, kKBlock, u.HBt, true) ||
-        !make_map(&map_ahi, t.red.act_hi, u.M, u.L, kKBlock, u.NT, true) ||
-        !make_map(&map_alo, t.red.act_lo, u.M, u.L, kKBlock, u.NT, true) ||
-        !make_map(&map_raw, u.raw, u.M, u.W, u.HBt, u.NT, false))
+        !make_map(&map_u, qu ? pp.x_hi : t.wu, qu ? M : W, qu ? W : u.L, kKBlock, u.HBt, true) ||
+        !make_map(&map_xhi, pp.x_hi, M, W, kKBlock, d.NT, true) ||
+        !make_map(&map_xlo, pp.x_lo, M, W, kKBlock, d.NT, true) ||
+        !make_map(&map_ahi, t.red.act_hi, M, u.L, kKBlock, u.NT, true) ||
+        !make_map(&map_alo, t.red.act_lo, M, u.L, kKBlock, u.NT, true) ||
+        !make_map(&map_nhi, pp.x_hi, M, W, u.HBt, u.NT, false) ||
+        !make_map(&map_nlo, pp.x_lo, M, W, u.HBt, u.NT, false))
         return cudaErrorInvalidValue;
 
-    auto kd = q ? hc_tc_down_kernel<1> : hc_tc_down_kernel<0>;
-    auto ku = u.wt == 1 ? hc_tc_up_kernel<1> : hc_tc_up_kernel<0>;
+    auto kd = qd ? hc_tc_down_kernel<1> : hc_tc_down_kernel<0>;
+    auto ku = qu ? hc_tc_up_kernel<1> : hc_tc_up_kernel<0>;
     cudaError_t e;
     if ((e = allow_smem_tc(kd)) != cudaSuccess) return e;
     if ((e = allow_smem_tc(ku)) != cudaSuccess) return e;
     if ((e = allow_smem_tc(hc_tc_reduce_kernel, false)) != cudaSuccess) return e;
-    const int ntiles = (d.M + d.NT - 1) / d.NT;
-    e = launch_tc(kd, dim3(d.CS, d.C * d.RT, ntiles), dim3(kThreads),
-                  tc_down_smem(d.NT, d.n_stages, d.wt), stream, d.CS, d, map_d, map_i);
+    if ((e = allow_smem_tc(hc_tc_prep_kernel, false)) != cudaSuccess) return e;
+    // Up to kPrepVec vectors per thread, so that the M * C CTAs fit the GPU at once.
+    const int prep_threads = std::min(kPrepThreads, ((pp.H / 8 + kPrepVec - 1) / kPrepVec + 31) / 32 * 32);
+    e = launch_tc(hc_tc_prep_kernel, dim3(M, pp.C), dim3(prep_threads), 0, stream, 0, pp);
     if (e != cudaSuccess)
         return e;
-    e = launch_tc(hc_tc_reduce_kernel, dim3((t.red.M + 31) / 32, (t.red.R + 31) / 32), dim3(1024), 0, stream, 0,
-                  t.red);
+    const int ntiles = (M + d.NT - 1) / d.NT;
+    e = launch_tc(kd, dim3(d.nchunk, (d.R + kTileRows - 1) / kTileRows, ntiles), dim3(kThreads),
+                  tc_down_smem(d.NT, d.n_stages, d.wt), stream, 0, d, map_d, map_i, map_xhi, map_xlo);
+    if (e != cudaSuccess)
+        return e;
+    const long nred = (long)t.red.M * t.red.R;
+    e = launch_tc(hc_tc_reduce_kernel, dim3((unsigned)((nred + kReduceThreads - 1) / kReduceThreads)),
+                  dim3(kReduceThreads), 0, stream, 0, t.red);
     if (e != cudaSuccess)
         return e;
     return launch_tc(ku, dim3((u.H + u.HBt - 1) / u.HBt, ntiles), dim3(kThreads),
-                     tc_up_smem(u.NT, u.n_stages, u.C, u.HBt, u.wt), stream, 0, u, map_u, map_ahi, map_alo, map_raw);
+                     tc_up_smem(u.NT, u.n_stages, u.C, u.HBt, u.wt), stream, 0, u, map_u, map_ahi, map_alo, map_nhi,
+                     map_nlo);
 }
 
 }  // namespace tshc

@@ -10,22 +10,58 @@ namespace tshc {
 
 constexpr int kTcMinTokens = 16;          // the batched path starts at this many tokens
 constexpr size_t kTcSmemLimit = 232448;   // 227 KB opt-in shared memory per CTA
+constexpr int kTcChunkCtas = 152;         // the down kernel's K split aims at about this many CTAs
 
-struct TcDownParams {
+// Tiling of one call on M tokens. It depends on the shape only, not on the
+// device, so the order of the split-K sums -- and every result bit -- does not
+// either.
+struct TcPlan {
+    int NT;       // tokens per tile (multiple of 16, <= 128)
+    int ntiles;   // token tiles
+    int Mp;       // ntiles * NT: the padded token count of the partials
+    int KBc;      // 64-wide K blocks per down CTA
+    int nchunk;   // K chunks over the C*H inputs
+};
+
+__host__ __device__ inline TcPlan tc_plan(int M, int L, int C, int W)
+{
+    TcPlan p;
+    p.NT = M >= 128 ? 128 : (M + 15) / 16 * 16;
+    p.ntiles = (M + p.NT - 1) / p.NT;
+    p.Mp = p.ntiles * p.NT;
+    const int RT = (L + C + 127) / 128;
+    const int KBT = W / 64;
+    const int per = kTcChunkCtas / (RT * p.ntiles);
+    const int target = per > 1 ? per : 1;
+    p.KBc = (KBT + target - 1) / target;
+    p.nchunk = (KBT + p.KBc - 1) / p.KBc;
+    return p;
+}
+
+// Prep: per (token, stream) the fused inject-add, inv_rms and normed = raw *
+// g * inv_rms, stored as bf16 hi + lo (normed = hi + lo to ~16 significant
+// bits) for the two GEMMs' TMA loads.
+struct TcPrepParams {
     const uint16_t *raw;      // bf16 [M][W]
     const uint16_t *g;        // bf16 [W]
-    float *part;              // [C][R][M]: per-stream partial z (un-normalised)
-    float *ssq;               // [C][M]:    per-stream sum of squares
-    int M, H, C, L, R, W;
-    int has_inject;
-    int RT;                   // row tiles of 128
-    int CS, chunk;            // CTAs per stream (cluster size), chunk width (multiple of 64)
-    int NT, n_stages;         // tokens per tile (multiple of 16, <= 128), pipeline depth
-    unsigned *status;
-    const uint16_t *inj_out;  // fused inject-add of the previous sublayer, or nullptr
-    const float *inj_gate;
+    uint16_t *raw_out;        // == raw when the inject-add is fused, else nullptr
+    const uint16_t *inj_out;  // bf16 [M][H]
+    const float *inj_gate;    // token m's previous gates at inj_gate + m * inj_stride
     long inj_stride;
-    // INT4-affine weights (wt == 1): the producers dequantise the weight tiles
+    uint16_t *x_hi, *x_lo;    // bf16 [M][W]
+    float *inv_rms;           // [M][C]
+    int M, H, C, W;
+    float eps, inv_H;
+};
+
+struct TcDownParams {
+    float *part;              // [nchunk][Mp][R]: partial z of K chunk kc
+    int M, L, C, R, W, Mp;
+    int has_inject;
+    int KBc, nchunk;          // K blocks per chunk, chunks
+    int NT, n_stages;         // tokens per tile, pipeline depth
+    unsigned *status;
+    // INT4-affine weights (wt == 1): producer warps dequantise the weight tiles
     // to bf16 hi + lo in place of the TMA loads of bf16 tiles (wt == 0).
     int wt;
     WeightView dw, iw;        // input_mix_weight_down, block_inject_weight
@@ -33,36 +69,28 @@ struct TcDownParams {
 
 struct TcReduceParams {
     const float *part;
-    const float *ssq;
     float *act;               // [M][L] fp32
     uint16_t *act_hi;         // [M][L] bf16
     uint16_t *act_lo;         // [M][L] bf16
-    float *inv_rms;           // [M][C]
     float *gate;              // token m's gates at gate + m * gate_stride
     long gate_stride;
-    int M, H, C, L, R;
-    float eps, inv_C;
+    int M, L, R, Mp, nchunk;
+    float inv_C;
 };
 
 struct TcUpParams {
-    const uint16_t *raw;      // bf16 [M][W]
-    const uint16_t *g;        // bf16 [W]
-    const float *inv_rms;     // [M][C]
     uint16_t *mixed;          // bf16 [M][H]
     int M, H, C, L, W;
     int HBt;                  // h values per CTA (C * HBt <= 128, multiple of 8)
     int NT, n_stages;
     float inv_C;
     unsigned *status;
-    uint16_t *raw_out;        // == raw when the inject-add is fused, else nullptr
-    const uint16_t *inj_out;
-    const float *inj_gate;
-    long inj_stride;
     int wt;                   // 1: INT4-affine up weights, dequantised by producer warps
     WeightView uw;
 };
 
 struct TcCall {
+    TcPrepParams prep;
     TcDownParams down;
     TcReduceParams red;
     TcUpParams up;

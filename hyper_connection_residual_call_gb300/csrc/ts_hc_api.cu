@@ -192,21 +192,15 @@ ts_status check_module(const ts_hc_module *m, bool with_inject, int H, int C, in
 
 namespace {
 
-// The batched tensor-core path: M >= kTcMinTokens, lowrank a multiple of 64,
-// and a stream split into CS chunks that are multiples of 64 (largest CS <= 8).
-// Returns CS, or 0 when the shape does not qualify.
-int tc_cluster_size(int M, int H, int C, int L)
+// The batched tensor-core path: M >= kTcMinTokens, H and lowrank multiples of
+// 64 (whole 64-wide K blocks), at most 8 streams.
+bool tc_path_ok(int M, int H, int C, int L)
 {
-    if (M < tshc::kTcMinTokens || L % 64 != 0 || C > 8)
-        return 0;
-    for (int cs = 8; cs >= 1; cs /= 2)
-        if (H % (64 * cs) == 0)
-            return H / cs <= 2048 ? cs : 0;  // a CTA stages its chunk of g (<= 2048 elements)
-    return 0;
+    return M >= tshc::kTcMinTokens && L % 64 == 0 && H % 64 == 0 && C <= 8;
 }
 
 struct WsLayout {
-    size_t inv_rms, act, part, ssq, act_hi, act_lo, part1, ssq1, total;
+    size_t inv_rms, act, x_hi, x_lo, part, act_hi, act_lo, part1, ssq1, total;
 };
 
 // Per-chunk partial dots and sums of squares of the one-token path: at most
@@ -224,11 +218,13 @@ WsLayout ws_layout(int M, int H, int C, int L)
         w.ssq1 = w.part1 + tshc::kPartCopies * align256(sizeof(float) * kPart1Chunks * ((size_t)L + C));
         w.total = w.ssq1 + tshc::kPartCopies * sizeof(float) * tshc::kSsqStride;
     }
-    if (tc_cluster_size(M, H, C, L) > 0) {
-        const size_t R = (size_t)L + C;
-        w.part = w.total;
-        w.ssq = w.part + align256(sizeof(float) * (size_t)C * R * M);
-        w.act_hi = w.ssq + align256(sizeof(float) * (size_t)C * M);
+    if (tc_path_ok(M, H, C, L)) {  // normed hi/lo, per-chunk partials, act hi/lo
+        const size_t R = (size_t)L + C, W = (size_t)C * H;
+        const tshc::TcPlan pl = tshc::tc_plan(M, L, C, (int)W);
+        w.x_hi = w.total;
+        w.x_lo = w.x_hi + align256(2 * (size_t)M * W);
+        w.part = w.x_lo + align256(2 * (size_t)M * W);
+        w.act_hi = w.part + align256(sizeof(float) * (size_t)pl.nchunk * R * pl.Mp);
         w.act_lo = w.act_hi + align256(2 * (size_t)M * L);
         w.total = w.act_lo + align256(2 * (size_t)M * L);
     }
@@ -304,66 +300,62 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
     float *inv_rms = reinterpret_cast<float *>(wsb + wl.inv_rms);
     float *act = reinterpret_cast<float *>(wsb + wl.act);
 
-    const int cs = tc_cluster_size(M, H, C, L);
     const bool all_bf16 = down->type == TS_W_BF16 && up->type == TS_W_BF16 && (!inject || inject->type == TS_W_BF16);
     // INT4-affine weights on the tensor cores: dequantised per tile to bf16 hi + lo.
     const bool all_int4 = down->type == TS_W_INT4_AFFINE && up->type == TS_W_INT4_AFFINE &&
                           (!inject || inject->type == TS_W_INT4_AFFINE) && down->group % 8 == 0 &&
                           up->group % 8 == 0;
-    if (cs > 0 && (all_bf16 || all_int4)) {
+    if (tc_path_ok(M, H, C, L) && (all_bf16 || all_int4)) {
+        const tshc::TcPlan pl = tshc::tc_plan(M, L, C, W);
         tshc::TcCall t{};
         const int R = L + (inject ? C : 0);
-        const int NT = M >= 128 ? 128 : (M + 15) / 16 * 16;
+        tshc::TcPrepParams &tp = t.prep;
+        tp.raw = static_cast<const uint16_t *>(raw);
+        tp.g = static_cast<const uint16_t *>(hc_norm_w);
+        if (fi) {
+            tp.raw_out = fi->raw;
+            tp.inj_out = fi->out;
+            tp.inj_gate = fi->gate;
+            tp.inj_stride = fi->stride;
+        }
+        tp.x_hi = reinterpret_cast<uint16_t *>(wsb + wl.x_hi);
+        tp.x_lo = reinterpret_cast<uint16_t *>(wsb + wl.x_lo);
+        tp.inv_rms = inv_rms;
+        tp.M = M; tp.H = H; tp.C = C; tp.W = W;
+        tp.eps = eps; tp.inv_H = 1.0f / (float)H;
         tshc::TcDownParams &td = t.down;
-        td.raw = static_cast<const uint16_t *>(raw);
-        td.g = static_cast<const uint16_t *>(hc_norm_w);
         td.part = reinterpret_cast<float *>(wsb + wl.part);
-        td.ssq = reinterpret_cast<float *>(wsb + wl.ssq);
-        td.M = M; td.H = H; td.C = C; td.L = L; td.R = R; td.W = W;
+        td.M = M; td.L = L; td.C = C; td.R = R; td.W = W; td.Mp = pl.Mp;
         td.has_inject = inject ? 1 : 0;
-        td.RT = (R + 127) / 128;
-        td.CS = cs; td.chunk = H / cs;
-        td.NT = NT;
+        td.KBc = pl.KBc; td.nchunk = pl.nchunk;
+        td.NT = pl.NT;
         td.wt = all_int4 ? 1 : 0;
         td.dw = view(down);
         td.iw = view(inject);
         td.n_stages = 4;
-        while (td.n_stages > 2 && tshc::tc_down_smem(NT, td.n_stages, td.wt) > tshc::kTcSmemLimit)
+        while (td.n_stages > 2 && tshc::tc_down_smem(pl.NT, td.n_stages, td.wt) > tshc::kTcSmemLimit)
             --td.n_stages;
         td.status = dev.status;
-        if (fi) {
-            td.inj_out = fi->out;
-            td.inj_gate = fi->gate;
-            td.inj_stride = fi->stride;
-        }
         tshc::TcReduceParams &tr = t.red;
-        tr.part = td.part; tr.ssq = td.ssq; tr.act = act;
+        tr.part = td.part; tr.act = act;
         tr.act_hi = reinterpret_cast<uint16_t *>(wsb + wl.act_hi);
         tr.act_lo = reinterpret_cast<uint16_t *>(wsb + wl.act_lo);
-        tr.inv_rms = inv_rms;
         tr.gate = inject ? inject_w : nullptr;
         tr.gate_stride = inject ? inject_stride : 0;
-        tr.M = M; tr.H = H; tr.C = C; tr.L = L; tr.R = R;
-        tr.eps = eps; tr.inv_C = 1.0f / (float)C;
+        tr.M = M; tr.L = L; tr.R = R; tr.Mp = pl.Mp; tr.nchunk = pl.nchunk;
+        tr.inv_C = 1.0f / (float)C;
         tshc::TcUpParams &tu = t.up;
-        tu.raw = td.raw; tu.g = td.g; tu.inv_rms = inv_rms;
         tu.mixed = static_cast<uint16_t *>(mixed);
         tu.M = M; tu.H = H; tu.C = C; tu.L = L; tu.W = W;
         tu.HBt = (128 / C) / 8 * 8;
-        tu.NT = NT;
+        tu.NT = pl.NT;
         tu.wt = td.wt;
         tu.uw = view(up);
         tu.n_stages = 3;
-        while (tu.n_stages > 2 && tshc::tc_up_smem(NT, tu.n_stages, C, tu.HBt, tu.wt) > tshc::kTcSmemLimit)
+        while (tu.n_stages > 2 && tshc::tc_up_smem(pl.NT, tu.n_stages, C, tu.HBt, tu.wt) > tshc::kTcSmemLimit)
             --tu.n_stages;
         tu.inv_C = tr.inv_C;
         tu.status = dev.status;
-        if (fi) {
-            tu.raw_out = fi->raw;
-            tu.inj_out = fi->out;
-            tu.inj_gate = fi->gate;
-            tu.inj_stride = fi->stride;
-        }
         t.wd = down->data;
         t.wi = inject ? inject->data : nullptr;
         t.wu = up->data;

@@ -156,7 +156,7 @@ ts_status ts_hc_mixer(const void *raw, const void *hc_norm_w,
  *
  *   - Shapes whose ts_hc_workspace_bytes() exceeds TS_HC_STATIC_SCRATCH_BYTES
  *     are refused with TS_ERR_WORKSPACE before anything is launched (at the
- *     full shape H=2560, C=4, lowrank=320 that allows up to 539 tokens).
+ *     full shape H=2560, C=4, lowrank=320 that allows up to 1373 tokens).
  *   - The first call on each device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
  *   - Every call on a device shares the one array and leaves its contents
@@ -167,7 +167,7 @@ ts_status ts_hc_mixer(const void *raw, const void *hc_norm_w,
  *
  * Arguments and results as for ts_hc_call, without workspace/workspace_bytes.
  */
-#define TS_HC_STATIC_SCRATCH_BYTES (4u * 1024u * 1024u)
+#define TS_HC_STATIC_SCRATCH_BYTES (64u * 1024u * 1024u)
 ts_status ts_hc_call_noalloc(const void *raw, const void *hc_norm_w,
                              const ts_weight *down, const ts_weight *up, const ts_weight *inject,
                              void *mixed, float *inject_w, long inject_stride,

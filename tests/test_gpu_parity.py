@@ -209,7 +209,10 @@ def test_prefill_microbatch(orc):
     # mlp_hc reads the residual after a bf16-rounded inject-add (chained input)
     check_fp32(inv_m, ref["inv_rms_mlp"], "mlp inv_rms", floor=CHAINED_RMS_FLOOR)
     check_fp32(act_m, ref["a_mlp"], "mlp act", floor=CHAINED_RMS_FLOOR)
-    check_bf16(raw_d, ref["raw_after_mlp"], "residual after mlp inject")
+    # The second inject-add starts from a bf16 residual that may already carry a
+    # legitimate rounding flip: the carried-residual bound applies.
+    peak = np.maximum(np.abs(to_np(raw)), np.maximum(np.abs(ref["raw_after_attn"]), np.abs(ref["raw_after_mlp"])))
+    check_bf16_carried(raw_d, ref["raw_after_mlp"], peak, "residual after mlp inject")
 
     # The same micro-batch as 128 single-token calls, each at its own gate row.
     raw_t = raw.cuda()
@@ -227,7 +230,7 @@ def test_prefill_microbatch(orc):
     torch.cuda.synchronize()
     check_fp32(gates_t.view(M, 2, C), ref["gates"], "per-token gate slots")
     check_bf16(mixed_t, ref["mixed_mlp"], "per-token mlp mixed")
-    check_bf16(raw_t, ref["raw_after_mlp"], "per-token residual")
+    check_bf16_carried(raw_t, ref["raw_after_mlp"], peak, "per-token residual")
 
 
 def run_stack_gpu(st, H, C):

@@ -57,8 +57,9 @@ def test_noalloc_matches_call_on_two_calls_in_a_row():
 
 def test_noalloc_refuses_more_tokens_than_its_scratch_holds():
     require_gpu()
-    M = 540  # ts_hc_workspace_bytes(540, 2560, 4, 320) > TS_HC_STATIC_SCRATCH_BYTES
+    M = 1374  # the first token count whose workspace exceeds TS_HC_STATIC_SCRATCH_BYTES at this shape
     assert B.ts_hc_workspace_bytes(M, H, C, L) > B.TS_HC_STATIC_SCRATCH_BYTES
+    assert B.ts_hc_workspace_bytes(M - 1, H, C, L) <= B.TS_HC_STATIC_SCRATCH_BYTES
     w, raw = _inputs(2, 503)
     st = B.ts_hc_call_noalloc(raw.data_ptr(), w.g.data_ptr(), B.weight_struct(w.down), B.weight_struct(w.up),
                               B.weight_struct(w.inject), raw.data_ptr(), raw.data_ptr(), C, M, H, C, L, EPS,
