@@ -50,6 +50,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 // ~1e-6, far inside the 1e-3 bar), for the per-element epilogues.
 __device__ __forceinline__ float sigm_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
+// sigmoid(x) = (1 + tanh(x / 2)) / 2 with the hardware tanh approximation
+// (one special-function op instead of two; absolute error below 3e-4 -- used
+// only where the result is mixed into a bf16 output, whose own rounding is
+// ~2e-3 relative).
+__device__ __forceinline__ float sigm_tanh(float x)
+{
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+    return fmaf(0.5f, t, 0.5f);
+}
+
 __device__ __forceinline__ void record_timeout(unsigned *status)
 {
     if (status)
@@ -118,6 +129,12 @@ __global__ void __launch_bounds__(kPrepThreads) hc_tc_prep_kernel(const TcPrepPa
     const size_t base = (size_t)m * p.W + (size_t)c * p.H;
     const bool fused = p.raw_out != nullptr;
     pdl_launch_dependents();
+    uint4 gq[kPrepVec];  // g is a weight: read before the dependency wait
+#pragma unroll
+    for (int k = 0; k < kPrepVec; ++k) {
+        const int v = tid + k * blockDim.x;
+        gq[k] = v < nv ? reinterpret_cast<const uint4 *>(p.g + (size_t)c * p.H)[v] : make_uint4(0, 0, 0, 0);
+    }
     pdl_wait();  // the residual, the sublayer output and the previous gates come from earlier kernels
 
     // Every load first (the residual is written back below).
@@ -168,9 +185,8 @@ __global__ void __launch_bounds__(kPrepThreads) hc_tc_prep_kernel(const TcPrepPa
         const int v = tid + k * blockDim.x;
         if (v >= nv)
             continue;
-        const uint4 gq = reinterpret_cast<const uint4 *>(p.g + (size_t)c * p.H)[v];
         const uint32_t w[4] = {rv[k].x, rv[k].y, rv[k].z, rv[k].w};
-        const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+        const uint32_t gw[4] = {gq[k].x, gq[k].y, gq[k].z, gq[k].w};
         uint32_t h[4], l[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -431,15 +447,30 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
 
 // One thread per (token, row): element i = m * R + r of every chunk's partial
 // tile, so the loads of a warp are contiguous; the chunks are summed in order,
-// every load of a thread in flight at once.
-constexpr int kReduceThreads = 256;
-constexpr int kReduceBatch = 20;
+// every load of a thread in flight at once. The host sizes the grid to about
+// one CTA per SM (and reserves shared memory to keep it so). Before the
+// dependency wait each CTA asks L2 for its share of the up kernel's weights,
+// whose CTAs can start only after this kernel's.
+constexpr int kReduceBatch = 40;
 
-__global__ void __launch_bounds__(kReduceThreads) hc_tc_reduce_kernel(const TcReduceParams p)
+__global__ void __launch_bounds__(1024) hc_tc_reduce_kernel(const TcReduceParams p)
 {
     pdl_launch_dependents();
+    if (threadIdx.x < 32) {
+        constexpr size_t kPiece = 16384;
+        const size_t nb = gridDim.x, b = blockIdx.x;
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            const size_t total = p.l2_next_bytes[i];
+            const size_t share = ((total + nb - 1) / nb + 15) & ~size_t(15);
+            const size_t lo = min(total, b * share), hi = min(total, lo + share);
+            for (size_t off = lo + (size_t)threadIdx.x * kPiece; off < hi; off += 32 * kPiece)
+                bulk_prefetch_l2(static_cast<const unsigned char *>(p.l2_next[i]) + off,
+                                 (uint32_t)min(kPiece, hi - off));
+        }
+    }
     pdl_wait();
-    const long i = (long)blockIdx.x * kReduceThreads + threadIdx.x;
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (long)p.M * p.R)
         return;
     const float *src = p.part + i;
@@ -670,7 +701,7 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                mix_s[(cc * NT + c0 + j) * HBt + hl] = sigm_fast(__uint_as_float(vr[j])) * x[j];
+                mix_s[(cc * NT + c0 + j) * HBt + hl] = sigm_tanh(__uint_as_float(vr[j])) * x[j];
         };
         const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16);
         uint32_t va[16], vb[16];
@@ -839,7 +870,7 @@ cudaError_t launch_tc_call(const TcCall &t, cudaStream_t stream)
     cudaError_t e;
     if ((e = allow_smem_tc(kd)) != cudaSuccess) return e;
     if ((e = allow_smem_tc(ku)) != cudaSuccess) return e;
-    if ((e = allow_smem_tc(hc_tc_reduce_kernel, false)) != cudaSuccess) return e;
+    if ((e = allow_smem_tc(hc_tc_reduce_kernel)) != cudaSuccess) return e;
     if ((e = allow_smem_tc(hc_tc_prep_kernel, false)) != cudaSuccess) return e;
     // Up to kPrepVec vectors per thread, so that the M * C CTAs fit the GPU at once.
     const int prep_threads = std::min(kPrepThreads, ((pp.H / 8 + kPrepVec - 1) / kPrepVec + 31) / 32 * 32);
@@ -851,9 +882,12 @@ cudaError_t launch_tc_call(const TcCall &t, cudaStream_t stream)
                   tc_down_smem(d.NT, d.n_stages, d.wt), stream, 0, d, map_d, map_i, map_xhi, map_xlo);
     if (e != cudaSuccess)
         return e;
+    // About one output per thread on one CTA per SM (more CTAs only past 1024 threads each).
     const long nred = (long)t.red.M * t.red.R;
-    e = launch_tc(hc_tc_reduce_kernel, dim3((unsigned)((nred + kReduceThreads - 1) / kReduceThreads)),
-                  dim3(kReduceThreads), 0, stream, 0, t.red);
+    const long per = (nred + kTcChunkCtas - 1) / kTcChunkCtas;
+    const int rthreads = (int)std::min<long>(1024, (per + 31) / 32 * 32);
+    e = launch_tc(hc_tc_reduce_kernel, dim3((unsigned)((nred + rthreads - 1) / rthreads)), dim3(rthreads),
+                  kTcReduceSmemReserve, stream, 0, t.red);
     if (e != cudaSuccess)
         return e;
     return launch_tc(ku, dim3((u.H + u.HBt - 1) / u.HBt, ntiles), dim3(kThreads),

@@ -11,6 +11,11 @@ namespace tshc {
 constexpr int kTcMinTokens = 16;          // the batched path starts at this many tokens
 constexpr size_t kTcSmemLimit = 232448;   // 227 KB opt-in shared memory per CTA
 constexpr int kTcChunkCtas = 152;         // the down kernel's K split aims at about this many CTAs
+// Shared memory the reduce kernel reserves (and does not use) so that at most
+// one of its CTAs runs per SM and none beside a down or up CTA: launched early
+// (programmatic dependent launch), its CTAs would otherwise pile onto the few
+// SMs the down kernel leaves free and run several times slower there.
+constexpr size_t kTcReduceSmemReserve = 120 * 1024;
 
 // Tiling of one call on M tokens. It depends on the shape only, not on the
 // device, so the order of the split-K sums -- and every result bit -- does not
@@ -76,6 +81,10 @@ struct TcReduceParams {
     long gate_stride;
     int M, L, R, Mp, nchunk;
     float inv_C;
+    // Byte ranges of the up kernel's weights (data, scales, biases) that the
+    // CTAs ask L2 to prefetch, split evenly over the grid; bytes == 0 if unused.
+    const void *l2_next[3];
+    size_t l2_next_bytes[3];
 };
 
 struct TcUpParams {

@@ -87,6 +87,13 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
         : "memory");
 }
 
+// Asks L2 to fetch [src, src + bytes) from HBM; nothing is waited for or
+// counted. src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---- programmatic dependent launch -----------------------------------------
 
 // Lets the next kernel in the stream start launching (its blocks then wait in

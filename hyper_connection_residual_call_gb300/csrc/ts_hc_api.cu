@@ -344,6 +344,18 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         tr.gate_stride = inject ? inject_stride : 0;
         tr.M = M; tr.L = L; tr.R = R; tr.Mp = pl.Mp; tr.nchunk = pl.nchunk;
         tr.inv_C = 1.0f / (float)C;
+        {  // the up weights, rounded inwards to 16-byte boundaries (an L2 hint only)
+            const size_t wbytes = up->type == TS_W_BF16 ? (size_t)W * L * 2 : (size_t)W * L / 2;
+            const size_t sbytes = up->type == TS_W_BF16 ? 0 : (size_t)W * (L / up->group) * 2;
+            const void *ranges[3] = {up->data, up->scales, up->biases};
+            const size_t sizes[3] = {wbytes, sbytes, sbytes};
+            for (int i = 0; i < 3; ++i) {
+                const uintptr_t a = reinterpret_cast<uintptr_t>(ranges[i]);
+                const uintptr_t lo = (a + 15) & ~uintptr_t(15), hi = (a + sizes[i]) & ~uintptr_t(15);
+                tr.l2_next[i] = reinterpret_cast<const void *>(lo);
+                tr.l2_next_bytes[i] = sizes[i] && hi > lo ? (size_t)(hi - lo) : 0;
+            }
+        }
         tshc::TcUpParams &tu = t.up;
         tu.mixed = static_cast<uint16_t *>(mixed);
         tu.M = M; tu.H = H; tu.C = C; tu.L = L; tu.W = W;
