@@ -622,17 +622,32 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
             wsc[j] = ok ? p.uw.scales + row * ngr : nullptr;
             wbi[j] = ok ? p.uw.biases + row * ngr : nullptr;
         }
+        // The next K block's codes, scales and biases are loaded while the
+        // current one is converted.
+        uint32_t qn[kItems];
+        uint16_t sn[kItems], bn[kItems];
+        auto fetch = [&](int kb) {
+            const int col = kb * kKBlock + 8 * ck;
+#pragma unroll
+            for (int j = 0; j < kItems; ++j) {
+                qn[j] = wq[j] ? *reinterpret_cast<const uint32_t *>(wq[j] + col / 2) : 0u;
+                sn[j] = wq[j] ? wsc[j][col / p.uw.group] : (uint16_t)0;
+                bn[j] = wq[j] ? wbi[j][col / p.uw.group] : (uint16_t)0;
+            }
+        };
+        fetch(0);
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % NS, u = kb / NS;
-            const int col = kb * kKBlock + 8 * ck;
             uint32_t q[kItems];
             uint16_t sc[kItems], bi[kItems];
 #pragma unroll
             for (int j = 0; j < kItems; ++j) {
-                q[j] = wq[j] ? *reinterpret_cast<const uint32_t *>(wq[j] + col / 2) : 0u;
-                sc[j] = wq[j] ? wsc[j][col / p.uw.group] : (uint16_t)0;
-                bi[j] = wq[j] ? wbi[j][col / p.uw.group] : (uint16_t)0;
+                q[j] = qn[j];
+                sc[j] = sn[j];
+                bi[j] = bn[j];
             }
+            if (kb + 1 < KB)
+                fetch(kb + 1);
             if (u > 0 && !mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
             uint8_t *ahi = smem + lay.ring + s * lay.stage_bytes;
             uint8_t *alo = ahi + lay.a_bytes;
