@@ -169,6 +169,26 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c)
     return d;
 }
 
+// d = a + b, lane-wise, round to nearest.
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Nibbles 2e and 2e+1 of an INT4 code word (elements 2e and 2e+1) as an exact
+// fp32 pair, without an int-to-float conversion: a value q < 2^23 OR-ed into
+// the mantissa of 2^23 is the float 2^23 + q, from which 2^23 is subtracted.
+__device__ __forceinline__ uint64_t nib2_f32x2(uint32_t codes, int e)
+{
+    const uint32_t lo = ((codes >> (8 * e)) & 0xFu) | 0x4B000000u;
+    const uint32_t hi = ((codes >> (8 * e + 4)) & 0xFu) | 0x4B000000u;
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return fadd2(r, 0xCB000000CB000000ull);  // + (-2^23, -2^23)
+}
+
 // Sum of the two lanes: low + high.
 __device__ __forceinline__ float f32x2_sum(uint64_t v)
 {
@@ -789,6 +809,12 @@ __global__ void __launch_bounds__(1024, 1) hc_down1_kernel(const DownParams p)
 #pragma unroll
     for (int e = 0; e < 4; ++e)
         xp[e] = f32x2(x[2 * e], x[2 * e + 1]);
+    float xsum = 0.f;  // INT4: the group's bias multiplies the sum of the inputs
+    if constexpr (WT == 1) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            xsum += x[e];
+    }
     float acc[kRowsPerGroup];
 #pragma unroll
     for (int j = 0; j < kRowsPerGroup; ++j) {
@@ -803,15 +829,14 @@ __global__ void __launch_bounds__(1024, 1) hc_down1_kernel(const DownParams p)
                 a = ffma2(bf16x2_as_f32x2(wq.z), xp[2], a);
                 a = ffma2(bf16x2_as_f32x2(wq.w), xp[3], a);
             } else {
+                // The thread's 8 inputs share one (scale, bias) group:
+                // sum (q s + b) x = s * sum q x + b * sum x.
                 const uint32_t codes = *reinterpret_cast<const uint32_t *>(wr + v * 4);
                 const float *sb = sb_s + 2 * ((gr0 + j) * ng + (v * 8) / p.down.group);
-                const uint64_t sc = f32x2(sb[0], sb[0]), bi = f32x2(sb[1], sb[1]);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint64_t q = f32x2((float)((codes >> (8 * e)) & 0xFu),
-                                             (float)((codes >> (8 * e + 4)) & 0xFu));
-                    a = ffma2(ffma2(q, sc, bi), xp[e], a);
-                }
+                for (int e = 0; e < 4; ++e)
+                    a = ffma2(nib2_f32x2(codes, e), xp[e], a);
+                a = f32x2(fmaf(sb[0], f32x2_sum(a), sb[1] * xsum), 0.f);
             }
             acc[j] = f32x2_sum(a);
         }
@@ -1018,8 +1043,12 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
             for (int c = 0; c < NC; ++c) acc[c] = f32x2_sum(a2[c]);
         } else {
             for (int v = lane; v < L / 8; v += 32) {
+                // The word's 8 act values share one (scale, bias) group of every
+                // row: sum (q s + b) a = s * sum q a + b * sum a.
                 const float4 xa = *reinterpret_cast<const float4 *>(act_s + v * 8);
                 const float4 xb = *reinterpret_cast<const float4 *>(act_s + v * 8 + 4);
+                const uint64_t ap[4] = {f32x2(xa.x, xa.y), f32x2(xa.z, xa.w), f32x2(xb.x, xb.y), f32x2(xb.z, xb.w)};
+                const float asum = ((xa.x + xa.y) + (xa.z + xa.w)) + ((xb.x + xb.y) + (xb.z + xb.w));
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     if (c < p.C) {
@@ -1027,17 +1056,11 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
                         const uint32_t codes =
                             *reinterpret_cast<const uint32_t *>(w_s + (size_t)srow * row_bytes + v * 4);
                         const float *sb = sb_s + 2 * (srow * ng + (v * 8) / p.up.group);
-                        const float sc = sb[0], bi = sb[1];
-                        float wf[8];
+                        uint64_t dq = 0;
 #pragma unroll
-                        for (int n = 0; n < 8; ++n)
-                            wf[n] = fmaf((float)((codes >> (4 * n)) & 0xFu), sc, bi);
-                        float a0 = acc[c], a1 = 0.f;
-                        a0 = fmaf(wf[0], xa.x, a0); a1 = fmaf(wf[1], xa.y, a1);
-                        a0 = fmaf(wf[2], xa.z, a0); a1 = fmaf(wf[3], xa.w, a1);
-                        a0 = fmaf(wf[4], xb.x, a0); a1 = fmaf(wf[5], xb.y, a1);
-                        a0 = fmaf(wf[6], xb.z, a0); a1 = fmaf(wf[7], xb.w, a1);
-                        acc[c] = a0 + a1;
+                        for (int e = 0; e < 4; ++e)
+                            dq = ffma2(nib2_f32x2(codes, e), ap[e], dq);
+                        acc[c] += fmaf(sb[0], f32x2_sum(dq), sb[1] * asum);
                     }
                 }
             }
