@@ -75,8 +75,7 @@ struct TcDownParams {
 struct TcReduceParams {
     const float *part;
     float *act;               // [M][L] fp32
-    uint16_t *act_hi;         // [M][L] bf16
-    uint16_t *act_lo;         // [M][L] bf16
+    uint16_t *act_hi;         // [M][L] bf16 (round to nearest): the up GEMM's B operand
     float *gate;              // token m's gates at gate + m * gate_stride
     long gate_stride;
     int M, L, R, Mp, nchunk;

@@ -200,7 +200,7 @@ bool tc_path_ok(int M, int H, int C, int L)
 }
 
 struct WsLayout {
-    size_t inv_rms, act, x_hi, x_lo, part, act_hi, act_lo, part1, ssq1, total;
+    size_t inv_rms, act, x_hi, x_lo, part, act_hi, part1, ssq1, total;
 };
 
 // Per-chunk partial dots and sums of squares of the one-token path: at most
@@ -218,15 +218,14 @@ WsLayout ws_layout(int M, int H, int C, int L)
         w.ssq1 = w.part1 + tshc::kPartCopies * align256(sizeof(float) * kPart1Chunks * ((size_t)L + C));
         w.total = w.ssq1 + tshc::kPartCopies * sizeof(float) * tshc::kSsqStride;
     }
-    if (tc_path_ok(M, H, C, L)) {  // normed hi/lo, per-chunk partials, act hi/lo
+    if (tc_path_ok(M, H, C, L)) {  // normed hi/lo, per-chunk partials, bf16 act
         const size_t R = (size_t)L + C, W = (size_t)C * H;
         const tshc::TcPlan pl = tshc::tc_plan(M, L, C, (int)W);
         w.x_hi = w.total;
         w.x_lo = w.x_hi + align256(2 * (size_t)M * W);
         w.part = w.x_lo + align256(2 * (size_t)M * W);
         w.act_hi = w.part + align256(sizeof(float) * (size_t)pl.nchunk * R * pl.Mp);
-        w.act_lo = w.act_hi + align256(2 * (size_t)M * L);
-        w.total = w.act_lo + align256(2 * (size_t)M * L);
+        w.total = w.act_hi + align256(2 * (size_t)M * L);
     }
     return w;
 }
@@ -339,7 +338,6 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         tshc::TcReduceParams &tr = t.red;
         tr.part = td.part; tr.act = act;
         tr.act_hi = reinterpret_cast<uint16_t *>(wsb + wl.act_hi);
-        tr.act_lo = reinterpret_cast<uint16_t *>(wsb + wl.act_lo);
         tr.gate = inject ? inject_w : nullptr;
         tr.gate_stride = inject ? inject_stride : 0;
         tr.M = M; tr.L = L; tr.R = R; tr.Mp = pl.Mp; tr.nchunk = pl.nchunk;
@@ -363,7 +361,7 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         tu.NT = pl.NT;
         tu.wt = td.wt;
         tu.uw = view(up);
-        tu.n_stages = 3;
+        tu.n_stages = 4;
         while (tu.n_stages > 2 && tshc::tc_up_smem(pl.NT, tu.n_stages, C, tu.HBt, tu.wt) > tshc::kTcSmemLimit)
             --tu.n_stages;
         tu.inv_C = tr.inv_C;

@@ -156,7 +156,7 @@ ts_status ts_hc_mixer(const void *raw, const void *hc_norm_w,
  *
  *   - Shapes whose ts_hc_workspace_bytes() exceeds TS_HC_STATIC_SCRATCH_BYTES
  *     are refused with TS_ERR_WORKSPACE before anything is launched (at the
- *     full shape H=2560, C=4, lowrank=320 that allows up to 1373 tokens).
+ *     full shape H=2560, C=4, lowrank=320 that allows up to 1394 tokens).
  *   - The first call on each device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
  *   - Every call on a device shares the one array and leaves its contents

@@ -41,11 +41,11 @@ def test_workspace_size_and_layout(lib):
     # the chunks' sums of squares (64-float stride)
     assert B.ts_hc_workspace_bytes(1, H, C, L) == 256 + 1280 + 8 * a256(4 * 8 * (L + C)) + 8 * 4 * 64
     # from 16 tokens the tensor-core path adds normed as bf16 hi + lo [M][C*H] x 2, the
-    # down kernel's per-chunk partials [nchunk][L+C][Mp] fp32 and the bf16 hi/lo
-    # activations [M][L] x 2. The K split aims at 152 CTAs: at M=128 (one 128-token
-    # tile, 3 row tiles) 160 K blocks of 64 go 4 to a chunk, 40 chunks.
+    # down kernel's per-chunk partials [nchunk][L+C][Mp] fp32 and the bf16 activations
+    # [M][L]. The K split aims at 152 CTAs: at M=128 (one 128-token tile, 3 row tiles)
+    # 160 K blocks of 64 go 4 to a chunk, 40 chunks.
     for M, nchunk, Mp in ((128, 40, 128), (16, 40, 16), (40, 40, 48), (300, 16, 384)):
-        tc = 2 * a256(2 * M * C * H) + a256(4 * nchunk * (L + C) * Mp) + 2 * a256(2 * M * L)
+        tc = 2 * a256(2 * M * C * H) + a256(4 * nchunk * (L + C) * Mp) + a256(2 * M * L)
         assert B.ts_hc_workspace_bytes(M, H, C, L) == a256(4 * M * C) + a256(4 * M * L) + tc, M
     assert B.ts_hc_workspace_bytes(15, H, C, L) == a256(4 * 15 * C) + a256(4 * 15 * L)
     assert B.ts_hc_workspace_bytes(0, H, C, L) == 0
