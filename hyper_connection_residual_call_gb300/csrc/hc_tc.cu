@@ -42,7 +42,7 @@ namespace {
 constexpr int kThreads = 256;  // 8 warps
 constexpr int kTileRows = 128; // UMMA M
 constexpr int kKBlock = 64;    // bf16 elements per 128-byte swizzled row
-constexpr int kProducers = 192; // warps 2-7 build the down kernel's activation tiles
+constexpr int kProducers = 192; // warps 2-7 dequantise INT4 weight tiles
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
@@ -97,8 +97,12 @@ __device__ __forceinline__ void int4x8_hilo(uint32_t codes, uint16_t sb, uint16_
     uint32_t h[4], l[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const float wa = fmaf((float)((codes >> (8 * e)) & 0xFu), sc, bi);
-        const float wb = fmaf((float)((codes >> (8 * e + 4)) & 0xFu), sc, bi);
+        // Nibbles 2e and 2e+1 as exact floats without a conversion: q OR-ed into
+        // the mantissa of 2^23 is the float 2^23 + q.
+        const float qa = __uint_as_float(((codes >> (8 * e)) & 0xFu) | 0x4B000000u) - 8388608.0f;
+        const float qb = __uint_as_float(((codes >> (8 * e + 4)) & 0xFu) | 0x4B000000u) - 8388608.0f;
+        const float wa = fmaf(qa, sc, bi);
+        const float wb = fmaf(qb, sc, bi);
         const uint32_t hh = pack_bf16x2(wa, wb);
         h[e] = hh;
         l[e] = pack_bf16x2(wa - bf16_lo(hh), wb - bf16_hi(hh));
@@ -261,7 +265,7 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&fullp[s], kProducers);
+            mbar_init(&fullp[s], kProducers / 32);  // one arrival per producer warp
             mbar_init(&empty[s], 1);
         }
         mbar_init(done, 1);
@@ -378,8 +382,12 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
                 *reinterpret_cast<uint4 *>(ahi + sw128_offset(rr, 8 * ck)) = hi;
                 *reinterpret_cast<uint4 *>(alo + sw128_offset(rr, 8 * ck)) = lo;
             }
+            // Each thread's tile writes become visible to the tensor cores; the
+            // warp then arrives once.
             fence_async_shared();
-            mbar_arrive(&fullp[s]);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&fullp[s]);
         }
     } else if (warp == 1 && lane == 0) {
         // MMA issuer.
@@ -552,7 +560,7 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&fullp[s], kProducers);
+            mbar_init(&fullp[s], kProducers / 32);  // one arrival per producer warp
         }
         mbar_init(done, 1);
         mbar_init(nbar, 1);
@@ -662,8 +670,12 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
                 *reinterpret_cast<uint4 *>(ahi + sw128_offset(rr, 8 * ck)) = hi;
                 *reinterpret_cast<uint4 *>(alo + sw128_offset(rr, 8 * ck)) = lo;
             }
+            // Each thread's tile writes become visible to the tensor cores; the
+            // warp then arrives once.
             fence_async_shared();
-            mbar_arrive(&fullp[s]);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&fullp[s]);
         }
     }
 

@@ -342,18 +342,21 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         tr.gate_stride = inject ? inject_stride : 0;
         tr.M = M; tr.L = L; tr.R = R; tr.Mp = pl.Mp; tr.nchunk = pl.nchunk;
         tr.inv_C = 1.0f / (float)C;
-        {  // the up weights, rounded inwards to 16-byte boundaries (an L2 hint only)
-            const size_t wbytes = up->type == TS_W_BF16 ? (size_t)W * L * 2 : (size_t)W * L / 2;
-            const size_t sbytes = up->type == TS_W_BF16 ? 0 : (size_t)W * (L / up->group) * 2;
-            const void *ranges[3] = {up->data, up->scales, up->biases};
+        // L2 prefetch hint: the up weights (by the reduce kernel), rounded
+        // inwards to 16-byte boundaries.
+        auto hint = [](const ts_weight *w, size_t rows, size_t cols, const void **ptr, size_t *bytes) {
+            const size_t wbytes = w->type == TS_W_BF16 ? rows * cols * 2 : rows * cols / 2;
+            const size_t sbytes = w->type == TS_W_BF16 ? 0 : rows * (cols / w->group) * 2;
+            const void *ranges[3] = {w->data, w->scales, w->biases};
             const size_t sizes[3] = {wbytes, sbytes, sbytes};
             for (int i = 0; i < 3; ++i) {
                 const uintptr_t a = reinterpret_cast<uintptr_t>(ranges[i]);
                 const uintptr_t lo = (a + 15) & ~uintptr_t(15), hi = (a + sizes[i]) & ~uintptr_t(15);
-                tr.l2_next[i] = reinterpret_cast<const void *>(lo);
-                tr.l2_next_bytes[i] = sizes[i] && hi > lo ? (size_t)(hi - lo) : 0;
+                ptr[i] = reinterpret_cast<const void *>(lo);
+                bytes[i] = sizes[i] && hi > lo ? (size_t)(hi - lo) : 0;
             }
-        }
+        };
+        hint(up, (size_t)W, (size_t)L, tr.l2_next, tr.l2_next_bytes);
         tshc::TcUpParams &tu = t.up;
         tu.mixed = static_cast<uint16_t *>(mixed);
         tu.M = M; tu.H = H; tu.C = C; tu.L = L; tu.W = W;
