@@ -76,8 +76,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&b);
 }
 
-__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
-
 __host__ __device__ constexpr uint32_t tmem_cols(int n)
 {
     return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : 256u;

@@ -97,10 +97,9 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
                  ::"r"(smem_addr(bar)) : "memory");
 }
 
-// 32 lanes x 32 bits, 16 consecutive columns: lane i of the warp receives
-// row (lane base + i), columns col .. col+15.
-// 32 lanes x 16 columns of fp32 from TMEM without waiting: the registers are
-// valid only after tmem_wait_ld(). Several loads can be in flight at once.
+// 32 lanes x 32 bits, 16 consecutive columns, without waiting: lane i of the
+// warp receives row (lane base + i), columns col .. col+15. The registers are
+// valid only after tmem_wait_ld(); several loads can be in flight at once.
 __device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16])
 {
     asm volatile(
@@ -123,22 +122,6 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16])
                    "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
                  :
                  : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
-{
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        v[i] = __uint_as_float(r[i]);
 }
 
 // ---- tensor-map TMA ----------------------------------------------------------
