@@ -39,10 +39,12 @@ namespace tshc {
 
 namespace {
 
-constexpr int kThreads = 256;  // 8 warps
+constexpr int kThreads = 256;  // down kernel: 8 warps
+constexpr int kUpThreads = 512;  // up kernel: 16 warps (the epilogue and the INT4 producers are latency-bound)
 constexpr int kTileRows = 128; // UMMA M
 constexpr int kKBlock = 64;    // bf16 elements per 128-byte swizzled row
-constexpr int kProducers = 192; // warps 2-7 dequantise INT4 weight tiles
+constexpr int kProducers = 192;  // down kernel: warps 2-7 dequantise INT4 weight tiles
+constexpr int kUpProducers = kUpThreads - 64;  // up kernel: warps 2-15
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
@@ -528,7 +530,7 @@ __host__ __device__ inline TcSmem up_tc_layout(int NT, int ns, int C, int HBt, i
 }
 
 template <int WT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kUpThreads, 1)
 hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
                 const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_nhi,
                 const __grid_constant__ CUtensorMap map_nlo)
@@ -558,7 +560,7 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&fullp[s], kProducers / 32);  // one arrival per producer warp
+            mbar_init(&fullp[s], kUpProducers / 32);  // one arrival per producer warp
         }
         mbar_init(done, 1);
         mbar_init(nbar, 1);
@@ -607,20 +609,20 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
             tma_load_2d(const_cast<uint16_t *>(nlo_s) + cc * NT * HBt, &map_nlo, cc * p.H + h0, tile * NT, nbar);
         }
     } else if (WT == 1 && warp >= 2) {
-        // INT4 weights: warps 2-7 dequantise the A tiles (rows (stream, h) of
+        // INT4 weights: warps 2-15 dequantise the A tiles (rows (stream, h) of
         // this CTA, 64 columns per stage) to bf16 hi + lo. Thread t handles the
-        // 16-byte chunks t + kProducers j: row / 8, chunk t % 8. Weights only:
+        // 16-byte chunks t + kUpProducers j: row / 8, chunk t % 8. Weights only:
         // no dependency wait.
         const int t = tid - 64;
         const int ck = t & 7;
-        constexpr int kItems = (kTileRows * 8 + kProducers - 1) / kProducers;
+        constexpr int kItems = (kTileRows * 8 + kUpProducers - 1) / kUpProducers;
         const uint8_t *wq[kItems];
         const uint16_t *wsc[kItems];
         const uint16_t *wbi[kItems];
         const int ngr = p.L / p.uw.group;
 #pragma unroll
         for (int j = 0; j < kItems; ++j) {
-            const int rr = (t + kProducers * j) >> 3;
+            const int rr = (t + kUpProducers * j) >> 3;
             const int cc = rr / HBt, hl = rr % HBt;
             const bool ok = rr < kTileRows && cc < C && h0 + hl < p.H;
             const size_t row = (size_t)cc * p.H + h0 + hl;
@@ -659,7 +661,7 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
             uint8_t *alo = ahi + lay.a_bytes;
 #pragma unroll
             for (int j = 0; j < kItems; ++j) {
-                const int rr = (t + kProducers * j) >> 3;
+                const int rr = (t + kUpProducers * j) >> 3;
                 if (rr >= kTileRows)
                     continue;
                 uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
@@ -699,21 +701,22 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
     }
     __syncthreads();  // reconverges the single-thread roles
 
-    // Epilogue on all 8 warps: warp w reads TMEM lanes 32*(w%4).. (rows = (stream,
-    // h) pairs) for the 16-column chunks of parity w/4.
+    // Epilogue on all 16 warps: warp w reads TMEM lanes 32*(w%4).. (rows = (stream,
+    // h) pairs) for the 16-column chunks 16*(w/4) + 64k.
     float *mix_s = reinterpret_cast<float *>(smem + lay.ring);  // [C][NT][HBt], over the ring
     {
         if (!mbar_wait_bounded(done, 0)) timed_out = true;
         if (!mbar_wait_bounded(nbar, 0)) timed_out = true;
         __syncwarp();  // the TMEM loads below are .aligned
         tc_fence_after();
-        const int quad = warp & 3, half = warp >> 2;
+        const int quad = warp & 3, part = warp >> 2;
+        constexpr int kStride = 16 * (kUpThreads / 128);  // columns between a warp's chunks
         const int row = quad * 32 + lane;
         const int cc = row / HBt, hl = row % HBt;
         const bool live = cc < C && h0 + hl < p.H;
-        // The warp's 16-column chunks c0 = 16*half + 32k: chunk k+1 is loaded from
-        // TMEM while chunk k is processed (two register buffers). A chunk's
-        // shared-memory loads are all issued before its stores.
+        // The warp's 16-column chunks: chunk k+1 is loaded from TMEM while chunk
+        // k is processed (two register buffers). A chunk's shared-memory loads
+        // are all issued before its stores.
         auto process = [&](int c0, const uint32_t (&vr)[16]) {
             if (!live)
                 return;
@@ -729,28 +732,28 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         };
         const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16);
         uint32_t va[16], vb[16];
-        int c0 = 16 * half;
+        int c0 = 16 * part;
         if (c0 < NT)  // warp-uniform
             tmem_ld16_async(tbase + c0, va);
         tmem_wait_ld(va);
 #pragma unroll 1
-        for (; c0 < NT; c0 += 64) {
-            if (c0 + 32 < NT)
-                tmem_ld16_async(tbase + c0 + 32, vb);
+        for (; c0 < NT; c0 += 2 * kStride) {
+            if (c0 + kStride < NT)
+                tmem_ld16_async(tbase + c0 + kStride, vb);
             process(c0, va);
             tmem_wait_ld(vb);
-            if (c0 + 32 >= NT)
+            if (c0 + kStride >= NT)
                 break;
-            if (c0 + 64 < NT)
-                tmem_ld16_async(tbase + c0 + 64, va);
-            process(c0 + 32, vb);
+            if (c0 + 2 * kStride < NT)
+                tmem_ld16_async(tbase + c0 + 2 * kStride, va);
+            process(c0 + kStride, vb);
             tmem_wait_ld(va);
         }
     }
     tc_fence_before();
     __syncthreads();
     // Mean over the streams, 8 consecutive h of one token per item (stream order).
-    for (int i = tid; i < NT * (HBt / 8); i += kThreads) {
+    for (int i = tid; i < NT * (HBt / 8); i += kUpThreads) {
         const int n = i / (HBt / 8), hv = (i % (HBt / 8)) * 8;
         const int m = tile * NT + n, h = h0 + hv;
         if (m < p.M && h + 8 <= p.H) {
@@ -913,7 +916,7 @@ cudaError_t launch_tc_call(const TcCall &t, cudaStream_t stream)
                   kTcReduceSmemReserve, stream, 0, t.red);
     if (e != cudaSuccess)
         return e;
-    return launch_tc(ku, dim3((u.H + u.HBt - 1) / u.HBt, ntiles), dim3(kThreads),
+    return launch_tc(ku, dim3((u.H + u.HBt - 1) / u.HBt, ntiles), dim3(kUpThreads),
                      tc_up_smem(u.NT, u.n_stages, u.C, u.HBt, u.wt), stream, 0, u, map_u, map_act, map_nhi, map_nlo);
 }
 
