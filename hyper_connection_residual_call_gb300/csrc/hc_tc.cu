@@ -39,11 +39,11 @@ namespace tshc {
 
 namespace {
 
-constexpr int kThreads = 256;  // down kernel: 8 warps
+constexpr int kThreads = 512;  // down kernel: 16 warps
 constexpr int kUpThreads = 512;  // up kernel: 16 warps (the epilogue and the INT4 producers are latency-bound)
 constexpr int kTileRows = 128; // UMMA M
 constexpr int kKBlock = 64;    // bf16 elements per 128-byte swizzled row
-constexpr int kProducers = 192;  // down kernel: warps 2-7 dequantise INT4 weight tiles
+constexpr int kProducers = kThreads - 64;  // down kernel: warps 2-15 dequantise INT4 weight tiles
 constexpr int kUpProducers = kUpThreads - 64;  // up kernel: warps 2-15
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
@@ -226,7 +226,7 @@ __host__ __device__ inline TcSmem down_tc_layout(int NT, int ns, int wt)
 
 // Grid (nchunk, row tiles, token tiles). Warp 0 lane 0 streams the weight
 // tiles (before the dependency wait) and the normed hi/lo tiles by TMA; with
-// INT4 weights, warps 2-7 dequantise the weight tiles instead. Warp 1 lane 0
+// INT4 weights, warps 2-15 dequantise the weight tiles instead. Warp 1 lane 0
 // issues the MMAs. All eight warps then move the fp32 tile from TMEM to
 // part[chunk][row][token].
 template <int WT>
@@ -326,7 +326,7 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
             load_b(kb, s);
         }
     } else if (WT == 1 && warp >= 2) {
-        // INT4 weights: warps 2-7 dequantise the A tiles (weights only, so no
+        // INT4 weights: warps 2-15 dequantise the A tiles (weights only, so no
         // dependency wait). Thread t handles the 16-byte chunks t + kProducers j
         // of the 128 x 64 tile: row / 8, chunk t % 8 (8 codes, one scale and bias).
         const int t = tid - 64;
@@ -338,11 +338,16 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
 #pragma unroll
         for (int j = 0; j < kItems; ++j) {
             const int rr = (t + kProducers * j) >> 3, gr = r0 + rr;
-            const WeightView *v = gr < p.L ? &p.dw : (p.has_inject && gr < p.L + p.C) ? &p.iw : nullptr;
-            const int row = gr < p.L ? gr : gr - p.L;
-            wq[j] = (v && rr < kTileRows) ? static_cast<const uint8_t *>(v->data) + (size_t)row * (p.W / 2) : nullptr;
-            wsc[j] = wq[j] ? v->scales + (size_t)row * (p.W / v->group) : nullptr;
-            wbi[j] = wq[j] ? v->biases + (size_t)row * (p.W / v->group) : nullptr;
+            // Fields picked by value: taking a parameter's address would move
+            // the parameters to local memory.
+            const bool isd = gr < p.L, isi = !isd && p.has_inject && gr < p.L + p.C;
+            const int row = isd ? gr : gr - p.L;
+            const size_t srow = (size_t)row * (p.W / p.dw.group);  // inject has down's group
+            wq[j] = ((isd || isi) && rr < kTileRows)
+                        ? static_cast<const uint8_t *>(isd ? p.dw.data : p.iw.data) + (size_t)row * (p.W / 2)
+                        : nullptr;
+            wsc[j] = wq[j] ? (isd ? p.dw.scales : p.iw.scales) + srow : nullptr;
+            wbi[j] = wq[j] ? (isd ? p.dw.biases : p.iw.biases) + srow : nullptr;
         }
         uint32_t qn[kItems];
         uint16_t sn[kItems], bn[kItems];
@@ -412,8 +417,8 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
         umma_commit(done);
     }
 
-    // Epilogue on all 8 warps: warp w reads TMEM lanes 32*(w%4).. (the tile's
-    // rows) for the 16-column chunks 16*(w/4) + 32k -- all of them before the
+    // Epilogue on all 16 warps: warp w reads TMEM lanes 32*(w%4).. (the tile's
+    // rows) for the 16-column chunks 16*(w/4) + 64k -- all of them before the
     // one wait -- and stores them to part[chunk][token][row]: the 32 lanes of a
     // store write 32 consecutive rows of one token (coalesced). The barrier
     // reconverges the single-thread roles.
@@ -422,22 +427,24 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
     __syncwarp();  // the TMEM loads below are .aligned
     tc_fence_after();
     {
-        const int quad = warp & 3, half = warp >> 2;
+        constexpr int kParts = kThreads / 128;      // warps sharing a TMEM lane quadrant
+        constexpr int kChunks = 128 / (16 * kParts);  // NT <= 128: chunks per warp
+        const int quad = warp & 3, part = warp >> 2;
         const int gr = r0 + quad * 32 + lane;
         const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16);
-        uint32_t v[4][16];  // NT <= 128: at most four chunks per warp
+        uint32_t v[kChunks][16];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            if (16 * half + 32 * k < NT)  // warp-uniform
-                tmem_ld16_async(tbase + 16 * half + 32 * k, v[k]);
+        for (int k = 0; k < kChunks; ++k)
+            if (16 * part + 16 * kParts * k < NT)  // warp-uniform
+                tmem_ld16_async(tbase + 16 * part + 16 * kParts * k, v[k]);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < kChunks; ++k)
             tmem_wait_ld(v[k]);
         if (gr < p.R) {
             float *dst = p.part + ((size_t)kc * p.Mp + (size_t)tile * NT) * p.R + gr;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int c0 = 16 * half + 32 * k;
+            for (int k = 0; k < kChunks; ++k) {
+                const int c0 = 16 * part + 16 * kParts * k;
                 if (c0 < NT) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
