@@ -28,7 +28,8 @@ RMS_EPS = 1e-6  # families/qwen4/mod.rs, RMS_EPS
 
 EXPORTS = ("ts_hc_workspace_bytes", "ts_hc_workspace_layout", "ts_hc_call", "ts_hc_inject_add",
            "ts_hc_mixer", "ts_hc_inject_call", "ts_hc_replicate_entry", "ts_hc_last_error",
-           "ts_hc_device_status", "ts_hc_call_noalloc", "ts_hc_stack_workspace_bytes", "ts_hc_stack")
+           "ts_hc_device_status", "ts_hc_call_noalloc", "ts_hc_stack_workspace_bytes", "ts_hc_stack",
+           "ts_hc_selftest_timeout")
 TS_HC_STATIC_SCRATCH_BYTES = 64 * 1024 * 1024  # include/ts_hc.h
 
 
@@ -99,6 +100,8 @@ def library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.ts_hc_stack_workspace_bytes.restype = sz
         lib.ts_hc_stack.argtypes = [vp, i, mp, mp, i, mp, SUBLAYER_FN, vp, vp, i, i, i, i, f, vp, sz, vp]
         lib.ts_hc_stack.restype = i
+        lib.ts_hc_selftest_timeout.argtypes = [vp]
+        lib.ts_hc_selftest_timeout.restype = i
         lib.ts_hc_last_error.argtypes = []
         lib.ts_hc_last_error.restype = ctypes.c_char_p
         lib.ts_hc_device_status.argtypes = [vp, ctypes.POINTER(i)]
@@ -168,6 +171,11 @@ def ts_hc_stack(emb, T, attn, mlp, n_layers, final_mixer, sublayer, user, mixed_
     return library().ts_hc_stack(emb, T, attn, mlp, n_layers, _wref(final_mixer),
                                  sublayer if sublayer is not None else SUBLAYER_FN(), user, mixed_out,
                                  max_chunk, H, C, lowrank, eps, workspace, workspace_bytes, stream)
+
+
+def ts_hc_selftest_timeout(stream) -> int:
+    """Launches the failure-path self-test (a bounded wait that must give up)."""
+    return library().ts_hc_selftest_timeout(stream)
 
 
 def ts_hc_last_error() -> str:

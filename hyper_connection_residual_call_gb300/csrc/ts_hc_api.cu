@@ -10,6 +10,7 @@
 
 #include "hc_kernels.h"
 #include "hc_tc.h"
+#include "ptx.cuh"
 #include "ts_hc.h"
 #include "ts_hc_internal.h"
 
@@ -623,6 +624,39 @@ ts_status ts_hc_replicate_entry(const void *emb, void *raw, int M, int H, int C,
 }
 
 const char *ts_hc_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"
+
+namespace {
+
+// One thread waits, with the kernels' own bounded wait, on a barrier that
+// nothing arrives at, and records the timeout as the kernels do.
+__global__ void hc_timeout_selftest_kernel(unsigned *status)
+{
+    __shared__ uint64_t bar;
+    tshc::mbar_init(&bar, 1);
+    tshc::mbar_fence_init();
+    if (!tshc::mbar_wait_bounded(&bar, 0))
+        atomicExch(status, tshc::kStatusTimeout);
+}
+
+}  // namespace
+
+extern "C" {
+
+ts_status ts_hc_selftest_timeout(cudaStream_t stream)
+{
+    g_last_error.clear();
+    DeviceInfo dev;
+    ts_status st = device_info(&dev);
+    if (st != TS_OK)
+        return st;
+    hc_timeout_selftest_kernel<<<1, 1, 0, stream>>>(dev.status);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launching the timeout self-test kernel");
+    return TS_OK;
+}
 
 ts_status ts_hc_device_status(cudaStream_t stream, int *status)
 {

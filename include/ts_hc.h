@@ -266,6 +266,17 @@ ts_status ts_hc_stack(const void *emb, int T, const ts_hc_module *attn, const ts
                       void *user, void *mixed_out, int max_chunk, int H, int C, int lowrank,
                       float eps, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Self-test of the failure path. Launches one thread that waits, with the same
+ * bounded wait the kernels use for their asynchronous copies, on a
+ * shared-memory barrier that nothing arrives at. After about one second it
+ * gives up and records TS_ERR_TIMEOUT in the device status word, as a kernel
+ * whose copy never completed would; ts_hc_device_status() then reports it and
+ * clears it. Nothing else is read or written, and the context stays usable.
+ * Returns TS_OK once launched (asynchronous on `stream`).
+ */
+ts_status ts_hc_selftest_timeout(cudaStream_t stream);
+
 /* The last error message of the calling thread ("" if none). */
 const char *ts_hc_last_error(void);
 

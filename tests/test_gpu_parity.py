@@ -465,5 +465,21 @@ def test_inject_add_strided_gates(orc):
     check_bf16(r, ref, "strided inject-add")
 
 
+def test_bounded_wait_records_a_timeout_and_the_context_stays_usable(orc):
+    """The kernels' bounded wait on a barrier that nothing arrives at gives up
+    (after about a second) and records TS_ERR_TIMEOUT in the status word; the
+    status clears once read, and a call afterwards runs and matches the oracle."""
+    import time
+    assert B.device_status() == B.TS_OK
+    t0 = time.time()
+    assert B.ts_hc_selftest_timeout(torch.cuda.current_stream().cuda_stream) == B.TS_OK
+    assert B.device_status() == B.TS_ERR_TIMEOUT
+    assert 0.5 < time.time() - t0 < 30
+    assert B.device_status() == B.TS_OK  # cleared by the read
+    res = call_and_inject(orc, inputs.TINY, inputs.SEEDS["tiny"])
+    assert res[0].shape == (1, inputs.TINY.H)
+    assert B.device_status() == B.TS_OK
+
+
 def test_device_status_clean():
     assert B.device_status() == B.TS_OK
