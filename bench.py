@@ -19,9 +19,9 @@ results read back inside the timed region.
 
 ``other_configs`` (skipped with --no-configs) times the rest of the workload
 family the same way, each over distinct weight sets: the M=128 prefill
-micro-batch (attn_hc + mlp_hc per batch, tensor-core path), the INT4-affine
-full shape at M=1 and M=64, and the 40-layer stack (entry replication, 80
-fused calls, exit mixer) at M=1 and M=16.
+micro-batch (attn_hc + mlp_hc per batch, tensor-core path), an 8-token decode
+batch, the INT4-affine full shape at M=1 and M=64, and the 40-layer stack
+(entry replication, 80 fused calls, exit mixer) at M=1 and M=16.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -349,6 +349,19 @@ def measure_other_configs(B, inputs, torch, dev, stream, sets_bf16, peak):
     del raw, outs, ws, mixed
 
     # INT4-affine (group 64), full shape, M = 1 and M = 64.
+    # A small decode batch (8 tokens, e.g. 8 sequences decoding together): fused calls.
+    Md = 8
+    raw = inputs.make_residual(Md, H, C, 1).to(dev)
+    outs = [inputs.make_sublayer_out(Md, H, 1, i).to(dev) for i in range(4)]
+    gates = torch.zeros((2, Md, C), dtype=torch.float32, device=dev)
+    slots = [(gates[0], C), (gates[1], C)]
+    mixed = torch.empty((Md, H), dtype=torch.bfloat16, device=dev)
+    ws = B.workspace(Md, H, C, L, dev)
+    n = 2 * len(sets_bf16)
+    ms = graph_ms(chain(raw, outs, gates, sets_bf16, n, mixed, ws, slots), 5)
+    record(f"decode_m{Md}_bf16", Md, ms, n, bytes_per_call(Md, sets_bf16[0].nbytes),
+           {"path": "tensor-core (tcgen05) kernels, one 16-token tile"})
+
     sets_q = [inputs.make_hc_weights(H, C, L, 4, i, kind="int4").to(dev) for i in range(len(sets_bf16))]
     for Mq in (1, 64):
         raw = inputs.make_residual(Mq, H, C, 4).to(dev)

@@ -1,4 +1,4 @@
-// hc_tc.cu -- the batched (M >= 16 tokens) hyper-connection call on the
+// hc_tc.cu -- the batched (M >= 2 tokens) hyper-connection call on the
 // 5th-generation tensor cores: tcgen05.mma with TMEM accumulators, operands
 // staged by tensor-map TMA in the 128-byte swizzled layout.
 //

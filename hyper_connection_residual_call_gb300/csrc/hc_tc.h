@@ -8,7 +8,10 @@
 
 namespace tshc {
 
-constexpr int kTcMinTokens = 16;          // the batched path starts at this many tokens
+// The batched path starts at 2 tokens: a 16-token tile serves 2..16 tokens in
+// about the time of one (absent tokens are TMA zero-fill), far faster than the
+// cluster split-K kernels beyond 2 tokens.
+constexpr int kTcMinTokens = 2;
 constexpr size_t kTcSmemLimit = 232448;   // 227 KB opt-in shared memory per CTA
 constexpr int kTcChunkCtas = 152;         // the down kernel's K split aims at about this many CTAs
 // Shared memory the reduce kernel reserves (and does not use) so that at most

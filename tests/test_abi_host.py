@@ -40,14 +40,16 @@ def test_workspace_size_and_layout(lib):
     # one token: inv_rms, act, and 8 copies of up to 8 chunks of per-row partials and of
     # the chunks' sums of squares (64-float stride)
     assert B.ts_hc_workspace_bytes(1, H, C, L) == 256 + 1280 + 8 * a256(4 * 8 * (L + C)) + 8 * 4 * 64
-    # from 16 tokens the tensor-core path adds normed as bf16 hi + lo [M][C*H] x 2, the
+    # from 2 tokens the tensor-core path adds normed as bf16 hi + lo [M][C*H] x 2, the
     # down kernel's per-chunk partials [nchunk][L+C][Mp] fp32 and the bf16 activations
     # [M][L]. The K split aims at 152 CTAs: at M=128 (one 128-token tile, 3 row tiles)
     # 160 K blocks of 64 go 4 to a chunk, 40 chunks.
-    for M, nchunk, Mp in ((128, 40, 128), (16, 40, 16), (40, 40, 48), (300, 16, 384)):
+    for M, nchunk, Mp in ((128, 40, 128), (2, 40, 16), (15, 40, 16), (16, 40, 16), (40, 40, 48),
+                          (300, 16, 384)):
         tc = 2 * a256(2 * M * C * H) + a256(4 * nchunk * (L + C) * Mp) + a256(2 * M * L)
         assert B.ts_hc_workspace_bytes(M, H, C, L) == a256(4 * M * C) + a256(4 * M * L) + tc, M
-    assert B.ts_hc_workspace_bytes(15, H, C, L) == a256(4 * 15 * C) + a256(4 * 15 * L)
+    # shapes the tensor-core path does not take (lowrank not a multiple of 64): inv_rms, act
+    assert B.ts_hc_workspace_bytes(15, H, C, 32) == a256(4 * 15 * C) + a256(4 * 15 * 32)
     assert B.ts_hc_workspace_bytes(0, H, C, L) == 0
     assert B.ts_hc_workspace_bytes(-1, H, C, L) == 0
     inv, act = B.ts_hc_workspace_layout(3, H, C, L)

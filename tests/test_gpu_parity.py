@@ -104,7 +104,8 @@ def test_shapes_and_ragged_tokens(orc, M, H, C, L):
     call_and_inject(orc, inputs.Shape(M=M, H=H, C=C, L=L), seed=100 + M)
 
 
-@pytest.mark.parametrize("M,H,C,L,group", [(3, 128, 2, 64, 32), (2, 256, 4, 64, 64), (5, 256, 1, 128, 128)])
+@pytest.mark.parametrize("M,H,C,L,group", [(3, 128, 2, 64, 32), (2, 256, 4, 64, 64), (5, 256, 1, 128, 128),
+                                           (4, 128, 2, 32, 32), (7, 96, 3, 32, 32)])
 def test_int4_shapes(orc, M, H, C, L, group):
     call_and_inject(orc, inputs.Shape(M=M, H=H, C=C, L=L), seed=200 + M, kind="int4", group=group)
 
@@ -117,7 +118,7 @@ def test_int4_tiny_up_group_32(orc):
 @pytest.mark.parametrize("M,H,C,L,group,up_group", [(16, 2560, 4, 320, 64, None), (40, 512, 2, 64, 32, None),
                                                       (128, 1024, 8, 128, 64, 32)])
 def test_int4_tensor_core_path(orc, M, H, C, L, group, up_group):
-    # INT4-affine weights from 16 tokens run on tcgen05: each weight tile is dequantised
+    # INT4-affine weights from 2 tokens run on tcgen05: each weight tile is dequantised
     # to bf16 hi + lo and multiplied against the activation's hi + lo (three MMAs)
     call_and_inject(orc, inputs.Shape(M=M, H=H, C=C, L=L), seed=400 + M, kind="int4", group=group,
                     up_group=up_group)
@@ -130,12 +131,13 @@ def test_int4_full_shape(orc, M):
                     group=inputs.INT4_GROUP)
 
 
-@pytest.mark.parametrize("M,H,C,L", [(16, 2560, 4, 320), (40, 2560, 4, 320),
+@pytest.mark.parametrize("M,H,C,L", [(2, 2560, 4, 320), (7, 1024, 8, 128), (15, 256, 1, 64),
+                                     (16, 2560, 4, 320), (40, 2560, 4, 320),
                                      (64, 2560, 4, 320), (100, 2560, 4, 320), (130, 2560, 4, 320),
                                      (256, 2560, 4, 320), (64, 512, 2, 64), (80, 1024, 8, 128),
                                      (70, 320, 3, 64), (96, 256, 1, 128)])
 def test_tensor_core_path(orc, M, H, C, L):
-    # M >= 16 with bf16 weights runs on tcgen05 (tiles of up to 128 tokens)
+    # M >= 2 with bf16 weights runs on tcgen05 (tiles of up to 128 tokens)
     call_and_inject(orc, inputs.Shape(M=M, H=H, C=C, L=L), seed=300 + M)
 
 
