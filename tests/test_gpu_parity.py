@@ -419,6 +419,46 @@ def test_stack_driver_feeds_mixed_to_the_sublayer(max_chunk):
     assert torch.equal(raw_last, raw), "driver's last-chunk residual differs"
 
 
+def test_stack_driver_int4_matches_oracle(orc):
+    """ts_hc_stack on INT4-affine modules (chunks of 4 and 1 tokens: the tensor-core
+    and the one-token INT4 paths) against the oracle's stack."""
+    H, C, L, M, n = 256, 4, 64, 5, 2
+    st = inputs.make_stack(M, H, C, L, n, 23, kind="int4")
+    ref = orc.stack(st.emb, st.layers, st.outs, st.final, H=H, C=C, L=L, eps=EPS, round_residual=True)
+    dev = inputs.StackInputs(st.emb, [(a.to("cuda"), m.to("cuda")) for a, m in st.layers],
+                             [(a.cuda(), m.cuda()) for a, m in st.outs], st.final.to("cuda"))
+    mixed, raw = run_stack_driver(dev, H, C, max_chunk=4)
+    check_bf16(mixed, ref["mixed"], "INT4 stack mixer output")
+    check_bf16_carried(raw, ref["raw"][-1:], ref["peak"][-1:], "INT4 stack residual (last chunk)")
+
+
+def test_stack_driver_captured_in_a_graph_is_bit_identical():
+    """A whole ts_hc_stack pass captured into one CUDA graph and replayed gives the
+    same bits as the pass run eagerly (the driver allocates nothing and never
+    synchronises)."""
+    s = inputs.FULL_DECODE
+    H, C, L, M, n = s.H, s.C, s.L, 3, 2
+    st = inputs.make_stack(M, H, C, L, n, 24)
+    layers = [(a.to("cuda"), m.to("cuda")) for a, m in st.layers]
+    outs = [(a.cuda(), m.cuda()) for a, m in st.outs]
+    final = st.final.to("cuda")
+    emb = st.emb.cuda()
+    ws = B.stack_workspace(M, H, C, L)
+    eager = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    sub = lambda l, w, t0, mixed: outs[l][w][t0:t0 + mixed.shape[0]]
+    B.hc_stack(emb, layers, final, sub, C=C, mixed_out=eager, ws=ws)
+    torch.cuda.synchronize()
+    replayed = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        B.hc_stack(emb, layers, final, sub, C=C, mixed_out=replayed, ws=ws)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(replayed, eager), "graph replay differs from the eager pass"
+    assert B.device_status() == B.TS_OK
+
+
 def test_stack_driver_rejects_bad_sublayer_outputs():
     s = inputs.TINY
     H, C, L, M = s.H, s.C, s.L, 2
