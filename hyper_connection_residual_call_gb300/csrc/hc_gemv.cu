@@ -68,7 +68,7 @@ __host__ __device__ inline DownSmem down_layout(const DownParams &p, int mt)
     const int VW = p.down.type == 0 ? 8 : 32;
     const int kcp = round_up(p.KC, 32 * VW);
     const size_t seg = p.down.type == 0 ? (size_t)p.KC * 2 : (size_t)p.KC / 2;
-    const int ng = p.down.type == 0 ? 0 : p.KC / p.down.group;
+    const int ng = p.down.type == 0 ? 0 : p.KC >> p.down.gshift;
     DownSmem s;
     s.bar = 0;
     s.w = 128;
@@ -92,7 +92,7 @@ struct UpSmem {
 __host__ __device__ inline UpSmem up_layout(const UpParams &p, int mt)
 {
     const size_t row = p.up.type == 0 ? (size_t)p.L * 2 : (size_t)p.L / 2;
-    const int ng = p.up.type == 0 ? 0 : p.L / p.up.group;
+    const int ng = p.up.type == 0 ? 0 : p.L >> p.up.gshift;
     UpSmem s;
     s.bar = 0;
     s.w = 128;
@@ -236,7 +236,7 @@ __device__ __forceinline__ void row_dot_bf16(const uint4 *wrow, int nvec, const 
 // INT4-affine: lane handles vectors of 32 codes (one group-aligned run of 32
 // inputs, so one scale and bias).
 template <int MT>
-__device__ __forceinline__ void row_dot_int4(const uint4 *wrow, int nvec, const float *sb, int group,
+__device__ __forceinline__ void row_dot_int4(const uint4 *wrow, int nvec, const float *sb, int gshift,
                                              const float *x, int xstride, int lane, float (&acc)[MT])
 {
     float a0[MT], a1[MT];
@@ -244,7 +244,7 @@ __device__ __forceinline__ void row_dot_int4(const uint4 *wrow, int nvec, const 
     for (int t = 0; t < MT; ++t) { a0[t] = 0.f; a1[t] = 0.f; }
     for (int v = lane; v < nvec; v += 32) {
         const uint4 q = wrow[v];
-        const int gi = (v * 32) / group;
+        const int gi = (v * 32) >> gshift;
         const float sc = sb[2 * gi], bi = sb[2 * gi + 1];
         const uint32_t words[4] = {q.x, q.y, q.z, q.w};
         const int base = (v >> 5) * 1024 + (v & 31) * 4;
@@ -315,13 +315,13 @@ __global__ void __launch_bounds__(512) hc_down_kernel(const DownParams p)
         }
     }
     if constexpr (WT == 1) {
-        const int ng = KC / p.down.group;
+        const int ng = KC >> p.down.gshift;
         for (int i = tid; i < nrows * ng; i += blockDim.x) {
             const int r = i / ng, gi = i % ng;
             const int gr = r0 + r;
             const WeightView &wv = gr < p.L ? p.down : p.inject;
             const int row = gr < p.L ? gr : gr - p.L;
-            const size_t off = (size_t)row * (p.W / wv.group) + k0 / wv.group + gi;
+            const size_t off = (size_t)row * (p.W >> wv.gshift) + (k0 >> wv.gshift) + gi;
             sb_s[2 * i] = half_bits_to_float(wv.scales[off]);
             sb_s[2 * i + 1] = half_bits_to_float(wv.biases[off]);
         }
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(512) hc_down_kernel(const DownParams p)
             if constexpr (WT == 0)
                 row_dot_bf16<MT>(wrow, nvec, x_s, kcp, lane, acc);
             else
-                row_dot_int4<MT>(wrow, nvec, sb_s + 2 * r * (KC / p.down.group), p.down.group, x_s, kcp,
+                row_dot_int4<MT>(wrow, nvec, sb_s + 2 * r * (KC >> p.down.gshift), p.down.gshift, x_s, kcp,
                                  lane, acc);
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(768, 1) hc_up_kernel(const UpParams p)
     const int hb = min(HB, p.H - h0);
     const int L = p.L;
     const size_t row_bytes = WT == 0 ? (size_t)L * 2 : (size_t)L / 2;
-    const int ng = WT == 0 ? 0 : L / p.up.group;
+    const int ng = WT == 0 ? 0 : L >> p.up.gshift;
 
     pdl_launch_dependents();
 
@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(768, 1) hc_up_kernel(const UpParams p)
                 const uint32_t *wrow32 = reinterpret_cast<const uint32_t *>(wrow);
                 for (int w = tl; w < L / 8; w += 8) {
                     const uint32_t codes = wrow32[w];
-                    const int gi = (w * 8) / p.up.group;
+                    const int gi = (w * 8) >> p.up.gshift;
                     const float sc = sb[2 * gi], bi = sb[2 * gi + 1];
                     float wf[8];
 #pragma unroll
@@ -685,7 +685,7 @@ struct Down1Smem {
 __host__ __device__ inline Down1Smem down1_layout(const DownParams &p)
 {
     const size_t seg = p.down.type == 0 ? (size_t)p.KC * 2 : (size_t)p.KC / 2;
-    const int ng = p.down.type == 0 ? 0 : p.KC / p.down.group;
+    const int ng = p.down.type == 0 ? 0 : p.KC >> p.down.gshift;
     Down1Smem s;
     s.bar = 0;
     s.w = 128;
@@ -749,14 +749,14 @@ __global__ void __launch_bounds__(1024, 1) hc_down1_kernel(const DownParams p)
             }
         }
     }
-    const int ng = WT == 0 ? 1 : KC / p.down.group;
+    const int ng = WT == 0 ? 1 : KC >> p.down.gshift;
     if constexpr (WT == 1) {
         for (int i = tid; i < nrows * ng; i += blockDim.x) {
             const int r = i / ng, gi = i % ng;
             const int gr = r0 + r;
             const WeightView &wv = gr < p.L ? p.down : p.inject;
             const int row = gr < p.L ? gr : gr - p.L;
-            const size_t off = (size_t)row * (p.W / wv.group) + k0 / wv.group + gi;
+            const size_t off = (size_t)row * (p.W >> wv.gshift) + (k0 >> wv.gshift) + gi;
             sb_s[2 * i] = half_bits_to_float(wv.scales[off]);
             sb_s[2 * i + 1] = half_bits_to_float(wv.biases[off]);
         }
@@ -832,7 +832,7 @@ __global__ void __launch_bounds__(1024, 1) hc_down1_kernel(const DownParams p)
                 // The thread's 8 inputs share one (scale, bias) group:
                 // sum (q s + b) x = s * sum q x + b * sum x.
                 const uint32_t codes = *reinterpret_cast<const uint32_t *>(wr + v * 4);
-                const float *sb = sb_s + 2 * ((gr0 + j) * ng + (v * 8) / p.down.group);
+                const float *sb = sb_s + 2 * ((gr0 + j) * ng + ((v * 8) >> p.down.gshift));
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     a = ffma2(nib2_f32x2(codes, e), xp[e], a);
@@ -877,7 +877,7 @@ struct Up1Smem {
 __host__ __device__ inline Up1Smem up1_layout(const UpParams &p)
 {
     const size_t row = p.up.type == 0 ? (size_t)p.L * 2 : (size_t)p.L / 2;
-    const int ng = p.up.type == 0 ? 0 : p.L / p.up.group;
+    const int ng = p.up.type == 0 ? 0 : p.L >> p.up.gshift;
     Up1Smem s;
     s.bar = 0;
     s.w = 128;
@@ -909,7 +909,7 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
     const int hb = min(HB, p.H - h0);
     const int L = p.L;
     const size_t row_bytes = WT == 0 ? (size_t)L * 2 : (size_t)L / 2;
-    const int ng = WT == 0 ? 1 : L / p.up.group;
+    const int ng = WT == 0 ? 1 : L >> p.up.gshift;
 
     // Thread 0 initialises the barrier and issues the weight copies at once;
     // no other thread touches the barrier before the first block-wide
@@ -1041,6 +1041,35 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
             }
 #pragma unroll
             for (int c = 0; c < NC; ++c) acc[c] = f32x2_sum(a2[c]);
+        } else if constexpr (CC == 4) {
+            // Lane owns stream c = lane & 3 and the code words v = lane / 4 + 8 i
+            // of that row, so every lane handles the same number of words. The
+            // word's 8 act values share one (scale, bias) group of the row:
+            // sum (q s + b) a = s * sum q a + b * sum a.
+            const int c = lane & 3;
+            const int srow = c * HB + hl;
+            const uint32_t *wr = reinterpret_cast<const uint32_t *>(w_s + (size_t)srow * row_bytes);
+            const float *sbr = sb_s + 2 * (size_t)srow * ng;
+            float a = 0.f;
+#pragma unroll 5
+            for (int v = lane >> 2; v < L / 8; v += 8) {
+                const float4 xa = *reinterpret_cast<const float4 *>(act_s + v * 8);
+                const float4 xb = *reinterpret_cast<const float4 *>(act_s + v * 8 + 4);
+                const uint64_t ap[4] = {f32x2(xa.x, xa.y), f32x2(xa.z, xa.w), f32x2(xb.x, xb.y), f32x2(xb.z, xb.w)};
+                const float asum = ((xa.x + xa.y) + (xa.z + xa.w)) + ((xb.x + xb.y) + (xb.z + xb.w));
+                const uint32_t codes = wr[v];
+                const float *sb = sbr + 2 * ((v * 8) >> p.up.gshift);
+                uint64_t dq = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    dq = ffma2(nib2_f32x2(codes, e), ap[e], dq);
+                a += fmaf(sb[0], f32x2_sum(dq), sb[1] * asum);
+            }
+            // Lanes with equal lane & 3 hold parts of the same row.
+            a += __shfl_xor_sync(0xffffffffu, a, 4);
+            a += __shfl_xor_sync(0xffffffffu, a, 8);
+            a += __shfl_xor_sync(0xffffffffu, a, 16);
+            acc[0] = a;
         } else {
             for (int v = lane; v < L / 8; v += 32) {
                 // The word's 8 act values share one (scale, bias) group of every
@@ -1049,13 +1078,15 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
                 const float4 xb = *reinterpret_cast<const float4 *>(act_s + v * 8 + 4);
                 const uint64_t ap[4] = {f32x2(xa.x, xa.y), f32x2(xa.z, xa.w), f32x2(xb.x, xb.y), f32x2(xb.z, xb.w)};
                 const float asum = ((xa.x + xa.y) + (xa.z + xa.w)) + ((xb.x + xb.y) + (xb.z + xb.w));
+                const int gi = (v * 8) >> p.up.gshift;
+                constexpr int NC = CC > 0 ? CC : 8;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    if (c < p.C) {
+                for (int c = 0; c < NC; ++c) {
+                    if (CC > 0 || c < p.C) {
                         const int srow = c * HB + hl;
                         const uint32_t codes =
                             *reinterpret_cast<const uint32_t *>(w_s + (size_t)srow * row_bytes + v * 4);
-                        const float *sb = sb_s + 2 * (srow * ng + (v * 8) / p.up.group);
+                        const float *sb = sb_s + 2 * (srow * ng + gi);
                         uint64_t dq = 0;
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
@@ -1065,7 +1096,13 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
                 }
             }
         }
-        const float d = warp_transpose_sum8(acc, lane);
+        // Lane 4c takes row c's total: from lane c in the INT4 four-stream
+        // layout, else from the transposed butterfly.
+        float d;
+        if constexpr (WT == 1 && CC == 4)
+            d = __shfl_sync(0xffffffffu, acc[0], (lane >> 2) & 3);
+        else
+            d = warp_transpose_sum8(acc, lane);
         float term = holder ? sigmoid_fast(d) * nvh : 0.f;
         term += __shfl_xor_sync(0xffffffffu, term, 4);
         term += __shfl_xor_sync(0xffffffffu, term, 8);
@@ -1274,7 +1311,7 @@ cudaError_t launch_one_token(const DownParams &d, const UpParams &u, const Launc
     if (!one_token_ok(d, u))
         return cudaErrorInvalidConfiguration;
     void (*kd)(DownParams) = d.down.type == 0 ? hc_down1_kernel<0> : hc_down1_kernel<1>;
-    void (*ku)(UpParams) = u.up.type != 0 ? hc_up1_kernel<1, 0>
+    void (*ku)(UpParams) = u.up.type != 0 ? (u.C == 4 ? hc_up1_kernel<1, 4> : hc_up1_kernel<1, 0>)
                            : u.C == 4     ? hc_up1_kernel<0, 4>
                                           : hc_up1_kernel<0, 0>;
     const size_t sd = down1_layout(d).total, su = up1_layout(u).total;

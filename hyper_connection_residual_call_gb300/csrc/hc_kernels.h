@@ -10,7 +10,8 @@ namespace tshc {
 // A [rows][cols] weight in device memory (rows = outputs).
 struct WeightView {
     int type;                 // 0 bf16, 1 INT4-affine
-    int group;                // INT4 group size
+    int group;                // INT4 group size: 32, 64 or 128
+    int gshift;               // log2(group): group indices are shifts, not divisions
     const void *data;         // bf16 [rows][cols] or uint8 [rows][cols/2]
     const uint16_t *scales;   // fp16 [rows][cols/group]
     const uint16_t *biases;   // fp16 [rows][cols/group]

@@ -342,7 +342,7 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
             // the parameters to local memory.
             const bool isd = gr < p.L, isi = !isd && p.has_inject && gr < p.L + p.C;
             const int row = isd ? gr : gr - p.L;
-            const size_t srow = (size_t)row * (p.W / p.dw.group);  // inject has down's group
+            const size_t srow = (size_t)row * (p.W >> p.dw.gshift);  // inject has down's group
             wq[j] = ((isd || isi) && rr < kTileRows)
                         ? static_cast<const uint8_t *>(isd ? p.dw.data : p.iw.data) + (size_t)row * (p.W / 2)
                         : nullptr;
@@ -356,8 +356,8 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
 #pragma unroll
             for (int j = 0; j < kItems; ++j) {
                 qn[j] = wq[j] ? *reinterpret_cast<const uint32_t *>(wq[j] + col / 2) : 0u;
-                sn[j] = wq[j] ? wsc[j][col / p.dw.group] : (uint16_t)0;
-                bn[j] = wq[j] ? wbi[j][col / p.dw.group] : (uint16_t)0;
+                sn[j] = wq[j] ? wsc[j][col >> p.dw.gshift] : (uint16_t)0;
+                bn[j] = wq[j] ? wbi[j][col >> p.dw.gshift] : (uint16_t)0;
             }
         };
         fetch(0);
@@ -626,7 +626,7 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         const uint8_t *wq[kItems];
         const uint16_t *wsc[kItems];
         const uint16_t *wbi[kItems];
-        const int ngr = p.L / p.uw.group;
+        const int ngr = p.L >> p.uw.gshift;
 #pragma unroll
         for (int j = 0; j < kItems; ++j) {
             const int rr = (t + kUpProducers * j) >> 3;
@@ -646,8 +646,8 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
 #pragma unroll
             for (int j = 0; j < kItems; ++j) {
                 qn[j] = wq[j] ? *reinterpret_cast<const uint32_t *>(wq[j] + col / 2) : 0u;
-                sn[j] = wq[j] ? wsc[j][col / p.uw.group] : (uint16_t)0;
-                bn[j] = wq[j] ? wbi[j][col / p.uw.group] : (uint16_t)0;
+                sn[j] = wq[j] ? wsc[j][col >> p.uw.gshift] : (uint16_t)0;
+                bn[j] = wq[j] ? wbi[j][col >> p.uw.gshift] : (uint16_t)0;
             }
         };
         fetch(0);

@@ -134,6 +134,8 @@ tshc::WeightView view(const ts_weight *w)
         return v;
     v.type = w->type;
     v.group = w->type == TS_W_INT4_AFFINE ? w->group : 0;
+    while (v.group > 0 && (1 << v.gshift) < v.group)
+        ++v.gshift;
     v.data = w->data;
     v.scales = static_cast<const uint16_t *>(w->scales);
     v.biases = static_cast<const uint16_t *>(w->biases);
