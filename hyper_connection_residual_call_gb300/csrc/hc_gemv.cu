@@ -144,49 +144,12 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
-// ---- packed fp32x2 arithmetic (two IEEE fp32 FMAs in one instruction) ----
-
-__device__ __forceinline__ uint64_t f32x2(float lo, float hi)
-{
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-
 // A bf16 pair (element 2i in the low half of the word) as an fp32 pair.
 __device__ __forceinline__ uint64_t bf16x2_as_f32x2(uint32_t w)
 {
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w << 16), "r"(w & 0xffff0000u));
     return r;
-}
-
-// d = a * b + c, lane-wise, round to nearest.
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c)
-{
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
-// d = a + b, lane-wise, round to nearest.
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-// Nibbles 2e and 2e+1 of an INT4 code word (elements 2e and 2e+1) as an exact
-// fp32 pair, without an int-to-float conversion: a value q < 2^23 OR-ed into
-// the mantissa of 2^23 is the float 2^23 + q, from which 2^23 is subtracted.
-__device__ __forceinline__ uint64_t nib2_f32x2(uint32_t codes, int e)
-{
-    const uint32_t lo = ((codes >> (8 * e)) & 0xFu) | 0x4B000000u;
-    const uint32_t hi = ((codes >> (8 * e + 4)) & 0xFu) | 0x4B000000u;
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-    return fadd2(r, 0xCB000000CB000000ull);  // + (-2^23, -2^23)
 }
 
 // Sum of the two lanes: low + high.
@@ -832,10 +795,11 @@ __global__ void __launch_bounds__(1024, 1) hc_down1_kernel(const DownParams p)
                 // The thread's 8 inputs share one (scale, bias) group:
                 // sum (q s + b) x = s * sum q x + b * sum x.
                 const uint32_t codes = *reinterpret_cast<const uint32_t *>(wr + v * 4);
+                const uint32_t nlo = int4_lo_nibbles(codes), nhi = int4_hi_nibbles(codes);
                 const float *sb = sb_s + 2 * ((gr0 + j) * ng + ((v * 8) >> p.down.gshift));
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    a = ffma2(nib2_f32x2(codes, e), xp[e], a);
+                    a = ffma2(int4_pair_f32x2(nlo, nhi, e), xp[e], a);
                 a = f32x2(fmaf(sb[0], f32x2_sum(a), sb[1] * xsum), 0.f);
             }
             acc[j] = f32x2_sum(a);
@@ -1058,11 +1022,12 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
                 const uint64_t ap[4] = {f32x2(xa.x, xa.y), f32x2(xa.z, xa.w), f32x2(xb.x, xb.y), f32x2(xb.z, xb.w)};
                 const float asum = ((xa.x + xa.y) + (xa.z + xa.w)) + ((xb.x + xb.y) + (xb.z + xb.w));
                 const uint32_t codes = wr[v];
+                const uint32_t nlo = int4_lo_nibbles(codes), nhi = int4_hi_nibbles(codes);
                 const float *sb = sbr + 2 * ((v * 8) >> p.up.gshift);
                 uint64_t dq = 0;
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    dq = ffma2(nib2_f32x2(codes, e), ap[e], dq);
+                    dq = ffma2(int4_pair_f32x2(nlo, nhi, e), ap[e], dq);
                 a += fmaf(sb[0], f32x2_sum(dq), sb[1] * asum);
             }
             // Lanes with equal lane & 3 hold parts of the same row.
@@ -1086,11 +1051,12 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
                         const int srow = c * HB + hl;
                         const uint32_t codes =
                             *reinterpret_cast<const uint32_t *>(w_s + (size_t)srow * row_bytes + v * 4);
+                        const uint32_t nlo = int4_lo_nibbles(codes), nhi = int4_hi_nibbles(codes);
                         const float *sb = sb_s + 2 * (srow * ng + gi);
                         uint64_t dq = 0;
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            dq = ffma2(nib2_f32x2(codes, e), ap[e], dq);
+                            dq = ffma2(int4_pair_f32x2(nlo, nhi, e), ap[e], dq);
                         acc[c] += fmaf(sb[0], f32x2_sum(dq), sb[1] * asum);
                     }
                 }

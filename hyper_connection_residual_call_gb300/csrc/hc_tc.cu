@@ -94,15 +94,14 @@ struct TcSmem {
 __device__ __forceinline__ void int4x8_hilo(uint32_t codes, uint16_t sb, uint16_t bb, uint4 &hi, uint4 &lo)
 {
     const float sc = __half2float(__ushort_as_half(sb)), bi = __half2float(__ushort_as_half(bb));
+    const uint64_t sc2 = f32x2(sc, sc), bi2 = f32x2(bi, bi);
+    const uint32_t nlo = int4_lo_nibbles(codes), nhi = int4_hi_nibbles(codes);
     uint32_t h[4], l[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        // Nibbles 2e and 2e+1 as exact floats without a conversion: q OR-ed into
-        // the mantissa of 2^23 is the float 2^23 + q.
-        const float qa = __uint_as_float(((codes >> (8 * e)) & 0xFu) | 0x4B000000u) - 8388608.0f;
-        const float qb = __uint_as_float(((codes >> (8 * e + 4)) & 0xFu) | 0x4B000000u) - 8388608.0f;
-        const float wa = fmaf(qa, sc, bi);
-        const float wb = fmaf(qb, sc, bi);
+        // Elements 2e and 2e+1, exact, then w = q * s + b for both in one packed FMA.
+        float wa, wb;
+        f32x2_unpack(ffma2(int4_pair_f32x2(nlo, nhi, e), sc2, bi2), wa, wb);
         const uint32_t hh = pack_bf16x2(wa, wb);
         h[e] = hh;
         l[e] = pack_bf16x2(wa - bf16_lo(hh), wb - bf16_hi(hh));

@@ -150,4 +150,55 @@ __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// INT4 code word (element 2i in the low nibble of byte i) split by nibble:
+// byte i of the low word holds element 2i, byte i of the high word 2i + 1.
+__device__ __forceinline__ uint32_t int4_lo_nibbles(uint32_t codes) { return codes & 0x0F0F0F0Fu; }
+__device__ __forceinline__ uint32_t int4_hi_nibbles(uint32_t codes) { return (codes >> 4) & 0x0F0F0F0Fu; }
+
+// Byte i of a nibble word placed in the mantissa of 2^23 (one byte permute):
+// the bits of the float 2^23 + q, exact for q < 2^23.
+__device__ __forceinline__ uint32_t nibble_2p23_bits(uint32_t nibbles, int i)
+{
+    return __byte_perm(nibbles, 0x4B000000u, 0x7440u | (uint32_t)i);
+}
+
+// ---- packed fp32x2 arithmetic (two IEEE fp32 operations in one instruction) ----
+
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// d = a * b + c, lane-wise, round to nearest.
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// d = a + b, lane-wise, round to nearest.
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Elements 2i and 2i + 1 of an INT4 code word, given by its two nibble words,
+// as an exact fp32 pair without an int-to-float conversion: (2^23 + q) - 2^23.
+__device__ __forceinline__ uint64_t int4_pair_f32x2(uint32_t lo_nibbles, uint32_t hi_nibbles, int i)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(nibble_2p23_bits(lo_nibbles, i)), "r"(nibble_2p23_bits(hi_nibbles, i)));
+    return fadd2(r, 0xCB000000CB000000ull);  // + (-2^23, -2^23)
+}
+
 }  // namespace tshc
