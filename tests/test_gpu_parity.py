@@ -105,7 +105,9 @@ def test_shapes_and_ragged_tokens(orc, M, H, C, L):
 
 
 @pytest.mark.parametrize("M,H,C,L,group", [(3, 128, 2, 64, 32), (2, 256, 4, 64, 64), (5, 256, 1, 128, 128),
-                                           (4, 128, 2, 32, 32), (7, 96, 3, 32, 32)])
+                                           (4, 128, 2, 32, 32), (7, 96, 3, 32, 32),
+                                           # one token: four streams (compiled-in C) and two, groups 128 and 32
+                                           (1, 256, 4, 128, 128), (1, 128, 2, 64, 32)])
 def test_int4_shapes(orc, M, H, C, L, group):
     call_and_inject(orc, inputs.Shape(M=M, H=H, C=C, L=L), seed=200 + M, kind="int4", group=group)
 
@@ -116,7 +118,7 @@ def test_int4_tiny_up_group_32(orc):
 
 
 @pytest.mark.parametrize("M,H,C,L,group,up_group", [(16, 2560, 4, 320, 64, None), (40, 512, 2, 64, 32, None),
-                                                      (128, 1024, 8, 128, 64, 32)])
+                                                      (128, 1024, 8, 128, 64, 32), (8, 512, 4, 128, 128, None)])
 def test_int4_tensor_core_path(orc, M, H, C, L, group, up_group):
     # INT4-affine weights from 2 tokens run on tcgen05: each weight tile is dequantised
     # to bf16 hi + lo and multiplied against the activation's hi + lo (three MMAs)
