@@ -118,7 +118,8 @@ def test_int4_tiny_up_group_32(orc):
 
 
 @pytest.mark.parametrize("M,H,C,L,group,up_group", [(16, 2560, 4, 320, 64, None), (40, 512, 2, 64, 32, None),
-                                                      (128, 1024, 8, 128, 64, 32), (8, 512, 4, 128, 128, None)])
+                                                      (128, 1024, 8, 128, 64, 32), (8, 512, 4, 128, 128, None),
+                                                      (130, 512, 4, 128, 64, None)])
 def test_int4_tensor_core_path(orc, M, H, C, L, group, up_group):
     # INT4-affine weights from 2 tokens run on tcgen05: each weight tile is dequantised
     # to bf16 hi + lo and multiplied against the activation's hi + lo (three MMAs)
