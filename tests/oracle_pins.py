@@ -110,6 +110,23 @@ def pin_int4_decode(orc):
     assert np.array_equal(orc.weight_values(w), dense), "INT4-affine decode"
 
 
+def pin_int4_decode_every_group(orc):
+    # Each supported group size (32, 64, 128 inputs per scale and bias), with
+    # scales and biases exact in fp16, so the dense weight is exact in fp64.
+    rows, cols = 3, 256
+    q = (np.arange(rows)[:, None] * 5 + np.arange(cols)[None, :] * 11) % 16
+    packed = (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
+    for group in (32, 64, 128):
+        ng = cols // group
+        r, j = np.arange(rows)[:, None], np.arange(ng)[None, :]
+        s = ((r * 5 + j * 3) % 8 + 1) * 0.125
+        b = ((r * 3 + j * 7) % 9 - 4) * 0.25
+        w = Weight("int4", rows, cols, torch.from_numpy(packed),
+                   torch.from_numpy(s.astype(np.float16)), torch.from_numpy(b.astype(np.float16)), group)
+        dense = q * np.repeat(s, group, axis=1) + np.repeat(b, group, axis=1)
+        assert np.array_equal(orc.weight_values(w), dense), f"INT4-affine decode, group {group}"
+
+
 def pin_gemv(orc):
     rng = np.random.default_rng(3)
     wt = _randn(rng, 7, 33)

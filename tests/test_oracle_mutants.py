@@ -45,6 +45,10 @@ MUTANTS = {
                              "(i % 2 == 0) ? (byte >> 4) : (byte & 0x0F)"),
     "int4 group index": ("int64_t gi = o * (w->cols / w->group) + i / w->group;",
                          "int64_t gi = o * (w->cols / w->group) + i % (w->cols / w->group);"),
+    "int4 group fixed at 64": ("int64_t gi = o * (w->cols / w->group) + i / w->group;",
+                               "int64_t gi = o * (w->cols / w->group) + i / 64;"),
+    "int4 groups per row fixed at 64": ("int64_t gi = o * (w->cols / w->group) + i / w->group;",
+                                        "int64_t gi = o * (w->cols / 64) + i / w->group;"),
     "int4 bias dropped": ("(double)q * orc_f16_value(w->scale[gi]) + orc_f16_value(w->bias[gi]);",
                           "(double)q * orc_f16_value(w->scale[gi]);"),
     "fp16 exponent bias": ("v = ldexp((double)(1024 + mantissa), exponent - 25);",
