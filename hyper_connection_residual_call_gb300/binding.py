@@ -6,9 +6,10 @@ runs in the library's CUDA kernels:
 * ``ts_hc_*``: the C entry points under their own names, taking raw device
   pointers (ints), a ``TsWeight`` struct and a CUDA stream handle; they return
   the ``ts_status`` code.
-* ``hc_call`` / ``hc_mixer`` / ``hc_inject_add``: the same calls for torch
-  CUDA tensors. They allocate outputs/workspace with torch when not given,
-  pass the current torch stream, and raise ``HCError`` on any error status.
+* ``hc_call`` / ``hc_inject_call`` / ``hc_mixer`` / ``hc_inject_add`` /
+  ``hc_replicate_entry`` / ``hc_stack``: the same calls for torch CUDA
+  tensors. They allocate outputs/workspace with torch when not given, pass
+  the current torch stream, and raise ``HCError`` on any error status.
 
 There is no fallback: if the library is not built or cannot be loaded, every
 call raises.
