@@ -69,16 +69,42 @@ def _peaks():
 
 
 # Sources of the kernels the headline times (the one-token path): the recorded
-# DRAM traffic is reported only while these are unchanged.
+# DRAM traffic is reported only while their code is unchanged.
 HEADLINE_KERNEL_SOURCES = ("hc_gemv.cu", "hc_kernels.h", "ptx.cuh")
+
+
+def _code_only(text: str) -> str:
+    """C/C++ source without its comments and blank lines (string and character
+    literals kept), so that editing a comment does not count as a code change."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        ch = text[i]
+        if ch in "\"'":
+            j = i + 1
+            while j < n and text[j] != ch and text[j] != "\n":
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(ch)
+            i += 1
+    lines = (l.rstrip() for l in "".join(out).split("\n"))
+    return "\n".join(l for l in lines if l)
 
 
 def _kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "hyper_connection_residual_call_gb300", "csrc")
     for name in HEADLINE_KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -607,12 +607,15 @@ __global__ void __launch_bounds__(768, 1) hc_up_kernel(const UpParams p)
 // hc_up1_kernel    Every CTA forms inv_rms, z = sum_s inv_rms[stream(s)] * P_s
 //                  and silu(z / C) for all rows from the partials in a fixed
 //                  order (CTA 0 also writes act, inv_rms and the gates out).
-//                  Warp w owns h = h0 + w: lane l owns act inputs [8v, 8v + 8)
-//                  for v = l, l + 32, ... and dots them with the C up rows
-//                  {c*H + h}; after the transposed butterfly, lane 4c holds
-//                  row c, applies the sigmoid and its term of the mean mix,
-//                  and lane 0 writes mixed[h]. With a fused inject-add, lane 4c
-//                  also writes the updated residual element back.
+//                  Warp w owns h = h0 + w and dots act with the C up rows
+//                  {c*H + h}. bf16: lane l owns the act pairs l + 32i of every
+//                  row. INT4: lane l owns the 8-input code words l + 32i of
+//                  every row, or, with C = 4 compiled in, the words l/4 + 8i
+//                  of row l & 3. Lane 4c then holds row c (after the transposed
+//                  butterfly, or one shuffle), applies the sigmoid and its term
+//                  of the mean mix, and lane 0 writes mixed[h]. With a fused
+//                  inject-add, lane 4c also writes the updated residual
+//                  element back.
 
 // Sums v[0..7] over the 32 lanes of a warp. On return lane l holds the total
 // of v[(l >> 2) & 7]. Every lane must take part; the order is fixed.
