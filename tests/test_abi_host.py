@@ -88,6 +88,14 @@ def _call(**kw):
     (dict(up=_w(typ=B.TS_W_INT4_AFFINE, group=64, scales=None, biases=FAKE)), B.TS_ERR_INVALID_ARG, "scales"),
     (dict(inject=_w(typ=B.TS_W_INT4_AFFINE, group=64, scales=FAKE, biases=FAKE)), B.TS_ERR_UNSUPPORTED,
      "same storage format"),
+    (dict(down=_w(typ=B.TS_W_INT4_AFFINE, group=16, scales=FAKE, biases=FAKE)), B.TS_ERR_UNSUPPORTED, "group = 16"),
+    (dict(up=_w(typ=B.TS_W_INT4_AFFINE, group=256, scales=FAKE, biases=FAKE)), B.TS_ERR_UNSUPPORTED, "group = 256"),
+    (dict(up=_w(typ=B.TS_W_INT4_AFFINE, group=128, scales=FAKE, biases=FAKE)), B.TS_ERR_UNSUPPORTED,
+     "320 inputs are not a multiple of the group 128"),
+    (dict(down=_w(typ=B.TS_W_INT4_AFFINE, group=64, scales=FAKE, biases=FAKE),
+          inject=_w(typ=B.TS_W_INT4_AFFINE, group=32, scales=FAKE, biases=FAKE)), B.TS_ERR_UNSUPPORTED,
+     "same storage format and group"),
+    (dict(down=_w(typ=B.TS_W_INT4_AFFINE, group=64, scales=FAKE, biases=None)), B.TS_ERR_INVALID_ARG, "biases"),
     (dict(eps=-1.0), B.TS_ERR_INVALID_ARG, "eps"),
     (dict(ws_bytes=16), B.TS_ERR_WORKSPACE, "workspace of 16 bytes"),
     (dict(ws=None), B.TS_ERR_WORKSPACE, "workspace"),
