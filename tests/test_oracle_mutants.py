@@ -33,6 +33,12 @@ MUTANTS = {
     "gate without /C": ("gate[m * gate_stride + c] = 2.0 * sigmoid(q[c] / (double)C);",
                         "gate[m * gate_stride + c] = 2.0 * sigmoid(q[c]);"),
     "gate stride ignored": ("gate[m * gate_stride + c] = 2.0", "gate[m * C + c] = 2.0"),
+    "silu with the sign flipped": ("static double silu(double x) { return x * sigmoid(x); }",
+                                   "static double silu(double x) { return x * sigmoid(-x); }"),
+    "down projection of raw, not normed": ("orc_gemv(down, normed, z, nthreads);", "orc_gemv(down, x, z, nthreads);"),
+    "inject projection of raw, not normed": ("orc_gemv(inject, normed, q, nthreads);",
+                                             "orc_gemv(inject, x, q, nthreads);"),
+    "up projection skips silu": ("orc_gemv(up, act, y, nthreads);", "orc_gemv(up, z, y, nthreads);"),
     "sigmoid sign flipped": ("return 1.0 / (1.0 + exp(-x));", "return 1.0 / (1.0 + exp(x));"),
     "inject-add layout transposed": ("result[m * W + c * H + h] =", "result[m * W + h * C + c] ="),
     "inject-add uses gate stride C": ("out[m * H + h] * gate[m * gate_stride + c];",
