@@ -28,7 +28,7 @@ TS_W_BF16, TS_W_INT4_AFFINE = 0, 1
 RMS_EPS = 1e-6  # families/qwen4/mod.rs, RMS_EPS
 
 EXPORTS = ("ts_hc_workspace_bytes", "ts_hc_workspace_layout", "ts_hc_call", "ts_hc_inject_add",
-           "ts_hc_mixer", "ts_hc_inject_call", "ts_hc_replicate_entry", "ts_hc_last_error",
+           "ts_hc_mixer", "ts_hc_call_debug", "ts_hc_inject_call", "ts_hc_replicate_entry", "ts_hc_last_error",
            "ts_hc_device_status", "ts_hc_call_noalloc", "ts_hc_stack_workspace_bytes", "ts_hc_stack",
            "ts_hc_selftest_timeout")
 TS_HC_STATIC_SCRATCH_BYTES = 64 * 1024 * 1024  # include/ts_hc.h
@@ -88,6 +88,8 @@ def library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.ts_hc_call.restype = i
         lib.ts_hc_mixer.argtypes = [vp, vp, wp, wp, vp, i, i, i, i, f, vp, sz, vp]
         lib.ts_hc_mixer.restype = i
+        lib.ts_hc_call_debug.argtypes = [vp, vp, wp, wp, wp, vp, vp, l, i, i, i, i, f, vp, sz, vp, vp]
+        lib.ts_hc_call_debug.restype = i
         lib.ts_hc_inject_add.argtypes = [vp, vp, vp, l, i, i, i, vp]
         lib.ts_hc_inject_add.restype = i
         lib.ts_hc_inject_call.argtypes = [vp, vp, vp, l, vp, wp, wp, wp, vp, vp, l, i, i, i, i, f, vp, sz, vp]
@@ -135,6 +137,14 @@ def ts_hc_mixer(raw, hc_norm_w, down, up, mixed, M, H, C, lowrank, eps, workspac
                 stream) -> int:
     return library().ts_hc_mixer(raw, hc_norm_w, _wref(down), _wref(up), mixed, M, H, C, lowrank, eps,
                                  workspace, workspace_bytes, stream)
+
+
+def ts_hc_call_debug(raw, hc_norm_w, down, up, inject, mixed, inject_w, inject_stride, M, H, C, lowrank,
+                     eps, workspace, workspace_bytes, w_out, stream) -> int:
+    """ts_hc_call (ts_hc_mixer when ``inject`` is None) that also writes w = sigmoid(up(act))."""
+    return library().ts_hc_call_debug(raw, hc_norm_w, _wref(down), _wref(up), _wref(inject), mixed, inject_w,
+                                      inject_stride, M, H, C, lowrank, eps, workspace, workspace_bytes, w_out,
+                                      stream)
 
 
 def ts_hc_inject_add(raw, out, inject_w, inject_stride, M, H, C, stream) -> int:
@@ -291,6 +301,40 @@ def hc_mixer(raw, weights, *, H: int, C: int, mixed=None, eps: float = RMS_EPS, 
                      ws.numel() * ws.element_size(), _stream_handle(stream))
     _check(st)
     return mixed
+
+
+def hc_call_debug(raw, weights, *, H: int, C: int, mixed=None, inject_w=None, inject_stride: Optional[int] = None,
+                  eps: float = RMS_EPS, ws=None, w_out=None, stream=None):
+    """``hc_call`` (or the mixer when ``weights.inject`` is None) through ``ts_hc_call_debug``.
+
+    Returns (mixed, inject_w or None, w) with w = sigmoid(up(act)) fp32 [M, C*H].
+    """
+    torch = _torch()
+    M = raw.shape[0]
+    L = weights.down.rows
+    _need(raw, "raw", torch.bfloat16, (M, C * H))
+    _need(weights.g, "hc_norm_w", torch.bfloat16, (C * H,))
+    if mixed is None:
+        mixed = torch.empty((M, H), dtype=torch.bfloat16, device=raw.device)
+    _need(mixed, "mixed", torch.bfloat16, (M, H))
+    has_inject = weights.inject is not None
+    if has_inject and inject_w is None:
+        inject_stride = C
+        inject_w = torch.empty((max(M, 1), C), dtype=torch.float32, device=raw.device)
+    if has_inject and inject_stride is None:
+        raise HCError(TS_ERR_INVALID_ARG, "inject_stride is required with a caller-given inject_w")
+    if w_out is None:
+        w_out = torch.empty((max(M, 1), C * H), dtype=torch.float32, device=raw.device)
+    _need(w_out, "w_out", torch.float32)
+    if ws is None:
+        ws = workspace(M, H, C, L, raw.device)
+    st = ts_hc_call_debug(raw.data_ptr(), weights.g.data_ptr(), weight_struct(weights.down),
+                          weight_struct(weights.up), weight_struct(weights.inject) if has_inject else None,
+                          mixed.data_ptr(), inject_w.data_ptr() if has_inject else None, inject_stride or 0, M, H,
+                          C, L, eps, ws.data_ptr(), ws.numel() * ws.element_size(), w_out.data_ptr(),
+                          _stream_handle(stream))
+    _check(st)
+    return mixed, (inject_w if has_inject else None), w_out[:M]
 
 
 def hc_inject_add(raw, out, inject_w, *, H: int, C: int, inject_stride: Optional[int] = None, stream=None):

@@ -567,7 +567,12 @@ __global__ void __launch_bounds__(768, 1) hc_up_kernel(const UpParams p)
                 v += __shfl_xor_sync(0xffffffffu, v, 4);
                 v += __shfl_xor_sync(0xffffffffu, v, 2);
                 v += __shfl_xor_sync(0xffffffffu, v, 1);
-                if (tl == 0 && row_ok) wv_s[(t * p.C + c) * HB + hl] = sigmoidf_(v);
+                if (tl == 0 && row_ok) {
+                    const float w = sigmoidf_(v);
+                    wv_s[(t * p.C + c) * HB + hl] = w;
+                    if (p.w_out && t < mt)  // debug output of w
+                        p.w_out[(size_t)(t0 + t) * p.W + (size_t)c * p.H + h0 + hl] = w;
+                }
             }
         }
         __syncthreads();
@@ -1072,7 +1077,10 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
             d = __shfl_sync(0xffffffffu, acc[0], (lane >> 2) & 3);
         else
             d = warp_transpose_sum8(acc, lane);
-        float term = holder ? sigmoid_fast(d) * nvh : 0.f;
+        const float wv = sigmoid_fast(d);
+        if (p.w_out && holder)  // debug output of w
+            p.w_out[hc * p.H + h] = wv;
+        float term = holder ? wv * nvh : 0.f;
         term += __shfl_xor_sync(0xffffffffu, term, 4);
         term += __shfl_xor_sync(0xffffffffu, term, 8);
         term += __shfl_xor_sync(0xffffffffu, term, 16);

@@ -85,6 +85,8 @@ struct UpParams {
     float *act_out;           // [L]
     float *inv_out;           // [C]
     float *gate;              // gates (R > L), or nullptr
+    // Optional debug output: w = sigmoid(up(act)) fp32 [M][W], or nullptr.
+    float *w_out;
 };
 
 struct InjectParams {

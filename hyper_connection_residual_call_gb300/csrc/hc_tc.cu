@@ -15,13 +15,15 @@
 //                      MMAs per K step (hi, lo); CTA (chunk, row tile, token
 //                      tile) writes its fp32 partial tile to part[chunk][token][row].
 //  hc_tc_reduce_kernel z = sum over chunks (fixed order); act = silu(z / C)
-//                      (fp32, and bf16 for the up GEMM), gates = 2 sigmoid(z / C).
-//  hc_tc_up_kernel     D[C*HBt rows][N] = Wu[rows {c*H + h}][L] * bf16(act)^T,
-//                      epilogue: w = sigmoid(D), mixed[h] = mean_c w * normed,
-//                      with the normed tile (hi + lo) staged by TMA. w only
-//                      enters the bf16 output mixed, through a sigmoid and a
-//                      mean: a bf16 act costs under 2% of mixed's error bar,
-//                      against ~18% for mixed's own bf16 rounding.
+//                      (fp32, and bf16 hi + lo for the up GEMM), gates =
+//                      2 sigmoid(z / C).
+//  hc_tc_up_kernel     D[C*HBt rows][N] = Wu[rows {c*H + h}][L] * (act_hi + act_lo)^T,
+//                      two MMAs per K step, epilogue: w = sigmoid(D),
+//                      mixed[h] = mean_c w * normed, with the normed tile
+//                      (hi + lo) staged by TMA. act keeps ~16 significant bits
+//                      so that w meets the fp32 bar where the sigmoid leaves
+//                      its linear region (a bf16 act moves a small w by up to
+//                      2^-9 of the up pre-activation, far past 1e-3 of w).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -54,17 +56,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 // Sigmoid from the fast exponential and division intrinsics (relative error
 // ~1e-6, far inside the 1e-3 bar), for the per-element epilogues.
 __device__ __forceinline__ float sigm_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
-
-// sigmoid(x) = (1 + tanh(x / 2)) / 2 with the hardware tanh approximation
-// (one special-function op instead of two; absolute error below 3e-4 -- used
-// only where the result is mixed into a bf16 output, whose own rounding is
-// ~2e-3 relative).
-__device__ __forceinline__ float sigm_tanh(float x)
-{
-    float t;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
-    return fmaf(0.5f, t, 0.5f);
-}
 
 __device__ __forceinline__ void record_timeout(unsigned *status)
 {
@@ -506,8 +497,10 @@ __global__ void __launch_bounds__(1024) hc_tc_reduce_kernel(const TcReduceParams
     const float zc = z * p.inv_C;
     if (r < p.L) {
         const float a = zc * sigm_fast(zc);
+        const __nv_bfloat16 ah = __float2bfloat16_rn(a);
         p.act[(size_t)m * p.L + r] = a;
-        p.act_hi[(size_t)m * p.L + r] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+        p.act_hi[(size_t)m * p.L + r] = __bfloat16_as_ushort(ah);
+        p.act_lo[(size_t)m * p.L + r] = __bfloat16_as_ushort(__float2bfloat16_rn(a - __bfloat162float(ah)));
     } else {
         p.gate[(size_t)m * p.gate_stride + (r - p.L)] = 2.0f * sigm_fast(zc);
     }
@@ -516,7 +509,8 @@ __global__ void __launch_bounds__(1024) hc_tc_reduce_kernel(const TcReduceParams
 // ---------------------------------------------------------------- up
 
 // Up kernel shared memory: a ring of stages [A_hi | A_lo (INT4 weights only) |
-// B = act], then the normed hi and lo tiles [C][NT][HBt] bf16, then the barriers.
+// B_hi | B_lo (act)], then the normed hi and lo tiles [C][NT][HBt] bf16, then
+// the barriers.
 __host__ __device__ inline uint32_t up_tc_tile_bytes(int NT, int C, int HBt)
 {
     return ((C * NT * HBt * 2 + 1023) / 1024) * 1024;
@@ -527,7 +521,7 @@ __host__ __device__ inline TcSmem up_tc_layout(int NT, int ns, int C, int HBt, i
     TcSmem s;
     s.a_bytes = kTileRows * 128;
     s.b_bytes = NT * 128;
-    s.stage_bytes = s.a_bytes * (1 + wt) + s.b_bytes;
+    s.stage_bytes = s.a_bytes * (1 + wt) + 2 * s.b_bytes;
     s.ring = 0;
     s.extra = s.ring + ns * s.stage_bytes;
     s.bars = s.extra + 2 * up_tc_tile_bytes(NT, C, HBt);
@@ -538,14 +532,14 @@ __host__ __device__ inline TcSmem up_tc_layout(int NT, int ns, int C, int HBt, i
 template <int WT>
 __global__ void __launch_bounds__(kUpThreads, 1)
 hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
-                const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_nhi,
-                const __grid_constant__ CUtensorMap map_nlo)
+                const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_alo,
+                const __grid_constant__ CUtensorMap map_nhi, const __grid_constant__ CUtensorMap map_nlo)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int NT = p.NT, NS = p.n_stages, C = p.C, HBt = p.HBt;
     const TcSmem lay = up_tc_layout(NT, NS, C, HBt, WT);
-    const uint32_t b_off = lay.a_bytes * (1 + WT);  // B (act) within a stage
+    const uint32_t b_off = lay.a_bytes * (1 + WT);  // B_hi (act), then B_lo, within a stage
     const uint16_t *nhi_s = reinterpret_cast<const uint16_t *>(smem + lay.extra);  // [C][NT][HBt]
     const uint16_t *nlo_s = nhi_s + up_tc_tile_bytes(NT, C, HBt) / 2;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
@@ -590,7 +584,7 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
             tma_prefetch_map(&map_u);
         for (int kb = 0; kb < npre; ++kb) {
             uint8_t *a = smem + lay.ring + kb * lay.stage_bytes;
-            mbar_arrive_expect_tx(&full[kb], C * HBt * 128 + NT * 128);
+            mbar_arrive_expect_tx(&full[kb], C * HBt * 128 + 2 * NT * 128);
             for (int cc = 0; cc < C; ++cc)
                 tma_load_2d(a + cc * HBt * 128, &map_u, kb * kKBlock, cc * p.H + h0, &full[kb]);
         }
@@ -600,14 +594,15 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
             uint8_t *a = smem + lay.ring + s * lay.stage_bytes;
             if (WT == 0 && kb >= npre) {
                 if (!mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
-                mbar_arrive_expect_tx(&full[s], C * HBt * 128 + NT * 128);
+                mbar_arrive_expect_tx(&full[s], C * HBt * 128 + 2 * NT * 128);
                 for (int cc = 0; cc < C; ++cc)
                     tma_load_2d(a + cc * HBt * 128, &map_u, kb * kKBlock, cc * p.H + h0, &full[s]);
             } else if (WT == 1) {
                 if (u > 0 && !mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
-                mbar_arrive_expect_tx(&full[s], NT * 128);
+                mbar_arrive_expect_tx(&full[s], 2 * NT * 128);
             }
             tma_load_2d(a + b_off, &map_act, kb * kKBlock, tile * NT, &full[s]);
+            tma_load_2d(a + b_off + lay.b_bytes, &map_alo, kb * kKBlock, tile * NT, &full[s]);
         }
         mbar_arrive_expect_tx(nbar, 2 * C * NT * HBt * 2);
         for (int cc = 0; cc < C; ++cc) {
@@ -694,11 +689,12 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
             tc_fence_after();
             const uint32_t a = smem_addr(smem + lay.ring + s * lay.stage_bytes);
             const uint32_t al = a + lay.a_bytes;  // A_lo (INT4 weights)
-            const uint32_t b = a + b_off;
+            const uint32_t b = a + b_off, bl = b + lay.b_bytes;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(b + 32 * k), idesc, (kb | k) != 0);
-                if (WT == 1)  // the weight's lo part
+                umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(bl + 32 * k), idesc, 1);
+                if (WT == 1)  // the weight's lo part against act's hi part
                     umma_bf16(tmem, umma_desc_sw128(al + 32 * k), umma_desc_sw128(b + 32 * k), idesc, 1);
             }
             umma_commit(&empty[s]);
@@ -733,8 +729,13 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
                 x[j] = __bfloat162float(__ushort_as_bfloat16(nhi_s[o])) + __bfloat162float(__ushort_as_bfloat16(nlo_s[o]));
             }
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                mix_s[(cc * NT + c0 + j) * HBt + hl] = sigm_tanh(__uint_as_float(vr[j])) * x[j];
+            for (int j = 0; j < 16; ++j) {
+                const float w = sigm_fast(__uint_as_float(vr[j]));
+                mix_s[(cc * NT + c0 + j) * HBt + hl] = w * x[j];
+                const int m = tile * NT + c0 + j;
+                if (p.w_out && m < p.M)  // debug output of w (uniform branch)
+                    p.w_out[(size_t)m * p.W + (size_t)cc * p.H + h0 + hl] = w;
+            }
         };
         const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16);
         uint32_t va[16], vb[16];
@@ -878,7 +879,7 @@ size_t tc_up_smem(int NT, int ns, int C, int HBt, int wt) { return up_tc_layout(
 
 cudaError_t launch_tc_call(const TcCall &t, cudaStream_t stream)
 {
-    CUtensorMap map_d, map_i, map_u, map_xhi, map_xlo, map_act, map_nhi, map_nlo;
+    CUtensorMap map_d, map_i, map_u, map_xhi, map_xlo, map_act, map_alo, map_nhi, map_nlo;
     const TcPrepParams &pp = t.prep;
     const TcDownParams &d = t.down;
     const TcUpParams &u = t.up;
@@ -893,6 +894,7 @@ cudaError_t launch_tc_call(const TcCall &t, cudaStream_t stream)
         !make_map(&map_xhi, pp.x_hi, M, W, kKBlock, d.NT, true) ||
         !make_map(&map_xlo, pp.x_lo, M, W, kKBlock, d.NT, true) ||
         !make_map(&map_act, t.red.act_hi, M, u.L, kKBlock, u.NT, true) ||
+        !make_map(&map_alo, t.red.act_lo, M, u.L, kKBlock, u.NT, true) ||
         !make_map(&map_nhi, pp.x_hi, M, W, u.HBt, u.NT, false) ||
         !make_map(&map_nlo, pp.x_lo, M, W, u.HBt, u.NT, false))
         return cudaErrorInvalidValue;
@@ -923,7 +925,8 @@ cudaError_t launch_tc_call(const TcCall &t, cudaStream_t stream)
     if (e != cudaSuccess)
         return e;
     return launch_tc(ku, dim3((u.H + u.HBt - 1) / u.HBt, ntiles), dim3(kUpThreads),
-                     tc_up_smem(u.NT, u.n_stages, u.C, u.HBt, u.wt), stream, 0, u, map_u, map_act, map_nhi, map_nlo);
+                     tc_up_smem(u.NT, u.n_stages, u.C, u.HBt, u.wt), stream, 0, u, map_u, map_act, map_alo, map_nhi,
+                     map_nlo);
 }
 
 }  // namespace tshc

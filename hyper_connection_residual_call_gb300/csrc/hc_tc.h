@@ -78,7 +78,8 @@ struct TcDownParams {
 struct TcReduceParams {
     const float *part;
     float *act;               // [M][L] fp32
-    uint16_t *act_hi;         // [M][L] bf16 (round to nearest): the up GEMM's B operand
+    uint16_t *act_hi;         // [M][L] bf16(act), round to nearest: the up GEMM's B operand ...
+    uint16_t *act_lo;         // [M][L] bf16(act - act_hi): ... and its low part (act = hi + lo to ~16 bits)
     float *gate;              // token m's gates at gate + m * gate_stride
     long gate_stride;
     int M, L, R, Mp, nchunk;
@@ -98,6 +99,7 @@ struct TcUpParams {
     unsigned *status;
     int wt;                   // 1: INT4-affine up weights, dequantised by producer warps
     WeightView uw;
+    float *w_out;             // optional fp32 [M][W]: w = sigmoid(up(act)) (debug output), or nullptr
 };
 
 struct TcCall {

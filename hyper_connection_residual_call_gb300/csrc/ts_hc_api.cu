@@ -203,7 +203,7 @@ bool tc_path_ok(int M, int H, int C, int L)
 }
 
 struct WsLayout {
-    size_t inv_rms, act, x_hi, x_lo, part, act_hi, part1, ssq1, total;
+    size_t inv_rms, act, x_hi, x_lo, part, act_hi, act_lo, part1, ssq1, total;
 };
 
 // Per-chunk partial dots and sums of squares of the one-token path: at most
@@ -221,14 +221,15 @@ WsLayout ws_layout(int M, int H, int C, int L)
         w.ssq1 = w.part1 + tshc::kPartCopies * align256(sizeof(float) * kPart1Chunks * ((size_t)L + C));
         w.total = w.ssq1 + tshc::kPartCopies * sizeof(float) * tshc::kSsqStride;
     }
-    if (tc_path_ok(M, H, C, L)) {  // normed hi/lo, per-chunk partials, bf16 act
+    if (tc_path_ok(M, H, C, L)) {  // normed hi/lo, per-chunk partials, act hi/lo
         const size_t R = (size_t)L + C, W = (size_t)C * H;
         const tshc::TcPlan pl = tshc::tc_plan(M, L, C, (int)W);
         w.x_hi = w.total;
         w.x_lo = w.x_hi + align256(2 * (size_t)M * W);
         w.part = w.x_lo + align256(2 * (size_t)M * W);
         w.act_hi = w.part + align256(sizeof(float) * (size_t)pl.nchunk * R * pl.Mp);
-        w.total = w.act_hi + align256(2 * (size_t)M * L);
+        w.act_lo = w.act_hi + align256(2 * (size_t)M * L);
+        w.total = w.act_lo + align256(2 * (size_t)M * L);
     }
     return w;
 }
@@ -257,7 +258,8 @@ struct FusedInject {
 ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *down,
                        const ts_weight *up, const ts_weight *inject, void *mixed, float *inject_w,
                        long inject_stride, int M, int H, int C, int L, float eps, void *workspace,
-                       size_t workspace_bytes, cudaStream_t stream, const FusedInject *fi = nullptr)
+                       size_t workspace_bytes, cudaStream_t stream, const FusedInject *fi = nullptr,
+                       float *w_out = nullptr)
 {
     ts_status st = check_shape(M, H, C, L);
     if (st != TS_OK)
@@ -341,6 +343,7 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         tshc::TcReduceParams &tr = t.red;
         tr.part = td.part; tr.act = act;
         tr.act_hi = reinterpret_cast<uint16_t *>(wsb + wl.act_hi);
+        tr.act_lo = reinterpret_cast<uint16_t *>(wsb + wl.act_lo);
         tr.gate = inject ? inject_w : nullptr;
         tr.gate_stride = inject ? inject_stride : 0;
         tr.M = M; tr.L = L; tr.R = R; tr.Mp = pl.Mp; tr.nchunk = pl.nchunk;
@@ -372,6 +375,7 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
             --tu.n_stages;
         tu.inv_C = tr.inv_C;
         tu.status = dev.status;
+        tu.w_out = w_out;
         t.wd = down->data;
         t.wi = inject ? inject->data : nullptr;
         t.wu = up->data;
@@ -422,6 +426,7 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
     u.HB = (H + dev.sm_count - 1) / dev.sm_count;
     u.inv_C = d.inv_C;
     u.status = dev.status;
+    u.w_out = w_out;
     if (fi) {
         u.raw_out = fi->raw;
         u.inj_out = fi->out;
@@ -514,6 +519,22 @@ ts_status ts_hc_mixer(const void *raw, const void *hc_norm_w, const ts_weight *d
     g_last_error.clear();
     return hc_call_impl(raw, hc_norm_w, down, up, nullptr, mixed, nullptr, 0, M, H, C, lowrank, eps,
                         workspace, workspace_bytes, stream);
+}
+
+ts_status ts_hc_call_debug(const void *raw, const void *hc_norm_w, const ts_weight *down,
+                           const ts_weight *up, const ts_weight *inject, void *mixed, float *inject_w,
+                           long inject_stride, int M, int H, int C, int lowrank, float eps, void *workspace,
+                           size_t workspace_bytes, float *w_out, cudaStream_t stream)
+{
+    g_last_error.clear();
+    if (M > 0) {
+        const ts_status st = check_ptr(w_out, "w_out", 4);
+        if (st != TS_OK)
+            return st;
+    }
+    return hc_call_impl(raw, hc_norm_w, down, up, inject, mixed, inject ? inject_w : nullptr,
+                        inject ? inject_stride : 0, M, H, C, lowrank, eps, workspace, workspace_bytes, stream,
+                        nullptr, w_out);
 }
 
 }  // extern "C"

@@ -115,13 +115,16 @@ class HCWeights:
 
 def make_hc_weights(H: int, C: int, L: int, config_seed: int, set_index: int = 0,
                     kind: str = "bf16", with_inject: bool = True, group: int = 64,
-                    up_group: Optional[int] = None) -> HCWeights:
+                    up_group: Optional[int] = None, std: float = 0.02) -> HCWeights:
+    """One module's weights. ``std`` is the standard deviation of the down, up and
+    inject draws (0.02 in the workload; larger values put silu and sigmoid outside
+    their near-linear range)."""
     W = C * H
     s = lambda tid: tensor_seed(config_seed, set_index, tid)
     g = bf16_normal((W,), s(G_ID), std=0.1, mean=1.0)
-    down = bf16_normal((L, W), s(DOWN_ID), std=0.02)
-    up = bf16_normal((W, L), s(UP_ID), std=0.02)
-    inj = bf16_normal((C, W), s(INJECT_ID), std=0.02) if with_inject else None
+    down = bf16_normal((L, W), s(DOWN_ID), std=std)
+    up = bf16_normal((W, L), s(UP_ID), std=std)
+    inj = bf16_normal((C, W), s(INJECT_ID), std=std) if with_inject else None
     if kind == "bf16":
         wrap = lambda t: None if t is None else Weight("bf16", t.shape[0], t.shape[1], t)
         return HCWeights(g, wrap(down), wrap(up), wrap(inj))

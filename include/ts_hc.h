@@ -142,21 +142,42 @@ ts_status ts_hc_mixer(const void *raw, const void *hc_norm_w,
                       void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Test and debugging aid: ts_hc_call (or, with inject == NULL, ts_hc_mixer)
+ * that also writes w, the output of the up projection's sigmoid
+ * (families/qwen4/mod.rs, "## Hyper-connections": w = sigmoid(up(act)), the
+ * per-element mixing weight that multiplies normed before the mean over the
+ * streams). The regular entry points keep w on chip.
+ *
+ *   w_out  fp32 [M][C*H], written: element m*C*H + c*H + h is token m's
+ *          weight for stream c at h (the values the same launch mixes)
+ *   inject, inject_w, inject_stride  as for ts_hc_call; inject may be NULL
+ *          (the exit mixer), and then inject_w is not used
+ * Every other output (mixed, the gates, the workspace intermediates) is bit
+ * for bit what ts_hc_call / ts_hc_mixer writes for the same inputs: the same
+ * kernels run, with one extra store per element of w.
+ */
+ts_status ts_hc_call_debug(const void *raw, const void *hc_norm_w,
+                           const ts_weight *down, const ts_weight *up, const ts_weight *inject,
+                           void *mixed, float *inject_w, long inject_stride,
+                           int M, int H, int C, int lowrank, float eps,
+                           void *workspace, size_t workspace_bytes, float *w_out,
+                           cudaStream_t stream);
+
+/*
  * ts_hc_call for callers that cannot allocate device memory. The pages have
  * no counterpart to this entry point; it exists for this library's users.
  *
  * Some callers cannot call cudaMalloc (or any allocator) at the point where
- * they run the call: code that runs while a stream is being captured with a
- * capture mode that forbids allocation, real-time loops that must not hit the
- * implicit synchronisation an allocation can cause, and hosts that hand this
- * library a fixed memory budget and no allocator. They pass inputs and outputs
+ * they run the call: real-time loops that must not hit the implicit
+ * synchronisation an allocation can cause, and hosts that hand this library a
+ * fixed memory budget and no allocator. They pass inputs and outputs
  * as for ts_hc_call but no workspace: the scratch lives in a file-scope device
  * array of TS_HC_STATIC_SCRATCH_BYTES that every GPU which loads this library
  * holds until the process exits.
  *
  *   - Shapes whose ts_hc_workspace_bytes() exceeds TS_HC_STATIC_SCRATCH_BYTES
  *     are refused with TS_ERR_WORKSPACE before anything is launched (at the
- *     full shape H=2560, C=4, lowrank=320 that allows up to 1394 tokens).
+ *     full shape H=2560, C=4, lowrank=320 that allows up to 1373 tokens).
  *   - The first call on each device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
  *   - Every call on a device shares the one array and leaves its contents

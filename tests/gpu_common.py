@@ -26,6 +26,8 @@ def require_gpu():
 
 
 def to_np(t) -> np.ndarray:
+    if isinstance(t, np.ndarray):
+        return t.astype(np.float64)
     return t.detach().float().cpu().double().numpy()
 
 
@@ -46,7 +48,31 @@ def bf16_ulp(x) -> np.ndarray:
     return 2.0 ** (np.floor(np.log2(x)) - 7)
 
 
+# The carried-residual rule (see check_bf16_carried). Measured on the oracle's
+# 40-layer stack at M = 1 and 16, with its gates perturbed by 2^-23, 1e-6 and
+# 1e-5 relative and the inject-add evaluated in fp32 (a correct evaluation in
+# another precision): per-element error up to 0.63 of the loose bound, at most
+# 14% of elements beyond the plain bf16 bar, error RMS at most 0.75 ulp of the
+# elements' peak magnitude. A layer's gate scaled by 0.9, a skipped inject-add
+# or two swapped streams give at least 1.5 of the loose bound, 42% of elements
+# and 2.0 ulps RMS.
 STACK_DRIFT_ULPS = 8
+CARRIED_MAX_FRAC_BEYOND_PLAIN = 0.25
+CARRIED_MAX_RMS_ULPS = 1.25
+
+
+def carried_stats(gpu, ref, peak) -> dict:
+    """Error statistics of a carried bf16 residual against the oracle's."""
+    g = to_np(gpu).reshape(np.shape(ref))
+    ref = np.asarray(ref, dtype=np.float64)
+    d = g - ref
+    plain = BF16_ATOL + BF16_RTOL * np.abs(ref)
+    ulp = bf16_ulp(peak)
+    loose = plain + STACK_DRIFT_ULPS * ulp
+    return {"finite": bool(np.all(np.isfinite(g))),
+            "max_loose": float((np.abs(d) / loose).max()) if d.size else 0.0,
+            "frac_beyond_plain": float(np.mean(np.abs(d) > plain)) if d.size else 0.0,
+            "rms_ulps": float(np.sqrt(np.mean((d / ulp) ** 2))) if d.size else 0.0}
 
 
 def check_bf16_carried(gpu, ref, peak, what: str) -> float:
@@ -54,19 +80,18 @@ def check_bf16_carried(gpu, ref, peak, what: str) -> float:
 
     Two correct evaluations (the fp64 oracle, the fp32 kernels) can take a
     rounding decision differently; each such flip leaves one ulp of the
-    element's magnitude at that step, which later adds do not undo. Bound:
-    the bf16 tolerance plus STACK_DRIFT_ULPS ulps of the element's peak |raw|
-    over the run (perturbing the oracle's own gates by 2^-23 relative moves
-    elements by up to 5 such ulps over 40 layers).
+    element's magnitude at that step, and later adds do not undo it. The rule:
+    every element within the bf16 tolerance plus STACK_DRIFT_ULPS ulps of its
+    peak |raw| over the run (``peak``), at most CARRIED_MAX_FRAC_BEYOND_PLAIN
+    of the elements beyond the plain bf16 tolerance, and an error RMS of at
+    most CARRIED_MAX_RMS_ULPS ulps of the peak. Returns the per-element ratio.
     """
-    g = to_np(gpu).reshape(np.shape(ref))
-    ref = np.asarray(ref, dtype=np.float64)
-    assert np.all(np.isfinite(g)), f"{what}: non-finite values"
-    lim = BF16_ATOL + BF16_RTOL * np.abs(ref) + STACK_DRIFT_ULPS * bf16_ulp(peak)
-    ratio = np.abs(g - ref) / lim
-    worst = float(ratio.max()) if ratio.size else 0.0
-    assert worst <= 1.0, f"{what}: worst |err|/limit = {worst:.3g} at {np.unravel_index(ratio.argmax(), ratio.shape)}"
-    return worst
+    st = carried_stats(gpu, ref, peak)
+    assert st["finite"], f"{what}: non-finite values"
+    assert st["max_loose"] <= 1.0, f"{what}: worst |err|/limit = {st['max_loose']:.3g} ({st})"
+    assert st["frac_beyond_plain"] <= CARRIED_MAX_FRAC_BEYOND_PLAIN, f"{what}: too many rounding departures ({st})"
+    assert st["rms_ulps"] <= CARRIED_MAX_RMS_ULPS, f"{what}: error RMS too large ({st})"
+    return st["max_loose"]
 
 
 # A call whose input residual came out of an earlier bf16-rounded inject-add

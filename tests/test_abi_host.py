@@ -41,12 +41,12 @@ def test_workspace_size_and_layout(lib):
     # the chunks' sums of squares (64-float stride)
     assert B.ts_hc_workspace_bytes(1, H, C, L) == 256 + 1280 + 8 * a256(4 * 8 * (L + C)) + 8 * 4 * 64
     # from 2 tokens the tensor-core path adds normed as bf16 hi + lo [M][C*H] x 2, the
-    # down kernel's per-chunk partials [nchunk][L+C][Mp] fp32 and the bf16 activations
-    # [M][L]. The K split aims at 152 CTAs: at M=128 (one 128-token tile, 3 row tiles)
-    # 160 K blocks of 64 go 4 to a chunk, 40 chunks.
+    # down kernel's per-chunk partials [nchunk][L+C][Mp] fp32 and the activations as
+    # bf16 hi + lo [M][L] x 2. The K split aims at 152 CTAs: at M=128 (one 128-token
+    # tile, 3 row tiles) 160 K blocks of 64 go 4 to a chunk, 40 chunks.
     for M, nchunk, Mp in ((128, 40, 128), (2, 40, 16), (15, 40, 16), (16, 40, 16), (40, 40, 48),
                           (300, 16, 384)):
-        tc = 2 * a256(2 * M * C * H) + a256(4 * nchunk * (L + C) * Mp) + a256(2 * M * L)
+        tc = 2 * a256(2 * M * C * H) + a256(4 * nchunk * (L + C) * Mp) + 2 * a256(2 * M * L)
         assert B.ts_hc_workspace_bytes(M, H, C, L) == a256(4 * M * C) + a256(4 * M * L) + tc, M
     # shapes the tensor-core path does not take (lowrank not a multiple of 64): inv_rms, act
     assert B.ts_hc_workspace_bytes(15, H, C, 32) == a256(4 * 15 * C) + a256(4 * 15 * 32)
@@ -109,6 +109,23 @@ def test_call_rejects(lib, kw, status, needle):
 def test_call_m0_is_noop(lib):
     assert _call(M=0, ws=None, ws_bytes=0) == B.TS_OK
     assert B.ts_hc_last_error() == ""
+
+
+def test_call_debug_rejects_a_missing_w_buffer(lib):
+    args = [FAKE, FAKE, _w(), _w(), _w(), FAKE, FAKE, C, 1, H, C, L, 1e-6, FAKE, 1 << 30]
+    assert B.ts_hc_call_debug(*args, None, None) == B.TS_ERR_INVALID_ARG
+    assert "w_out is NULL" in B.ts_hc_last_error()
+    assert B.ts_hc_call_debug(*args, FAKE + 2, None) == B.TS_ERR_INVALID_ARG
+    assert "w_out is not 4-byte aligned" in B.ts_hc_last_error()
+    # the rest of the call's validation still applies
+    bad = list(args)
+    bad[0] = None
+    assert B.ts_hc_call_debug(*bad, FAKE, None) == B.TS_ERR_INVALID_ARG
+    assert "raw is NULL" in B.ts_hc_last_error()
+    # M == 0: a no-op that examines no pointer
+    zero = list(args)
+    zero[8] = 0
+    assert B.ts_hc_call_debug(*zero, None, None) == B.TS_OK
 
 
 def test_mixer_rejects(lib):
