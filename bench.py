@@ -200,15 +200,19 @@ def aggregate_ranks(local_ms: float, calls_per_rank: int, device="cpu"):
     return ms, calls_per_rank * world / (ms / 1e3)
 
 
-def _config():
-    return {"workload": "full-shape decode hyper-connection call + inject-add: M=1, H=2560, C=4 "
+def _config(reference: bool = False):
+    base = {"workload": "full-shape decode hyper-connection call + inject-add: M=1, H=2560, C=4 "
                         "(wide 10240), hc_lowrank=320, bf16 weights",
-            "M": M, "H": H, "C": C, "hc_lowrank": L, "calls_per_step": CALLS_PER_STEP,
-            "weight_sets": WEIGHT_SETS,
+            "M": M, "H": H, "C": C, "hc_lowrank": L, "parallelism": "replicas"}
+    if reference:
+        return {**base, "calls_per_step": 1, "weight_sets": 1,
+                "sequence": "one fp64 oracle call + inject-add per step, each call on the previous "
+                            "call's residual",
+                "l2": "not applicable (host cores)"}
+    return {**base, "calls_per_step": CALLS_PER_STEP, "weight_sets": WEIGHT_SETS,
             "sequence": "ts_hc_call, then ts_hc_inject_call (previous inject-add fused) for each later "
                         "call, then a final ts_hc_inject_add",
-            "l2": "inputs larger than L2: 48 distinct weight sets, 634 MB per pass, cycled",
-            "parallelism": "replicas"}
+            "l2": "inputs larger than L2: 48 distinct weight sets, 634 MB per pass, cycled"}
 
 
 def run_reference(args):
@@ -243,32 +247,41 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": _config(),
+        "config": _config(reference=True),
         "cpu_baseline": {"value": value, "unit": "calls/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "calls/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(budget_s: float = 12.0):
+def cpu_baseline(budget_s: float = 12.0, single_budget_s: float = 6.0):
+    """The fp64 oracle on the host cores (OpenMP over output rows), and once on
+    one thread, each on a bounded sample of chained full-shape calls."""
     import oracle
     from hyper_connection_residual_call_gb300 import inputs
 
     orc = oracle.get()
     threads = oracle.default_threads()
     w = inputs.make_hc_weights(H, C, L, CONFIG_SEED)
-    raw = inputs.make_residual(M, H, C, CONFIG_SEED).double().numpy()
+    raw0 = inputs.make_residual(M, H, C, CONFIG_SEED).double().numpy()
     out = inputs.make_sublayer_out(M, H, CONFIG_SEED)
-    n = 0
-    t0 = time.perf_counter()
-    while time.perf_counter() - t0 < budget_s and n < 20000:
-        res = orc.hc_call(raw, w.g, w.down, w.up, w.inject, H=H, C=C, L=L, threads=threads)
-        raw = orc.inject_add(raw, out, res["gate"], H=H, C=C)
-        n += 1
-    dt = time.perf_counter() - t0
+
+    def run(nthreads, budget):
+        raw, n = raw0, 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < budget and n < 20000:
+            res = orc.hc_call(raw, w.g, w.down, w.up, w.inject, H=H, C=C, L=L, threads=nthreads)
+            raw = orc.inject_add(raw, out, res["gate"], H=H, C=C)
+            n += 1
+        return n, time.perf_counter() - t0
+
+    n, dt = run(threads, budget_s)
+    n1, dt1 = run(1, single_budget_s)
     return {"value": n / dt, "unit": "calls/s", "cores": threads, "kind": "oracle",
             "sample": f"{n} full-shape calls + inject-adds (M=1, H=2560, C=4, L=320) in {dt:.1f} s, "
-                      f"fp64 oracle, OpenMP over output rows"}
+                      f"fp64 oracle, OpenMP over output rows",
+            "single_thread": {"value": n1 / dt1, "unit": "calls/s", "cores": 1,
+                              "sample": f"{n1} calls + inject-adds in {dt1:.1f} s on one thread"}}
 
 
 def parity_check(B, w0_d, w0, raw0, out0):
@@ -550,6 +563,20 @@ def run_ours(args):
     t1 = time.time()
     clocks = sampler.stop(t0, t1)
 
+    # Per-call time distribution: each replay (CALLS_PER_STEP calls) timed on its own.
+    reps = []
+    with torch.cuda.stream(stream):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(40)]
+        for a, b in evs:
+            a.record(stream)
+            graphs["fused"].replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    reps = sorted(1e3 * a.elapsed_time(b) / CALLS_PER_STEP for a, b in evs)
+    pick = lambda q: reps[min(len(reps) - 1, int(round(q * (len(reps) - 1))))]
+    per_call = {"median": pick(0.5), "p10": pick(0.1), "p90": pick(0.9), "unit": "us",
+                "replays": len(reps), "calls_per_replay": CALLS_PER_STEP}
+
     # e2e: per step, the step's inputs (initial residual + the 48 sublayer
     # outputs) from pinned host memory, the graph, and the results read back.
     raw_pin = raw_h.pin_memory()
@@ -571,6 +598,35 @@ def run_ours(args):
     ms_e2e = timed(e2e_steps, e2e_step)
     h2d = raw_pin.numel() * 2 + outs_pin.numel() * 2
     d2h = mixed_pin.numel() * 2 + res_pin.numel() * 2
+
+    # One call with a host round trip: this token's residual and sublayer output
+    # from pinned host memory, one fused call + inject-add, mixed and the new
+    # residual read back, synchronised on the host every call.
+    out_pin1 = outs_h[0].pin_memory()
+    raw1 = torch.empty_like(raw)
+    out1 = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+
+    def one_call():
+        raw1.copy_(raw_pin, non_blocking=True)
+        out1.copy_(out_pin1, non_blocking=True)
+        B.hc_call(raw1, sets[0], H=H, C=C, mixed=mixed, inject_w=gates[0], inject_stride=C, ws=wsp)
+        B.hc_inject_add(raw1, out1, gates[0], H=H, C=C)
+        mixed_pin.copy_(mixed, non_blocking=True)
+        res_pin.copy_(raw1, non_blocking=True)
+        stream.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(20):
+            one_call()
+        t_host = time.perf_counter()
+        n_single = 400
+        for _ in range(n_single):
+            one_call()
+        t_host = time.perf_counter() - t_host
+    single_call = {"value": n_single / t_host, "unit": "calls/s", "us_per_call": 1e6 * t_host / n_single,
+                   "h2d_bytes_per_call": raw_pin.numel() * 2 + out_pin1.numel() * 2,
+                   "d2h_bytes_per_call": mixed_pin.numel() * 2 + res_pin.numel() * 2,
+                   "timing": "host wall clock, a stream synchronisation after every call"}
 
     n_calls = args.steps * CALLS_PER_STEP
     value = n_calls * ws / (ms / 1e3)
@@ -603,8 +659,10 @@ def run_ours(args):
                                 "us_per_call": 1e3 * ms_sep / n_calls, "hbm_gbs": achieved_sep,
                                 "frac": achieved_sep / peak,
                                 "sequence": "ts_hc_call + ts_hc_inject_add per call"},
+            "per_call_us": per_call,
             "e2e": {"value": e2e_value, "unit": "calls/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
+            "e2e_single_call": single_call,
             "gpu_launches": launches_per_step["fused"] * args.steps,
             "clocks": clocks,
             "cpu_baseline": base,

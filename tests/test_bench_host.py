@@ -54,3 +54,5 @@ def test_reference_arm_prints_one_contract_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert "workload" in d["config"]
+    # the line describes what this arm ran: one oracle call + inject-add per step, one weight set
+    assert d["config"]["calls_per_step"] == 1 and d["config"]["weight_sets"] == 1
