@@ -28,7 +28,9 @@ TS_W_BF16, TS_W_INT4_AFFINE = 0, 1
 RMS_EPS = 1e-6  # families/qwen4/mod.rs, RMS_EPS
 
 EXPORTS = ("ts_hc_workspace_bytes", "ts_hc_workspace_layout", "ts_hc_call", "ts_hc_inject_add",
-           "ts_hc_mixer", "ts_hc_call_debug", "ts_hc_inject_call", "ts_hc_replicate_entry", "ts_hc_last_error",
+           "ts_hc_mixer", "ts_hc_call_debug", "ts_hc_inject_call", "ts_hc_entry_call", "ts_hc_exit_logits",
+           "ts_hc_replicate_entry",
+           "ts_hc_last_error",
            "ts_hc_device_status", "ts_hc_call_noalloc", "ts_hc_stack_workspace_bytes", "ts_hc_stack",
            "ts_hc_selftest_timeout")
 TS_HC_STATIC_SCRATCH_BYTES = 64 * 1024 * 1024  # include/ts_hc.h
@@ -94,6 +96,10 @@ def library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.ts_hc_inject_add.restype = i
         lib.ts_hc_inject_call.argtypes = [vp, vp, vp, l, vp, wp, wp, wp, vp, vp, l, i, i, i, i, f, vp, sz, vp]
         lib.ts_hc_inject_call.restype = i
+        lib.ts_hc_entry_call.argtypes = [vp, vp, vp, wp, wp, wp, vp, vp, l, i, i, i, i, f, vp, sz, vp]
+        lib.ts_hc_entry_call.restype = i
+        lib.ts_hc_exit_logits.argtypes = [vp, vp, vp, l, vp, wp, wp, vp, i, vp, vp, i, i, i, i, f, vp, sz, vp]
+        lib.ts_hc_exit_logits.restype = i
         lib.ts_hc_call_noalloc.argtypes = [vp, vp, wp, wp, wp, vp, vp, l, i, i, i, i, f, vp]
         lib.ts_hc_call_noalloc.restype = i
         lib.ts_hc_replicate_entry.argtypes = [vp, vp, i, i, i, vp]
@@ -157,6 +163,21 @@ def ts_hc_inject_call(raw, out, prev_inject_w, prev_inject_stride, hc_norm_w, do
     return library().ts_hc_inject_call(raw, out, prev_inject_w, prev_inject_stride, hc_norm_w, _wref(down),
                                        _wref(up), _wref(inject), mixed, inject_w, inject_stride, M, H, C,
                                        lowrank, eps, workspace, workspace_bytes, stream)
+
+
+def ts_hc_entry_call(emb, raw, hc_norm_w, down, up, inject, mixed, inject_w, inject_stride, M, H, C, lowrank,
+                     eps, workspace, workspace_bytes, stream) -> int:
+    """Entry replication fused into the first call: raw = repeat(emb, C), then the call on it."""
+    return library().ts_hc_entry_call(emb, raw, hc_norm_w, _wref(down), _wref(up), _wref(inject), mixed, inject_w,
+                                      inject_stride, M, H, C, lowrank, eps, workspace, workspace_bytes, stream)
+
+
+def ts_hc_exit_logits(raw, out, prev_inject_w, prev_inject_stride, hc_norm_w, down, up, lm_head, V, mixed, logits,
+                      M, H, C, lowrank, eps, workspace, workspace_bytes, stream) -> int:
+    """The exit: (inject-add,) hyper_connection_mixer, then lm_head into fp32 logits."""
+    return library().ts_hc_exit_logits(raw, out, prev_inject_w, prev_inject_stride, hc_norm_w, _wref(down), _wref(up),
+                                       lm_head, V, mixed, logits, M, H, C, lowrank, eps, workspace, workspace_bytes,
+                                       stream)
 
 
 def ts_hc_call_noalloc(raw, hc_norm_w, down, up, inject, mixed, inject_w, inject_stride, M, H, C, lowrank,
@@ -384,6 +405,73 @@ def hc_inject_call(raw, out, prev_inject_w, weights, *, H: int, C: int, prev_inj
                            ws.data_ptr(), ws.numel() * ws.element_size(), _stream_handle(stream))
     _check(st)
     return mixed, (inject_w if has_inject else None)
+
+
+def hc_entry_call(emb, weights, *, C: int, raw=None, mixed=None, inject_w=None, inject_stride: Optional[int] = None,
+                  eps: float = RMS_EPS, ws=None, stream=None):
+    """The entry replication fused into the first call: raw [M, C*H] = emb [M, H] repeated C
+    times (written), then attn_hc on it -- or the mixer when weights.inject is None.
+    Returns (raw, mixed, inject_w or None)."""
+    torch = _torch()
+    M, H = emb.shape
+    L = weights.down.rows
+    _need(emb, "emb", torch.bfloat16, (M, H))
+    _need(weights.g, "hc_norm_w", torch.bfloat16, (C * H,))
+    if raw is None:
+        raw = torch.empty((M, C * H), dtype=torch.bfloat16, device=emb.device)
+    _need(raw, "raw", torch.bfloat16, (M, C * H))
+    if mixed is None:
+        mixed = torch.empty((M, H), dtype=torch.bfloat16, device=emb.device)
+    _need(mixed, "mixed", torch.bfloat16, (M, H))
+    has_inject = weights.inject is not None
+    if has_inject and inject_w is None:
+        inject_stride = C
+        inject_w = torch.empty((max(M, 1), C), dtype=torch.float32, device=emb.device)
+    if has_inject and inject_stride is None:
+        raise HCError(TS_ERR_INVALID_ARG, "inject_stride is required with a caller-given inject_w")
+    if ws is None:
+        ws = workspace(M, H, C, L, emb.device)
+    st = ts_hc_entry_call(emb.data_ptr(), raw.data_ptr(), weights.g.data_ptr(), weight_struct(weights.down),
+                          weight_struct(weights.up), weight_struct(weights.inject) if has_inject else None,
+                          mixed.data_ptr(), inject_w.data_ptr() if has_inject else None, inject_stride or 0, M, H, C,
+                          L, eps, ws.data_ptr(), ws.numel() * ws.element_size(), _stream_handle(stream))
+    _check(st)
+    return raw, mixed, (inject_w if has_inject else None)
+
+
+def hc_exit_logits(raw, weights, lm_head, *, H: int, C: int, out=None, prev_inject_w=None,
+                   prev_inject_stride: Optional[int] = None, mixed=None, logits=None, eps: float = RMS_EPS, ws=None,
+                   stream=None):
+    """The decoder's exit: with ``out`` given, raw += out * prev gates (in place) first; then the
+    mixer (``weights``: g, down, up) and lm_head [V, H] bf16. Returns (mixed [M, H] bf16,
+    logits [M, V] fp32)."""
+    torch = _torch()
+    M = raw.shape[0]
+    L = weights.down.rows
+    V = lm_head.shape[0]
+    _need(raw, "raw", torch.bfloat16, (M, C * H))
+    _need(weights.g, "hc_norm_w", torch.bfloat16, (C * H,))
+    _need(lm_head, "lm_head", torch.bfloat16, (V, H))
+    if mixed is None:
+        mixed = torch.empty((M, H), dtype=torch.bfloat16, device=raw.device)
+    _need(mixed, "mixed", torch.bfloat16, (M, H))
+    if logits is None:
+        logits = torch.empty((M, V), dtype=torch.float32, device=raw.device)
+    _need(logits, "logits", torch.float32, (M, V))
+    if out is not None:
+        _need(out, "out", torch.bfloat16, (M, H))
+        if prev_inject_w is None or not prev_inject_w.is_cuda or prev_inject_w.dtype != torch.float32:
+            raise HCError(TS_ERR_INVALID_ARG, "prev_inject_w must be a CUDA float32 tensor with out")
+    if ws is None:
+        ws = workspace(M, H, C, L, raw.device)
+    st = ts_hc_exit_logits(raw.data_ptr(), out.data_ptr() if out is not None else None,
+                           prev_inject_w.data_ptr() if out is not None else None,
+                           (C if prev_inject_stride is None else prev_inject_stride) if out is not None else 0,
+                           weights.g.data_ptr(), weight_struct(weights.down), weight_struct(weights.up),
+                           lm_head.data_ptr(), V, mixed.data_ptr(), logits.data_ptr(), M, H, C, L, eps, ws.data_ptr(),
+                           ws.numel() * ws.element_size(), _stream_handle(stream))
+    _check(st)
+    return mixed, logits
 
 
 def hc_replicate_entry(emb, *, C: int, raw=None, stream=None):

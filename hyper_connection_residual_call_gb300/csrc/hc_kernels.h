@@ -22,7 +22,9 @@ struct WeightView {
 // S = C * sps CTAs shares one block of rows; CTA s of the cluster owns input
 // columns [s*KC, (s+1)*KC), which lie inside stream s / sps.
 struct DownParams {
-    const uint16_t *raw;      // bf16 [M][W]
+    const uint16_t *raw;      // bf16: element (m, c, h) at raw + m*raw_mstride + c*raw_cstride + h
+    long raw_mstride;         // W for a [M][W] residual; H when every stream reads one
+    int raw_cstride;          // H for a [M][W] residual; 0 when every stream reads one [M][H] row (entry)
     const uint16_t *g;        // bf16 [W]
     WeightView down;          // [L][W]
     WeightView inject;        // [C][W]; data == nullptr for the mixer
@@ -38,6 +40,7 @@ struct DownParams {
     unsigned *status;
     // Optional fused inject-add of the previous sublayer: the call sees
     // raw + out * prev_gate (rounded to bf16) in place of raw. Not written here.
+    // (The residual the call sees is written back by the up kernel.)
     const uint16_t *inj_out;  // bf16 [M][H], or nullptr
     const float *inj_gate;    // token m's previous gates at inj_gate + m * inj_stride
     long inj_stride;
@@ -57,7 +60,9 @@ constexpr long kSsqStride = 64;  // floats between the copies of the sums of squ
 // Up projection + sigmoid + mean mix: CTA b owns h in [b*HB, b*HB + HB) of
 // every stream, i.e. up rows {c*H + h}.
 struct UpParams {
-    const uint16_t *raw;      // bf16 [M][W]
+    const uint16_t *raw;      // bf16, read through the same view as DownParams::raw
+    long raw_mstride;
+    int raw_cstride;
     const uint16_t *g;        // bf16 [W]
     WeightView up;            // [W][L]
     const float *act;         // [M][L]
@@ -68,10 +73,12 @@ struct UpParams {
     int mt;                   // tokens per tile (1, 2, 4 or 8)
     float inv_C;
     unsigned *status;
-    // Optional fused inject-add (see DownParams): each CTA owns its h-block of
-    // every stream, recomputes raw + out * prev_gate there and writes it back.
-    uint16_t *raw_out;        // == raw when fused, else nullptr
-    const uint16_t *inj_out;
+    // Optional write-back of the residual the call sees (see DownParams): each
+    // CTA owns its h-block of every stream and writes it to raw_out [M][W]
+    // (raw + out * prev_gate with a fused inject-add, in place; the replicated
+    // embedding row for the entry call).
+    uint16_t *raw_out;        // or nullptr
+    const uint16_t *inj_out;  // or nullptr (no fused inject-add)
     const float *inj_gate;
     long inj_stride;
     // One-token path (launch_one_token): every CTA forms inv_rms, act and the
@@ -103,6 +110,23 @@ struct ReplicateParams {
     int M, H, C;
 };
 
+// lm_head after the exit mixer: logits[m][v] = sum_h w[v][h] * mixed[m][h].
+// CTA b owns vocabulary rows [b * rows_per_cta, ...); they stream through a
+// ring of n_stages stages of rs rows each (bulk copies), and warp j of the
+// block dots row j of a stage with every token.
+struct LmHeadParams {
+    const uint16_t *mixed;    // bf16 [M][H]
+    const uint16_t *w;        // bf16 [V][H]
+    float *logits;            // fp32 token m's logits at logits + m * logits_stride
+    long logits_stride;
+    int M, H, V;              // M <= kLmHeadMaxTokens
+    int rows_per_cta, rs, n_stages;
+    unsigned *status;
+};
+constexpr int kLmHeadMaxTokens = 16;
+constexpr int kLmHeadThreads = 384;  // 12 warps: one row of a stage each
+constexpr size_t kLmHeadSmem = 160 * 1024;
+
 struct LaunchCfg {
     int sm_count;
     bool pdl;                 // launch as a programmatic dependent of the previous kernel
@@ -126,6 +150,9 @@ cudaError_t launch_one_token(const DownParams &d, const UpParams &u, const Launc
 
 cudaError_t launch_up(const UpParams &p, const LaunchCfg &cfg, cudaStream_t stream);
 cudaError_t launch_inject(const InjectParams &p, const LaunchCfg &cfg, cudaStream_t stream);
+// Fills rows_per_cta, rs and n_stages for M tokens; false if H is too wide for the ring.
+bool lm_head_plan(LmHeadParams &p, int sm_count);
+cudaError_t launch_lm_head(const LmHeadParams &p, const LaunchCfg &cfg, cudaStream_t stream);
 cudaError_t launch_replicate(const ReplicateParams &p, const LaunchCfg &cfg, cudaStream_t stream);
 
 }  // namespace tshc

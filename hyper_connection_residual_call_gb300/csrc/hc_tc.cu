@@ -48,11 +48,6 @@ constexpr int kKBlock = 64;    // bf16 elements per 128-byte swizzled row
 constexpr int kProducers = kThreads - 64;  // down kernel: warps 2-15 dequantise INT4 weight tiles
 constexpr int kUpProducers = kUpThreads - 64;  // up kernel: warps 2-15
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
 // Sigmoid from the fast exponential and division intrinsics (relative error
 // ~1e-6, far inside the 1e-3 bar), for the per-element epilogues.
 __device__ __forceinline__ float sigm_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
@@ -123,8 +118,10 @@ __global__ void __launch_bounds__(kPrepThreads) hc_tc_prep_kernel(const TcPrepPa
     const int m = blockIdx.x, c = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
     const int nv = p.H / 8;
-    const size_t base = (size_t)m * p.W + (size_t)c * p.H;
-    const bool fused = p.raw_out != nullptr;
+    const size_t base = (size_t)m * p.W + (size_t)c * p.H;                        // [M][W] outputs
+    const size_t rbase = (size_t)m * p.raw_mstride + (size_t)c * p.raw_cstride;  // the residual's view
+    const bool fused = p.inj_out != nullptr;
+    const bool write_back = p.raw_out != nullptr;
     pdl_launch_dependents();
     uint4 gq[kPrepVec];  // g is a weight: read before the dependency wait
 #pragma unroll
@@ -139,7 +136,7 @@ __global__ void __launch_bounds__(kPrepThreads) hc_tc_prep_kernel(const TcPrepPa
 #pragma unroll
     for (int k = 0; k < kPrepVec; ++k) {
         const int v = tid + k * blockDim.x;
-        rv[k] = v < nv ? reinterpret_cast<const uint4 *>(p.raw + base)[v] : make_uint4(0, 0, 0, 0);
+        rv[k] = v < nv ? reinterpret_cast<const uint4 *>(p.raw + rbase)[v] : make_uint4(0, 0, 0, 0);
         ov[k] = (fused && v < nv) ? reinterpret_cast<const uint4 *>(p.inj_out + (size_t)m * p.H)[v]
                                   : make_uint4(0, 0, 0, 0);
     }
@@ -157,8 +154,9 @@ __global__ void __launch_bounds__(kPrepThreads) hc_tc_prep_kernel(const TcPrepPa
             for (int e = 0; e < 4; ++e)
                 w[e] = pack_bf16x2(fmaf(bf16_lo(o[e]), gate, bf16_lo(w[e])), fmaf(bf16_hi(o[e]), gate, bf16_hi(w[e])));
             rv[k] = make_uint4(w[0], w[1], w[2], w[3]);
-            reinterpret_cast<uint4 *>(p.raw_out + base)[v] = rv[k];
         }
+        if (write_back)
+            reinterpret_cast<uint4 *>(p.raw_out + base)[v] = rv[k];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float a = bf16_lo(w[e]), b = bf16_hi(w[e]);

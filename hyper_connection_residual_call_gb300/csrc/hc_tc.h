@@ -50,10 +50,12 @@ __host__ __device__ inline TcPlan tc_plan(int M, int L, int C, int W)
 // g * inv_rms, stored as bf16 hi + lo (normed = hi + lo to ~16 significant
 // bits) for the two GEMMs' TMA loads.
 struct TcPrepParams {
-    const uint16_t *raw;      // bf16 [M][W]
+    const uint16_t *raw;      // bf16: element (m, c, h) at raw + m*raw_mstride + c*raw_cstride + h
+    long raw_mstride;         // W, or H when every stream reads one [M][H] row (entry)
+    int raw_cstride;          // H, or 0 (entry)
     const uint16_t *g;        // bf16 [W]
-    uint16_t *raw_out;        // == raw when the inject-add is fused, else nullptr
-    const uint16_t *inj_out;  // bf16 [M][H]
+    uint16_t *raw_out;        // bf16 [M][W]: the residual the call sees, written back; or nullptr
+    const uint16_t *inj_out;  // bf16 [M][H] with a fused inject-add, else nullptr
     const float *inj_gate;    // token m's previous gates at inj_gate + m * inj_stride
     long inj_stride;
     uint16_t *x_hi, *x_lo;    // bf16 [M][W]

@@ -246,19 +246,25 @@ int choose_sps(int H, int C, int align)
     return best;
 }
 
-// The previous sublayer's inject-add, fused into a call (ts_hc_inject_call).
-struct FusedInject {
-    const uint16_t *out;
-    const float *gate;
+// How a call reads and writes the residual, when not plainly ([M][C*H], read only).
+//   ts_hc_inject_call: the previous sublayer's inject-add fused in (raw +
+//     out * gate is what the call sees), written back in place by the up kernel;
+//   ts_hc_entry_call: every stream reads one embedding row (stream stride 0),
+//     and the replicated residual is written to raw_out.
+struct ResidualIO {
+    long mstride;             // elements between tokens of the residual the kernels read
+    int cstride;              // elements between its streams (0: one row read by every stream)
+    uint16_t *raw_out;        // [M][C*H] write-back of the residual the call sees
+    const uint16_t *out;      // the previous sublayer's output, or nullptr
+    const float *gate;        // and its gates
     long stride;
-    uint16_t *raw;  // the residual, written back by the up kernel
 };
 
 // The shared part of ts_hc_call, ts_hc_mixer and ts_hc_inject_call.
 ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *down,
                        const ts_weight *up, const ts_weight *inject, void *mixed, float *inject_w,
                        long inject_stride, int M, int H, int C, int L, float eps, void *workspace,
-                       size_t workspace_bytes, cudaStream_t stream, const FusedInject *fi = nullptr,
+                       size_t workspace_bytes, cudaStream_t stream, const ResidualIO *fi = nullptr,
                        float *w_out = nullptr)
 {
     ts_status st = check_shape(M, H, C, L);
@@ -315,9 +321,11 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         const int R = L + (inject ? C : 0);
         tshc::TcPrepParams &tp = t.prep;
         tp.raw = static_cast<const uint16_t *>(raw);
+        tp.raw_mstride = fi ? fi->mstride : W;
+        tp.raw_cstride = fi ? fi->cstride : H;
         tp.g = static_cast<const uint16_t *>(hc_norm_w);
         if (fi) {
-            tp.raw_out = fi->raw;
+            tp.raw_out = fi->raw_out;
             tp.inj_out = fi->out;
             tp.inj_gate = fi->gate;
             tp.inj_stride = fi->stride;
@@ -387,6 +395,8 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
 
     tshc::DownParams d{};
     d.raw = static_cast<const uint16_t *>(raw);
+    d.raw_mstride = fi ? fi->mstride : W;
+    d.raw_cstride = fi ? fi->cstride : H;
     d.g = static_cast<const uint16_t *>(hc_norm_w);
     d.down = view(down);
     d.inject = view(inject);
@@ -417,6 +427,8 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
 
     tshc::UpParams u{};
     u.raw = d.raw;
+    u.raw_mstride = d.raw_mstride;
+    u.raw_cstride = d.raw_cstride;
     u.g = d.g;
     u.up = view(up);
     u.act = act;
@@ -428,7 +440,7 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
     u.status = dev.status;
     u.w_out = w_out;
     if (fi) {
-        u.raw_out = fi->raw;
+        u.raw_out = fi->raw_out;
         u.inj_out = fi->out;
         u.inj_gate = fi->gate;
         u.inj_stride = fi->stride;
@@ -579,10 +591,83 @@ ts_status ts_hc_inject_call(void *raw, const void *out, const float *prev_inject
     if (inject && inject_w && M > 0 && inject_stride >= C &&
         gates_overlap(prev_inject_w, prev_inject_stride, inject_w, inject_stride, M, C))
         return fail(TS_ERR_INVALID_ARG, "inject_w shares elements with prev_inject_w");
-    const FusedInject fi{static_cast<const uint16_t *>(out), prev_inject_w, prev_inject_stride,
-                         static_cast<uint16_t *>(raw)};
+    const ResidualIO fi{(long)C * H, H, static_cast<uint16_t *>(raw), static_cast<const uint16_t *>(out),
+                        prev_inject_w, prev_inject_stride};
     return hc_call_impl(raw, hc_norm_w, down, up, inject, mixed, inject_w, inject_stride, M, H, C, lowrank,
                         eps, workspace, workspace_bytes, stream, &fi);
+}
+
+ts_status ts_hc_exit_logits(void *raw, const void *out, const float *prev_inject_w, long prev_inject_stride,
+                            const void *hc_norm_w, const ts_weight *down, const ts_weight *up, const void *lm_head,
+                            int V, void *mixed, float *logits, int M, int H, int C, int lowrank, float eps,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    g_last_error.clear();
+    ts_status st = check_shape(M, H, C, lowrank);
+    if (st != TS_OK)
+        return st;
+    if (V < 1)
+        return fail(TS_ERR_INVALID_ARG, "V = %d must be >= 1", V);
+    if (M == 0)  // nothing is read or written: pointers are not examined
+        return TS_OK;
+    if ((st = check_ptr(lm_head, "lm_head", 16)) != TS_OK) return st;
+    if ((st = check_ptr(logits, "logits", 4)) != TS_OK) return st;
+    if (out) {
+        if ((st = check_ptr(out, "out", 16)) != TS_OK) return st;
+        if ((st = check_ptr(prev_inject_w, "prev_inject_w", 4)) != TS_OK) return st;
+        if (prev_inject_stride < C)
+            return fail(TS_ERR_INVALID_ARG, "prev_inject_stride = %ld must be >= C = %d", prev_inject_stride, C);
+    }
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != TS_OK)
+        return st;
+    tshc::LmHeadParams lp{};
+    lp.M = std::min(M, tshc::kLmHeadMaxTokens);
+    lp.H = H;
+    lp.V = V;
+    if (!tshc::lm_head_plan(lp, dev.sm_count))
+        return fail(TS_ERR_UNSUPPORTED, "H = %d is too wide for the lm_head kernel's ring", H);
+    const ResidualIO io{(long)C * H, H, static_cast<uint16_t *>(raw), static_cast<const uint16_t *>(out),
+                        prev_inject_w, prev_inject_stride};
+    st = hc_call_impl(raw, hc_norm_w, down, up, nullptr, mixed, nullptr, 0, M, H, C, lowrank, eps, workspace,
+                      workspace_bytes, stream, out ? &io : nullptr);
+    if (st != TS_OK)
+        return st;
+    // lm_head over tiles of at most kLmHeadMaxTokens tokens, each a dependent of the launch before it.
+    for (int t0 = 0; t0 < M; t0 += tshc::kLmHeadMaxTokens) {
+        lp.M = std::min(tshc::kLmHeadMaxTokens, M - t0);
+        tshc::lm_head_plan(lp, dev.sm_count);
+        lp.mixed = static_cast<const uint16_t *>(mixed) + (size_t)t0 * H;
+        lp.w = static_cast<const uint16_t *>(lm_head);
+        lp.logits = logits + (size_t)t0 * V;
+        lp.logits_stride = V;
+        lp.status = dev.status;
+        const cudaError_t e = tshc::launch_lm_head(lp, tshc::LaunchCfg{dev.sm_count, true}, stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "launching the lm_head kernel");
+    }
+    return TS_OK;
+}
+
+ts_status ts_hc_entry_call(const void *emb, void *raw, const void *hc_norm_w, const ts_weight *down,
+                           const ts_weight *up, const ts_weight *inject, void *mixed, float *inject_w,
+                           long inject_stride, int M, int H, int C, int lowrank, float eps, void *workspace,
+                           size_t workspace_bytes, cudaStream_t stream)
+{
+    g_last_error.clear();
+    ts_status st = check_shape(M, H, C, lowrank);
+    if (st != TS_OK)
+        return st;
+    if (M == 0)  // nothing is read or written: pointers are not examined
+        return TS_OK;
+    if ((st = check_ptr(emb, "emb", 16)) != TS_OK) return st;
+    if ((st = check_ptr(raw, "raw", 16)) != TS_OK) return st;
+    const char *e = static_cast<const char *>(emb), *r = static_cast<const char *>(raw);
+    if (e < r + 2 * (size_t)M * C * H && r < e + 2 * (size_t)M * H)
+        return fail(TS_ERR_INVALID_ARG, "raw overlaps emb");
+    const ResidualIO io{H, 0, static_cast<uint16_t *>(raw), nullptr, nullptr, 0};
+    return hc_call_impl(emb, hc_norm_w, down, up, inject, mixed, inject_w, inject_stride, M, H, C, lowrank, eps,
+                        workspace, workspace_bytes, stream, &io);
 }
 
 ts_status ts_hc_inject_add(void *raw, const void *out, const float *inject_w, long inject_stride,

@@ -115,18 +115,23 @@ ts_status ts_hc_stack(const void *emb, int T, const ts_hc_module *attn, const ts
 
     for (int t0 = 0; t0 < T; t0 += max_chunk) {
         const int M = std::min(max_chunk, T - t0);
-        st = ts_hc_replicate_entry(static_cast<const char *>(emb) + 2 * (size_t)t0 * H, raw, M, H, C, stream);
-        if (st != TS_OK)
-            return st;
+        const void *emb_t = static_cast<const char *>(emb) + 2 * (size_t)t0 * H;
+        if (n_layers == 0) {  // the exit mixer reads the replicated embedding directly
+            st = ts_hc_replicate_entry(emb_t, raw, M, H, C, stream);
+            if (st != TS_OK)
+                return st;
+        }
         const void *prev_out = nullptr;  // the last sublayer output, not yet injected
         const float *prev_gate = nullptr;
         for (int l = 0; l < n_layers; ++l) {
             for (int which = 0; which < 2; ++which) {
                 const ts_hc_module &m = which == 0 ? attn[l] : mlp[l];
                 float *slot = gates + which * C;
-                st = prev_out == nullptr
-                         ? ts_hc_call(raw, m.hc_norm_w, &m.down, &m.up, &m.inject, mixed, slot, gstride, M, H,
-                                      C, lowrank, eps, cws, lay.call_bytes, stream)
+                // Layer 0's attn_hc reads the embedding row in every stream and
+                // writes the replicated residual (the entry line, fused).
+                st = l == 0 && which == 0
+                         ? ts_hc_entry_call(emb_t, raw, m.hc_norm_w, &m.down, &m.up, &m.inject, mixed, slot,
+                                            gstride, M, H, C, lowrank, eps, cws, lay.call_bytes, stream)
                          : ts_hc_inject_call(raw, prev_out, prev_gate, gstride, m.hc_norm_w, &m.down, &m.up,
                                              &m.inject, mixed, slot, gstride, M, H, C, lowrank, eps, cws,
                                              lay.call_bytes, stream);

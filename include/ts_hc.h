@@ -219,6 +219,53 @@ ts_status ts_hc_inject_call(void *raw, const void *out, const float *prev_inject
                             void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * The decoder's exit (families/qwen4/mod.rs, decoder pseudocode, exit lines:
+ * hidden = hyper_connection_mixer(hidden); logits = lm_head(hidden), with no
+ * softcap and no separate final norm), with the last sublayer's inject-add
+ * fused in front when `out` is given:
+ *     raw += out * prev_inject_w                    (only if out != NULL)
+ *     mixed = hyper_connection_mixer(raw)           bf16 [M][H]
+ *     logits[m][v] = sum_h lm_head[v][h] * mixed[m][h]   (fp32, mixed as stored)
+ * The lm_head GEMV launches as a programmatic dependent of the mixer and
+ * streams its first weight rows before the mixer has finished.
+ *
+ *   raw             bf16 [M][C*H]; read, and written with the fused inject-add
+ *   out, prev_inject_w, prev_inject_stride   as for ts_hc_inject_call, or
+ *                   out == NULL (then the other two are not used)
+ *   hc_norm_w, down, up   the exit mixer's module (no inject weight)
+ *   lm_head         bf16 [V][H] (lm_head.weight), 16-byte aligned
+ *   mixed           bf16 [M][H], written (the lm_head reads it back)
+ *   logits          fp32 [M][V], written
+ * Other arguments as for ts_hc_mixer; the workspace is ts_hc_workspace_bytes(M, ...).
+ * Returns TS_ERR_UNSUPPORTED when H is too wide for the lm_head kernel
+ * (one row of 2*H bytes must fit its shared-memory ring).
+ */
+ts_status ts_hc_exit_logits(void *raw, const void *out, const float *prev_inject_w, long prev_inject_stride,
+                            const void *hc_norm_w, const ts_weight *down, const ts_weight *up,
+                            const void *lm_head, int V, void *mixed, float *logits,
+                            int M, int H, int C, int lowrank, float eps,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Entry replication fused into the stack's first call (families/qwen4/mod.rs,
+ * decoder pseudocode: the entry line hidden = embed_tokens(ids).repeat(1, 1, C),
+ * followed by layer 0's attn_hc). Equivalent, bit for bit, to
+ *     ts_hc_replicate_entry(emb, raw, M, H, C, stream);
+ *     ts_hc_call(raw, ...)            (or ts_hc_mixer when inject == NULL)
+ * with one kernel fewer: the call reads every stream from the embedding row
+ * and writes the replicated residual to raw.
+ *
+ *   emb   bf16 [M][H], read
+ *   raw   bf16 [M][C*H], written (must not overlap emb; refused otherwise)
+ * Other arguments as for ts_hc_call; inject may be NULL (then inject_w is not used).
+ */
+ts_status ts_hc_entry_call(const void *emb, void *raw, const void *hc_norm_w,
+                           const ts_weight *down, const ts_weight *up, const ts_weight *inject,
+                           void *mixed, float *inject_w, long inject_stride,
+                           int M, int H, int C, int lowrank, float eps,
+                           void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Entry replication (families/qwen4/mod.rs, decoder pseudocode, entry line:
  * the embedding row is repeated C times, not padded):
  * raw[m][c*H + h] = emb[m][h] for every stream c.

@@ -17,6 +17,7 @@ the way the turbospark-runtime 0.3.0 pages describe:
   and families/qwen4/mod.rs, "Chunked prefill is wired".
 * ``stack``: families/qwen4/mod.rs decoder-layer pseudocode (entry
   replication, two calls and two inject-adds per layer, the exit mixer).
+* ``lm_head``: the same pseudocode's exit line, logits = lm_head(mixer output).
 
 Every function is pinned by ``tests/test_oracle_pins.py`` (closed forms,
 invariants, library special cases); ``tests/test_oracle_mutants.py`` plants
@@ -142,6 +143,18 @@ def _weight(w) -> Optional[_Marshalled]:
     return _Marshalled(s, keep)
 
 
+@dataclass
+class _LinearBf16:
+    """A bf16 [rows][cols] weight in the form ``_weight`` marshals."""
+    rows: int
+    cols: int
+    data: object
+    kind: str = "bf16"
+    scale: object = None
+    bias: object = None
+    group: int = 0
+
+
 def _wptr(m: Optional[_Marshalled]):
     return None if m is None else ctypes.byref(m.struct)
 
@@ -256,6 +269,19 @@ class Oracle:
         self.lib.orc_inject_add(M, H, C, _dptr(raw), _dptr(out), _dptr(gate), gate_stride,
                                 _dptr(res))
         return res
+
+    def lm_head(self, mixed, lm_head_w, *, threads: Optional[int] = None) -> np.ndarray:
+        """logits = lm_head(mixed), one plain GEMV per token (families/qwen4/mod.rs,
+        decoder pseudocode, exit lines: the mixer's output goes straight to lm_head,
+        with no softcap and no separate final norm).
+
+        ``mixed`` [M, H] values; ``lm_head_w`` bf16 [V][H] (a tensor). Returns [M, V].
+        """
+        mixed = _f64(mixed)
+        V, H = lm_head_w.shape
+        w = _LinearBf16(V, H, lm_head_w)
+        return np.stack([self.gemv(w, mixed[m], threads=threads or default_threads())
+                         for m in range(mixed.shape[0])])
 
     def replicate_entry(self, emb, *, H: int, C: int) -> np.ndarray:
         emb = _f64(emb).reshape(-1, H)

@@ -436,4 +436,19 @@ def pin_stack_closed_form(orc):
            what="stack exit mixer")
 
 
+def pin_lm_head(orc):
+    """logits = lm_head(mixed): one-hot rows read single elements of mixed, and a
+    random weight agrees with numpy's matmul."""
+    rng = np.random.default_rng(11)
+    H, V = 16, 7
+    mixed = _randn(rng, 3, H).double().numpy()
+    one_hot = torch.zeros((V, H))
+    cols = [(5 * v + 2) % H for v in range(V)]
+    one_hot[torch.arange(V), torch.tensor(cols)] = 1.0
+    got = orc.lm_head(mixed, one_hot.to(torch.bfloat16))
+    assert np.array_equal(got, mixed[:, cols]), "one-hot lm_head rows"
+    w = _randn(rng, V, H, std=0.3)
+    _close(orc.lm_head(mixed, w), mixed @ w.double().numpy().T, what="lm_head vs numpy")
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -128,6 +128,35 @@ def test_call_debug_rejects_a_missing_w_buffer(lib):
     assert B.ts_hc_call_debug(*zero, None, None) == B.TS_OK
 
 
+def test_entry_call_rejects(lib):
+    args = dict(emb=FAKE, raw=FAKE + (1 << 20), M=2)
+
+    def call(emb, raw, M, inject=_w()):
+        return B.ts_hc_entry_call(emb, raw, FAKE, _w(), _w(), inject, FAKE, FAKE, C, M, H, C, L, 1e-6, FAKE, 1 << 30,
+                                  None)
+
+    assert call(**{**args, "emb": None}) == B.TS_ERR_INVALID_ARG and "emb is NULL" in B.ts_hc_last_error()
+    assert call(**{**args, "raw": FAKE + 8}) == B.TS_ERR_INVALID_ARG and "not 16-byte aligned" in B.ts_hc_last_error()
+    # the replicated residual must not overwrite the embedding rows it is built from
+    assert call(**{**args, "raw": FAKE + 2 * H}) == B.TS_ERR_INVALID_ARG
+    assert "raw overlaps emb" in B.ts_hc_last_error()
+    assert call(**{**args, "M": 0, "emb": None, "raw": None}) == B.TS_OK
+
+
+def test_exit_logits_rejects(lib):
+    def call(lm_head=FAKE, V=1000, logits=FAKE, out=None, prev=None, prev_stride=C, M=1, H_=H):
+        return B.ts_hc_exit_logits(FAKE, out, prev, prev_stride, FAKE, _w(), _w(), lm_head, V, FAKE, logits, M, H_,
+                                   C, L, 1e-6, FAKE, 1 << 30, None)
+
+    assert call(V=0) == B.TS_ERR_INVALID_ARG and "V = 0" in B.ts_hc_last_error()
+    assert call(lm_head=None) == B.TS_ERR_INVALID_ARG and "lm_head is NULL" in B.ts_hc_last_error()
+    assert call(lm_head=FAKE + 8) == B.TS_ERR_INVALID_ARG and "lm_head is not 16-byte" in B.ts_hc_last_error()
+    assert call(logits=FAKE + 2) == B.TS_ERR_INVALID_ARG and "logits is not 4-byte" in B.ts_hc_last_error()
+    assert call(out=FAKE, prev=None) == B.TS_ERR_INVALID_ARG and "prev_inject_w is NULL" in B.ts_hc_last_error()
+    assert call(out=FAKE, prev=FAKE, prev_stride=C - 1) == B.TS_ERR_INVALID_ARG
+    assert call(M=0, lm_head=None, logits=None) == B.TS_OK
+
+
 def test_mixer_rejects(lib):
     st = B.ts_hc_mixer(None, FAKE, _w(), _w(), FAKE, 1, H, C, L, 1e-6, FAKE, 1 << 20, None)
     assert st == B.TS_ERR_INVALID_ARG and "raw is NULL" in B.ts_hc_last_error()

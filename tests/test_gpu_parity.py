@@ -479,6 +479,71 @@ def test_stack_driver_rejects_bad_sublayer_outputs():
     assert B.device_status() == B.TS_OK
 
 
+@pytest.mark.parametrize("M,H,C,L,kind", [(1, 2560, 4, 320, "bf16"), (1, 256, 4, 32, "bf16"), (3, 256, 4, 32, "bf16"),
+                                          (16, 2560, 4, 320, "bf16"), (1, 2560, 4, 320, "int4"),
+                                          (64, 2560, 4, 320, "int4"), (3, 40, 3, 24, "bf16")])
+@pytest.mark.parametrize("with_inject", [True, False])
+def test_entry_call_is_replicate_then_call(M, H, C, L, kind, with_inject):
+    """The entry replication fused into the first call (one-token, cluster and tensor-core
+    paths) equals ts_hc_replicate_entry followed by ts_hc_call / ts_hc_mixer, bit for bit."""
+    w = inputs.make_hc_weights(H, C, L, 800 + M, kind=kind, with_inject=with_inject).to("cuda")
+    emb = inputs.make_embedding(M, H, 800 + M).cuda()
+    raw_a = B.hc_replicate_entry(emb, C=C)
+    if with_inject:
+        mixed_a, gates_a = B.hc_call(raw_a, w, H=H, C=C)
+    else:
+        mixed_a, gates_a = B.hc_mixer(raw_a, w, H=H, C=C), None
+    raw_b, rwhole = guarded((M, C * H), torch.bfloat16, -3.0)
+    _, mixed_b, gates_b = B.hc_entry_call(emb, w, C=C, raw=raw_b)
+    torch.cuda.synchronize()
+    assert guard_intact(rwhole, M * C * H, -3.0), "write past the end of raw"
+    assert torch.equal(raw_b, raw_a) and torch.equal(raw_b, emb.repeat(1, C))
+    assert torch.equal(mixed_b, mixed_a)
+    if with_inject:
+        assert torch.equal(gates_b, gates_a)
+    assert B.device_status() == B.TS_OK
+
+
+# The lm_head reads mixed as stored (bf16). The kernels' mixed may sit one bf16
+# rounding step away from the oracle's rounded mixed in a few elements (a
+# decision at a tie point); each such element moves a logit by |w[v][h]| times
+# that step, so the logits keep the chained fp32 floor (1e-3 of their RMS).
+EXIT_CASES = [(1, 2560, 4, 320, 1000), (1, 2560, 4, 320, 32768), (5, 2560, 4, 320, 1000), (20, 2560, 4, 320, 500),
+              (3, 256, 4, 32, 777), (1, 256, 4, 32, 152)]
+
+
+@pytest.mark.parametrize("M,H,C,L,V", EXIT_CASES)
+def test_exit_logits(orc, M, H, C, L, V):
+    """The decoder's exit: the last inject-add fused in front of the mixer, then lm_head
+    (one-token, cluster and tensor-core mixers; one and two 16-token lm_head tiles;
+    vocabularies that leave the last CTA's row block ragged)."""
+    w = inputs.make_hc_weights(H, C, L, 900 + M, with_inject=False)
+    lm = inputs.bf16_normal((V, H), 900 + V, std=0.02)
+    raw = inputs.make_residual(M, H, C, 900 + M)
+    out = inputs.make_sublayer_out(M, H, 900 + M)
+    gate = torch.rand((M, C), generator=torch.Generator().manual_seed(M)) * 2
+    ref_raw = orc.round_to_bf16(orc.inject_add(raw, out, gate.double().numpy(), H=H, C=C))
+    ref_mixed = orc.mixer(ref_raw, w.g, w.down, w.up, H=H, C=C, L=L, eps=EPS)["mixed"]
+    ref_logits = orc.lm_head(orc.round_to_bf16(ref_mixed), lm)
+    w_d, lm_d = w.to("cuda"), lm.cuda()
+    raw_d = raw.cuda()
+    logits, lwhole = guarded((M, V), torch.float32, float("nan"))
+    mixed, logits = B.hc_exit_logits(raw_d, w_d, lm_d, H=H, C=C, out=out.cuda(), prev_inject_w=gate.cuda(),
+                                     logits=logits, eps=EPS)
+    torch.cuda.synchronize()
+    assert guard_intact(lwhole, M * V, float("nan")), "write past the end of the logits"
+    check_bf16(raw_d, ref_raw, "residual after the fused inject-add")
+    check_bf16(mixed, ref_mixed, "exit mixer output")
+    check_fp32(logits, ref_logits, "logits", floor=CHAINED_RMS_FLOOR)
+    # the same exit without the fused inject-add, on the injected residual: bit for bit
+    raw2 = raw.cuda()
+    B.hc_inject_add(raw2, out.cuda(), gate.cuda(), H=H, C=C)
+    mixed2, logits2 = B.hc_exit_logits(raw2, w_d, lm_d, H=H, C=C, eps=EPS)
+    torch.cuda.synchronize()
+    assert torch.equal(raw2, raw_d) and torch.equal(mixed2, mixed) and torch.equal(logits2, logits)
+    assert B.device_status() == B.TS_OK
+
+
 def test_replicate_entry():
     emb = inputs.make_embedding(3, 256, 5).cuda()
     raw, whole = guarded((3, 4 * 256), torch.bfloat16, -9.0)
