@@ -31,6 +31,7 @@ from typing import List, Optional, Tuple
 import torch
 
 G_ID, DOWN_ID, UP_ID, INJECT_ID, RAW_ID, OUT_ID, EMB_ID = range(7)
+PLE_TABLE_ID, PLE_KEY_ID, PLE_VALUE_ID, PLE_NORMS_ID, PLE_CONV_ID, PLE_ROWS_ID, PLE_STATE_ID = range(7, 14)
 
 
 def tensor_seed(config_seed: int, set_index: int, tensor_id: int) -> int:
@@ -192,3 +193,46 @@ def make_stack(M: int, H: int, C: int, L: int, n_layers: int, config_seed: int,
                      make_sublayer_out(M, H, config_seed, 2 * l + 1)))
     final = make_hc_weights(H, C, L, config_seed, 2 * n_layers, kind, with_inject=False)
     return StackInputs(emb, layers, outs, final)
+
+
+@dataclass
+class PleWeights:
+    """The PLE module's tensors (families/qwen4/mod.rs, "## PLE"): a synthetic
+    embedding table of n_rows rows of H/16, key_proj [C*H][H], value_proj [H][H],
+    the three norm scales [C*H] and the depthwise conv taps [C*H][4] (bf16)."""
+    table: torch.Tensor
+    key_proj: torch.Tensor
+    value_proj: torch.Tensor
+    norm_key: torch.Tensor
+    norm_query: torch.Tensor
+    norm_conv: torch.Tensor
+    conv_w: torch.Tensor
+
+    def to(self, device) -> "PleWeights":
+        return PleWeights(*(t.to(device) for t in (self.table, self.key_proj, self.value_proj, self.norm_key,
+                                                   self.norm_query, self.norm_conv, self.conv_w)))
+
+
+def make_ple_weights(H: int, C: int, config_seed: int, n_rows: int = 4096, std: float = 0.02) -> PleWeights:
+    """Synthetic PLE weights: table rows N(0, 1), projections N(0, std), norm
+    scales 1 + N(0, 0.1), conv taps N(0, 0.5) (bf16)."""
+    W = C * H
+    s = lambda tid, k=0: tensor_seed(config_seed, k, tid)
+    return PleWeights(bf16_normal((n_rows, H // 16), s(PLE_TABLE_ID)),
+                      bf16_normal((W, H), s(PLE_KEY_ID), std=std), bf16_normal((H, H), s(PLE_VALUE_ID), std=std),
+                      bf16_normal((W,), s(PLE_NORMS_ID, 0), std=0.1, mean=1.0),
+                      bf16_normal((W,), s(PLE_NORMS_ID, 1), std=0.1, mean=1.0),
+                      bf16_normal((W,), s(PLE_NORMS_ID, 2), std=0.1, mean=1.0),
+                      bf16_normal((W, 4), s(PLE_CONV_ID), std=0.5))
+
+
+def make_ple_rows(M: int, n_rows: int, config_seed: int) -> torch.Tensor:
+    """16 row ids per token, uniform in [0, n_rows) (int32 [M][16])."""
+    gen = torch.Generator(device="cpu").manual_seed(tensor_seed(config_seed, 0, PLE_ROWS_ID))
+    return torch.randint(0, n_rows, (M, 16), generator=gen, dtype=torch.int32)
+
+
+def make_ple_state(H: int, C: int, config_seed: int) -> torch.Tensor:
+    """The conv inputs of 9 earlier tokens, N(0, 1) fp32 [9][C*H]."""
+    gen = torch.Generator(device="cpu").manual_seed(tensor_seed(config_seed, 0, PLE_STATE_ID))
+    return torch.randn((9, C * H), generator=gen, dtype=torch.float32)

@@ -18,6 +18,8 @@ the way the turbospark-runtime 0.3.0 pages describe:
 * ``stack``: families/qwen4/mod.rs decoder-layer pseudocode (entry
   replication, two calls and two inject-adds per layer, the exit mixer).
 * ``lm_head``: the same pseudocode's exit line, logits = lm_head(mixer output).
+* ``ple``: families/qwen4/mod.rs, "## PLE" (layer index 1 only), with the
+  readings listed beside ``orc_ple`` in ``hc_oracle.c``.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` (closed forms,
 invariants, library special cases); ``tests/test_oracle_mutants.py`` plants
@@ -181,6 +183,11 @@ class Oracle:
         lib.orc_hc_call.restype = ctypes.c_int
         lib.orc_inject_add.argtypes = [ctypes.c_int64] * 3 + [_D, _D, _D, ctypes.c_int64, _D]
         lib.orc_replicate_entry.argtypes = [ctypes.c_int64] * 3 + [_D, _D]
+        lib.orc_ple.argtypes = ([ctypes.c_int64] * 3 + [ctypes.c_double, _D, ctypes.c_void_p, ctypes.c_void_p,
+                                                        ctypes.c_int64, ctypes.POINTER(_OrcWeight),
+                                                        ctypes.POINTER(_OrcWeight), _D, _D, _D, ctypes.c_void_p, _D,
+                                                        _D, _D, _D, _D, _D, _D, ctypes.c_int])
+        lib.orc_ple.restype = ctypes.c_int
         self.lib = lib
 
     # ------------------------------------------------------------ scalars
@@ -282,6 +289,45 @@ class Oracle:
         w = _LinearBf16(V, H, lm_head_w)
         return np.stack([self.gemv(w, mixed[m], threads=threads or default_threads())
                          for m in range(mixed.shape[0])])
+
+    def ple(self, hidden, rows, table, key_proj, value_proj, norm_key, norm_query, norm_conv, conv_w, state, *,
+            H: int, C: int, eps: float = RMS_EPS, threads: Optional[int] = None) -> dict:
+        """The PLE gate on M consecutive tokens of one sequence (families/qwen4/mod.rs,
+        "## PLE"): hidden + gv + silu(dilated_conv(norm_conv(gv))).
+
+        hidden [M, C*H] values; rows int [M, 16]; table bf16 [n_rows, H/16];
+        key_proj bf16 [C*H, H]; value_proj bf16 [H, H]; norm_key / norm_query /
+        norm_conv [C*H]; conv_w bf16 [C*H, 4]; state [9, C*H] (the conv inputs of
+        the 9 tokens before the chunk, oldest first). Returns float64 ``result``
+        [M, C*H] (hidden + out, unrounded), ``state`` [9, C*H] after the chunk, and
+        the intermediates ``key`` [M, C*H] (normed), ``value`` [M, H], ``gate``
+        [M, C] (after the sigmoid), ``x`` [M, C*H] (the conv input).
+        """
+        W = C * H
+        hidden = _f64(hidden).reshape(-1, W)
+        M = hidden.shape[0]
+        rows = np.ascontiguousarray(np.asarray(rows.cpu() if hasattr(rows, "cpu") else rows, dtype=np.int32))
+        assert rows.shape == (M, 16)
+        table_bits = _np_bits(table).view(np.uint16)
+        conv_bits = _np_bits(conv_w).view(np.uint16)
+        assert conv_bits.shape == (W, 4) and table_bits.shape[1] == H // 16
+        mk = _weight(_LinearBf16(W, H, key_proj))
+        mv = _weight(_LinearBf16(H, H, value_proj))
+        nk, nq, nc = (_f64(v).reshape(W) for v in (norm_key, norm_query, norm_conv))
+        state = _f64(state).reshape(9, W)
+        result = np.empty((M, W))
+        state_out = np.empty((9, W))
+        key = np.empty((M, W))
+        value = np.empty((M, H))
+        gate = np.empty((M, C))
+        x = np.empty((M, W))
+        rc = self.lib.orc_ple(M, H, C, eps, _dptr(hidden), rows.ctypes.data, table_bits.ctypes.data,
+                              table_bits.shape[0], _wptr(mk), _wptr(mv), _dptr(nk), _dptr(nq), _dptr(nc),
+                              conv_bits.ctypes.data, _dptr(state), _dptr(result), _dptr(state_out), _dptr(key),
+                              _dptr(value), _dptr(gate), _dptr(x), threads or default_threads())
+        if rc != 0:
+            raise ValueError("oracle: inconsistent PLE arguments")
+        return {"result": result, "state": state_out, "key": key, "value": value, "gate": gate, "x": x}
 
     def replicate_entry(self, emb, *, H: int, C: int) -> np.ndarray:
         emb = _f64(emb).reshape(-1, H)

@@ -10,7 +10,8 @@
  *   [mod]  families/qwen4/mod.rs, module doc:
  *          "## The decoder layer, as pseudocode" (entry replication, the
  *          inject-add, the exit mixer), "THE INJECTION TRAP",
- *          "## Hyper-connections" (the call itself), and `RMS_EPS = 1e-6`.
+ *          "## Hyper-connections" (the call itself), "## PLE" (orc_ple, with
+ *          its own readings), and `RMS_EPS = 1e-6`.
  *   [hc]   families/qwen4/hc.rs, `encode_hyper_connection`: step order, the
  *          weight shapes as (rows = outputs, cols = inputs), the remark that
  *          there are exactly two divisions by C, and the per-token inject row.
@@ -46,6 +47,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define ORC_WEIGHT_BF16 0
@@ -259,4 +261,117 @@ void orc_replicate_entry(int64_t M, int64_t H, int64_t C, const double *emb, dou
         for (int64_t c = 0; c < C; ++c)
             for (int64_t h = 0; h < H; ++h)
                 raw[m * C * H + c * H + h] = emb[m * H + h];
+}
+
+/*
+ * PLE, the per-layer embedding gate on the wide residual ([mod] "## PLE",
+ * layer index 1 only; decoder pseudocode: hidden = hidden + ple(hidden, ids)
+ * before that layer's attn_hc). [mod] warns that this formula, unlike the
+ * hyper-connection one, was not cross-checked against the upstream source.
+ * Readings taken where the section is open:
+ *   P1  The 16 row ids per token (ngram_hash of the token history) are inputs:
+ *       the hash is not on the pages. emb is the concatenation of the 16 table
+ *       rows, each H/16 wide, in row-id order.
+ *   P2  key_proj [C*H][H] and value_proj [H][H] are bias-free [out][in] weights.
+ *   P3  norm_key, norm_query and norm_conv are each "grouped scaled" RMS norms
+ *       of a C*H vector in the hyper-connection norm's form (R1, R2): groups of
+ *       H, eps inside the root, a direct scale with one entry per element.
+ *   P4  gate_c = sum_h key[c][h] * query[c][h] / sqrt(H), then the signed square
+ *       root sign(g) * sqrt(max(|g|, 1e-6)) (sign(0) = 0), then sigmoid.
+ *   P5  gv[c][h] = sigmoid(gate_c) * value[h] (value broadcast to every stream).
+ *   P6  dilated_conv is a depthwise causal convolution along the token axis:
+ *       channel j of token t is sum_{i<4} conv_w[j][i] * x[t - 3*(3 - i)][j],
+ *       x = norm_conv(gv); tokens before the first come from `state` (the x of
+ *       the 9 tokens before this chunk, oldest first), and state_out holds the
+ *       x of the chunk's last 9 tokens (taken from state where M < 9).
+ *   P7  out = gv + silu(conv); the result is hidden + out (the caller stores it).
+ *
+ *   hidden [M][W], rows [M][16], table [n_rows][H/16] (bf16 bits), conv_w [W][4]
+ *   (bf16 bits), norm scales [W] each (values), state [9][W]; outputs: result
+ *   [M][W], state_out [9][W], and optional intermediates key [M][W], value
+ *   [M][H], gate [M][C] (after the sigmoid), x [M][W] (NULL skips).
+ * Returns 0, or -1 on inconsistent arguments (a row id out of range included).
+ */
+int orc_ple(int64_t M, int64_t H, int64_t C, double eps, const double *hidden, const int32_t *rows,
+            const uint16_t *table, int64_t n_rows, const orc_weight *key_proj, const orc_weight *value_proj,
+            const double *norm_key, const double *norm_query, const double *norm_conv,
+            const uint16_t *conv_w, const double *state, double *result, double *state_out,
+            double *key_out, double *value_out, double *gate_out, double *x_out, int nthreads)
+{
+    const int64_t W = C * H, seg = H / 16;
+    if (M < 0 || H < 16 || H % 16 != 0 || C < 1)
+        return -1;
+    if (key_proj->rows != W || key_proj->cols != H || value_proj->rows != H || value_proj->cols != H)
+        return -1;
+    double *xs = (double *)malloc(sizeof(double) * (size_t)(M + 9) * (size_t)W);  /* state, then the chunk's x */
+    if (!xs)
+        return -1;
+    memcpy(xs, state, sizeof(double) * 9 * (size_t)W);
+    for (int64_t m = 0; m < M; ++m) {
+        double emb[H], key[W], value[H], query[W], gv[W];
+        /* emb = concat(table[rows[h]] for h in 0..16)   (P1) */
+        for (int64_t r = 0; r < 16; ++r) {
+            const int64_t id = rows[m * 16 + r];
+            if (id < 0 || id >= n_rows) {
+                free(xs);
+                return -1;
+            }
+            for (int64_t e = 0; e < seg; ++e)
+                emb[r * seg + e] = orc_bf16_value(table[id * seg + e]);
+        }
+        /* key = norm_key(key_proj(emb)), value = value_proj(emb)   (P2, P3) */
+        orc_gemv(key_proj, emb, key, nthreads);
+        orc_gemv(value_proj, emb, value, nthreads);
+        const double *hm = hidden + m * W;
+        double gate[C];
+        for (int64_t c = 0; c < C; ++c) {
+            double sk = 0.0, sq = 0.0;
+            for (int64_t h = 0; h < H; ++h) {
+                sk += key[c * H + h] * key[c * H + h];
+                sq += hm[c * H + h] * hm[c * H + h];
+            }
+            const double rk = 1.0 / sqrt(sk / (double)H + eps), rq = 1.0 / sqrt(sq / (double)H + eps);
+            double dot = 0.0;
+            for (int64_t h = 0; h < H; ++h) {
+                const double kn = key[c * H + h] * rk * norm_key[c * H + h];
+                query[c * H + h] = hm[c * H + h] * rq * norm_query[c * H + h];
+                dot += kn * query[c * H + h];
+                key[c * H + h] = kn;
+            }
+            /* gate = (key * query).sum(-1) / sqrt(H), signed square root   (P4) */
+            const double g = dot / sqrt((double)H);
+            const double sg = (g > 0.0) - (g < 0.0);
+            gate[c] = sigmoid(sg * sqrt(fmax(fabs(g), 1e-6)));
+        }
+        /* gv = sigmoid(gate) * value, x = norm_conv(gv)   (P5, P3) */
+        double *x = xs + (9 + m) * W;
+        for (int64_t c = 0; c < C; ++c) {
+            double sv = 0.0;
+            for (int64_t h = 0; h < H; ++h) {
+                gv[c * H + h] = gate[c] * value[h];
+                sv += gv[c * H + h] * gv[c * H + h];
+            }
+            const double r = 1.0 / sqrt(sv / (double)H + eps);
+            for (int64_t h = 0; h < H; ++h)
+                x[c * H + h] = gv[c * H + h] * r * norm_conv[c * H + h];
+        }
+        /* out = gv + silu(dilated_conv(x)); result = hidden + out   (P6, P7) */
+        for (int64_t j = 0; j < W; ++j) {
+            double y = 0.0;
+            for (int64_t i = 0; i < 4; ++i)
+                y += orc_bf16_value(conv_w[j * 4 + i]) * xs[(9 + m - 3 * (3 - i)) * W + j];
+            result[m * W + j] = hm[j] + (gv[j] + silu(y));
+        }
+        if (key_out)
+            memcpy(key_out + m * W, key, sizeof(double) * (size_t)W);
+        if (value_out)
+            memcpy(value_out + m * H, value, sizeof(double) * (size_t)H);
+        if (gate_out)
+            memcpy(gate_out + m * C, gate, sizeof(double) * (size_t)C);
+        if (x_out)
+            memcpy(x_out + m * W, x, sizeof(double) * (size_t)W);
+    }
+    memcpy(state_out, xs + M * W, sizeof(double) * 9 * (size_t)W);
+    free(xs);
+    return 0;
 }

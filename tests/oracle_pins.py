@@ -451,4 +451,77 @@ def pin_lm_head(orc):
     _close(orc.lm_head(mixed, w), mixed @ w.double().numpy().T, what="lm_head vs numpy")
 
 
+def _ple_case(rng, M=11, H=16, C=2, n_rows=20, key_std=0.3):
+    W = C * H
+    return dict(hidden=_randn(rng, M, W), rows=torch.as_tensor(rng.integers(0, n_rows, (M, 16)), dtype=torch.int32),
+                table=_randn(rng, n_rows, H // 16), key_proj=_randn(rng, W, H, std=key_std),
+                value_proj=_randn(rng, H, H, std=0.3), norm_key=_bf(1 + 0.1 * rng.standard_normal(W)),
+                norm_query=_bf(1 + 0.1 * rng.standard_normal(W)), norm_conv=_bf(1 + 0.1 * rng.standard_normal(W)),
+                conv_w=_randn(rng, W, 4, std=0.5), state=torch.as_tensor(rng.standard_normal((9, W))), H=H, C=C)
+
+
+def _ple_torch(hidden, rows, table, key_proj, value_proj, norm_key, norm_query, norm_conv, conv_w, state, H, C):
+    """The PLE in torch fp64 library calls: indexing for the table rows, F.linear,
+    F.rms_norm per stream, F.conv1d (dilation 3, one group per channel) over the
+    state followed by the chunk."""
+    d = lambda t: torch.as_tensor(t).double()
+    M, W = hidden.shape
+    hid = d(hidden)
+    emb = d(table)[rows.long()].reshape(M, H)
+    gnorm = lambda x, s: (F.rms_norm(x.view(-1, C, H), (H,), eps=EPS) * d(s).view(C, H)).reshape(-1, W)
+    key = gnorm(F.linear(emb, d(key_proj)), norm_key).view(M, C, H)
+    value = F.linear(emb, d(value_proj))
+    query = gnorm(hid, norm_query).view(M, C, H)
+    g = (key * query).sum(-1) / math.sqrt(H)
+    gate = torch.sigmoid(torch.sign(g) * torch.sqrt(torch.clamp(g.abs(), min=1e-6)))
+    gv = (gate.unsqueeze(-1) * value.unsqueeze(1)).reshape(M, W)
+    x = gnorm(gv, norm_conv)
+    seq = torch.cat([d(state), x], dim=0).t().unsqueeze(0)          # [1, W, 9 + M]
+    y = F.conv1d(seq, d(conv_w).unsqueeze(1), dilation=3, groups=W)  # [1, W, M]
+    out = gv + F.silu(y[0].t())
+    return {"result": hid + out, "gate": gate, "x": x, "state": torch.cat([d(state), x])[-9:],
+            "value": value, "key": key.reshape(M, W)}
+
+
+def pin_ple_library_formulation(orc):
+    rng = np.random.default_rng(21)
+    for key_std in (0.3, 1e-9):  # the second keeps |gate| below the 1e-6 floor of the signed root
+        case = _ple_case(rng, key_std=key_std)
+        got = orc.ple(**case)
+        want = _ple_torch(**case)
+        for k in ("result", "gate", "x", "state", "value", "key"):
+            _close(got[k], want[k].numpy(), rtol=1e-11, atol=1e-13, what=f"PLE {k} (key std {key_std})")
+
+
+def pin_ple_zero_key_gives_half_gate(orc):
+    """A zero key projection: the normed key is zero, the gate's dot is zero, the
+    signed root of zero is zero and the gate is sigmoid(0) = 1/2 exactly; gv is
+    value / 2 in every stream."""
+    rng = np.random.default_rng(22)
+    case = _ple_case(rng)
+    case["key_proj"] = torch.zeros_like(case["key_proj"])
+    got = orc.ple(**case)
+    assert np.all(got["gate"] == 0.5), "zero key: gate = sigmoid(0)"
+    H, C = case["H"], case["C"]
+    value = got["value"]
+    gv = np.repeat(0.5 * value[:, None, :], C, axis=1).reshape(-1, C * H)
+    d = torch.as_tensor(gv)
+    x = (F.rms_norm(d.view(-1, C, H), (H,), eps=EPS) * case["norm_conv"].double().view(C, H)).reshape(-1, C * H)
+    _close(got["x"], x.numpy(), rtol=1e-12, atol=1e-14, what="zero key: conv input = norm_conv(value / 2)")
+
+
+def pin_ple_state_carries_across_chunks(orc):
+    """Tokens are one sequence: a chunk of 11 equals chunks of 4 and 7 with the
+    conv state handed over."""
+    rng = np.random.default_rng(23)
+    case = _ple_case(rng)
+    whole = orc.ple(**case)
+    a = dict(case, hidden=case["hidden"][:4], rows=case["rows"][:4])
+    ra = orc.ple(**a)
+    b = dict(case, hidden=case["hidden"][4:], rows=case["rows"][4:], state=ra["state"])
+    rb = orc.ple(**b)
+    assert np.array_equal(np.concatenate([ra["result"], rb["result"]]), whole["result"])
+    assert np.array_equal(rb["state"], whole["state"])
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

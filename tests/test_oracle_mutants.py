@@ -63,6 +63,23 @@ MUTANTS = {
                            "v = ldexp((double)(128 + mantissa), exponent - 133);"),
     "rounding ties away from zero": ("double r = nearbyint(scaled);", "double r = round(scaled);"),
     "gemv drops the last column": ("for (int64_t i = 0; i < cols; ++i)", "for (int64_t i = 0; i + 1 < cols; ++i)"),
+    "PLE conv norm with eps outside the root": ("1.0 / sqrt(sv / (double)H + eps)", "1.0 / sqrt(sv / (double)H) + eps"),
+    "PLE key norm over the whole vector": ("sk += key[c * H + h] * key[c * H + h];", "sk += key[h] * key[h];"),
+    "PLE conv without dilation": ("xs[(9 + m - 3 * (3 - i)) * W + j]", "xs[(9 + m - (3 - i)) * W + j]"),
+    "PLE conv taps reversed": ("orc_bf16_value(conv_w[j * 4 + i])", "orc_bf16_value(conv_w[j * 4 + 3 - i])"),
+    "PLE gate root without sign": ("gate[c] = sigmoid(sg * sqrt(fmax(fabs(g), 1e-6)));",
+                                   "gate[c] = sigmoid(sqrt(fmax(fabs(g), 1e-6)));"),
+    "PLE gate root floor dropped": ("gate[c] = sigmoid(sg * sqrt(fmax(fabs(g), 1e-6)));",
+                                    "gate[c] = sigmoid(sg * sqrt(fabs(g)));"),
+    "PLE gate without 1/sqrt(H)": ("const double g = dot / sqrt((double)H);", "const double g = dot;"),
+    "PLE query from the raw residual": ("dot += kn * query[c * H + h];", "dot += kn * hm[c * H + h];"),
+    "PLE residual add dropped": ("result[m * W + j] = hm[j] + (gv[j] + silu(y));",
+                                 "result[m * W + j] = gv[j] + silu(y);"),
+    "PLE silu dropped": ("result[m * W + j] = hm[j] + (gv[j] + silu(y));", "result[m * W + j] = hm[j] + (gv[j] + y);"),
+    "PLE value to stream 0 only": ("gv[c * H + h] = gate[c] * value[h];",
+                                   "gv[c * H + h] = c == 0 ? gate[c] * value[h] : 0.0;"),
+    "PLE table row order": ("emb[r * seg + e] = orc_bf16_value(table[id * seg + e]);",
+                            "emb[(15 - r) * seg + e] = orc_bf16_value(table[id * seg + e]);"),
 }
 
 
