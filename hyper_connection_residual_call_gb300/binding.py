@@ -29,7 +29,7 @@ RMS_EPS = 1e-6  # families/qwen4/mod.rs, RMS_EPS
 
 EXPORTS = ("ts_hc_workspace_bytes", "ts_hc_workspace_layout", "ts_hc_call", "ts_hc_inject_add",
            "ts_hc_mixer", "ts_hc_call_debug", "ts_hc_inject_call", "ts_hc_entry_call", "ts_hc_exit_logits",
-           "ts_hc_replicate_entry",
+           "ts_hc_replicate_entry", "ts_hc_ple_workspace_bytes", "ts_hc_ple_workspace_layout", "ts_hc_ple",
            "ts_hc_last_error",
            "ts_hc_device_status", "ts_hc_call_noalloc", "ts_hc_stack_workspace_bytes", "ts_hc_stack",
            "ts_hc_selftest_timeout")
@@ -100,6 +100,12 @@ def library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.ts_hc_entry_call.restype = i
         lib.ts_hc_exit_logits.argtypes = [vp, vp, vp, l, vp, wp, wp, vp, i, vp, vp, i, i, i, i, f, vp, sz, vp]
         lib.ts_hc_exit_logits.restype = i
+        lib.ts_hc_ple_workspace_bytes.argtypes = [i, i, i]
+        lib.ts_hc_ple_workspace_bytes.restype = sz
+        lib.ts_hc_ple_workspace_layout.argtypes = [i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz), ctypes.POINTER(sz)]
+        lib.ts_hc_ple_workspace_layout.restype = i
+        lib.ts_hc_ple.argtypes = [vp, vp, vp, l, vp, vp, vp, vp, vp, vp, vp, i, i, i, f, vp, sz, vp]
+        lib.ts_hc_ple.restype = i
         lib.ts_hc_call_noalloc.argtypes = [vp, vp, wp, wp, wp, vp, vp, l, i, i, i, i, f, vp]
         lib.ts_hc_call_noalloc.restype = i
         lib.ts_hc_replicate_entry.argtypes = [vp, vp, i, i, i, vp]
@@ -178,6 +184,23 @@ def ts_hc_exit_logits(raw, out, prev_inject_w, prev_inject_stride, hc_norm_w, do
     return library().ts_hc_exit_logits(raw, out, prev_inject_w, prev_inject_stride, hc_norm_w, _wref(down), _wref(up),
                                        lm_head, V, mixed, logits, M, H, C, lowrank, eps, workspace, workspace_bytes,
                                        stream)
+
+
+def ts_hc_ple_workspace_bytes(M: int, H: int, C: int) -> int:
+    return library().ts_hc_ple_workspace_bytes(M, H, C)
+
+
+def ts_hc_ple_workspace_layout(M: int, H: int, C: int) -> Tuple[int, int, int]:
+    a, b, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(library().ts_hc_ple_workspace_layout(M, H, C, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
+    return a.value, b.value, c.value
+
+
+def ts_hc_ple(hidden, rows, table, n_rows, key_proj, value_proj, norm_key_w, norm_query_w, norm_conv_w, conv_w,
+              conv_state, M, H, C, eps, workspace, workspace_bytes, stream) -> int:
+    """The PLE gate added to the wide residual (in place), for M consecutive tokens."""
+    return library().ts_hc_ple(hidden, rows, table, n_rows, key_proj, value_proj, norm_key_w, norm_query_w,
+                               norm_conv_w, conv_w, conv_state, M, H, C, eps, workspace, workspace_bytes, stream)
 
 
 def ts_hc_call_noalloc(raw, hc_norm_w, down, up, inject, mixed, inject_w, inject_stride, M, H, C, lowrank,
@@ -472,6 +495,35 @@ def hc_exit_logits(raw, weights, lm_head, *, H: int, C: int, out=None, prev_inje
                            ws.numel() * ws.element_size(), _stream_handle(stream))
     _check(st)
     return mixed, logits
+
+
+def hc_ple(hidden, rows, weights, conv_state, *, C: int, eps: float = RMS_EPS, ws=None, stream=None):
+    """The PLE gate on hidden [M, C*H] bf16 (in place) for M consecutive tokens of one
+    sequence. ``rows`` int32 [M, 16] table row ids; ``weights`` has table, key_proj,
+    value_proj, norm_key, norm_query, norm_conv, conv_w; ``conv_state`` fp32 [9, C*H]
+    (updated). Returns (hidden, the workspace)."""
+    torch = _torch()
+    M = hidden.shape[0]
+    H = weights.value_proj.shape[0]
+    W = C * H
+    _need(hidden, "hidden", torch.bfloat16, (M, W))
+    _need(rows, "rows", torch.int32, (M, 16))
+    _need(weights.table, "table", torch.bfloat16)
+    _need(weights.key_proj, "key_proj", torch.bfloat16, (W, H))
+    _need(weights.value_proj, "value_proj", torch.bfloat16, (H, H))
+    for name in ("norm_key", "norm_query", "norm_conv"):
+        _need(getattr(weights, name), name, torch.bfloat16, (W,))
+    _need(weights.conv_w, "conv_w", torch.bfloat16, (W, 4))
+    _need(conv_state, "conv_state", torch.float32, (9, W))
+    if ws is None:
+        ws = torch.empty(max(ts_hc_ple_workspace_bytes(M, H, C), 256), dtype=torch.uint8, device=hidden.device)
+    st = ts_hc_ple(hidden.data_ptr(), rows.data_ptr(), weights.table.data_ptr(), weights.table.shape[0],
+                   weights.key_proj.data_ptr(), weights.value_proj.data_ptr(), weights.norm_key.data_ptr(),
+                   weights.norm_query.data_ptr(), weights.norm_conv.data_ptr(), weights.conv_w.data_ptr(),
+                   conv_state.data_ptr(), M, H, C, eps, ws.data_ptr(), ws.numel() * ws.element_size(),
+                   _stream_handle(stream))
+    _check(st)
+    return hidden, ws
 
 
 def hc_replicate_entry(emb, *, C: int, raw=None, stream=None):

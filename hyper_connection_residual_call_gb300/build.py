@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libts_hc.so")
 
-SOURCES = ["ts_hc_api.cu", "ts_hc_stack.cu", "hc_gemv.cu", "hc_tc.cu"]
+SOURCES = ["ts_hc_api.cu", "ts_hc_stack.cu", "hc_gemv.cu", "hc_tc.cu", "hc_ple.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -127,6 +127,24 @@ constexpr int kLmHeadMaxTokens = 16;
 constexpr int kLmHeadThreads = 384;  // 12 warps: one row of a stage each
 constexpr size_t kLmHeadSmem = 160 * 1024;
 
+// The PLE gate on the wide residual (hc_ple.cu).
+struct PleParams {
+    uint16_t *hidden;            // bf16 [M][C*H], read and written
+    const int32_t *rows;         // [M][16] table row ids
+    const uint16_t *table;       // bf16 [n_rows][H/16]
+    long n_rows;
+    const uint16_t *key_proj;    // bf16 [C*H][H]
+    const uint16_t *value_proj;  // bf16 [H][H]
+    const uint16_t *norm_key, *norm_query, *norm_conv;  // bf16 [C*H]
+    const uint16_t *conv_w;      // bf16 [C*H][4], 8-byte aligned rows
+    float *state;                // fp32 [9][C*H], read and written
+    uint16_t *emb;               // workspace: bf16 [M][H]
+    float *key, *value, *gate, *x;  // workspace: [M][C*H], [M][H], [M][C], [M][C*H]
+    int M, H, C;
+    float eps, inv_H, inv_sqrt_H;
+    unsigned *status;
+};
+
 struct LaunchCfg {
     int sm_count;
     bool pdl;                 // launch as a programmatic dependent of the previous kernel
@@ -153,6 +171,7 @@ cudaError_t launch_inject(const InjectParams &p, const LaunchCfg &cfg, cudaStrea
 // Fills rows_per_cta, rs and n_stages for M tokens; false if H is too wide for the ring.
 bool lm_head_plan(LmHeadParams &p, int sm_count);
 cudaError_t launch_lm_head(const LmHeadParams &p, const LaunchCfg &cfg, cudaStream_t stream);
+cudaError_t launch_ple(const PleParams &p, const LaunchCfg &cfg, cudaStream_t stream);
 cudaError_t launch_replicate(const ReplicateParams &p, const LaunchCfg &cfg, cudaStream_t stream);
 
 }  // namespace tshc

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -646,6 +647,123 @@ ts_status ts_hc_exit_logits(void *raw, const void *out, const float *prev_inject
         if (e != cudaSuccess)
             return cuda_fail(e, "launching the lm_head kernel");
     }
+    return TS_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+struct PleWs {
+    size_t emb, key, value, gate, x, total;
+};
+
+PleWs ple_ws(int M, int H, int C)
+{
+    PleWs w{};
+    const size_t m = (size_t)M, W = (size_t)C * H;
+    w.emb = 0;
+    w.key = align256(2 * m * H);
+    w.value = w.key + align256(4 * m * W);
+    w.gate = w.value + align256(4 * m * H);
+    w.x = w.gate + align256(4 * m * C);
+    w.total = w.x + align256(4 * m * W);
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ts_hc_ple_workspace_bytes(int M, int H, int C)
+{
+    if (M < 0 || H < 128 || H % 128 != 0 || H > kMaxH || C < 1 || C > kMaxC)
+        return 0;
+    return ple_ws(M, H, C).total;
+}
+
+ts_status ts_hc_ple_workspace_layout(int M, int H, int C, size_t *value_offset, size_t *gate_offset,
+                                     size_t *x_offset)
+{
+    if (ts_hc_ple_workspace_bytes(M, H, C) == 0 && M != 0)
+        return fail(TS_ERR_INVALID_ARG, "invalid PLE shape");
+    const PleWs w = ple_ws(M, H, C);
+    if (value_offset) *value_offset = w.value;
+    if (gate_offset) *gate_offset = w.gate;
+    if (x_offset) *x_offset = w.x;
+    return TS_OK;
+}
+
+ts_status ts_hc_ple(void *hidden, const int32_t *rows, const void *table, long n_rows, const void *key_proj,
+                    const void *value_proj, const void *norm_key_w, const void *norm_query_w,
+                    const void *norm_conv_w, const void *conv_w, float *conv_state, int M, int H, int C,
+                    float eps, void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    g_last_error.clear();
+    if (M < 0)
+        return fail(TS_ERR_INVALID_ARG, "M = %d must be >= 0", M);
+    if (H < 128 || H % 128 != 0 || H > kMaxH)
+        return fail(TS_ERR_INVALID_ARG, "H = %d must be a multiple of 128 in [128, %d] (16 table segments of 8k)",
+                    H, kMaxH);
+    if (C < 1 || C > kMaxC)
+        return fail(TS_ERR_INVALID_ARG, "C = %d must be in [1, %d]", C, kMaxC);
+    if (M == 0)  // nothing is read or written: pointers are not examined
+        return TS_OK;
+    if (n_rows < 1)
+        return fail(TS_ERR_INVALID_ARG, "n_rows = %ld must be >= 1", n_rows);
+    ts_status st;
+    if ((st = check_ptr(hidden, "hidden", 16)) != TS_OK) return st;
+    if ((st = check_ptr(rows, "rows", 4)) != TS_OK) return st;
+    if ((st = check_ptr(table, "table", 16)) != TS_OK) return st;
+    if ((st = check_ptr(key_proj, "key_proj", 16)) != TS_OK) return st;
+    if ((st = check_ptr(value_proj, "value_proj", 16)) != TS_OK) return st;
+    if ((st = check_ptr(norm_key_w, "norm_key_w", 16)) != TS_OK) return st;
+    if ((st = check_ptr(norm_query_w, "norm_query_w", 16)) != TS_OK) return st;
+    if ((st = check_ptr(norm_conv_w, "norm_conv_w", 16)) != TS_OK) return st;
+    if ((st = check_ptr(conv_w, "conv_w", 16)) != TS_OK) return st;
+    if ((st = check_ptr(conv_state, "conv_state", 16)) != TS_OK) return st;
+    if (!(eps >= 0.0f) || eps > 1.0f)
+        return fail(TS_ERR_INVALID_ARG, "eps = %g must be in [0, 1]", (double)eps);
+    const PleWs lay = ple_ws(M, H, C);
+    if (!workspace || workspace_bytes < lay.total)
+        return fail(TS_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace_bytes, lay.total);
+    if (!aligned(workspace, 256))
+        return fail(TS_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != TS_OK)
+        return st;
+    tshc::LmHeadParams probe{};
+    probe.M = std::min(M, tshc::kLmHeadMaxTokens);
+    probe.H = H;
+    probe.V = C * H;
+    if (!tshc::lm_head_plan(probe, dev.sm_count))
+        return fail(TS_ERR_UNSUPPORTED, "H = %d is too wide for the projection kernel's ring", H);
+    char *ws = static_cast<char *>(workspace);
+    tshc::PleParams p{};
+    p.hidden = static_cast<uint16_t *>(hidden);
+    p.rows = rows;
+    p.table = static_cast<const uint16_t *>(table);
+    p.n_rows = n_rows;
+    p.key_proj = static_cast<const uint16_t *>(key_proj);
+    p.value_proj = static_cast<const uint16_t *>(value_proj);
+    p.norm_key = static_cast<const uint16_t *>(norm_key_w);
+    p.norm_query = static_cast<const uint16_t *>(norm_query_w);
+    p.norm_conv = static_cast<const uint16_t *>(norm_conv_w);
+    p.conv_w = static_cast<const uint16_t *>(conv_w);
+    p.state = conv_state;
+    p.emb = reinterpret_cast<uint16_t *>(ws + lay.emb);
+    p.key = reinterpret_cast<float *>(ws + lay.key);
+    p.value = reinterpret_cast<float *>(ws + lay.value);
+    p.gate = reinterpret_cast<float *>(ws + lay.gate);
+    p.x = reinterpret_cast<float *>(ws + lay.x);
+    p.M = M; p.H = H; p.C = C;
+    p.eps = eps;
+    p.inv_H = 1.0f / (float)H;
+    p.inv_sqrt_H = 1.0f / sqrtf((float)H);
+    p.status = dev.status;
+    const cudaError_t e = tshc::launch_ple(p, tshc::LaunchCfg{dev.sm_count, true}, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launching the PLE kernels");
     return TS_OK;
 }
 

@@ -247,6 +247,49 @@ ts_status ts_hc_exit_logits(void *raw, const void *out, const float *prev_inject
                             void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * PLE, the per-layer embedding gate on the wide residual (families/qwen4/mod.rs,
+ * "## PLE": added to the residual before layer index 1's attn_hc, and only
+ * there). For M consecutive tokens of one sequence:
+ *   emb   = concat of the 16 table rows rows[m][0..16), each H/16 wide
+ *   key   = norm_key(key_proj(emb))        value = value_proj(emb)
+ *   query = norm_query(hidden)
+ *   gate  = sigmoid(s * sqrt(max(|d|, 1e-6))), d = sum_h key[c][h] query[c][h] / sqrt(H),
+ *           s the sign of d, per stream c
+ *   gv    = gate * value                   (value broadcast to every stream)
+ *   hidden += gv + silu(conv(norm_conv(gv)))    (rounded to bf16, in place)
+ * The norms are grouped RMS norms in the hyper-connection norm's form (groups
+ * of H, eps inside the root, a direct scale per element). conv is depthwise and
+ * causal along the token axis: channel j of token t is
+ * sum_i conv_w[j][i] * x[t - 3*(3 - i)][j], dilation 3, four taps; the inputs
+ * of the 9 tokens before the chunk come from conv_state, which is updated to
+ * the chunk's last 9 (zero it for a new sequence). The page notes that this
+ * formula was not cross-checked upstream; the hash that picks the row ids is
+ * not on the pages, so the caller supplies them.
+ *
+ *   hidden           bf16 [M][C*H], read and written
+ *   rows             int32 [M][16], each in [0, n_rows); an id out of range reads
+ *                    zeros and records TS_ERR_INVALID_ARG in the device status word
+ *   table            bf16 [n_rows][H/16]
+ *   key_proj         bf16 [C*H][H];  value_proj  bf16 [H][H]
+ *   norm_*_w         bf16 [C*H] each
+ *   conv_w           bf16 [C*H][4]
+ *   conv_state       fp32 [9][C*H], oldest token first; read and written
+ *   H                a multiple of 128
+ *   workspace        >= ts_hc_ple_workspace_bytes(M, H, C) bytes, 256-byte
+ *                    aligned; after the call it holds value fp32 [M][H], the
+ *                    gates fp32 [M][C] and the conv input x fp32 [M][C*H] at the
+ *                    offsets ts_hc_ple_workspace_layout() reports
+ */
+size_t ts_hc_ple_workspace_bytes(int M, int H, int C);
+ts_status ts_hc_ple_workspace_layout(int M, int H, int C, size_t *value_offset, size_t *gate_offset,
+                                     size_t *x_offset);
+ts_status ts_hc_ple(void *hidden, const int32_t *rows, const void *table, long n_rows,
+                    const void *key_proj, const void *value_proj, const void *norm_key_w,
+                    const void *norm_query_w, const void *norm_conv_w, const void *conv_w,
+                    float *conv_state, int M, int H, int C, float eps,
+                    void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Entry replication fused into the stack's first call (families/qwen4/mod.rs,
  * decoder pseudocode: the entry line hidden = embed_tokens(ids).repeat(1, 1, C),
  * followed by layer 0's attn_hc). Equivalent, bit for bit, to

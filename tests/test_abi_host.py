@@ -157,6 +157,26 @@ def test_exit_logits_rejects(lib):
     assert call(M=0, lm_head=None, logits=None) == B.TS_OK
 
 
+def test_ple_workspace_and_rejects(lib):
+    a256 = lambda n: (n + 255) // 256 * 256
+    M, W = 3, C * H
+    assert B.ts_hc_ple_workspace_bytes(M, H, C) == (a256(2 * M * H) + a256(4 * M * W) + a256(4 * M * H)
+                                                   + a256(4 * M * C) + a256(4 * M * W))
+    assert B.ts_hc_ple_workspace_bytes(M, 200, C) == 0  # H not a multiple of 128
+
+    def call(hidden=FAKE, rows=FAKE, n_rows=100, H_=H, M_=1, ws_bytes=1 << 30, conv_state=FAKE):
+        return B.ts_hc_ple(hidden, rows, FAKE, n_rows, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, conv_state, M_, H_, C,
+                           1e-6, FAKE, ws_bytes, None)
+
+    assert call(H_=200) == B.TS_ERR_INVALID_ARG and "multiple of 128" in B.ts_hc_last_error()
+    assert call(hidden=None) == B.TS_ERR_INVALID_ARG and "hidden is NULL" in B.ts_hc_last_error()
+    assert call(rows=FAKE + 2) == B.TS_ERR_INVALID_ARG and "rows is not 4-byte" in B.ts_hc_last_error()
+    assert call(n_rows=0) == B.TS_ERR_INVALID_ARG and "n_rows" in B.ts_hc_last_error()
+    assert call(conv_state=FAKE + 4) == B.TS_ERR_INVALID_ARG and "conv_state" in B.ts_hc_last_error()
+    assert call(ws_bytes=16) == B.TS_ERR_WORKSPACE
+    assert call(M_=0, hidden=None, rows=None) == B.TS_OK
+
+
 def test_mixer_rejects(lib):
     st = B.ts_hc_mixer(None, FAKE, _w(), _w(), FAKE, 1, H, C, L, 1e-6, FAKE, 1 << 20, None)
     assert st == B.TS_ERR_INVALID_ARG and "raw is NULL" in B.ts_hc_last_error()
