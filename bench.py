@@ -20,8 +20,10 @@ results read back inside the timed region.
 ``other_configs`` (skipped with --no-configs) times the rest of the workload
 family the same way, each over distinct weight sets: the M=128 prefill
 micro-batch (attn_hc + mlp_hc per batch, tensor-core path), an 8-token decode
-batch, the INT4-affine full shape at M=1 and M=64, and the 40-layer stack
-(entry replication, 80 fused calls, exit mixer) at M=1 and M=16.
+batch, the INT4-affine full shape at M=1 and M=64, the decoder's exit (mixer +
+lm_head at a synthetic vocabulary of 32768) and the PLE gate at M=1 and M=16,
+and the 40-layer stack (entry fused into layer 0, 80 fused calls, exit mixer)
+at M=1 and M=16.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -321,6 +323,24 @@ def bytes_per_call(M: int, weight_bytes: int, inject: bool = True) -> int:
     return b
 
 
+def fused_chain(B, raw, outs, sets, n_calls, mixed, ws, slots):
+    """A body of n_calls dependent fused calls (each applies the previous call's
+    inject-add), then the last inject-add; call i writes its gates to slot i % 2."""
+    def body():
+        for i in range(n_calls):
+            w = sets[i % len(sets)]
+            sl, st = slots[i % 2]
+            if i == 0:
+                B.hc_call(raw, w, H=H, C=C, mixed=mixed, inject_w=sl, inject_stride=st, ws=ws)
+            else:
+                psl, pst = slots[(i - 1) % 2]
+                B.hc_inject_call(raw, outs[(i - 1) % len(outs)], psl, w, H=H, C=C, prev_inject_stride=pst,
+                                 mixed=mixed, inject_w=sl, inject_stride=st, ws=ws)
+        psl, pst = slots[(n_calls - 1) % 2]
+        B.hc_inject_add(raw, outs[(n_calls - 1) % len(outs)], psl, H=H, C=C, inject_stride=pst)
+    return body
+
+
 def measure_other_configs(B, inputs, torch, dev, stream, sets_bf16, peak):
     """The workload family's other configurations, each a CUDA graph over
     distinct weight sets (every pass is larger than the 129 MB L2), timed with
@@ -351,20 +371,7 @@ def measure_other_configs(B, inputs, torch, dev, stream, sets_bf16, peak):
         return e0.elapsed_time(e1) / reps
 
     def chain(raw, outs, gates, sets, n_calls, mixed, ws, slots):
-        """n_calls fused calls; call i writes its gates to slot i % 2 of `gates`."""
-        def body():
-            for i in range(n_calls):
-                w = sets[i % len(sets)]
-                sl, st = slots[i % 2]
-                if i == 0:
-                    B.hc_call(raw, w, H=H, C=C, mixed=mixed, inject_w=sl, inject_stride=st, ws=ws)
-                else:
-                    psl, pst = slots[(i - 1) % 2]
-                    B.hc_inject_call(raw, outs[(i - 1) % len(outs)], psl, w, H=H, C=C, prev_inject_stride=pst,
-                                     mixed=mixed, inject_w=sl, inject_stride=st, ws=ws)
-            psl, pst = slots[(n_calls - 1) % 2]
-            B.hc_inject_add(raw, outs[(n_calls - 1) % len(outs)], psl, H=H, C=C, inject_stride=pst)
-        return body
+        return fused_chain(B, raw, outs, sets, n_calls, mixed, ws, slots)
 
     def record(name, Mx, ms, n_calls, bytes_call, extra=None):
         gbs = bytes_call * n_calls / (ms / 1e3) / 1e9
@@ -415,6 +422,61 @@ def measure_other_configs(B, inputs, torch, dev, stream, sets_bf16, peak):
                {"path": "CUDA-core one-token kernels" if Mq == 1
                 else "tensor-core (tcgen05) kernels, INT4 dequantised to bf16 hi + lo per tile"})
     del sets_q
+
+    # The decoder's exit: the last inject-add fused into the exit mixer, then lm_head
+    # (ts_hc_exit_logits), at a synthetic vocabulary of 32768 rows (the pages give
+    # none). Two lm_head copies of 168 MB alternate, so every call streams its
+    # lm_head from HBM; calls depend on each other through the residual.
+    V = 32768
+    lm = [inputs.bf16_normal((V, H), 9000 + i, std=0.02).to(dev) for i in range(2)]
+    mixers = [inputs.HCWeights(w.g, w.down, w.up, None) for w in sets_bf16[:8]]
+    for Me in (1, 16):
+        raw = inputs.make_residual(Me, H, C, 5).to(dev)
+        oute = [inputs.make_sublayer_out(Me, H, 5, i).to(dev) for i in range(2)]
+        gate = torch.full((Me, C), 0.5, dtype=torch.float32, device=dev)
+        mixed = torch.empty((Me, H), dtype=torch.bfloat16, device=dev)
+        logits = torch.empty((Me, V), dtype=torch.float32, device=dev)
+        ws = B.workspace(Me, H, C, L, dev)
+        n = 16
+
+        def exits():
+            for i in range(n):
+                B.hc_exit_logits(raw, mixers[i % len(mixers)], lm[i % 2], H=H, C=C, out=oute[i % 2], prev_inject_w=gate,
+                                 mixed=mixed, logits=logits, ws=ws)
+
+        ms = graph_ms(exits, 5)
+        # mixer bytes + the write-back of raw, the sublayer output and the gates read,
+        # lm_head once and the logits written
+        b = (bytes_per_call(Me, mixers[0].nbytes, inject=False) + 2 * Me * C * H + 2 * Me * H + 4 * Me * C
+             + V * H * 2 + 4 * Me * V)
+        record(f"exit_logits_m{Me}_v{V}", Me, ms, n, b,
+               {"path": "inject-add fused into the exit mixer, then the lm_head GEMV (dependent launch)",
+                "vocab": V})
+    del lm
+
+    # PLE on the wide residual (ts_hc_ple), four weight sets of 66 MB cycled (264 MB,
+    # more than the 129 MB L2), each call on the residual the previous one left.
+    psets = [inputs.make_ple_weights(H, C, 60 + i, n_rows=4096).to(dev) for i in range(4)]
+    for Mq in (1, 16):
+        hid = inputs.make_residual(Mq, H, C, 6).to(dev)
+        rows = inputs.make_ple_rows(Mq, 4096, 6).to(dev)
+        state = torch.zeros((9, C * H), dtype=torch.float32, device=dev)
+        pws = torch.empty(B.ts_hc_ple_workspace_bytes(Mq, H, C), dtype=torch.uint8, device=dev)
+        n = 8
+
+        def ples():
+            for i in range(n):
+                B.hc_ple(hid, rows, psets[i % 4], state, C=C, ws=pws)
+
+        ms = graph_ms(ples, 5)
+        # key_proj, value_proj, the table rows picked, the three norm scales, the conv
+        # taps, the conv state read and written, the residual read and written, the ids
+        W = C * H
+        b = (W * H * 2 + H * H * 2 + Mq * H * 2 + 3 * W * 2 + W * 4 * 2 + 2 * 9 * W * 4 + 2 * Mq * W * 2
+             + Mq * 16 * 4)
+        record(f"ple_m{Mq}", Mq, ms, n, b,
+               {"path": "row gather, key/value projections (GEMV kernel), gate, causal conv + residual add"})
+    del psets
 
     # Full-depth stack through the native driver (ts_hc_stack): entry replication,
     # 40 x (attn_hc + inject, mlp_hc + inject), exit mixer fused with the last inject-add.
@@ -468,7 +530,8 @@ def run_ours(args):
     outs = torch.stack([o.to(dev) for o in outs_h])          # [sets, M, H]
 
     parity = None
-    if rank == 0 and not (args.profile_calls or args.profile_prefill):
+    if rank == 0 and not (args.profile_calls or args.profile_prefill or args.profile_graph or args.profile_exit
+                          or args.profile_ple):
         parity = parity_check(B, sets[0], sets_h[0], raw_h, outs_h[0])
 
     raw = raw_h.to(dev)
@@ -511,6 +574,58 @@ def run_ours(args):
         stream.synchronize()
         if rank == 0:
             print(f"ran {args.profile_prefill} M={Mp} calls (profiling run)")
+        return
+    if args.profile_exit or args.profile_ple:
+        # Eager exits (mixer + lm_head, vocabulary 32768) or PLE gates at M =
+        # --profile-tokens, for a profiler that captures single launches.
+        Mx = args.profile_tokens
+        hid = inputs.make_residual(Mx, H, C, 5).to(dev)
+        with torch.cuda.stream(stream):
+            if args.profile_exit:
+                lm = inputs.bf16_normal((32768, H), 9000, std=0.02).to(dev)
+                mixer_w = inputs.HCWeights(sets[0].g, sets[0].down, sets[0].up, None)
+                mixedx = torch.empty((Mx, H), dtype=torch.bfloat16, device=dev)
+                logits = torch.empty((Mx, 32768), dtype=torch.float32, device=dev)
+                wsx = B.workspace(Mx, H, C, L, dev)
+                for _ in range(args.profile_exit):
+                    B.hc_exit_logits(hid, mixer_w, lm, H=H, C=C, mixed=mixedx, logits=logits, ws=wsx)
+            else:
+                pw = inputs.make_ple_weights(H, C, 60, n_rows=4096).to(dev)
+                rows = inputs.make_ple_rows(Mx, 4096, 6).to(dev)
+                state = torch.zeros((9, C * H), dtype=torch.float32, device=dev)
+                for _ in range(args.profile_ple):
+                    B.hc_ple(hid, rows, pw, state, C=C)
+        stream.synchronize()
+        if rank == 0:
+            what = "exits" if args.profile_exit else "PLE gates"
+            print(f"ran {args.profile_exit or args.profile_ple} M={Mx} {what} (profiling run)")
+        return
+    if args.profile_graph:
+        # Replays of one CUDA graph of 8 dependent fused M-token calls (the prefill
+        # chain of other_configs), for a profiler that measures whole graphs: DRAM
+        # traffic of the chain as the kernels overlap in it.
+        Mp = args.profile_tokens
+        psets = sets[:8] if not args.profile_int4 else [
+            inputs.make_hc_weights(H, C, L, 4, i, kind="int4").to(dev) for i in range(8)]
+        rawp = inputs.make_residual(Mp, H, C, 2).to(dev)
+        outp = [inputs.make_sublayer_out(Mp, H, 2, i).to(dev) for i in range(2)]
+        gatep = torch.zeros((Mp, 2 * C), dtype=torch.float32, device=dev)
+        slots = [(gatep[:, :C], 2 * C), (gatep[:, C:], 2 * C)]
+        mixedp = torch.empty((Mp, H), dtype=torch.bfloat16, device=dev)
+        wsp2 = B.workspace(Mp, H, C, L, dev)
+        body = fused_chain(B, rawp, outp, psets, 8, mixedp, wsp2, slots)
+        with torch.cuda.stream(stream):
+            body()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            body()
+        with torch.cuda.stream(stream):
+            for _ in range(args.profile_graph):
+                g.replay()
+        stream.synchronize()
+        if rank == 0:
+            print(f"replayed a graph of 8 M={Mp} fused calls {args.profile_graph} times (profiling run)")
         return
     if args.profile_calls:
         # A short eager chain of the fused call for a profiler that captures
@@ -687,6 +802,13 @@ def main():
                     help="run this many eager M-token calls and exit (for ncu captures)")
     ap.add_argument("--profile-tokens", type=int, default=128, help="M for --profile-prefill")
     ap.add_argument("--profile-int4", action="store_true", help="INT4-affine weights for --profile-prefill")
+    ap.add_argument("--profile-exit", type=int, default=0,
+                    help="eager exits (mixer + lm_head at vocabulary 32768) at M = --profile-tokens, for a profiler")
+    ap.add_argument("--profile-ple", type=int, default=0,
+                    help="eager PLE gates at M = --profile-tokens, for a profiler")
+    ap.add_argument("--profile-graph", type=int, default=0,
+                    help="replays of a CUDA graph of 8 fused M-token calls (--profile-tokens, --profile-int4), "
+                         "for a profiler that measures whole graphs; no timing")
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="run this many eager fused calls of the workload and exit (for ncu captures)")
     args = ap.parse_args()

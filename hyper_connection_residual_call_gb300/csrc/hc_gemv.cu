@@ -1094,115 +1094,6 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
         mbar_wait_bounded(bar, 0);
 }
 
-// ---- lm_head after the exit mixer -------------------------------------------
-//
-// logits = lm_head(mixed), no softcap and no further norm (families/qwen4/
-// mod.rs, decoder pseudocode, exit lines). A weight-streaming GEMV: CTA b owns
-// a contiguous block of vocabulary rows, which stream through a ring of
-// n_stages shared-memory stages of rs rows (one bulk copy per stage). The first
-// stages are requested before the dependency wait, so they arrive while the
-// mixer still runs. Warp j dots row j of each stage with every token (lanes
-// over 8-element chunks of h, fixed order), lane 0 writes the logit.
-
-__host__ __device__ inline size_t lm_head_smem(const LmHeadParams &p)
-{
-    return 128 + (size_t)p.n_stages * p.rs * p.H * 2 + round_up_sz((size_t)p.M * p.H * 2, 128);
-}
-
-__global__ void __launch_bounds__(kLmHeadThreads, 3) hc_lm_head_kernel(const LmHeadParams p)
-{
-    extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-    uint64_t *empty = full + 4;
-    const size_t row_bytes = (size_t)p.H * 2;
-    unsigned char *ring = smem + 128;
-    const uint16_t *mixed_s = reinterpret_cast<const uint16_t *>(ring + (size_t)p.n_stages * p.rs * row_bytes);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int kWarps = kLmHeadThreads / 32;
-    const int v0 = blockIdx.x * p.rows_per_cta;
-    const int nrows = max(0, min(p.rows_per_cta, p.V - v0));
-    const int nst = (nrows + p.rs - 1) / p.rs;
-    const int nchunk = p.H / 8;
-
-    if (tid == 0) {
-        for (int s = 0; s < p.n_stages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kWarps);
-        }
-        mbar_fence_init();
-    }
-    __syncthreads();
-    auto load_stage = [&](int i) {  // one thread
-        const int rows = min(p.rs, nrows - i * p.rs);
-        uint64_t *bar = &full[i % p.n_stages];
-        mbar_arrive_expect_tx(bar, (uint32_t)(rows * row_bytes));
-        bulk_copy_g2s(ring + (size_t)(i % p.n_stages) * p.rs * row_bytes, p.w + (size_t)(v0 + i * p.rs) * p.H,
-                      (uint32_t)(rows * row_bytes), bar);
-    };
-    // Weights do not depend on the mixer: the first stages are requested now.
-    if (tid == 0)
-        for (int i = 0; i < min(p.n_stages, nst); ++i)
-            load_stage(i);
-    pdl_launch_dependents();
-    pdl_wait();  // mixed comes from the mixer
-    for (int i = tid; i < p.M * nchunk; i += blockDim.x)
-        reinterpret_cast<uint4 *>(const_cast<uint16_t *>(mixed_s))[i] = reinterpret_cast<const uint4 *>(p.mixed)[i];
-    __syncthreads();
-
-    bool timed_out = false;
-    for (int i = 0; i < nst; ++i) {
-        const int s = i % p.n_stages, u = i / p.n_stages;
-        const int rows = min(p.rs, nrows - i * p.rs);
-        if (!mbar_wait_bounded(&full[s], u & 1))
-            timed_out = true;
-        if (warp < rows) {  // warp-uniform
-            const uint4 *wr = reinterpret_cast<const uint4 *>(ring + ((size_t)s * p.rs + warp) * row_bytes);
-            float acc[kLmHeadMaxTokens];
-#pragma unroll
-            for (int m = 0; m < kLmHeadMaxTokens; ++m) acc[m] = 0.f;
-            for (int c = lane; c < nchunk; c += 32) {
-                float wf[8];
-                unpack_bf16x8(wr[c], wf);
-#pragma unroll
-                for (int m = 0; m < kLmHeadMaxTokens; ++m) {
-                    if (m < p.M) {
-                        float xf[8];
-                        unpack_bf16x8(reinterpret_cast<const uint4 *>(mixed_s + (size_t)m * p.H)[c], xf);
-                        float a = acc[m];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) a = fmaf(wf[e], xf[e], a);
-                        acc[m] = a;
-                    }
-                }
-            }
-            const int v = v0 + i * p.rs + warp;
-#pragma unroll
-            for (int m = 0; m < kLmHeadMaxTokens; ++m) {
-                if (m < p.M) {
-                    const float t = warp_sum(acc[m]);
-                    if (lane == 0)
-                        p.logits[(size_t)m * p.logits_stride + v] = t;
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&empty[s]);
-        // Thread 0 refills this stage once every warp has read it.
-        if (tid == 0 && i + p.n_stages < nst) {
-            if (!mbar_wait_bounded(&empty[s], u & 1))
-                timed_out = true;
-            load_stage(i + p.n_stages);
-        }
-    }
-    if (timed_out) {
-        record_timeout(p.status);
-        // do not leave with a copy into this CTA's shared memory in flight
-        if (tid == 0)
-            for (int i = max(0, nst - p.n_stages); i < nst; ++i)
-                mbar_wait_bounded(&full[i % p.n_stages], (i / p.n_stages) & 1);
-    }
-}
 
 __global__ void __launch_bounds__(256) hc_inject_kernel(const InjectParams p)
 {
@@ -1420,32 +1311,6 @@ cudaError_t launch_one_token(const DownParams &d, const UpParams &u, const Launc
 cudaError_t launch_up(const UpParams &p, const LaunchCfg &cfg, cudaStream_t stream)
 {
     return p.up.type == 0 ? launch_up_wt<0>(p, cfg, stream) : launch_up_wt<1>(p, cfg, stream);
-}
-
-bool lm_head_plan(LmHeadParams &p, int sm_count)
-{
-    if (p.M < 1 || p.M > kLmHeadMaxTokens || p.H % 8 != 0 || p.V < 1)
-        return false;
-    p.n_stages = 2;
-    const size_t fixed = 128 + round_up_sz((size_t)p.M * p.H * 2, 128);
-    if (fixed >= kLmHeadSmem)
-        return false;
-    const size_t per_stage = (kLmHeadSmem - fixed) / p.n_stages;
-    p.rs = (int)std::min<size_t>(kLmHeadThreads / 32, per_stage / ((size_t)p.H * 2));
-    if (p.rs < 1)
-        return false;
-    p.rows_per_cta = (p.V + sm_count - 1) / sm_count;
-    return lm_head_smem(p) <= kLmHeadSmem;
-}
-
-cudaError_t launch_lm_head(const LmHeadParams &p, const LaunchCfg &cfg, cudaStream_t stream)
-{
-    const size_t smem = lm_head_smem(p);
-    const cudaError_t e = allow_smem(hc_lm_head_kernel, smem);
-    if (e != cudaSuccess)
-        return e;
-    const int grid = (p.V + p.rows_per_cta - 1) / p.rows_per_cta;
-    return launch_ex(hc_lm_head_kernel, dim3(grid), dim3(kLmHeadThreads), smem, stream, 0, cfg.pdl, p);
 }
 
 cudaError_t launch_inject(const InjectParams &p, const LaunchCfg &cfg, cudaStream_t stream)

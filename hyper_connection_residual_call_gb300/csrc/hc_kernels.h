@@ -110,22 +110,17 @@ struct ReplicateParams {
     int M, H, C;
 };
 
-// lm_head after the exit mixer: logits[m][v] = sum_h w[v][h] * mixed[m][h].
-// CTA b owns vocabulary rows [b * rows_per_cta, ...); they stream through a
-// ring of n_stages stages of rs rows each (bulk copies), and warp j of the
-// block dots row j of a stage with every token.
+// lm_head after the exit mixer: logits[m][v] = sum_h w[v][h] * mixed[m][h], on
+// the tensor cores (hc_tc.cu): 128-row vocabulary tiles against the token rows.
 struct LmHeadParams {
     const uint16_t *mixed;    // bf16 [M][H]
     const uint16_t *w;        // bf16 [V][H]
     float *logits;            // fp32 token m's logits at logits + m * logits_stride
     long logits_stride;
     int M, H, V;              // M <= kLmHeadMaxTokens
-    int rows_per_cta, rs, n_stages;
     unsigned *status;
 };
 constexpr int kLmHeadMaxTokens = 16;
-constexpr int kLmHeadThreads = 384;  // 12 warps: one row of a stage each
-constexpr size_t kLmHeadSmem = 160 * 1024;
 
 // The PLE gate on the wide residual (hc_ple.cu).
 struct PleParams {
@@ -169,7 +164,9 @@ cudaError_t launch_one_token(const DownParams &d, const UpParams &u, const Launc
 cudaError_t launch_up(const UpParams &p, const LaunchCfg &cfg, cudaStream_t stream);
 cudaError_t launch_inject(const InjectParams &p, const LaunchCfg &cfg, cudaStream_t stream);
 // Fills rows_per_cta, rs and n_stages for M tokens; false if H is too wide for the ring.
-bool lm_head_plan(LmHeadParams &p, int sm_count);
+// Shapes the lm_head kernel takes: 1 <= M <= kLmHeadMaxTokens, H a multiple of 8
+// (16-byte rows for TMA), V >= 1.
+bool lm_head_shape_ok(int M, int H, int V);
 cudaError_t launch_lm_head(const LmHeadParams &p, const LaunchCfg &cfg, cudaStream_t stream);
 cudaError_t launch_ple(const PleParams &p, const LaunchCfg &cfg, cudaStream_t stream);
 cudaError_t launch_replicate(const ReplicateParams &p, const LaunchCfg &cfg, cudaStream_t stream);

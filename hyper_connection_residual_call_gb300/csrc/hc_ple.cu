@@ -19,13 +19,17 @@
 //   hc_ple_gather_kernel  the 16 rows per token -> emb bf16 [M][H]; a row id out
 //                         of range records TS_ERR_INVALID_ARG in the device
 //                         status word and reads zeros
-//   (lm_head GEMV kernel) key_proj and value_proj rows against emb -> fp32
-//   hc_ple_gate_kernel    one CTA per token: the norms' sums of squares, the
-//                         gate, and the conv input x = norm_conv(gv) [M][W]
+//   (lm_head kernel)      key_proj and value_proj rows against emb -> fp32, on
+//                         the tensor cores
+//   hc_ple_gate_kernel    one CTA per (stream, token): the norms' sums of
+//                         squares, the gate, and the conv input
+//                         x = norm_conv(gv) [M][W]
 //   hc_ple_conv_kernel    one thread per channel: the causal conv over the
 //                         state and the chunk, silu, gv, the residual add
 //                         (rounded to bf16), and the new state.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "hc_kernels.h"
 #include "ptx.cuh"
@@ -40,22 +44,6 @@ constexpr int kPleThreads = 512;
 __device__ __forceinline__ float bf16_at(const uint16_t *p, size_t i)
 {
     return __bfloat162float(__ushort_as_bfloat16(p[i]));
-}
-
-__device__ __forceinline__ float block_sum_into(float v, float *red, int tid)
-{
-    // Sum over the block in fixed order (warps, then the warp totals in order).
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v += __shfl_xor_sync(0xffffffffu, v, o);
-    if ((tid & 31) == 0)
-        red[tid >> 5] = v;
-    __syncthreads();
-    float t = 0.f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
-        t += red[w];
-    __syncthreads();  // red may be reused
-    return t;
 }
 
 // Grid M: token m's 16 row segments of H/16, one 16-byte vector per thread and step.
@@ -77,61 +65,92 @@ __global__ void __launch_bounds__(256) hc_ple_gather_kernel(const PleParams p)
     }
 }
 
-// Grid M, one CTA per token. Per stream c: sums of squares of the key and of
-// the residual, and their raw dot (the norms' factors are applied after the
-// sums, they are per stream); the value's sum of squares (shared by the
-// streams); then the gate, and x = norm_conv(gate * value).
+// Grid (C, M): CTA (c, m) owns stream c of token m, thread t the 8-element
+// chunks t, t + blockDim, ... of it. Sums of squares of the key and of the
+// residual, their dot with the norms' scales applied (the norms' 1/rms factors
+// are per stream, so they come after the sums), and the value's sum of squares
+// (the same in every stream); one fixed-order block reduction of the four;
+// then the gate and x = norm_conv(gate * value) for the stream.
 __global__ void __launch_bounds__(kPleThreads) hc_ple_gate_kernel(const PleParams p)
 {
-    __shared__ float red[kPleThreads / 32];
-    __shared__ float gate_s[8], rc_s[8];
+    __shared__ float red[4][kPleThreads / 32];
+    __shared__ float gate_rc[2];
     pdl_launch_dependents();
     pdl_wait();  // key and value come from the projection kernels
-    const int m = blockIdx.x, tid = threadIdx.x;
-    const int H = p.H, C = p.C, W = C * H;
-    const float *key = p.key + (size_t)m * W;
+    const int c = blockIdx.x, m = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = p.H, C = p.C, W = C * H, nch = H / 8;
+    const size_t so = (size_t)c * H;
+    const float *key = p.key + (size_t)m * W + so;
     const float *value = p.value + (size_t)m * H;
-    const uint16_t *hid = p.hidden + (size_t)m * W;
+    const uint16_t *hid = p.hidden + (size_t)m * W + so;
 
-    float vv = 0.f;
-    for (int h = tid; h < H; h += blockDim.x)
-        vv = fmaf(value[h], value[h], vv);
-    const float sum_vv = block_sum_into(vv, red, tid);
-
-    for (int c = 0; c < C; ++c) {
-        float kk = 0.f, qq = 0.f, kq = 0.f;
-        for (int h = tid; h < H; h += blockDim.x) {
-            const size_t j = (size_t)c * H + h;
-            const float k = key[j], q = bf16_at(hid, j);
-            kk = fmaf(k, k, kk);
-            qq = fmaf(q, q, qq);
-            kq = fmaf(k * bf16_at(p.norm_key, j), q * bf16_at(p.norm_query, j), kq);
-        }
-        const float skk = block_sum_into(kk, red, tid);
-        const float sqq = block_sum_into(qq, red, tid);
-        const float skq = block_sum_into(kq, red, tid);
-        if (tid == 0) {
-            const float rk = rsqrtf(fmaf(skk, p.inv_H, p.eps)), rq = rsqrtf(fmaf(sqq, p.inv_H, p.eps));
-            const float g = skq * rk * rq * p.inv_sqrt_H;
-            const float sg = (g > 0.f) - (g < 0.f);
-            const float gate = 1.0f / (1.0f + expf(-sg * sqrtf(fmaxf(fabsf(g), 1e-6f))));
-            gate_s[c] = gate;
-            // norm_conv of gate * value: sum over h of (gate v)^2 = gate^2 sum v^2
-            rc_s[c] = rsqrtf(fmaf(gate * gate * sum_vv, p.inv_H, p.eps));
-            p.gate[(size_t)m * C + c] = gate;
+    float kk = 0.f, qq = 0.f, kq = 0.f, vv = 0.f;
+    for (int i = tid; i < nch; i += blockDim.x) {
+        const float4 k0 = reinterpret_cast<const float4 *>(key)[2 * i], k1 = reinterpret_cast<const float4 *>(key)[2 * i + 1];
+        const float4 v0 = reinterpret_cast<const float4 *>(value)[2 * i], v1 = reinterpret_cast<const float4 *>(value)[2 * i + 1];
+        const uint4 q = reinterpret_cast<const uint4 *>(hid)[i];
+        const uint4 gk = reinterpret_cast<const uint4 *>(p.norm_key + so)[i];
+        const uint4 gq = reinterpret_cast<const uint4 *>(p.norm_query + so)[i];
+        const float kf[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+        const float vf[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        const uint32_t qw[4] = {q.x, q.y, q.z, q.w}, kw[4] = {gk.x, gk.y, gk.z, gk.w}, gw[4] = {gq.x, gq.y, gq.z, gq.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float qf = (e & 1) ? bf16_hi(qw[e / 2]) : bf16_lo(qw[e / 2]);
+            const float sk = (e & 1) ? bf16_hi(kw[e / 2]) : bf16_lo(kw[e / 2]);
+            const float sq = (e & 1) ? bf16_hi(gw[e / 2]) : bf16_lo(gw[e / 2]);
+            kk = fmaf(kf[e], kf[e], kk);
+            qq = fmaf(qf, qf, qq);
+            kq = fmaf(kf[e] * sk, qf * sq, kq);
+            vv = fmaf(vf[e], vf[e], vv);
         }
     }
+    float acc[4] = {kk, qq, kq, vv};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
+        if (lane == 0)
+            red[k][warp] = acc[k];
+    }
     __syncthreads();
-    for (int j = tid; j < W; j += blockDim.x) {
-        const int c = j / H, h = j % H;
-        p.x[(size_t)m * W + j] = gate_s[c] * value[h] * rc_s[c] * bf16_at(p.norm_conv, j);
+    if (tid == 0) {
+        float t[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w)  // warps in order
+            for (int k = 0; k < 4; ++k)
+                t[k] += red[k][w];
+        const float rk = rsqrtf(fmaf(t[0], p.inv_H, p.eps)), rq = rsqrtf(fmaf(t[1], p.inv_H, p.eps));
+        const float g = t[2] * rk * rq * p.inv_sqrt_H;
+        const float sg = (g > 0.f) - (g < 0.f);
+        const float gate = 1.0f / (1.0f + expf(-sg * sqrtf(fmaxf(fabsf(g), 1e-6f))));
+        // norm_conv of gate * value: the sum over h of (gate v)^2 is gate^2 sum v^2
+        gate_rc[0] = gate;
+        gate_rc[1] = rsqrtf(fmaf(gate * gate * t[3], p.inv_H, p.eps));
+        p.gate[(size_t)m * C + c] = gate;
+    }
+    __syncthreads();
+    const float f = gate_rc[0] * gate_rc[1];
+    float *x = p.x + (size_t)m * W + so;
+    for (int i = tid; i < nch; i += blockDim.x) {
+        const float4 v0 = reinterpret_cast<const float4 *>(value)[2 * i], v1 = reinterpret_cast<const float4 *>(value)[2 * i + 1];
+        const uint4 gc = reinterpret_cast<const uint4 *>(p.norm_conv + so)[i];
+        reinterpret_cast<float4 *>(x)[2 * i] =
+            make_float4(f * v0.x * bf16_lo(gc.x), f * v0.y * bf16_hi(gc.x), f * v0.z * bf16_lo(gc.y), f * v0.w * bf16_hi(gc.y));
+        reinterpret_cast<float4 *>(x)[2 * i + 1] =
+            make_float4(f * v1.x * bf16_lo(gc.z), f * v1.y * bf16_hi(gc.z), f * v1.z * bf16_lo(gc.w), f * v1.w * bf16_hi(gc.w));
     }
 }
 
-// One thread per channel j: for each token of the chunk in order, the causal
-// conv over the nine earlier inputs (state, then the chunk's own), silu, gv
-// and the residual add; then the last nine inputs become the state.
-__global__ void __launch_bounds__(256) hc_ple_conv_kernel(const PleParams p)
+// One thread per channel j: the tokens of the chunk in order, in batches of
+// kConvBatch whose loads are all issued before the batch's first residual
+// store; per token the causal conv over the nine earlier inputs (state, then
+// the chunk's own), silu, gv and the residual add; then the last nine inputs
+// become the state.
+constexpr int kConvBatch = 8;
+constexpr int kConvThreads = 128;
+
+__global__ void __launch_bounds__(kConvThreads) hc_ple_conv_kernel(const PleParams p)
 {
     pdl_launch_dependents();
     pdl_wait();  // x and the gates come from the gate kernel
@@ -146,17 +165,30 @@ __global__ void __launch_bounds__(256) hc_ple_conv_kernel(const PleParams p)
 #pragma unroll
     for (int i = 0; i < 9; ++i)
         win[i] = p.state[(size_t)i * W + j];
-    for (int t = 0; t < p.M; ++t) {
-        const float xt = p.x[(size_t)t * W + j];
-        const float y = fmaf(w0, win[0], fmaf(w1, win[3], fmaf(w2, win[6], w3 * xt)));
-        const float gv = p.gate[(size_t)t * p.C + c] * p.value[(size_t)t * p.H + h];
-        const float out = gv + y / (1.0f + expf(-y));
-        const size_t o = (size_t)t * W + j;
-        p.hidden[o] = __bfloat16_as_ushort(__float2bfloat16_rn(bf16_at(p.hidden, o) + out));
+    for (int t0 = 0; t0 < p.M; t0 += kConvBatch) {
+        float xs[kConvBatch], gv[kConvBatch], hs[kConvBatch];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            win[i] = win[i + 1];
-        win[8] = xt;
+        for (int k = 0; k < kConvBatch; ++k) {
+            const int t = t0 + k;
+            if (t < p.M) {
+                xs[k] = p.x[(size_t)t * W + j];
+                gv[k] = p.gate[(size_t)t * p.C + c] * p.value[(size_t)t * p.H + h];
+                hs[k] = bf16_at(p.hidden, (size_t)t * W + j);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kConvBatch; ++k) {
+            const int t = t0 + k;
+            if (t < p.M) {
+                const float y = fmaf(w0, win[0], fmaf(w1, win[3], fmaf(w2, win[6], w3 * xs[k])));
+                const float out = gv[k] + y / (1.0f + expf(-y));
+                p.hidden[(size_t)t * W + j] = __bfloat16_as_ushort(__float2bfloat16_rn(hs[k] + out));
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    win[i] = win[i + 1];
+                win[8] = xs[k];
+            }
+        }
     }
 #pragma unroll
     for (int i = 0; i < 9; ++i)
@@ -183,7 +215,8 @@ cudaError_t launch_ple(const PleParams &p, const LaunchCfg &cfg, cudaStream_t st
     if (e != cudaSuccess)
         return e;
     // key = key_proj(emb) [M][W], value = value_proj(emb) [M][H]: bf16 weight rows
-    // against emb, the lm_head GEMV kernel, in tiles of kLmHeadMaxTokens tokens.
+    // against emb on the tensor cores (the lm_head kernel), in tiles of
+    // kLmHeadMaxTokens tokens.
     for (int t0 = 0; t0 < p.M; t0 += kLmHeadMaxTokens) {
         for (int which = 0; which < 2; ++which) {
             LmHeadParams g{};
@@ -195,16 +228,16 @@ cudaError_t launch_ple(const PleParams &p, const LaunchCfg &cfg, cudaStream_t st
             g.logits = which == 0 ? p.key + (size_t)t0 * p.C * p.H : p.value + (size_t)t0 * p.H;
             g.logits_stride = g.V;
             g.status = p.status;
-            if (!lm_head_plan(g, cfg.sm_count))
-                return cudaErrorInvalidValue;
             if ((e = launch_lm_head(g, cfg, stream)) != cudaSuccess)
                 return e;
         }
     }
-    if ((e = launch(hc_ple_gate_kernel, dim3(p.M), dim3(kPleThreads))) != cudaSuccess)
+    // The gate kernel: about one 8-element chunk of the stream per thread.
+    const int gate_threads = std::min(kPleThreads, std::max(32, (p.H / 8 + 31) / 32 * 32));
+    if ((e = launch(hc_ple_gate_kernel, dim3(p.C, p.M), dim3(gate_threads))) != cudaSuccess)
         return e;
     const int W = p.C * p.H;
-    return launch(hc_ple_conv_kernel, dim3((W + 255) / 256), dim3(256));
+    return launch(hc_ple_conv_kernel, dim3((W + kConvThreads - 1) / kConvThreads), dim3(kConvThreads));
 }
 
 }  // namespace tshc

@@ -454,14 +454,16 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
 // One thread per (token, row): element i = m * R + r of every chunk's partial
 // tile, so the loads of a warp are contiguous; the chunks are summed in order,
 // every load of a thread in flight at once. The host sizes the grid to about
-// one CTA per SM (and reserves shared memory to keep it so). Before the
-// dependency wait each CTA asks L2 for its share of the up kernel's weights,
-// whose CTAs can start only after this kernel's.
+// one CTA per SM (and reserves shared memory to keep it so), on the SMs that
+// the up kernel's CTAs leave free when those all fit beside it: the up CTAs
+// then start, set up and stream their weights while this kernel runs. Before
+// the dependency wait each CTA asks L2 for its share of the up kernel's
+// weights. It triggers the up kernel only after that wait, so that the up
+// kernel may read the prep kernel's normed tiles before its own.
 constexpr int kReduceBatch = 40;
 
 __global__ void __launch_bounds__(1024) hc_tc_reduce_kernel(const TcReduceParams p)
 {
-    pdl_launch_dependents();
     if (threadIdx.x < 32) {
         constexpr size_t kPiece = 16384;
         const size_t nb = gridDim.x, b = blockIdx.x;
@@ -476,6 +478,7 @@ __global__ void __launch_bounds__(1024) hc_tc_reduce_kernel(const TcReduceParams
         }
     }
     pdl_wait();
+    pdl_launch_dependents();  // after the wait: the up kernel may read what came before this kernel
     const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (long)p.M * p.R)
         return;
@@ -586,7 +589,14 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
             for (int cc = 0; cc < C; ++cc)
                 tma_load_2d(a + cc * HBt * 128, &map_u, kb * kKBlock, cc * p.H + h0, &full[kb]);
         }
-        pdl_wait();  // ... then the activations and the normed tiles
+        // The normed tiles come from the prep kernel, two kernels back: the reduce
+        // kernel triggers only after its own wait, so they are complete here.
+        mbar_arrive_expect_tx(nbar, 2 * C * NT * HBt * 2);
+        for (int cc = 0; cc < C; ++cc) {
+            tma_load_2d(const_cast<uint16_t *>(nhi_s) + cc * NT * HBt, &map_nhi, cc * p.H + h0, tile * NT, nbar);
+            tma_load_2d(const_cast<uint16_t *>(nlo_s) + cc * NT * HBt, &map_nlo, cc * p.H + h0, tile * NT, nbar);
+        }
+        pdl_wait();  // ... then the activations
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % NS, u = kb / NS;
             uint8_t *a = smem + lay.ring + s * lay.stage_bytes;
@@ -601,11 +611,6 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
             }
             tma_load_2d(a + b_off, &map_act, kb * kKBlock, tile * NT, &full[s]);
             tma_load_2d(a + b_off + lay.b_bytes, &map_alo, kb * kKBlock, tile * NT, &full[s]);
-        }
-        mbar_arrive_expect_tx(nbar, 2 * C * NT * HBt * 2);
-        for (int cc = 0; cc < C; ++cc) {
-            tma_load_2d(const_cast<uint16_t *>(nhi_s) + cc * NT * HBt, &map_nhi, cc * p.H + h0, tile * NT, nbar);
-            tma_load_2d(const_cast<uint16_t *>(nlo_s) + cc * NT * HBt, &map_nlo, cc * p.H + h0, tile * NT, nbar);
         }
     } else if (WT == 1 && warp >= 2) {
         // INT4 weights: warps 2-15 dequantise the A tiles (rows (stream, h) of
@@ -781,6 +786,149 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
         tmem_dealloc(tmem, ncols);
 }
 
+// ---------------------------------------------------------------- lm_head
+
+// logits[m][v] = sum_h W[v][h] * mixed[m][h] for up to 16 tokens (families/qwen4/
+// mod.rs, decoder pseudocode, exit lines: lm_head on the mixer's output, no
+// softcap, no further norm). A plain bf16 GEMM: both operands are exact in bf16,
+// so one MMA per K step, fp32 accumulation in TMEM. Persistent grid: CTA b takes
+// the 128-row vocabulary tiles b, b + grid, ...; every K block of every tile
+// (128 weight rows x 64 and the 16 token rows x 64, absent tokens and the ragged
+// ends zero-filled by TMA) streams through one ring, the first stages' weights
+// requested before the dependency wait. Two TMEM accumulators of 16 columns
+// alternate between tiles, so that a tile's epilogue overlaps the next tile's
+// MMAs. Roles: warp 0 lane 0 TMA, warp 1 lane 0 MMA, warps 2-5 the epilogue
+// (TMEM lane quadrant warp % 4: 32 vocabulary rows, 16 tokens), whose stores
+// of one token are 32 consecutive logits.
+constexpr int kLmTcThreads = 192;
+constexpr int kLmTcNT = kLmHeadMaxTokens;  // one 16-token tile, MMA N = 16
+constexpr int kLmTcStages = 8;
+constexpr uint32_t kLmTcA = kTileRows * 128;  // one weight box: 128 rows x 128 bytes
+constexpr uint32_t kLmTcB = kLmTcNT * 128;     // one token box: 16 rows x 128 bytes
+constexpr uint32_t kLmTcStage = kLmTcA + kLmTcB;
+constexpr uint32_t kLmTcBars = kLmTcStages * kLmTcStage;
+constexpr size_t kLmTcSmem = kLmTcBars + 8 * (2 * kLmTcStages + 4) + 16 + 1024;
+
+__global__ void __launch_bounds__(kLmTcThreads, 1)
+hc_lm_head_tc_kernel(const LmHeadParams p, const __grid_constant__ CUtensorMap map_w,
+                     const __grid_constant__ CUtensorMap map_x)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kLmTcBars);
+    uint64_t *empty = full + kLmTcStages;
+    uint64_t *tfull = empty + kLmTcStages;  // [2] an accumulator's tile is complete
+    uint64_t *tempty = tfull + 2;           // [2] the epilogue has read it
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(tempty + 2);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ntiles = (p.V + kTileRows - 1) / kTileRows;
+    const int KB = (p.H + kKBlock - 1) / kKBlock;
+    const int my_tiles = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int nsteps = my_tiles * KB;
+
+    pdl_launch_dependents();
+    if (tid == 0) {
+        for (int s = 0; s < kLmTcStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+        }
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        __syncwarp();
+        tmem_alloc(tslot, 2 * kLmTcNT);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    bool timed_out = false;
+
+    if (warp == 0 && lane == 0) {
+        // Step g: K block g % KB of the CTA's tile g / KB, in ring stage g % stages.
+        auto load_w = [&](int g) {
+            const int t = (int)blockIdx.x + (g / KB) * (int)gridDim.x;
+            tma_load_2d(smem + (g % kLmTcStages) * kLmTcStage, &map_w, (g % KB) * kKBlock, t * kTileRows,
+                        &full[g % kLmTcStages]);
+        };
+        auto load_x = [&](int g) {
+            tma_load_2d(smem + (g % kLmTcStages) * kLmTcStage + kLmTcA, &map_x, (g % KB) * kKBlock, 0,
+                        &full[g % kLmTcStages]);
+        };
+        tma_prefetch_map(&map_w);
+        const int npre = nsteps < kLmTcStages ? nsteps : kLmTcStages;
+        for (int g = 0; g < npre; ++g) {  // weights: independent of the kernels before
+            mbar_arrive_expect_tx(&full[g], kLmTcStage);
+            load_w(g);
+        }
+        pdl_wait();  // the tokens come from the kernel before
+        for (int g = 0; g < npre; ++g)
+            load_x(g);
+        for (int g = npre; g < nsteps; ++g) {
+            const int s = g % kLmTcStages, u = g / kLmTcStages;
+            if (!mbar_wait_bounded(&empty[s], (u - 1) & 1)) timed_out = true;
+            mbar_arrive_expect_tx(&full[s], kLmTcStage);
+            load_w(g);
+            load_x(g);
+        }
+    } else if (warp == 1 && lane == 0) {
+        const uint32_t idesc = umma_idesc_bf16(kTileRows, kLmTcNT);
+        int g = 0;
+        for (int j = 0; j < my_tiles; ++j) {
+            const int b = j & 1;
+            // The accumulator's previous tile (j - 2) must have been read out.
+            if (j >= 2 && !mbar_wait_bounded(&tempty[b], ((j >> 1) - 1) & 1)) timed_out = true;
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(b * kLmTcNT);
+            for (int kb = 0; kb < KB; ++kb, ++g) {
+                const int s = g % kLmTcStages, u = g / kLmTcStages;
+                if (!mbar_wait_bounded(&full[s], u & 1)) timed_out = true;
+                tc_fence_after();
+                const uint32_t a = smem_addr(smem + s * kLmTcStage), x = a + kLmTcA;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    umma_bf16(d, umma_desc_sw128(a + 32 * k), umma_desc_sw128(x + 32 * k), idesc, (kb | k) != 0);
+                umma_commit(&empty[s]);
+            }
+            umma_commit(&tfull[b]);
+        }
+    } else if (warp >= 2) {
+        const int quad = warp & 3;
+        for (int j = 0; j < my_tiles; ++j) {
+            const int b = j & 1;
+            if (!mbar_wait_bounded(&tfull[b], (j >> 1) & 1)) timed_out = true;
+            __syncwarp();  // the TMEM load below is .aligned
+            tc_fence_after();
+            uint32_t v[16];
+            tmem_ld16_async(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kLmTcNT), v);
+            tmem_wait_ld(v);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&tempty[b]);
+            const int row = ((int)blockIdx.x + j * (int)gridDim.x) * kTileRows + quad * 32 + lane;
+            if (row < p.V) {
+#pragma unroll
+                for (int m = 0; m < kLmTcNT; ++m)
+                    if (m < p.M)
+                        p.logits[(size_t)m * p.logits_stride + row] = __uint_as_float(v[m]);
+            }
+        }
+    }
+    if (timed_out) record_timeout(p.status);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        tmem_dealloc(tmem, 2 * kLmTcNT);
+}
+
 // ---------------------------------------------------------------- host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -873,6 +1021,23 @@ cudaError_t allow_smem_tc(K kernel, bool dynamic = true)
 }  // namespace
 
 size_t tc_down_smem(int NT, int ns, int wt) { return down_tc_layout(NT, ns, wt).total + 1024; }
+
+bool lm_head_shape_ok(int M, int H, int V) { return M >= 1 && M <= kLmTcNT && H >= 8 && H % 8 == 0 && V >= 1; }
+
+cudaError_t launch_lm_head(const LmHeadParams &p, const LaunchCfg &cfg, cudaStream_t stream)
+{
+    CUtensorMap map_w, map_x;
+    if (!lm_head_shape_ok(p.M, p.H, p.V) ||
+        !make_map(&map_w, p.w, (uint64_t)p.V, (uint64_t)p.H, kKBlock, kTileRows, true) ||
+        !make_map(&map_x, p.mixed, (uint64_t)p.M, (uint64_t)p.H, kKBlock, kLmTcNT, true))
+        return cudaErrorInvalidValue;
+    const cudaError_t e = allow_smem_tc(hc_lm_head_tc_kernel);
+    if (e != cudaSuccess)
+        return e;
+    const int ntiles = (p.V + kTileRows - 1) / kTileRows;
+    return launch_tc(hc_lm_head_tc_kernel, dim3((unsigned)std::min(ntiles, cfg.sm_count)), dim3(kLmTcThreads),
+                     kLmTcSmem, stream, 0, p, map_w, map_x);
+}
 size_t tc_up_smem(int NT, int ns, int C, int HBt, int wt) { return up_tc_layout(NT, ns, C, HBt, wt).total + 1024; }
 
 cudaError_t launch_tc_call(const TcCall &t, cudaStream_t stream)
@@ -914,9 +1079,12 @@ cudaError_t launch_tc_call(const TcCall &t, cudaStream_t stream)
                   tc_down_smem(d.NT, d.n_stages, d.wt), stream, 0, d, map_d, map_i, map_xhi, map_xlo);
     if (e != cudaSuccess)
         return e;
-    // About one output per thread on one CTA per SM (more CTAs only past 1024 threads each).
+    // About one output per thread on one CTA per SM (more CTAs only past 1024 threads each),
+    // on the SMs the up kernel's CTAs leave free when they all fit beside it.
     const long nred = (long)t.red.M * t.red.R;
-    const long per = (nred + kTcChunkCtas - 1) / kTcChunkCtas;
+    const int up_ctas = (int)(((u.H + u.HBt - 1) / u.HBt) * ntiles);
+    const int red_ctas = up_ctas <= kTcChunkCtas - 32 ? kTcChunkCtas - up_ctas : kTcChunkCtas;
+    const long per = (nred + red_ctas - 1) / red_ctas;
     const int rthreads = (int)std::min<long>(1024, (per + 31) / 32 * 32);
     e = launch_tc(hc_tc_reduce_kernel, dim3((unsigned)((nred + rthreads - 1) / rthreads)), dim3(rthreads),
                   kTcReduceSmemReserve, stream, 0, t.red);

@@ -622,12 +622,8 @@ ts_status ts_hc_exit_logits(void *raw, const void *out, const float *prev_inject
     DeviceInfo dev;
     if ((st = device_info(&dev)) != TS_OK)
         return st;
-    tshc::LmHeadParams lp{};
-    lp.M = std::min(M, tshc::kLmHeadMaxTokens);
-    lp.H = H;
-    lp.V = V;
-    if (!tshc::lm_head_plan(lp, dev.sm_count))
-        return fail(TS_ERR_UNSUPPORTED, "H = %d is too wide for the lm_head kernel's ring", H);
+    if (!tshc::lm_head_shape_ok(std::min(M, tshc::kLmHeadMaxTokens), H, V))
+        return fail(TS_ERR_UNSUPPORTED, "the lm_head kernel does not take H = %d, V = %d", H, V);
     const ResidualIO io{(long)C * H, H, static_cast<uint16_t *>(raw), static_cast<const uint16_t *>(out),
                         prev_inject_w, prev_inject_stride};
     st = hc_call_impl(raw, hc_norm_w, down, up, nullptr, mixed, nullptr, 0, M, H, C, lowrank, eps, workspace,
@@ -635,9 +631,11 @@ ts_status ts_hc_exit_logits(void *raw, const void *out, const float *prev_inject
     if (st != TS_OK)
         return st;
     // lm_head over tiles of at most kLmHeadMaxTokens tokens, each a dependent of the launch before it.
+    tshc::LmHeadParams lp{};
+    lp.H = H;
+    lp.V = V;
     for (int t0 = 0; t0 < M; t0 += tshc::kLmHeadMaxTokens) {
         lp.M = std::min(tshc::kLmHeadMaxTokens, M - t0);
-        tshc::lm_head_plan(lp, dev.sm_count);
         lp.mixed = static_cast<const uint16_t *>(mixed) + (size_t)t0 * H;
         lp.w = static_cast<const uint16_t *>(lm_head);
         lp.logits = logits + (size_t)t0 * V;
@@ -732,12 +730,8 @@ ts_status ts_hc_ple(void *hidden, const int32_t *rows, const void *table, long n
     DeviceInfo dev;
     if ((st = device_info(&dev)) != TS_OK)
         return st;
-    tshc::LmHeadParams probe{};
-    probe.M = std::min(M, tshc::kLmHeadMaxTokens);
-    probe.H = H;
-    probe.V = C * H;
-    if (!tshc::lm_head_plan(probe, dev.sm_count))
-        return fail(TS_ERR_UNSUPPORTED, "H = %d is too wide for the projection kernel's ring", H);
+    if (!tshc::lm_head_shape_ok(std::min(M, tshc::kLmHeadMaxTokens), H, C * H))
+        return fail(TS_ERR_UNSUPPORTED, "the projection kernel does not take H = %d", H);
     char *ws = static_cast<char *>(workspace);
     tshc::PleParams p{};
     p.hidden = static_cast<uint16_t *>(hidden);

@@ -226,8 +226,10 @@ ts_status ts_hc_inject_call(void *raw, const void *out, const float *prev_inject
  *     raw += out * prev_inject_w                    (only if out != NULL)
  *     mixed = hyper_connection_mixer(raw)           bf16 [M][H]
  *     logits[m][v] = sum_h lm_head[v][h] * mixed[m][h]   (fp32, mixed as stored)
- * The lm_head GEMV launches as a programmatic dependent of the mixer and
- * streams its first weight rows before the mixer has finished.
+ * lm_head runs on the tensor cores (bf16 operands, fp32 accumulation) in
+ * launches of at most 16 tokens; each launches as a programmatic dependent of
+ * the kernel before it and streams its first weight tiles before that kernel
+ * has finished.
  *
  *   raw             bf16 [M][C*H]; read, and written with the fused inject-add
  *   out, prev_inject_w, prev_inject_stride   as for ts_hc_inject_call, or
@@ -237,8 +239,8 @@ ts_status ts_hc_inject_call(void *raw, const void *out, const float *prev_inject
  *   mixed           bf16 [M][H], written (the lm_head reads it back)
  *   logits          fp32 [M][V], written
  * Other arguments as for ts_hc_mixer; the workspace is ts_hc_workspace_bytes(M, ...).
- * Returns TS_ERR_UNSUPPORTED when H is too wide for the lm_head kernel
- * (one row of 2*H bytes must fit its shared-memory ring).
+ * Any V >= 1 is taken; the shape rules are those of the call (H a multiple
+ * of 8 and the rest as for ts_hc_mixer).
  */
 ts_status ts_hc_exit_logits(void *raw, const void *out, const float *prev_inject_w, long prev_inject_stride,
                             const void *hc_norm_w, const ts_weight *down, const ts_weight *up,
