@@ -112,12 +112,18 @@ struct ReplicateParams {
 
 // lm_head after the exit mixer: logits[m][v] = sum_h w[v][h] * mixed[m][h], on
 // the tensor cores (hc_tc.cu): 128-row vocabulary tiles against the token rows.
+// An optional second weight w2 [V2][H] over the same tokens (V2 = 0: none) runs
+// in the same launch: logits2[m][v] = sum_h w2[v][h] * mixed[m][h].
 struct LmHeadParams {
     const uint16_t *mixed;    // bf16 [M][H]
     const uint16_t *w;        // bf16 [V][H]
     float *logits;            // fp32 token m's logits at logits + m * logits_stride
     long logits_stride;
     int M, H, V;              // M <= kLmHeadMaxTokens
+    const uint16_t *w2;       // bf16 [V2][H], or unused when V2 == 0
+    float *logits2;
+    long logits2_stride;
+    int V2;
     unsigned *status;
 };
 constexpr int kLmHeadMaxTokens = 16;
@@ -165,7 +171,7 @@ cudaError_t launch_up(const UpParams &p, const LaunchCfg &cfg, cudaStream_t stre
 cudaError_t launch_inject(const InjectParams &p, const LaunchCfg &cfg, cudaStream_t stream);
 // Fills rows_per_cta, rs and n_stages for M tokens; false if H is too wide for the ring.
 // Shapes the lm_head kernel takes: 1 <= M <= kLmHeadMaxTokens, H a multiple of 8
-// (16-byte rows for TMA), V >= 1.
+// (16-byte rows for TMA), V >= 1 (and V2 >= 0).
 bool lm_head_shape_ok(int M, int H, int V);
 cudaError_t launch_lm_head(const LmHeadParams &p, const LaunchCfg &cfg, cudaStream_t stream);
 cudaError_t launch_ple(const PleParams &p, const LaunchCfg &cfg, cudaStream_t stream);

@@ -20,7 +20,7 @@
 //                         of range records TS_ERR_INVALID_ARG in the device
 //                         status word and reads zeros
 //   (lm_head kernel)      key_proj and value_proj rows against emb -> fp32, on
-//                         the tensor cores
+//                         the tensor cores, both weights in one launch
 //   hc_ple_gate_kernel    one CTA per (stream, token): the norms' sums of
 //                         squares, the gate, and the conv input
 //                         x = norm_conv(gv) [M][W]
@@ -214,23 +214,25 @@ cudaError_t launch_ple(const PleParams &p, const LaunchCfg &cfg, cudaStream_t st
     cudaError_t e = launch(hc_ple_gather_kernel, dim3(p.M), dim3(256));
     if (e != cudaSuccess)
         return e;
-    // key = key_proj(emb) [M][W], value = value_proj(emb) [M][H]: bf16 weight rows
-    // against emb on the tensor cores (the lm_head kernel), in tiles of
-    // kLmHeadMaxTokens tokens.
+    // key = key_proj(emb) [M][W] and value = value_proj(emb) [M][H] in one launch of
+    // the lm_head kernel (tensor cores; the two weights' tiles side by side), in
+    // tiles of kLmHeadMaxTokens tokens.
     for (int t0 = 0; t0 < p.M; t0 += kLmHeadMaxTokens) {
-        for (int which = 0; which < 2; ++which) {
-            LmHeadParams g{};
-            g.M = p.M - t0 < kLmHeadMaxTokens ? p.M - t0 : kLmHeadMaxTokens;
-            g.H = p.H;
-            g.V = which == 0 ? p.C * p.H : p.H;
-            g.mixed = p.emb + (size_t)t0 * p.H;
-            g.w = which == 0 ? p.key_proj : p.value_proj;
-            g.logits = which == 0 ? p.key + (size_t)t0 * p.C * p.H : p.value + (size_t)t0 * p.H;
-            g.logits_stride = g.V;
-            g.status = p.status;
-            if ((e = launch_lm_head(g, cfg, stream)) != cudaSuccess)
-                return e;
-        }
+        LmHeadParams g{};
+        g.M = p.M - t0 < kLmHeadMaxTokens ? p.M - t0 : kLmHeadMaxTokens;
+        g.H = p.H;
+        g.mixed = p.emb + (size_t)t0 * p.H;
+        g.w = p.key_proj;
+        g.V = p.C * p.H;
+        g.logits = p.key + (size_t)t0 * p.C * p.H;
+        g.logits_stride = g.V;
+        g.w2 = p.value_proj;
+        g.V2 = p.H;
+        g.logits2 = p.value + (size_t)t0 * p.H;
+        g.logits2_stride = p.H;
+        g.status = p.status;
+        if ((e = launch_lm_head(g, cfg, stream)) != cudaSuccess)
+            return e;
     }
     // The gate kernel: about one 8-element chunk of the stream per thread.
     const int gate_threads = std::min(kPleThreads, std::max(32, (p.H / 8 + 31) / 32 * 32));

@@ -792,7 +792,8 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
 // mod.rs, decoder pseudocode, exit lines: lm_head on the mixer's output, no
 // softcap, no further norm). A plain bf16 GEMM: both operands are exact in bf16,
 // so one MMA per K step, fp32 accumulation in TMEM. Persistent grid: CTA b takes
-// the 128-row vocabulary tiles b, b + grid, ...; every K block of every tile
+// the 128-row vocabulary tiles b, b + grid, ... (the tiles of w, then those of
+// the optional second weight w2 against the same tokens); every K block of every tile
 // (128 weight rows x 64 and the 16 token rows x 64, absent tokens and the ragged
 // ends zero-filled by TMA) streams through one ring, the first stages' weights
 // requested before the dependency wait. Two TMEM accumulators of 16 columns
@@ -811,7 +812,7 @@ constexpr size_t kLmTcSmem = kLmTcBars + 8 * (2 * kLmTcStages + 4) + 16 + 1024;
 
 __global__ void __launch_bounds__(kLmTcThreads, 1)
 hc_lm_head_tc_kernel(const LmHeadParams p, const __grid_constant__ CUtensorMap map_w,
-                     const __grid_constant__ CUtensorMap map_x)
+                     const __grid_constant__ CUtensorMap map_w2, const __grid_constant__ CUtensorMap map_x)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -822,7 +823,8 @@ hc_lm_head_tc_kernel(const LmHeadParams p, const __grid_constant__ CUtensorMap m
     uint32_t *tslot = reinterpret_cast<uint32_t *>(tempty + 2);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int ntiles = (p.V + kTileRows - 1) / kTileRows;
+    const int nt1 = (p.V + kTileRows - 1) / kTileRows;  // tiles of w; those of w2 follow
+    const int ntiles = nt1 + (p.V2 + kTileRows - 1) / kTileRows;
     const int KB = (p.H + kKBlock - 1) / kKBlock;
     const int my_tiles = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int nsteps = my_tiles * KB;
@@ -854,8 +856,9 @@ hc_lm_head_tc_kernel(const LmHeadParams p, const __grid_constant__ CUtensorMap m
         // Step g: K block g % KB of the CTA's tile g / KB, in ring stage g % stages.
         auto load_w = [&](int g) {
             const int t = (int)blockIdx.x + (g / KB) * (int)gridDim.x;
-            tma_load_2d(smem + (g % kLmTcStages) * kLmTcStage, &map_w, (g % KB) * kKBlock, t * kTileRows,
-                        &full[g % kLmTcStages]);
+            const bool first = t < nt1;
+            tma_load_2d(smem + (g % kLmTcStages) * kLmTcStage, first ? &map_w : &map_w2, (g % KB) * kKBlock,
+                        (first ? t : t - nt1) * kTileRows, &full[g % kLmTcStages]);
         };
         auto load_x = [&](int g) {
             tma_load_2d(smem + (g % kLmTcStages) * kLmTcStage + kLmTcA, &map_x, (g % KB) * kKBlock, 0,
@@ -912,12 +915,16 @@ hc_lm_head_tc_kernel(const LmHeadParams p, const __grid_constant__ CUtensorMap m
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&tempty[b]);
-            const int row = ((int)blockIdx.x + j * (int)gridDim.x) * kTileRows + quad * 32 + lane;
-            if (row < p.V) {
+            const int t = (int)blockIdx.x + j * (int)gridDim.x;
+            const bool first = t < nt1;
+            const int row = (first ? t : t - nt1) * kTileRows + quad * 32 + lane;
+            float *out = first ? p.logits : p.logits2;
+            const long stride = first ? p.logits_stride : p.logits2_stride;
+            if (row < (first ? p.V : p.V2)) {
 #pragma unroll
                 for (int m = 0; m < kLmTcNT; ++m)
                     if (m < p.M)
-                        p.logits[(size_t)m * p.logits_stride + row] = __uint_as_float(v[m]);
+                        out[(size_t)m * stride + row] = __uint_as_float(v[m]);
             }
         }
     }
@@ -1026,17 +1033,19 @@ bool lm_head_shape_ok(int M, int H, int V) { return M >= 1 && M <= kLmTcNT && H 
 
 cudaError_t launch_lm_head(const LmHeadParams &p, const LaunchCfg &cfg, cudaStream_t stream)
 {
-    CUtensorMap map_w, map_x;
-    if (!lm_head_shape_ok(p.M, p.H, p.V) ||
+    CUtensorMap map_w, map_w2, map_x;
+    if (!lm_head_shape_ok(p.M, p.H, p.V) || p.V2 < 0 ||
         !make_map(&map_w, p.w, (uint64_t)p.V, (uint64_t)p.H, kKBlock, kTileRows, true) ||
+        !make_map(&map_w2, p.V2 > 0 ? p.w2 : p.w, (uint64_t)(p.V2 > 0 ? p.V2 : p.V), (uint64_t)p.H, kKBlock,
+                  kTileRows, true) ||
         !make_map(&map_x, p.mixed, (uint64_t)p.M, (uint64_t)p.H, kKBlock, kLmTcNT, true))
         return cudaErrorInvalidValue;
     const cudaError_t e = allow_smem_tc(hc_lm_head_tc_kernel);
     if (e != cudaSuccess)
         return e;
-    const int ntiles = (p.V + kTileRows - 1) / kTileRows;
+    const int ntiles = (p.V + kTileRows - 1) / kTileRows + (p.V2 + kTileRows - 1) / kTileRows;
     return launch_tc(hc_lm_head_tc_kernel, dim3((unsigned)std::min(ntiles, cfg.sm_count)), dim3(kLmTcThreads),
-                     kLmTcSmem, stream, 0, p, map_w, map_x);
+                     kLmTcSmem, stream, 0, p, map_w, map_w2, map_x);
 }
 size_t tc_up_smem(int NT, int ns, int C, int HBt, int wt) { return up_tc_layout(NT, ns, C, HBt, wt).total + 1024; }
 

@@ -509,14 +509,14 @@ def test_entry_call_is_replicate_then_call(M, H, C, L, kind, with_inject):
 # decision at a tie point); each such element moves a logit by |w[v][h]| times
 # that step, so the logits keep the chained fp32 floor (1e-3 of their RMS).
 EXIT_CASES = [(1, 2560, 4, 320, 1000), (1, 2560, 4, 320, 32768), (5, 2560, 4, 320, 1000), (20, 2560, 4, 320, 500),
-              (3, 256, 4, 32, 777), (1, 256, 4, 32, 152)]
+              (3, 256, 4, 32, 777), (1, 256, 4, 32, 152), (1, 256, 4, 32, 7), (2, 2560, 4, 320, 4869)]
 
 
 @pytest.mark.parametrize("M,H,C,L,V", EXIT_CASES)
 def test_exit_logits(orc, M, H, C, L, V):
     """The decoder's exit: the last inject-add fused in front of the mixer, then lm_head
     (one-token, cluster and tensor-core mixers; one and two 16-token lm_head tiles;
-    vocabularies that leave the last CTA's row block ragged)."""
+    vocabularies below one 16-row box and ones that leave the last CTA's rows ragged)."""
     w = inputs.make_hc_weights(H, C, L, 900 + M, with_inject=False)
     lm = inputs.bf16_normal((V, H), 900 + V, std=0.02)
     raw = inputs.make_residual(M, H, C, 900 + M)
