@@ -170,8 +170,8 @@ cudaError_t launch_one_token(const DownParams &d, const UpParams &u, const Launc
 cudaError_t launch_up(const UpParams &p, const LaunchCfg &cfg, cudaStream_t stream);
 cudaError_t launch_inject(const InjectParams &p, const LaunchCfg &cfg, cudaStream_t stream);
 // Fills rows_per_cta, rs and n_stages for M tokens; false if H is too wide for the ring.
-// Shapes the lm_head kernel takes: 1 <= M <= kLmHeadMaxTokens, H a multiple of 8
-// (16-byte rows for TMA), V >= 1 (and V2 >= 0).
+// Shapes the lm_head kernel takes: 1 <= M <= kLmHeadMaxTokens, H a multiple of 64
+// (whole K blocks), V >= 1 (and V2 >= 0).
 bool lm_head_shape_ok(int M, int H, int V);
 cudaError_t launch_lm_head(const LmHeadParams &p, const LaunchCfg &cfg, cudaStream_t stream);
 cudaError_t launch_ple(const PleParams &p, const LaunchCfg &cfg, cudaStream_t stream);

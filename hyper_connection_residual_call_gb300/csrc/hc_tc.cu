@@ -793,19 +793,23 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
 // softcap, no further norm). A plain bf16 GEMM: both operands are exact in bf16,
 // so one MMA per K step, fp32 accumulation in TMEM. Persistent grid: CTA b takes
 // the 128-row vocabulary tiles b, b + grid, ... (the tiles of w, then those of
-// the optional second weight w2 against the same tokens); every K block of every tile
-// (128 weight rows x 64 and the 16 token rows x 64, absent tokens and the ragged
-// ends zero-filled by TMA) streams through one ring, the first stages' weights
-// requested before the dependency wait. Two TMEM accumulators of 16 columns
+// the optional second weight w2 against the same tokens). The tiles stream
+// through one ring of stages of four K blocks: one 3-D TMA box of the weights
+// (128 rows x 4 K blocks, so that each row yields 512 contiguous bytes per
+// request instead of 128; it lands as four ordinary 128-row K-block tiles) and
+// four 16-row token boxes (absent tokens and the ragged ends zero-filled by
+// TMA). The first stages' weights are requested before the dependency wait.
+// Two TMEM accumulators of 16 columns
 // alternate between tiles, so that a tile's epilogue overlaps the next tile's
 // MMAs. Roles: warp 0 lane 0 TMA, warp 1 lane 0 MMA, warps 2-5 the epilogue
 // (TMEM lane quadrant warp % 4: 32 vocabulary rows, 16 tokens), whose stores
 // of one token are 32 consecutive logits.
 constexpr int kLmTcThreads = 192;
 constexpr int kLmTcNT = kLmHeadMaxTokens;  // one 16-token tile, MMA N = 16
-constexpr int kLmTcStages = 8;
-constexpr uint32_t kLmTcA = kTileRows * 128;  // one weight box: 128 rows x 128 bytes
-constexpr uint32_t kLmTcB = kLmTcNT * 128;     // one token box: 16 rows x 128 bytes
+constexpr int kLmTcStages = 3;
+constexpr int kLmKbs = 4;                        // K blocks per stage (one 3-D weight box)
+constexpr uint32_t kLmTcA = kLmKbs * kTileRows * 128;  // weight box: KBS K-block tiles of 128 rows x 128 bytes
+constexpr uint32_t kLmTcB = kLmKbs * kLmTcNT * 128;    // token boxes: KBS x 16 rows x 128 bytes
 constexpr uint32_t kLmTcStage = kLmTcA + kLmTcB;
 constexpr uint32_t kLmTcBars = kLmTcStages * kLmTcStage;
 constexpr size_t kLmTcSmem = kLmTcBars + 8 * (2 * kLmTcStages + 4) + 16 + 1024;
@@ -825,7 +829,7 @@ hc_lm_head_tc_kernel(const LmHeadParams p, const __grid_constant__ CUtensorMap m
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nt1 = (p.V + kTileRows - 1) / kTileRows;  // tiles of w; those of w2 follow
     const int ntiles = nt1 + (p.V2 + kTileRows - 1) / kTileRows;
-    const int KB = (p.H + kKBlock - 1) / kKBlock;
+    const int KB = (p.H + kKBlock * kLmKbs - 1) / (kKBlock * kLmKbs);  // stages per tile
     const int my_tiles = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int nsteps = my_tiles * KB;
 
@@ -857,12 +861,13 @@ hc_lm_head_tc_kernel(const LmHeadParams p, const __grid_constant__ CUtensorMap m
         auto load_w = [&](int g) {
             const int t = (int)blockIdx.x + (g / KB) * (int)gridDim.x;
             const bool first = t < nt1;
-            tma_load_2d(smem + (g % kLmTcStages) * kLmTcStage, first ? &map_w : &map_w2, (g % KB) * kKBlock,
-                        (first ? t : t - nt1) * kTileRows, &full[g % kLmTcStages]);
+            tma_load_3d(smem + (g % kLmTcStages) * kLmTcStage, first ? &map_w : &map_w2, 0,
+                        (first ? t : t - nt1) * kTileRows, (g % KB) * kLmKbs, &full[g % kLmTcStages]);
         };
         auto load_x = [&](int g) {
-            tma_load_2d(smem + (g % kLmTcStages) * kLmTcStage + kLmTcA, &map_x, (g % KB) * kKBlock, 0,
-                        &full[g % kLmTcStages]);
+            for (int q = 0; q < kLmKbs; ++q)
+                tma_load_2d(smem + (g % kLmTcStages) * kLmTcStage + kLmTcA + q * kLmTcNT * 128, &map_x,
+                            ((g % KB) * kLmKbs + q) * kKBlock, 0, &full[g % kLmTcStages]);
         };
         tma_prefetch_map(&map_w);
         const int npre = nsteps < kLmTcStages ? nsteps : kLmTcStages;
@@ -893,10 +898,15 @@ hc_lm_head_tc_kernel(const LmHeadParams p, const __grid_constant__ CUtensorMap m
                 const int s = g % kLmTcStages, u = g / kLmTcStages;
                 if (!mbar_wait_bounded(&full[s], u & 1)) timed_out = true;
                 tc_fence_after();
-                const uint32_t a = smem_addr(smem + s * kLmTcStage), x = a + kLmTcA;
+                const uint32_t a0 = smem_addr(smem + s * kLmTcStage), x0 = a0 + kLmTcA;
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    umma_bf16(d, umma_desc_sw128(a + 32 * k), umma_desc_sw128(x + 32 * k), idesc, (kb | k) != 0);
+                for (int q = 0; q < kLmKbs; ++q) {
+                    const uint32_t a = a0 + q * kTileRows * 128, x = x0 + q * kLmTcNT * 128;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        umma_bf16(d, umma_desc_sw128(a + 32 * k), umma_desc_sw128(x + 32 * k), idesc,
+                                  (kb | q | k) != 0);
+                }
                 umma_commit(&empty[s]);
             }
             umma_commit(&tfull[b]);
@@ -974,6 +984,24 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 3-D view of a bf16 [rows][cols] matrix for K-block boxes: dims (64 elements,
+// rows, cols / 64), so that a box (64, box_rows, kbs) lands as kbs consecutive
+// K-block tiles of box_rows x 128 bytes (128-byte swizzle).
+bool make_map_kblocks(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                      uint32_t kbs)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[3] = {64, rows, (cols + 63) / 64};
+    const cuuint64_t strides[2] = {cols * 2, 128};
+    const cuuint32_t box[3] = {64, box_rows, kbs};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_tc(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                       int cluster_x, Args &&...args)
@@ -1029,15 +1057,15 @@ cudaError_t allow_smem_tc(K kernel, bool dynamic = true)
 
 size_t tc_down_smem(int NT, int ns, int wt) { return down_tc_layout(NT, ns, wt).total + 1024; }
 
-bool lm_head_shape_ok(int M, int H, int V) { return M >= 1 && M <= kLmTcNT && H >= 8 && H % 8 == 0 && V >= 1; }
+bool lm_head_shape_ok(int M, int H, int V) { return M >= 1 && M <= kLmTcNT && H >= 64 && H % 64 == 0 && V >= 1; }
 
 cudaError_t launch_lm_head(const LmHeadParams &p, const LaunchCfg &cfg, cudaStream_t stream)
 {
     CUtensorMap map_w, map_w2, map_x;
     if (!lm_head_shape_ok(p.M, p.H, p.V) || p.V2 < 0 ||
-        !make_map(&map_w, p.w, (uint64_t)p.V, (uint64_t)p.H, kKBlock, kTileRows, true) ||
-        !make_map(&map_w2, p.V2 > 0 ? p.w2 : p.w, (uint64_t)(p.V2 > 0 ? p.V2 : p.V), (uint64_t)p.H, kKBlock,
-                  kTileRows, true) ||
+        !make_map_kblocks(&map_w, p.w, (uint64_t)p.V, (uint64_t)p.H, kTileRows, kLmKbs) ||
+        !make_map_kblocks(&map_w2, p.V2 > 0 ? p.w2 : p.w, (uint64_t)(p.V2 > 0 ? p.V2 : p.V), (uint64_t)p.H,
+                          kTileRows, kLmKbs) ||
         !make_map(&map_x, p.mixed, (uint64_t)p.M, (uint64_t)p.H, kKBlock, kLmTcNT, true))
         return cudaErrorInvalidValue;
     const cudaError_t e = allow_smem_tc(hc_lm_head_tc_kernel);

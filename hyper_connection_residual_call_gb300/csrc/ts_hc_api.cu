@@ -619,11 +619,11 @@ ts_status ts_hc_exit_logits(void *raw, const void *out, const float *prev_inject
         if (prev_inject_stride < C)
             return fail(TS_ERR_INVALID_ARG, "prev_inject_stride = %ld must be >= C = %d", prev_inject_stride, C);
     }
+    if (!tshc::lm_head_shape_ok(std::min(M, tshc::kLmHeadMaxTokens), H, V))
+        return fail(TS_ERR_UNSUPPORTED, "the lm_head kernel does not take H = %d (a multiple of 64)", H);
     DeviceInfo dev;
     if ((st = device_info(&dev)) != TS_OK)
         return st;
-    if (!tshc::lm_head_shape_ok(std::min(M, tshc::kLmHeadMaxTokens), H, V))
-        return fail(TS_ERR_UNSUPPORTED, "the lm_head kernel does not take H = %d, V = %d", H, V);
     const ResidualIO io{(long)C * H, H, static_cast<uint16_t *>(raw), static_cast<const uint16_t *>(out),
                         prev_inject_w, prev_inject_stride};
     st = hc_call_impl(raw, hc_norm_w, down, up, nullptr, mixed, nullptr, 0, M, H, C, lowrank, eps, workspace,

@@ -239,8 +239,8 @@ ts_status ts_hc_inject_call(void *raw, const void *out, const float *prev_inject
  *   mixed           bf16 [M][H], written (the lm_head reads it back)
  *   logits          fp32 [M][V], written
  * Other arguments as for ts_hc_mixer; the workspace is ts_hc_workspace_bytes(M, ...).
- * Any V >= 1 is taken; the shape rules are those of the call (H a multiple
- * of 8 and the rest as for ts_hc_mixer).
+ * Any V >= 1 is taken; H must be a multiple of 64 (TS_ERR_UNSUPPORTED
+ * otherwise), the other shape rules are those of ts_hc_mixer.
  */
 ts_status ts_hc_exit_logits(void *raw, const void *out, const float *prev_inject_w, long prev_inject_stride,
                             const void *hc_norm_w, const ts_weight *down, const ts_weight *up,

@@ -154,6 +154,7 @@ def test_exit_logits_rejects(lib):
     assert call(logits=FAKE + 2) == B.TS_ERR_INVALID_ARG and "logits is not 4-byte" in B.ts_hc_last_error()
     assert call(out=FAKE, prev=None) == B.TS_ERR_INVALID_ARG and "prev_inject_w is NULL" in B.ts_hc_last_error()
     assert call(out=FAKE, prev=FAKE, prev_stride=C - 1) == B.TS_ERR_INVALID_ARG
+    assert call(H_=H + 8) == B.TS_ERR_UNSUPPORTED and "multiple of 64" in B.ts_hc_last_error()
     assert call(M=0, lm_head=None, logits=None) == B.TS_OK
 
 
