@@ -32,7 +32,7 @@ EXPORTS = ("ts_hc_workspace_bytes", "ts_hc_workspace_layout", "ts_hc_call", "ts_
            "ts_hc_replicate_entry", "ts_hc_ple_workspace_bytes", "ts_hc_ple_workspace_layout", "ts_hc_ple",
            "ts_hc_last_error",
            "ts_hc_device_status", "ts_hc_call_noalloc", "ts_hc_stack_workspace_bytes", "ts_hc_stack",
-           "ts_hc_selftest_timeout")
+           "ts_hc_stack_ple_workspace_bytes", "ts_hc_stack_ple", "ts_hc_selftest_timeout")
 TS_HC_STATIC_SCRATCH_BYTES = 64 * 1024 * 1024  # include/ts_hc.h
 
 
@@ -59,6 +59,20 @@ class TsHcModule(ctypes.Structure):
         ("down", TsWeight),
         ("up", TsWeight),
         ("inject", TsWeight),
+    ]
+
+
+class TsHcPleModule(ctypes.Structure):
+    """``ts_hc_ple_module``: a stack's PLE tensors."""
+    _fields_ = [
+        ("table", ctypes.c_void_p),
+        ("n_rows", ctypes.c_long),
+        ("key_proj", ctypes.c_void_p),
+        ("value_proj", ctypes.c_void_p),
+        ("norm_key_w", ctypes.c_void_p),
+        ("norm_query_w", ctypes.c_void_p),
+        ("norm_conv_w", ctypes.c_void_p),
+        ("conv_w", ctypes.c_void_p),
     ]
 
 
@@ -115,6 +129,11 @@ def library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.ts_hc_stack_workspace_bytes.restype = sz
         lib.ts_hc_stack.argtypes = [vp, i, mp, mp, i, mp, SUBLAYER_FN, vp, vp, i, i, i, i, f, vp, sz, vp]
         lib.ts_hc_stack.restype = i
+        lib.ts_hc_stack_ple_workspace_bytes.argtypes = [i, i, i, i]
+        lib.ts_hc_stack_ple_workspace_bytes.restype = sz
+        lib.ts_hc_stack_ple.argtypes = [vp, i, mp, mp, i, mp, ctypes.POINTER(TsHcPleModule), vp, vp, SUBLAYER_FN,
+                                        vp, vp, i, i, i, i, f, vp, sz, vp]
+        lib.ts_hc_stack_ple.restype = i
         lib.ts_hc_selftest_timeout.argtypes = [vp]
         lib.ts_hc_selftest_timeout.restype = i
         lib.ts_hc_last_error.argtypes = []
@@ -226,6 +245,20 @@ def ts_hc_stack(emb, T, attn, mlp, n_layers, final_mixer, sublayer, user, mixed_
     return library().ts_hc_stack(emb, T, attn, mlp, n_layers, _wref(final_mixer),
                                  sublayer if sublayer is not None else SUBLAYER_FN(), user, mixed_out,
                                  max_chunk, H, C, lowrank, eps, workspace, workspace_bytes, stream)
+
+
+def ts_hc_stack_ple_workspace_bytes(max_chunk: int, H: int, C: int, lowrank: int) -> int:
+    return library().ts_hc_stack_ple_workspace_bytes(max_chunk, H, C, lowrank)
+
+
+def ts_hc_stack_ple(emb, T, attn, mlp, n_layers, final_mixer, ple, ple_rows, ple_conv_state, sublayer, user,
+                    mixed_out, max_chunk, H, C, lowrank, eps, workspace, workspace_bytes, stream) -> int:
+    """As ``ts_hc_stack``, with ``ple`` a ``TsHcPleModule`` (or None) and the row ids and
+    conv state as device pointers."""
+    return library().ts_hc_stack_ple(emb, T, attn, mlp, n_layers, _wref(final_mixer),
+                                     None if ple is None else ctypes.byref(ple), ple_rows, ple_conv_state,
+                                     sublayer if sublayer is not None else SUBLAYER_FN(), user, mixed_out,
+                                     max_chunk, H, C, lowrank, eps, workspace, workspace_bytes, stream)
 
 
 def ts_hc_selftest_timeout(stream) -> int:
@@ -554,22 +587,38 @@ def module_struct(w) -> TsHcModule:
     return m
 
 
-def stack_workspace(max_chunk: int, H: int, C: int, L: int, device=None):
+def stack_workspace(max_chunk: int, H: int, C: int, L: int, device=None, with_ple: bool = False):
     torch = _torch()
-    n = max(ts_hc_stack_workspace_bytes(max_chunk, H, C, L), 256)
-    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    n = (ts_hc_stack_ple_workspace_bytes if with_ple else ts_hc_stack_workspace_bytes)(max_chunk, H, C, L)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def ple_module_struct(w) -> TsHcPleModule:
+    """A ``TsHcPleModule`` for PLE weights with attributes table, key_proj, value_proj,
+    norm_key, norm_query, norm_conv, conv_w."""
+    m = TsHcPleModule()
+    m.table = w.table.data_ptr()
+    m.n_rows = w.table.shape[0]
+    m.key_proj, m.value_proj = w.key_proj.data_ptr(), w.value_proj.data_ptr()
+    m.norm_key_w, m.norm_query_w = w.norm_key.data_ptr(), w.norm_query.data_ptr()
+    m.norm_conv_w, m.conv_w = w.norm_conv.data_ptr(), w.conv_w.data_ptr()
+    return m
 
 
 def hc_stack(emb, layers, final, sublayer, *, C: int, max_chunk: Optional[int] = None, mixed_out=None,
-             eps: float = RMS_EPS, ws=None, stream=None):
-    """The decoder stack's hyper-connection path on T tokens through ``ts_hc_stack``.
+             eps: float = RMS_EPS, ws=None, stream=None, ple=None, ple_rows=None, ple_state=None):
+    """The decoder stack's hyper-connection path on T tokens through ``ts_hc_stack``
+    (``ts_hc_stack_ple`` when ``ple`` is given).
 
     ``emb`` [T, H] bf16; ``layers``: a sequence of (attn, mlp) weights (g, down, up,
     inject); ``final``: the exit mixer's weights. ``sublayer(layer, which, t0, mixed)``
     gets the call's output ``mixed`` ([M, H] bf16, a view into the workspace) and
     returns the sublayer output, a CUDA bf16 tensor [M, H] that it may compute on the
-    current stream; the driver injects it with the call's gates. Returns
-    (mixed_out [T, H], the last chunk's residual [M, C*H] -- a view into ``ws``).
+    current stream; the driver injects it with the call's gates. ``ple``: PLE weights
+    (table, key_proj, value_proj, norm_key, norm_query, norm_conv, conv_w) applied
+    before layer 1's attn_hc, with ``ple_rows`` int32 [T, 16] and ``ple_state`` fp32
+    [9, C*H] (updated). Returns (mixed_out [T, H], the last chunk's residual
+    [M, C*H] -- a view into ``ws``).
     """
     torch = _torch()
     T, H = emb.shape
@@ -579,8 +628,11 @@ def hc_stack(emb, layers, final, sublayer, *, C: int, max_chunk: Optional[int] =
     if mixed_out is None:
         mixed_out = torch.empty((T, H), dtype=torch.bfloat16, device=emb.device)
     _need(mixed_out, "mixed_out", torch.bfloat16, (T, H))
+    if ple is not None:
+        _need(ple_rows, "ple_rows", torch.int32, (T, 16))
+        _need(ple_state, "ple_state", torch.float32, (9, C * H))
     if ws is None:
-        ws = stack_workspace(max_chunk, H, C, L, emb.device)
+        ws = stack_workspace(max_chunk, H, C, L, emb.device, with_ple=ple is not None)
     n = len(layers)
     attn = (TsHcModule * max(n, 1))(*[module_struct(a) for a, _ in layers])
     mlp = (TsHcModule * max(n, 1))(*[module_struct(m) for _, m in layers])
@@ -604,8 +656,13 @@ def hc_stack(emb, layers, final, sublayer, *, C: int, max_chunk: Optional[int] =
             return TS_ERR_INVALID_ARG
 
     fn = SUBLAYER_FN(trampoline)
-    st = ts_hc_stack(emb.data_ptr(), T, attn, mlp, n, fin, fn, None, mixed_out.data_ptr(), max_chunk, H, C,
-                     L, eps, base, ws.numel() * ws.element_size(), _stream_handle(stream))
+    if ple is None:
+        st = ts_hc_stack(emb.data_ptr(), T, attn, mlp, n, fin, fn, None, mixed_out.data_ptr(), max_chunk, H, C,
+                         L, eps, base, ws.numel() * ws.element_size(), _stream_handle(stream))
+    else:
+        st = ts_hc_stack_ple(emb.data_ptr(), T, attn, mlp, n, fin, ple_module_struct(ple), ple_rows.data_ptr(),
+                             ple_state.data_ptr(), fn, None, mixed_out.data_ptr(), max_chunk, H, C, L, eps, base,
+                             ws.numel() * ws.element_size(), _stream_handle(stream))
     if errors:
         raise errors[0]
     _check(st)

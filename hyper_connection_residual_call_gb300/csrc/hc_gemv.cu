@@ -653,18 +653,16 @@ __device__ __forceinline__ float warp_transpose_sum8(float (&v)[8], int lane)
 constexpr int kRowsPerGroup = 8;  // rows one thread of hc_down1_kernel dots
 
 struct Down1Smem {
-    size_t bar, w, sb, g, red, total;
+    size_t bar, w, g, red, total;
 };
 
 __host__ __device__ inline Down1Smem down1_layout(const DownParams &p)
 {
     const size_t seg = p.down.type == 0 ? (size_t)p.KC * 2 : (size_t)p.KC / 2;
-    const int ng = p.down.type == 0 ? 0 : p.KC >> p.down.gshift;
     Down1Smem s;
     s.bar = 0;
     s.w = 128;
-    s.sb = round_up_sz(s.w + seg * p.rows_per_block, 128);
-    s.g = round_up_sz(s.sb + sizeof(float) * 2 * (size_t)ng * p.rows_per_block, 128);
+    s.g = round_up_sz(s.w + seg * p.rows_per_block, 128);
     s.red = round_up_sz(s.g + (size_t)p.KC * 2, 128);
     s.total = round_up_sz(s.red + sizeof(float) * 32 * (kRowsPerGroup + 1), 128);
     return s;
@@ -685,7 +683,6 @@ __global__ void __launch_bounds__(1024, 1) hc_down1_kernel(const DownParams p)
     const Down1Smem lay = down1_layout(p);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + lay.bar);
     const unsigned char *w_s = smem + lay.w;
-    float *sb_s = reinterpret_cast<float *>(smem + lay.sb);
     const uint16_t *g_s = reinterpret_cast<const uint16_t *>(smem + lay.g);
     float *red_s = reinterpret_cast<float *>(smem + lay.red);
 
@@ -723,18 +720,25 @@ __global__ void __launch_bounds__(1024, 1) hc_down1_kernel(const DownParams p)
             }
         }
     }
-    const int ng = WT == 0 ? 1 : KC >> p.down.gshift;
+    // INT4: this thread's 8 inputs share one (scale, bias) group of every row, so
+    // it loads one scale and one bias per row of its group now, into registers;
+    // they are used after the dots, so nothing waits for them here.
+    uint16_t sc_r[kRowsPerGroup], bi_r[kRowsPerGroup];
     if constexpr (WT == 1) {
-        for (int i = tid; i < nrows * ng; i += blockDim.x) {
-            const int r = i / ng, gi = i % ng;
-            const int gr = r0 + r;
-            const WeightView &wv = gr < p.L ? p.down : p.inject;
-            const int row = gr < p.L ? gr : gr - p.L;
-            const size_t off = (size_t)row * (p.W >> wv.gshift) + (k0 >> wv.gshift) + gi;
-            sb_s[2 * i] = half_bits_to_float(wv.scales[off]);
-            sb_s[2 * i + 1] = half_bits_to_float(wv.biases[off]);
+        const int gi = (v * 8) >> p.down.gshift;
+#pragma unroll
+        for (int j = 0; j < kRowsPerGroup; ++j) {
+            sc_r[j] = 0;
+            bi_r[j] = 0;
+            if (v < nv && j < gnr) {
+                const int gr = r0 + gr0 + j;
+                const WeightView &wv = gr < p.L ? p.down : p.inject;
+                const int row = gr < p.L ? gr : gr - p.L;
+                const size_t off = (size_t)row * (p.W >> wv.gshift) + (k0 >> wv.gshift) + gi;
+                sc_r[j] = wv.scales[off];
+                bi_r[j] = wv.biases[off];
+            }
         }
-        __syncthreads();  // other warps read these scales (no later barrier precedes the dots)
     }
 
     pdl_wait();  // the residual and the previous gates come from earlier kernels
@@ -807,11 +811,10 @@ __global__ void __launch_bounds__(1024, 1) hc_down1_kernel(const DownParams p)
                 // sum (q s + b) x = s * sum q x + b * sum x.
                 const uint32_t codes = *reinterpret_cast<const uint32_t *>(wr + v * 4);
                 const uint32_t nlo = int4_lo_nibbles(codes), nhi = int4_hi_nibbles(codes);
-                const float *sb = sb_s + 2 * ((gr0 + j) * ng + ((v * 8) >> p.down.gshift));
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     a = ffma2(int4_pair_f32x2(nlo, nhi, e), xp[e], a);
-                a = f32x2(fmaf(sb[0], f32x2_sum(a), sb[1] * xsum), 0.f);
+                a = f32x2(fmaf(half_bits_to_float(sc_r[j]), f32x2_sum(a), half_bits_to_float(bi_r[j]) * xsum), 0.f);
             }
             acc[j] = f32x2_sum(a);
         }
@@ -846,7 +849,7 @@ __global__ void __launch_bounds__(1024, 1) hc_down1_kernel(const DownParams p)
 }
 
 struct Up1Smem {
-    size_t bar, w, sb, act, ssq, invq, inv, total;
+    size_t bar, w, sb, act, asum, ssq, invq, inv, total;
 };
 
 __host__ __device__ inline Up1Smem up1_layout(const UpParams &p)
@@ -858,7 +861,8 @@ __host__ __device__ inline Up1Smem up1_layout(const UpParams &p)
     s.w = 128;
     s.sb = round_up_sz(s.w + row * p.C * p.HB, 128);
     s.act = round_up_sz(s.sb + sizeof(float) * 2 * (size_t)ng * p.C * p.HB, 128);
-    s.ssq = round_up_sz(s.act + sizeof(float) * (size_t)p.L, 128);
+    s.asum = round_up_sz(s.act + sizeof(float) * (size_t)p.L, 128);
+    s.ssq = round_up_sz(s.asum + sizeof(float) * (size_t)(p.up.type == 0 ? 0 : p.L / 8), 128);
     s.invq = round_up_sz(s.ssq + sizeof(float) * kMaxCluster, 16);
     s.inv = round_up_sz(s.invq + sizeof(float) * kMaxCluster, 16);
     s.total = round_up_sz(s.inv + sizeof(float) * kMaxCluster, 128);
@@ -875,6 +879,7 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
     const unsigned char *w_s = smem + lay.w;
     float *sb_s = reinterpret_cast<float *>(smem + lay.sb);
     float *act_s = reinterpret_cast<float *>(smem + lay.act);
+    float *asum_s = reinterpret_cast<float *>(smem + lay.asum);  // INT4: act summed over each 8-input word
     float *ssq_s = reinterpret_cast<float *>(smem + lay.ssq);    // sum of squares of chunk q
     float *invq_s = reinterpret_cast<float *>(smem + lay.invq);  // inv_rms of chunk q's stream
     float *inv_s = reinterpret_cast<float *>(smem + lay.inv);
@@ -962,6 +967,7 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
         }
     }
     __syncthreads();
+    float a_k = 0.f;  // act[k], 0 past L
     if (k < p.R) {
         float z = 0.f;
 #pragma unroll
@@ -971,11 +977,23 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
         if (k < L) {
             const float a = zc * sigmoid_fast(zc);
             act_s[k] = a;
+            a_k = a;
             if (blockIdx.x == 0)
                 p.act_out[k] = a;
         } else if (blockIdx.x == 0 && p.gate) {
             p.gate[k - L] = 2.0f * sigmoid_fast(zc);
         }
+    }
+    if constexpr (WT == 1) {
+        // The sum of each 8-input word's act values, which the dots multiply by the
+        // group's bias: lanes 8w .. 8w+7 of a warp hold act[8w .. 8w+7] (L is a
+        // multiple of 8), summed as ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)).
+        float t = a_k;
+        t += __shfl_xor_sync(0xffffffffu, t, 1);
+        t += __shfl_xor_sync(0xffffffffu, t, 2);
+        t += __shfl_xor_sync(0xffffffffu, t, 4);
+        if ((k & 7) == 0 && k < L)
+            asum_s[k >> 3] = t;
     }
     const bool timed_out = !mbar_wait_bounded(bar, 0);
     if (timed_out)
@@ -1031,7 +1049,7 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
                 const float4 xa = *reinterpret_cast<const float4 *>(act_s + v * 8);
                 const float4 xb = *reinterpret_cast<const float4 *>(act_s + v * 8 + 4);
                 const uint64_t ap[4] = {f32x2(xa.x, xa.y), f32x2(xa.z, xa.w), f32x2(xb.x, xb.y), f32x2(xb.z, xb.w)};
-                const float asum = ((xa.x + xa.y) + (xa.z + xa.w)) + ((xb.x + xb.y) + (xb.z + xb.w));
+                const float asum = asum_s[v];
                 const uint32_t codes = wr[v];
                 const uint32_t nlo = int4_lo_nibbles(codes), nhi = int4_hi_nibbles(codes);
                 const float *sb = sbr + 2 * ((v * 8) >> p.up.gshift);

@@ -162,6 +162,32 @@ ts_status api_error(ts_status st, const char *fmt, ...)
 
 ts_status check_shape_api(int M, int H, int C, int lowrank) { return check_shape(M, H, C, lowrank); }
 
+ts_status check_ple_shape(int H, int C)
+{
+    if (H < 128 || H % 128 != 0 || H > kMaxH)
+        return fail(TS_ERR_INVALID_ARG, "H = %d must be a multiple of 128 in [128, %d] (16 table segments of 8k)",
+                    H, kMaxH);
+    if (C < 1 || C > kMaxC)
+        return fail(TS_ERR_INVALID_ARG, "C = %d must be in [1, %d]", C, kMaxC);
+    return TS_OK;
+}
+
+ts_status check_ple_module(const ts_hc_ple_module *m)
+{
+    if (!m)
+        return fail(TS_ERR_INVALID_ARG, "ple is NULL");
+    if (m->n_rows < 1)
+        return fail(TS_ERR_INVALID_ARG, "n_rows = %ld must be >= 1", m->n_rows);
+    ts_status st;
+    if ((st = check_ptr(m->table, "table", 16)) != TS_OK) return st;
+    if ((st = check_ptr(m->key_proj, "key_proj", 16)) != TS_OK) return st;
+    if ((st = check_ptr(m->value_proj, "value_proj", 16)) != TS_OK) return st;
+    if ((st = check_ptr(m->norm_key_w, "norm_key_w", 16)) != TS_OK) return st;
+    if ((st = check_ptr(m->norm_query_w, "norm_query_w", 16)) != TS_OK) return st;
+    if ((st = check_ptr(m->norm_conv_w, "norm_conv_w", 16)) != TS_OK) return st;
+    return check_ptr(m->conv_w, "conv_w", 16);
+}
+
 ts_status check_ptr_api(const void *p, const char *name, size_t align) { return check_ptr(p, name, align); }
 
 ts_status check_module(const ts_hc_module *m, bool with_inject, int H, int C, int lowrank, const char *name)
@@ -700,25 +726,15 @@ ts_status ts_hc_ple(void *hidden, const int32_t *rows, const void *table, long n
     g_last_error.clear();
     if (M < 0)
         return fail(TS_ERR_INVALID_ARG, "M = %d must be >= 0", M);
-    if (H < 128 || H % 128 != 0 || H > kMaxH)
-        return fail(TS_ERR_INVALID_ARG, "H = %d must be a multiple of 128 in [128, %d] (16 table segments of 8k)",
-                    H, kMaxH);
-    if (C < 1 || C > kMaxC)
-        return fail(TS_ERR_INVALID_ARG, "C = %d must be in [1, %d]", C, kMaxC);
+    ts_status st = tshc::check_ple_shape(H, C);
+    if (st != TS_OK)
+        return st;
     if (M == 0)  // nothing is read or written: pointers are not examined
         return TS_OK;
-    if (n_rows < 1)
-        return fail(TS_ERR_INVALID_ARG, "n_rows = %ld must be >= 1", n_rows);
-    ts_status st;
+    const ts_hc_ple_module mod{table, n_rows, key_proj, value_proj, norm_key_w, norm_query_w, norm_conv_w, conv_w};
     if ((st = check_ptr(hidden, "hidden", 16)) != TS_OK) return st;
     if ((st = check_ptr(rows, "rows", 4)) != TS_OK) return st;
-    if ((st = check_ptr(table, "table", 16)) != TS_OK) return st;
-    if ((st = check_ptr(key_proj, "key_proj", 16)) != TS_OK) return st;
-    if ((st = check_ptr(value_proj, "value_proj", 16)) != TS_OK) return st;
-    if ((st = check_ptr(norm_key_w, "norm_key_w", 16)) != TS_OK) return st;
-    if ((st = check_ptr(norm_query_w, "norm_query_w", 16)) != TS_OK) return st;
-    if ((st = check_ptr(norm_conv_w, "norm_conv_w", 16)) != TS_OK) return st;
-    if ((st = check_ptr(conv_w, "conv_w", 16)) != TS_OK) return st;
+    if ((st = tshc::check_ple_module(&mod)) != TS_OK) return st;
     if ((st = check_ptr(conv_state, "conv_state", 16)) != TS_OK) return st;
     if (!(eps >= 0.0f) || eps > 1.0f)
         return fail(TS_ERR_INVALID_ARG, "eps = %g must be in [0, 1]", (double)eps);

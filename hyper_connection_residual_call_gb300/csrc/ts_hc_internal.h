@@ -18,5 +18,8 @@ ts_status check_ptr_api(const void *p, const char *name, size_t align);
 // and the inject weight when `with_inject` (same format and group as down).
 ts_status check_module(const ts_hc_module *m, bool with_inject, int H, int C, int lowrank,
                        const char *name);
+// The PLE's shape rules (H a multiple of 128, C in range) and its module's tensors.
+ts_status check_ple_shape(int H, int C);
+ts_status check_ple_module(const ts_hc_ple_module *m);
 
 }  // namespace tshc

@@ -1,5 +1,5 @@
 // ts_hc_stack.cu -- the decoder stack's hyper-connection path over a prompt,
-// chunk by chunk (ts_hc_stack in include/ts_hc.h). Host code only: it
+// chunk by chunk (ts_hc_stack and ts_hc_stack_ple in include/ts_hc.h). Host code only: it
 // sequences the library's own entry points on one stream and allocates
 // nothing.
 //
@@ -24,13 +24,13 @@ namespace {
 size_t a256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Workspace of the driver: the chunk's residual, the calls' mixed output, the
-// chunk's [M][2][C] gate buffer, then the calls' own workspace (the largest
-// any chunk size up to max_chunk needs).
+// chunk's [M][2][C] gate buffer, the calls' own workspace (the largest any
+// chunk size up to max_chunk needs), then, with the PLE, its workspace.
 struct StackWs {
-    size_t raw, mixed, gates, call, call_bytes, total;
+    size_t raw, mixed, gates, call, call_bytes, ple, ple_bytes, total;
 };
 
-StackWs stack_ws(int max_chunk, int H, int C, int L)
+StackWs stack_ws(int max_chunk, int H, int C, int L, bool with_ple)
 {
     StackWs w{};
     const size_t M = (size_t)max_chunk, W = (size_t)C * H;
@@ -42,32 +42,27 @@ StackWs stack_ws(int max_chunk, int H, int C, int L)
     for (int m = 1; m <= max_chunk; ++m)
         need = std::max(need, ts_hc_workspace_bytes(m, H, C, L));
     w.call_bytes = a256(need);
-    w.total = w.call + w.call_bytes;
+    w.ple = w.call + w.call_bytes;
+    w.ple_bytes = with_ple ? a256(ts_hc_ple_workspace_bytes(max_chunk, H, C)) : 0;  // grows with M
+    w.total = w.ple + w.ple_bytes;
     return w;
 }
 
 const char *sublayer_name(int which) { return which == 0 ? "attention" : "MoE"; }
 
-}  // namespace
+// The PLE step of a stack: module, row ids [T][16], conv state.
+struct StackPle {
+    const ts_hc_ple_module *mod;
+    const int32_t *rows;
+    float *state;
+};
 
-extern "C" {
-
-size_t ts_hc_stack_workspace_bytes(int max_chunk, int H, int C, int lowrank)
-{
-    if (max_chunk < 1 || tshc::check_shape_api(max_chunk, H, C, lowrank) != TS_OK) {
-        tshc::clear_error();
-        return 0;
-    }
-    return stack_ws(max_chunk, H, C, lowrank).total;
-}
-
-ts_status ts_hc_stack(const void *emb, int T, const ts_hc_module *attn, const ts_hc_module *mlp,
-                      int n_layers, const ts_hc_module *final_mixer, ts_hc_sublayer_fn sublayer,
-                      void *user, void *mixed_out, int max_chunk, int H, int C, int lowrank,
-                      float eps, void *workspace, size_t workspace_bytes, cudaStream_t stream)
+ts_status stack_impl(const void *emb, int T, const ts_hc_module *attn, const ts_hc_module *mlp, int n_layers,
+                     const ts_hc_module *final_mixer, const StackPle *ple, ts_hc_sublayer_fn sublayer,
+                     void *user, void *mixed_out, int max_chunk, int H, int C, int lowrank, float eps,
+                     void *workspace, size_t workspace_bytes, cudaStream_t stream)
 {
     using tshc::api_error;
-    tshc::clear_error();
     if (T < 0)
         return api_error(TS_ERR_INVALID_ARG, "T = %d must be >= 0", T);
     if (n_layers < 0)
@@ -100,7 +95,15 @@ ts_status ts_hc_stack(const void *emb, int T, const ts_hc_module *attn, const ts
     }
     if ((st = tshc::check_module(final_mixer, false, H, C, lowrank, "final_mixer")) != TS_OK)
         return st;
-    const StackWs lay = stack_ws(max_chunk, H, C, lowrank);
+    if (ple) {
+        if (n_layers < 2)
+            return api_error(TS_ERR_INVALID_ARG, "the PLE runs before layer 1, but n_layers = %d", n_layers);
+        if ((st = tshc::check_ple_shape(H, C)) != TS_OK) return st;
+        if ((st = tshc::check_ple_module(ple->mod)) != TS_OK) return st;
+        if ((st = tshc::check_ptr_api(ple->rows, "ple_rows", 4)) != TS_OK) return st;
+        if ((st = tshc::check_ptr_api(ple->state, "ple_conv_state", 16)) != TS_OK) return st;
+    }
+    const StackWs lay = stack_ws(max_chunk, H, C, lowrank, ple != nullptr);
     if (!workspace || workspace_bytes < lay.total)
         return api_error(TS_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace_bytes, lay.total);
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
@@ -127,14 +130,28 @@ ts_status ts_hc_stack(const void *emb, int T, const ts_hc_module *attn, const ts
             for (int which = 0; which < 2; ++which) {
                 const ts_hc_module &m = which == 0 ? attn[l] : mlp[l];
                 float *slot = gates + which * C;
-                // Layer 0's attn_hc reads the embedding row in every stream and
-                // writes the replicated residual (the entry line, fused).
-                st = l == 0 && which == 0
-                         ? ts_hc_entry_call(emb_t, raw, m.hc_norm_w, &m.down, &m.up, &m.inject, mixed, slot,
-                                            gstride, M, H, C, lowrank, eps, cws, lay.call_bytes, stream)
-                         : ts_hc_inject_call(raw, prev_out, prev_gate, gstride, m.hc_norm_w, &m.down, &m.up,
-                                             &m.inject, mixed, slot, gstride, M, H, C, lowrank, eps, cws,
-                                             lay.call_bytes, stream);
+                if (ple && l == 1 && which == 0) {
+                    // Layer 1: layer 0's last inject-add, the PLE on the residual, then attn_hc.
+                    const ts_hc_ple_module &q = *ple->mod;
+                    if ((st = ts_hc_inject_add(raw, prev_out, prev_gate, gstride, M, H, C, stream)) != TS_OK)
+                        return st;
+                    st = ts_hc_ple(raw, ple->rows + 16 * (size_t)t0, q.table, q.n_rows, q.key_proj, q.value_proj,
+                                   q.norm_key_w, q.norm_query_w, q.norm_conv_w, q.conv_w, ple->state, M, H, C, eps,
+                                   ws + lay.ple, lay.ple_bytes, stream);
+                    if (st != TS_OK)
+                        return st;
+                    st = ts_hc_call(raw, m.hc_norm_w, &m.down, &m.up, &m.inject, mixed, slot, gstride, M, H, C,
+                                    lowrank, eps, cws, lay.call_bytes, stream);
+                } else {
+                    // Layer 0's attn_hc reads the embedding row in every stream and
+                    // writes the replicated residual (the entry line, fused).
+                    st = l == 0 && which == 0
+                             ? ts_hc_entry_call(emb_t, raw, m.hc_norm_w, &m.down, &m.up, &m.inject, mixed, slot,
+                                                gstride, M, H, C, lowrank, eps, cws, lay.call_bytes, stream)
+                             : ts_hc_inject_call(raw, prev_out, prev_gate, gstride, m.hc_norm_w, &m.down, &m.up,
+                                                 &m.inject, mixed, slot, gstride, M, H, C, lowrank, eps, cws,
+                                                 lay.call_bytes, stream);
+                }
                 if (st != TS_OK)
                     return st;
                 const void *out = nullptr;
@@ -167,6 +184,51 @@ ts_status ts_hc_stack(const void *emb, int T, const ts_hc_module *attn, const ts
             return st;
     }
     return TS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ts_hc_stack_workspace_bytes(int max_chunk, int H, int C, int lowrank)
+{
+    if (max_chunk < 1 || tshc::check_shape_api(max_chunk, H, C, lowrank) != TS_OK) {
+        tshc::clear_error();
+        return 0;
+    }
+    return stack_ws(max_chunk, H, C, lowrank, false).total;
+}
+
+size_t ts_hc_stack_ple_workspace_bytes(int max_chunk, int H, int C, int lowrank)
+{
+    if (max_chunk < 1 || tshc::check_shape_api(max_chunk, H, C, lowrank) != TS_OK ||
+        tshc::check_ple_shape(H, C) != TS_OK) {
+        tshc::clear_error();
+        return 0;
+    }
+    return stack_ws(max_chunk, H, C, lowrank, true).total;
+}
+
+ts_status ts_hc_stack(const void *emb, int T, const ts_hc_module *attn, const ts_hc_module *mlp,
+                      int n_layers, const ts_hc_module *final_mixer, ts_hc_sublayer_fn sublayer,
+                      void *user, void *mixed_out, int max_chunk, int H, int C, int lowrank,
+                      float eps, void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    tshc::clear_error();
+    return stack_impl(emb, T, attn, mlp, n_layers, final_mixer, nullptr, sublayer, user, mixed_out, max_chunk, H, C,
+                      lowrank, eps, workspace, workspace_bytes, stream);
+}
+
+ts_status ts_hc_stack_ple(const void *emb, int T, const ts_hc_module *attn, const ts_hc_module *mlp,
+                          int n_layers, const ts_hc_module *final_mixer, const ts_hc_ple_module *ple,
+                          const int32_t *ple_rows, float *ple_conv_state, ts_hc_sublayer_fn sublayer,
+                          void *user, void *mixed_out, int max_chunk, int H, int C, int lowrank,
+                          float eps, void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    tshc::clear_error();
+    const StackPle p{ple, ple_rows, ple_conv_state};
+    return stack_impl(emb, T, attn, mlp, n_layers, final_mixer, &p, sublayer, user, mixed_out, max_chunk, H, C,
+                      lowrank, eps, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -330,7 +330,7 @@ ts_status ts_hc_replicate_entry(const void *emb, void *raw, int M, int H, int C,
  * Tokens do not interact in this path, so the T tokens are processed in
  * chunks of at most max_chunk tokens, one after the other. For each chunk of
  * M tokens starting at token t0:
- *   raw = repeat(emb[t0 .. t0+M), C)                        ts_hc_replicate_entry
+ *   raw = repeat(emb[t0 .. t0+M), C), fused into layer 0's attn_hc   ts_hc_entry_call
  *   for layer l: attn_hc(attn[l]) -> sublayer(l, 0) -> mlp_hc(mlp[l]) -> sublayer(l, 1),
  *                each inject-add fused into the call after it   ts_hc_inject_call
  *   mixed_out[t0 .. t0+M) = hyper_connection_mixer(final)   (fused with the last inject-add)
@@ -370,6 +370,23 @@ typedef struct {
     ts_weight inject;         /* [C][C*H]; not read for the exit mixer */
 } ts_hc_module;
 
+/*
+ * A stack's PLE module (families/qwen4/mod.rs, "## PLE"), the tensors ts_hc_ple
+ * takes: table bf16 [n_rows][H/16]; key_proj bf16 [C*H][H]; value_proj bf16
+ * [H][H]; norm_key_w, norm_query_w, norm_conv_w bf16 [C*H] each; conv_w bf16
+ * [C*H][4]. Every pointer 16-byte aligned.
+ */
+typedef struct {
+    const void *table;
+    long n_rows;
+    const void *key_proj;
+    const void *value_proj;
+    const void *norm_key_w;
+    const void *norm_query_w;
+    const void *norm_conv_w;
+    const void *conv_w;
+} ts_hc_ple_module;
+
 typedef ts_status (*ts_hc_sublayer_fn)(void *user, int layer, int which, int t0, int M,
                                        const void *mixed, const void **out, cudaStream_t stream);
 
@@ -378,6 +395,30 @@ ts_status ts_hc_stack(const void *emb, int T, const ts_hc_module *attn, const ts
                       int n_layers, const ts_hc_module *final_mixer, ts_hc_sublayer_fn sublayer,
                       void *user, void *mixed_out, int max_chunk, int H, int C, int lowrank,
                       float eps, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * ts_hc_stack with the PLE gate at layer index 1 (families/qwen4/mod.rs, decoder
+ * pseudocode: `if layer_idx == 1: hidden = hidden + ple(hidden, input_ids)`
+ * before that layer's attn_hc). For each chunk, layer 0's last inject-add is
+ * applied on its own (ts_hc_inject_add), then ts_hc_ple on the residual, then
+ * layer 1's attn_hc (ts_hc_call); every other step is as in ts_hc_stack.
+ *
+ *   ple             the PLE module (all of it validated before any launch)
+ *   ple_rows        int32 [T][16], token t's 16 table row ids
+ *   ple_conv_state  fp32 [9][C*H], the conv inputs of the 9 tokens before token 0
+ *                   (zero for a new sequence); read and updated chunk by chunk, so
+ *                   on return it holds the last 9 tokens' inputs
+ *   n_layers        >= 2 (the PLE layer must exist)
+ *   H               a multiple of 128
+ *   workspace       >= ts_hc_stack_ple_workspace_bytes(max_chunk, H, C, lowrank)
+ * Other arguments and results as for ts_hc_stack.
+ */
+size_t ts_hc_stack_ple_workspace_bytes(int max_chunk, int H, int C, int lowrank);
+ts_status ts_hc_stack_ple(const void *emb, int T, const ts_hc_module *attn, const ts_hc_module *mlp,
+                          int n_layers, const ts_hc_module *final_mixer, const ts_hc_ple_module *ple,
+                          const int32_t *ple_rows, float *ple_conv_state, ts_hc_sublayer_fn sublayer,
+                          void *user, void *mixed_out, int max_chunk, int H, int C, int lowrank,
+                          float eps, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Self-test of the failure path. Launches one thread that waits, with the same

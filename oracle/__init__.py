@@ -368,32 +368,48 @@ class Oracle:
                 "inv_rms_mlp": r2["inv_rms"], "a_mlp": r2["a"]}
 
     def stack(self, emb, layers: Sequence, outs: Sequence, final, *, H: int, C: int, L: int,
-              eps: float = RMS_EPS, round_residual: bool = True,
+              eps: float = RMS_EPS, round_residual: bool = True, ple=None, ple_rows=None, ple_state=None,
               threads: Optional[int] = None) -> dict:
-        """The decoder stack's hyper-connection path on M tokens.
+        """The decoder stack's hyper-connection path on M tokens (one sequence, in order).
 
         entry: raw = emb repeated C times; per layer l, with ``layers[l]`` =
         (attn, mlp) and ``outs[l]`` = (out_attn, out_mlp): attn_hc + inject,
         mlp_hc + inject; exit: the final mixer with ``final`` (g, down, up).
+        With ``ple`` (PLE weights: table, key_proj, value_proj, norm_key,
+        norm_query, norm_conv, conv_w), ``ple_rows`` [M, 16] and ``ple_state``
+        [9, C*H]: raw = ple(raw) before layer 1's attn_hc (families/qwen4/mod.rs,
+        decoder pseudocode, layer_idx == 1 only).
 
         ``round_residual``: the residual is a bf16 tensor between calls, so it
-        is rounded to bf16 (ties to even) after every inject-add, as stored.
-        Each call itself is exact in fp64.
+        is rounded to bf16 (ties to even) after every inject-add and after the
+        PLE, as stored. Each call itself is exact in fp64.
 
         Also returns ``peak``: per element, the largest |raw| the residual held
-        at entry or after any inject-add (a bf16 rounding decision taken at
-        that magnitude moves the element by one ulp of it).
+        at entry, after any inject-add or after the PLE (a bf16 rounding decision
+        taken at that magnitude moves the element by one ulp of it), and, with
+        the PLE, ``ple_state`` after the tokens.
         """
         raw = self.replicate_entry(emb, H=H, C=C)
         peak = np.abs(raw)
-        for (attn, mlp), (o_attn, o_mlp) in zip(layers, outs):
+        state_out = None
+        for layer, ((attn, mlp), (o_attn, o_mlp)) in enumerate(zip(layers, outs)):
+            if ple is not None and layer == 1:
+                p = self.ple(raw, ple_rows, ple.table, ple.key_proj, ple.value_proj, ple.norm_key,
+                             ple.norm_query, ple.norm_conv, ple.conv_w, ple_state, H=H, C=C, eps=eps,
+                             threads=threads)
+                raw = self.round_to_bf16(p["result"]) if round_residual else p["result"]
+                state_out = p["state"]
+                peak = np.maximum(peak, np.abs(raw))
             r = self.prefill_pair(raw, attn, o_attn, mlp, o_mlp, H=H, C=C, L=L, eps=eps,
                                   round_residual=round_residual, threads=threads)
             peak = np.maximum(peak, np.maximum(np.abs(r["raw_after_attn"]), np.abs(r["raw_after_mlp"])))
             raw = r["raw_after_mlp"]
         fin = self.mixer(raw, final.g, final.down, final.up, H=H, C=C, L=L, eps=eps,
                          threads=threads)
-        return {"mixed": fin["mixed"], "raw": raw, "peak": peak}
+        out = {"mixed": fin["mixed"], "raw": raw, "peak": peak}
+        if ple is not None:
+            out["ple_state"] = state_out
+        return out
 
 
 _lock = threading.Lock()

@@ -27,6 +27,7 @@ import torch
 import torch.nn.functional as F
 from scipy.special import expit
 
+from hyper_connection_residual_call_gb300 import inputs
 from hyper_connection_residual_call_gb300.inputs import Weight, quantize_int4_affine
 
 EPS = 1e-6
@@ -522,6 +523,34 @@ def pin_ple_state_carries_across_chunks(orc):
     rb = orc.ple(**b)
     assert np.array_equal(np.concatenate([ra["result"], rb["result"]]), whole["result"])
     assert np.array_equal(rb["state"], whole["state"])
+
+
+def pin_stack_ple_zero_value_adds_nothing(orc):
+    """The stack with the PLE before layer 1: a PLE whose value projection and conv
+    state are zero adds exactly nothing (gv = 0, every conv input and tap product is
+    0, silu(0) = 0), so the stack equals the stack without it, bit for bit; with a
+    non-zero value projection the stack's output changes, and the state the stack
+    hands back is the PLE's own on the residual after layer 0."""
+    H, C, L, M = 32, 2, 8, 3
+    st = inputs.make_stack(M, H, C, L, 3, 31)
+    pw = inputs.make_ple_weights(H, C, 31, n_rows=12, std=0.3)
+    rows = inputs.make_ple_rows(M, 12, 31)
+    zero_state = torch.zeros((9, C * H), dtype=torch.float64)
+    plain = orc.stack(st.emb, st.layers, st.outs, st.final, H=H, C=C, L=L, eps=EPS)
+    quiet = inputs.PleWeights(pw.table, pw.key_proj, torch.zeros_like(pw.value_proj), pw.norm_key, pw.norm_query,
+                              pw.norm_conv, pw.conv_w)
+    with_quiet = orc.stack(st.emb, st.layers, st.outs, st.final, H=H, C=C, L=L, eps=EPS, ple=quiet,
+                           ple_rows=rows, ple_state=zero_state)
+    assert np.array_equal(with_quiet["mixed"], plain["mixed"]) and np.array_equal(with_quiet["raw"], plain["raw"])
+    assert not np.any(with_quiet["ple_state"]), "a zero value projection leaves a zero conv state"
+    live = orc.stack(st.emb, st.layers, st.outs, st.final, H=H, C=C, L=L, eps=EPS, ple=pw, ple_rows=rows,
+                     ple_state=zero_state)
+    assert not np.allclose(live["mixed"], plain["mixed"], rtol=1e-6, atol=0), "the PLE changes the stack"
+    after0 = orc.prefill_pair(orc.replicate_entry(st.emb, H=H, C=C), st.layers[0][0], st.outs[0][0],
+                              st.layers[0][1], st.outs[0][1], H=H, C=C, L=L, eps=EPS, round_residual=True)
+    own = orc.ple(after0["raw_after_mlp"], rows, pw.table, pw.key_proj, pw.value_proj, pw.norm_key, pw.norm_query,
+                  pw.norm_conv, pw.conv_w, zero_state, H=H, C=C, eps=EPS)
+    assert np.array_equal(live["ple_state"], own["state"]), "the PLE runs on the residual after layer 0"
 
 
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

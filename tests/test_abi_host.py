@@ -273,6 +273,49 @@ def _stack(**kw):
                          kw.get("ws", FAKE), kw.get("ws_bytes", 1 << 30), None)
 
 
+def _ple_module(**kw):
+    m = B.TsHcPleModule()
+    m.table, m.n_rows = kw.get("table", FAKE), kw.get("n_rows", 100)
+    m.key_proj, m.value_proj = kw.get("key_proj", FAKE), kw.get("value_proj", FAKE)
+    m.norm_key_w, m.norm_query_w, m.norm_conv_w = FAKE, kw.get("norm_query_w", FAKE), FAKE
+    m.conv_w = kw.get("conv_w", FAKE)
+    return m
+
+
+def _stack_ple(**kw):
+    n = kw.get("n_layers", 2)
+    attn = (B.TsHcModule * max(n, 1))(*[_module() for _ in range(n)])
+    mlp = (B.TsHcModule * max(n, 1))(*[_module() for _ in range(n)])
+    ple = kw.get("ple", _ple_module())
+    return B.ts_hc_stack_ple(FAKE, 5, attn, mlp, n, _module(inject=_w(data=None)), ple, kw.get("rows", FAKE),
+                             kw.get("state", FAKE), B.SUBLAYER_FN(lambda *a: B.TS_OK), None, FAKE, 4,
+                             kw.get("H_", H), C, L, 1e-6, FAKE, kw.get("ws_bytes", 1 << 30), None)
+
+
+def test_stack_ple_workspace_bytes(lib):
+    a256 = lambda n: (n + 255) // 256 * 256
+    for chunk in (1, 7, 16):
+        assert (B.ts_hc_stack_ple_workspace_bytes(chunk, H, C, L)
+                == B.ts_hc_stack_workspace_bytes(chunk, H, C, L) + a256(B.ts_hc_ple_workspace_bytes(chunk, H, C)))
+    assert B.ts_hc_stack_ple_workspace_bytes(4, 2560 + 64, C, L) == 0  # H not a multiple of 128
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(n_layers=1), B.TS_ERR_INVALID_ARG, "n_layers = 1"),
+    (dict(ple=None), B.TS_ERR_INVALID_ARG, "ple is NULL"),
+    (dict(ple=_ple_module(n_rows=0)), B.TS_ERR_INVALID_ARG, "n_rows"),
+    (dict(ple=_ple_module(key_proj=FAKE + 8)), B.TS_ERR_INVALID_ARG, "key_proj is not 16-byte aligned"),
+    (dict(ple=_ple_module(norm_query_w=None)), B.TS_ERR_INVALID_ARG, "norm_query_w is NULL"),
+    (dict(rows=FAKE + 2), B.TS_ERR_INVALID_ARG, "ple_rows is not 4-byte aligned"),
+    (dict(state=None), B.TS_ERR_INVALID_ARG, "ple_conv_state is NULL"),
+    (dict(H_=2560 + 64), B.TS_ERR_INVALID_ARG, "multiple of 128"),
+    (dict(ws_bytes=1 << 20), B.TS_ERR_WORKSPACE, "workspace"),
+])
+def test_stack_ple_rejects(lib, kw, status, needle):
+    assert _stack_ple(**kw) == status
+    assert needle in B.ts_hc_last_error()
+
+
 def test_stack_workspace_bytes(lib):
     a256 = lambda n: (n + 255) // 256 * 256
     for chunk in (1, 7, 16, 40):

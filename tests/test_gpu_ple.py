@@ -14,7 +14,7 @@ import torch
 import oracle
 from hyper_connection_residual_call_gb300 import binding as B
 from hyper_connection_residual_call_gb300 import inputs
-from gpu_common import check_bf16, check_fp32, require_gpu
+from gpu_common import CHAINED_RMS_FLOOR, check_bf16, check_bf16_carried, check_fp32, require_gpu
 
 pytestmark = pytest.mark.gpu
 EPS = 1e-6
@@ -104,3 +104,32 @@ def test_ple_row_id_out_of_range_is_reported():
     assert B.device_status() == B.TS_ERR_INVALID_ARG
     assert B.device_status() == B.TS_OK  # cleared by the read
     assert torch.isfinite(hidden.float()).all()
+
+
+@pytest.mark.parametrize("max_chunk", [2, 5])
+def test_stack_with_ple_matches_oracle(orc, max_chunk):
+    """ts_hc_stack_ple: the PLE before layer 1's attn_hc inside the stack driver,
+    chunk by chunk with the conv state carried (chunks of 2: tensor-core calls and a
+    one-token tail), against the oracle's stack with the PLE on all 5 tokens at once."""
+    H, C, L, M, n = 256, 4, 64, 5, 3
+    st = inputs.make_stack(M, H, C, L, n, 41)
+    pw = inputs.make_ple_weights(H, C, 41, n_rows=64)
+    rows = inputs.make_ple_rows(M, 64, 41)
+    state = inputs.make_ple_state(H, C, 41)
+    ref = orc.stack(st.emb, st.layers, st.outs, st.final, H=H, C=C, L=L, eps=EPS, round_residual=True, ple=pw,
+                    ple_rows=rows, ple_state=state)
+    layers = [(a.to("cuda"), m.to("cuda")) for a, m in st.layers]
+    outs = [(a.cuda(), m.cuda()) for a, m in st.outs]
+    state_d = state.cuda()
+
+    def sublayer(layer, which, t0, mixed):
+        return outs[layer][which][t0:t0 + mixed.shape[0]]
+
+    mixed, raw = B.hc_stack(st.emb.cuda(), layers, st.final.to("cuda"), sublayer, C=C, max_chunk=max_chunk,
+                            eps=EPS, ple=pw.to("cuda"), ple_rows=rows.cuda(), ple_state=state_d)
+    torch.cuda.synchronize()
+    last = raw.shape[0]
+    check_bf16(mixed, ref["mixed"], f"stack with PLE: mixer output (chunks of {max_chunk})")
+    check_bf16_carried(raw, ref["raw"][-last:], ref["peak"][-last:], "stack with PLE: last chunk's residual")
+    check_fp32(state_d, ref["ple_state"], "stack with PLE: conv state", floor=CHAINED_RMS_FLOOR)
+    assert B.device_status() == B.TS_OK
