@@ -14,6 +14,7 @@ namespace tshc {
 constexpr int kTcMinTokens = 2;
 constexpr size_t kTcSmemLimit = 232448;   // 227 KB opt-in shared memory per CTA
 constexpr int kTcChunkCtas = 152;         // the down kernel's K split aims at about this many CTAs
+constexpr int kTcMaxChunkKb = 16;         // and cuts K into chunks of at most this many 64-wide blocks
 // Shared memory the reduce kernel reserves (and does not use) so that at most
 // one of its CTAs runs per SM and none beside a down or up CTA: launched early
 // (programmatic dependent launch), its CTAs would otherwise pile onto the few
@@ -42,6 +43,11 @@ __host__ __device__ inline TcPlan tc_plan(int M, int L, int C, int W)
     const int per = kTcChunkCtas / (RT * p.ntiles);
     const int target = per > 1 ? per : 1;
     p.KBc = (KBT + target - 1) / target;
+    // A chunk's partial accumulates in one TMEM accumulator, and the error of that sum
+    // grows with its length (1024 MMAs for 128 K blocks at the widest residual put act
+    // past the fp32 bar); longer K is cut into more chunks, summed by the reduce kernel.
+    if (p.KBc > kTcMaxChunkKb)
+        p.KBc = kTcMaxChunkKb;
     p.nchunk = (KBT + p.KBc - 1) / p.KBc;
     return p;
 }

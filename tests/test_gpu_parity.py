@@ -104,6 +104,19 @@ def test_shapes_and_ragged_tokens(orc, M, H, C, L):
     call_and_inject(orc, inputs.Shape(M=M, H=H, C=C, L=L), seed=100 + M)
 
 
+# The API's maxima (H = 16384, C = 8, lowrank = 1024; a wide residual of 131072): one
+# token, the tensor-core path, the largest lowrank at the full shape's H.
+@pytest.mark.parametrize("M,H,C,L", [(1, 16384, 8, 1024), (3, 16384, 8, 1024), (1, 2560, 8, 1024),
+                                     (20, 2560, 4, 1024)])
+def test_maximum_shapes(orc, M, H, C, L):
+    call_and_inject(orc, inputs.Shape(M=M, H=H, C=C, L=L), seed=150 + M)
+
+
+@pytest.mark.parametrize("M", [1, 17])
+def test_int4_maximum_shape(orc, M):
+    call_and_inject(orc, inputs.Shape(M=M, H=16384, C=8, L=1024), seed=250 + M, kind="int4", group=128)
+
+
 @pytest.mark.parametrize("M,H,C,L,group", [(3, 128, 2, 64, 32), (2, 256, 4, 64, 64), (5, 256, 1, 128, 128),
                                            (4, 128, 2, 32, 32), (7, 96, 3, 32, 32),
                                            # one token: four streams (compiled-in C) and two, groups 128 and 32
