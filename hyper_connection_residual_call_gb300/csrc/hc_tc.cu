@@ -799,14 +799,17 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
 // request instead of 128; it lands as four ordinary 128-row K-block tiles) and
 // four 16-row token boxes (absent tokens and the ragged ends zero-filled by
 // TMA). The first stages' weights are requested before the dependency wait.
-// Two TMEM accumulators of 16 columns
-// alternate between tiles, so that a tile's epilogue overlaps the next tile's
-// MMAs. Roles: warp 0 lane 0 TMA, warp 1 lane 0 MMA, warps 2-5 the epilogue
+// A tile's K range is accumulated in segments of at most kLmSegStages stages (64
+// MMAs), alternating between two TMEM accumulators of 16 columns; the epilogue
+// adds a tile's segments in fp32, in order, while the next segment accumulates. Roles: warp 0 lane 0 TMA, warp 1 lane 0 MMA, warps 2-5 the epilogue
 // (TMEM lane quadrant warp % 4: 32 vocabulary rows, 16 tokens), whose stores
 // of one token are 32 consecutive logits.
 constexpr int kLmTcThreads = 192;
 constexpr int kLmTcNT = kLmHeadMaxTokens;  // one 16-token tile, MMA N = 16
 constexpr int kLmTcStages = 3;
+// Stages one TMEM accumulation takes at most (64 MMAs): longer sums in one
+// accumulator drift past the fp32 bar at H = 16384 (1024 MMAs).
+constexpr int kLmSegStages = 4;
 constexpr int kLmKbs = 4;                        // K blocks per stage (one 3-D weight box)
 constexpr uint32_t kLmTcA = kLmKbs * kTileRows * 128;  // weight box: KBS K-block tiles of 128 rows x 128 bytes
 constexpr uint32_t kLmTcB = kLmKbs * kLmTcNT * 128;    // token boxes: KBS x 16 rows x 128 bytes
@@ -886,45 +889,58 @@ hc_lm_head_tc_kernel(const LmHeadParams p, const __grid_constant__ CUtensorMap m
             load_x(g);
         }
     } else if (warp == 1 && lane == 0) {
+        // A tile's K range in segments of at most kLmSegStages stages, each accumulated
+        // in one of the two TMEM accumulators (alternating per segment) and added up
+        // by the epilogue in fp32, in order.
         const uint32_t idesc = umma_idesc_bf16(kTileRows, kLmTcNT);
-        int g = 0;
+        int g = 0, acc = 0;  // acc: segments issued so far; accumulator acc & 1
         for (int j = 0; j < my_tiles; ++j) {
-            const int b = j & 1;
-            // The accumulator's previous tile (j - 2) must have been read out.
-            if (j >= 2 && !mbar_wait_bounded(&tempty[b], ((j >> 1) - 1) & 1)) timed_out = true;
-            tc_fence_after();
-            const uint32_t d = tmem + (uint32_t)(b * kLmTcNT);
-            for (int kb = 0; kb < KB; ++kb, ++g) {
-                const int s = g % kLmTcStages, u = g / kLmTcStages;
-                if (!mbar_wait_bounded(&full[s], u & 1)) timed_out = true;
+            for (int k0 = 0; k0 < KB; k0 += kLmSegStages, ++acc) {
+                const int b = acc & 1;
+                // The accumulator's previous segment (acc - 2) must have been read out.
+                if (acc >= 2 && !mbar_wait_bounded(&tempty[b], ((acc >> 1) - 1) & 1)) timed_out = true;
                 tc_fence_after();
-                const uint32_t a0 = smem_addr(smem + s * kLmTcStage), x0 = a0 + kLmTcA;
+                const uint32_t d = tmem + (uint32_t)(b * kLmTcNT);
+                const int k1 = min(KB, k0 + kLmSegStages);
+                for (int kb = k0; kb < k1; ++kb, ++g) {
+                    const int s = g % kLmTcStages, u = g / kLmTcStages;
+                    if (!mbar_wait_bounded(&full[s], u & 1)) timed_out = true;
+                    tc_fence_after();
+                    const uint32_t a0 = smem_addr(smem + s * kLmTcStage), x0 = a0 + kLmTcA;
 #pragma unroll
-                for (int q = 0; q < kLmKbs; ++q) {
-                    const uint32_t a = a0 + q * kTileRows * 128, x = x0 + q * kLmTcNT * 128;
+                    for (int q = 0; q < kLmKbs; ++q) {
+                        const uint32_t a = a0 + q * kTileRows * 128, x = x0 + q * kLmTcNT * 128;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        umma_bf16(d, umma_desc_sw128(a + 32 * k), umma_desc_sw128(x + 32 * k), idesc,
-                                  (kb | q | k) != 0);
+                        for (int k = 0; k < 4; ++k)
+                            umma_bf16(d, umma_desc_sw128(a + 32 * k), umma_desc_sw128(x + 32 * k), idesc,
+                                      (kb != k0 || q != 0 || k != 0) ? 1u : 0u);
+                    }
+                    umma_commit(&empty[s]);
                 }
-                umma_commit(&empty[s]);
+                umma_commit(&tfull[b]);
             }
-            umma_commit(&tfull[b]);
         }
     } else if (warp >= 2) {
         const int quad = warp & 3;
+        int acc = 0;
         for (int j = 0; j < my_tiles; ++j) {
-            const int b = j & 1;
-            if (!mbar_wait_bounded(&tfull[b], (j >> 1) & 1)) timed_out = true;
-            __syncwarp();  // the TMEM load below is .aligned
-            tc_fence_after();
-            uint32_t v[16];
-            tmem_ld16_async(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kLmTcNT), v);
-            tmem_wait_ld(v);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&tempty[b]);
+            float sum[kLmTcNT];
+            for (int k0 = 0; k0 < KB; k0 += kLmSegStages, ++acc) {
+                const int b = acc & 1;
+                if (!mbar_wait_bounded(&tfull[b], (acc >> 1) & 1)) timed_out = true;
+                __syncwarp();  // the TMEM load below is .aligned
+                tc_fence_after();
+                uint32_t v[16];
+                tmem_ld16_async(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kLmTcNT), v);
+                tmem_wait_ld(v);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&tempty[b]);
+#pragma unroll
+                for (int m = 0; m < kLmTcNT; ++m)
+                    sum[m] = k0 == 0 ? __uint_as_float(v[m]) : sum[m] + __uint_as_float(v[m]);
+            }
             const int t = (int)blockIdx.x + j * (int)gridDim.x;
             const bool first = t < nt1;
             const int row = (first ? t : t - nt1) * kTileRows + quad * 32 + lane;
@@ -934,7 +950,7 @@ hc_lm_head_tc_kernel(const LmHeadParams p, const __grid_constant__ CUtensorMap m
 #pragma unroll
                 for (int m = 0; m < kLmTcNT; ++m)
                     if (m < p.M)
-                        out[(size_t)m * stride + row] = __uint_as_float(v[m]);
+                        out[(size_t)m * stride + row] = sum[m];
             }
         }
     }

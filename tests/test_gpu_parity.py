@@ -522,7 +522,8 @@ def test_entry_call_is_replicate_then_call(M, H, C, L, kind, with_inject):
 # decision at a tie point); each such element moves a logit by |w[v][h]| times
 # that step, so the logits keep the chained fp32 floor (1e-3 of their RMS).
 EXIT_CASES = [(1, 2560, 4, 320, 1000), (1, 2560, 4, 320, 32768), (5, 2560, 4, 320, 1000), (20, 2560, 4, 320, 500),
-              (3, 256, 4, 32, 777), (1, 256, 4, 32, 152), (1, 256, 4, 32, 7), (2, 2560, 4, 320, 4869)]
+              (3, 256, 4, 32, 777), (1, 256, 4, 32, 152), (1, 256, 4, 32, 7), (2, 2560, 4, 320, 4869),
+              (1, 16384, 8, 1024, 1000), (17, 16384, 2, 128, 300)]
 
 
 @pytest.mark.parametrize("M,H,C,L,V", EXIT_CASES)

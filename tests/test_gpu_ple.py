@@ -45,7 +45,7 @@ def run_gpu(hidden, rows, w, state, C):
 
 
 @pytest.mark.parametrize("M,H,C", [(1, 2560, 4), (5, 2560, 4), (12, 2560, 4), (20, 2560, 4), (3, 128, 4),
-                                   (10, 256, 2)])
+                                   (10, 256, 2), (3, 16384, 1)])
 def test_ple_matches_oracle(orc, M, H, C):
     w = inputs.make_ple_weights(H, C, 30 + M, n_rows=2048)
     rows = inputs.make_ple_rows(M, 2048, 30 + M)
