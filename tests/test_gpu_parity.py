@@ -107,7 +107,9 @@ def test_shapes_and_ragged_tokens(orc, M, H, C, L):
 # The API's maxima (H = 16384, C = 8, lowrank = 1024; a wide residual of 131072): one
 # token, the tensor-core path, the largest lowrank at the full shape's H.
 @pytest.mark.parametrize("M,H,C,L", [(1, 16384, 8, 1024), (3, 16384, 8, 1024), (1, 2560, 8, 1024),
-                                     (20, 2560, 4, 1024)])
+                                     (20, 2560, 4, 1024),
+                                     # H and lowrank not multiples of 64: the cluster split-K kernels
+                                     (3, 16376, 8, 1000), (1, 16376, 8, 1000)])
 def test_maximum_shapes(orc, M, H, C, L):
     call_and_inject(orc, inputs.Shape(M=M, H=H, C=C, L=L), seed=150 + M)
 
