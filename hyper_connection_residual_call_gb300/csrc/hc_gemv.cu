@@ -1112,6 +1112,342 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
         mbar_wait_bounded(bar, 0);
 }
 
+// ---- few tokens (2 <= M <= kFewMaxTokens), bf16 weights -----------------------
+//
+// The one-token kernels' layout with the token loop inside: the down kernel
+// streams its weight rows once and dots them with every token's chunk; the up
+// kernel reduces every token's partials and loops over the tokens in its dots
+// and mix. Two kernels per call, as at one token, in place of the tensor-core
+// path's four. Partials: token m of chunk s at part1[copy][s][m][row], its sum of
+// squares at ssq1[copy][s * M + m].
+
+struct DownmSmem {
+    size_t bar, w, g, red, total;
+};
+
+__host__ __device__ inline DownmSmem downm_layout(const DownParams &p, int nwarps)
+{
+    DownmSmem s;
+    s.bar = 0;
+    s.w = 128;
+    s.g = round_up_sz(s.w + (size_t)p.KC * 2 * p.rows_per_block, 128);
+    s.red = round_up_sz(s.g + (size_t)p.KC * 2, 128);
+    s.total = round_up_sz(s.red + sizeof(float) * (size_t)nwarps * p.M * (kRowsPerGroup + 1), 128);
+    return s;
+}
+
+__global__ void __launch_bounds__(1024, 1) hc_downm_kernel(const DownParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int nwarps = blockDim.x >> 5;
+    const DownmSmem lay = downm_layout(p, nwarps);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + lay.bar);
+    const unsigned char *w_s = smem + lay.w;
+    const uint16_t *g_s = reinterpret_cast<const uint16_t *>(smem + lay.g);
+    float *red_s = reinterpret_cast<float *>(smem + lay.red);  // [warp][token][kRowsPerGroup + 1]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int s = blockIdx.x;
+    const int r0 = blockIdx.y * p.rows_per_block;
+    const int nrows = min(p.rows_per_block, p.R - r0);
+    const int KC = p.KC, k0 = s * KC, nv = KC / 8, M = p.M;
+    const size_t seg = (size_t)KC * 2;
+    const int tpg = down1_group_threads(p), wpg = tpg / 32;
+    const int ngroups = blockDim.x / tpg;
+    const int rpg = (nrows + ngroups - 1) / ngroups;
+    const int grp = tid / tpg, v = tid % tpg;
+    const int gr0 = grp * rpg, gnr = max(0, min(rpg, nrows - gr0));
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0)
+            mbar_arrive_expect_tx(bar, (uint32_t)(seg * nrows + (size_t)KC * 2));
+        __syncwarp();
+        for (int j = lane; j <= nrows; j += 32) {
+            if (j == nrows) {
+                bulk_copy_g2s(smem + lay.g, p.g + k0, (uint32_t)KC * 2, bar);
+            } else {
+                const int gr = r0 + j;
+                const uint16_t *src = gr < p.L ? static_cast<const uint16_t *>(p.down.data) + (size_t)gr * p.W
+                                               : static_cast<const uint16_t *>(p.inject.data) + (size_t)(gr - p.L) * p.W;
+                bulk_copy_g2s(smem + lay.w + j * seg, src + k0, (uint32_t)seg, bar);
+            }
+        }
+    }
+
+    pdl_wait();  // the residual and the previous gates come from earlier kernels
+
+    const bool has_v = v < nv;
+    const long roff = (long)(k0 / p.H) * p.raw_cstride + k0 % p.H + v * 8;
+    auto load_tok = [&](int t, uint4 &rv, uint4 &ov, float &gt) {
+        rv = make_uint4(0, 0, 0, 0);
+        ov = make_uint4(0, 0, 0, 0);
+        gt = 0.f;
+        if (has_v && t < M) {
+            rv = *reinterpret_cast<const uint4 *>(p.raw + (size_t)t * p.raw_mstride + roff);
+            if (p.inj_out) {
+                ov = *reinterpret_cast<const uint4 *>(p.inj_out + (size_t)t * p.H + k0 % p.H + v * 8);
+                gt = p.inj_gate[(size_t)t * p.inj_stride + k0 / p.H];
+            }
+        }
+    };
+    uint4 rvn, ovn;
+    float gtn;
+    load_tok(0, rvn, ovn, gtn);
+    // The up kernel may read the residual and the previous gates before its own
+    // wait once every CTA of this kernel has passed its wait.
+    pdl_launch_dependents();
+    const bool timed_out = !mbar_wait_bounded(bar, 0);
+    if (timed_out)
+        record_timeout(p.status);
+    float gf[8];
+    unpack_bf16x8(has_v ? *reinterpret_cast<const uint4 *>(g_s + v * 8) : make_uint4(0, 0, 0, 0), gf);
+
+    for (int t = 0; t < M; ++t) {
+        const uint4 rvv = rvn, ovv = ovn;
+        const float gt = gtn;
+        load_tok(t + 1, rvn, ovn, gtn);  // the next token's loads, in flight during this one
+        float x[8], q = 0.f;
+        {
+            float rf[8];
+            unpack_bf16x8(rvv, rf);
+            if (p.inj_out) {
+                float of[8];
+                unpack_bf16x8(ovv, of);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    rf[e] = __bfloat162float(__float2bfloat16_rn(fmaf(of[e], gt, rf[e])));
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                q = fmaf(rf[e], rf[e], q);
+                x[e] = rf[e] * gf[e];
+            }
+        }
+        uint64_t xp[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            xp[e] = f32x2(x[2 * e], x[2 * e + 1]);
+        float acc[kRowsPerGroup];
+#pragma unroll
+        for (int j = 0; j < kRowsPerGroup; ++j) {
+            acc[j] = 0.f;
+            if (has_v && j < gnr) {
+                const uint4 wq = *reinterpret_cast<const uint4 *>(w_s + (size_t)(gr0 + j) * seg + v * 16);
+                uint64_t a = 0;
+                a = ffma2(bf16x2_as_f32x2(wq.x), xp[0], a);
+                a = ffma2(bf16x2_as_f32x2(wq.y), xp[1], a);
+                a = ffma2(bf16x2_as_f32x2(wq.z), xp[2], a);
+                a = ffma2(bf16x2_as_f32x2(wq.w), xp[3], a);
+                acc[j] = f32x2_sum(a);
+            }
+        }
+        const float rsum = warp_transpose_sum8(acc, lane);
+        float *rw = red_s + ((size_t)warp * M + t) * (kRowsPerGroup + 1);
+        if ((lane & 3) == 0)
+            rw[lane >> 2] = rsum;
+        q = warp_sum(q);
+        if (lane == 0)
+            rw[kRowsPerGroup] = q;
+    }
+    __syncthreads();
+
+    for (int i = tid; i < nrows * M; i += blockDim.x) {  // (token, row of the block)
+        const int t = i / nrows, r = i % nrows;
+        const int g = r / rpg, j = r % rpg;
+        float sum = 0.f;
+        for (int w = 0; w < wpg; ++w)
+            sum += red_s[((size_t)(g * wpg + w) * M + t) * (kRowsPerGroup + 1) + j];
+#pragma unroll
+        for (int c = 0; c < kPartCopies; ++c)
+            p.part1[c * p.part1_stride + ((size_t)s * M + t) * p.R + r0 + r] = sum;
+    }
+    if (blockIdx.y == 0 && tid < M) {  // every group saw the same inputs: use group 0
+        float sum = 0.f;
+        for (int w = 0; w < wpg; ++w)
+            sum += red_s[((size_t)w * M + tid) * (kRowsPerGroup + 1) + kRowsPerGroup];
+#pragma unroll
+        for (int c = 0; c < kPartCopies; ++c)
+            p.ssq1[c * kSsqStride + s * M + tid] = sum;
+    }
+    if (timed_out)
+        mbar_wait_bounded(bar, 0);
+}
+
+struct UpmSmem {
+    size_t bar, w, act, ssq, inv, total;
+};
+
+__host__ __device__ inline UpmSmem upm_layout(const UpParams &p)
+{
+    UpmSmem s;
+    s.bar = 0;
+    s.w = 128;
+    s.act = round_up_sz(s.w + (size_t)p.L * 2 * p.C * p.HB, 128);
+    s.ssq = round_up_sz(s.act + sizeof(float) * (size_t)p.M * p.L, 128);
+    s.inv = round_up_sz(s.ssq + sizeof(float) * (size_t)p.M * kMaxCluster, 16);
+    s.total = round_up_sz(s.inv + sizeof(float) * (size_t)p.M * kMaxCluster, 128);
+    return s;
+}
+
+// CC: the stream count when it is a compile-time constant (4), else 0.
+template <int CC>
+__global__ void __launch_bounds__(1024, 1) hc_upm_kernel(const UpParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const UpmSmem lay = upm_layout(p);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + lay.bar);
+    const unsigned char *w_s = smem + lay.w;
+    float *act_s = reinterpret_cast<float *>(smem + lay.act);    // [M][L]
+    float *ssq_s = reinterpret_cast<float *>(smem + lay.ssq);    // [M][S]
+    float *invq_s = reinterpret_cast<float *>(smem + lay.inv);   // [M][S]: inv_rms of chunk q's stream
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int HB = p.HB, h0 = blockIdx.x * HB;
+    const int hb = min(HB, p.H - h0);
+    const int L = p.L, M = p.M, S = p.S;
+    const size_t row_bytes = (size_t)L * 2;
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+        mbar_arrive_expect_tx(bar, (uint32_t)(row_bytes * hb * p.C));
+        for (int c = 0; c < p.C; ++c)
+            bulk_copy_g2s(smem + lay.w + (size_t)c * HB * row_bytes,
+                          static_cast<const unsigned char *>(p.up.data) + ((size_t)c * p.H + h0) * row_bytes,
+                          (uint32_t)(row_bytes * hb), bar);
+    }
+
+    const int hl = warp, h = h0 + hl;
+    const bool h_ok = hl < hb;
+    const int hc = lane >> 2;
+    const bool holder = h_ok && (lane & 3) == 0 && hc < p.C;
+    // Read before the dependency wait (the down kernel triggers after its own
+    // wait): g, and each token's residual element and previous gate (.cg).
+    float gval = 0.f, rv[kFewMaxTokens], ov[kFewMaxTokens], gp[kFewMaxTokens];
+#pragma unroll
+    for (int t = 0; t < kFewMaxTokens; ++t) {
+        rv[t] = ov[t] = gp[t] = 0.f;
+        if (holder && t < M) {
+            rv[t] = __bfloat162float(__ushort_as_bfloat16(__ldcg(p.raw + (size_t)t * p.raw_mstride +
+                                                                 (size_t)hc * p.raw_cstride + h)));
+            if (p.inj_out) {
+                ov[t] = __bfloat162float(__ushort_as_bfloat16(__ldcg(p.inj_out + (size_t)t * p.H + h)));
+                gp[t] = __ldcg(p.inj_gate + (size_t)t * p.inj_stride + hc);
+            }
+        }
+    }
+    if (holder)
+        gval = __bfloat162float(__ushort_as_bfloat16(p.g[hc * p.H + h]));
+
+    pdl_wait();  // the partials come from the down kernel
+
+    const int copy = blockIdx.x % kPartCopies;
+    const float *part = p.part1 + copy * p.part1_stride;
+    const float *ssq = p.ssq1 + copy * kSsqStride;
+    for (int i = tid; i < M * S; i += blockDim.x)
+        ssq_s[i] = ssq[i];  // [s][m] as written
+    pdl_launch_dependents();
+    __syncthreads();
+    for (int i = tid; i < M * S; i += blockDim.x) {  // token m = i % M, chunk q = i / M: its stream's inv_rms
+        const int m = i % M, q = i / M, c = q / p.sps;
+        float t = 0.f;
+        for (int j = 0; j < p.sps; ++j)
+            t += ssq_s[(c * p.sps + j) * M + m];
+        const float iv = rsqrtf(fmaf(t, p.inv_H, p.eps));
+        invq_s[q * M + m] = iv;
+        if (blockIdx.x == 0 && q % p.sps == 0)
+            p.inv_out[(size_t)m * p.C + c] = iv;
+    }
+    __syncthreads();
+    // act for every (token, row): the chunks' partials summed in order; a thread's
+    // pairs two at a time, all their loads in flight together.
+    constexpr int kPairs = 2;
+    for (int i0 = tid; i0 < M * p.R; i0 += kPairs * blockDim.x) {
+        float pv[kPairs][kMaxCluster];
+#pragma unroll
+        for (int u = 0; u < kPairs; ++u) {
+            const int i = i0 + u * blockDim.x, m = i / p.R, k = i % p.R;
+#pragma unroll
+            for (int q = 0; q < kMaxCluster; ++q)
+                pv[u][q] = (i < M * p.R && q < S) ? part[((size_t)q * M + m) * p.R + k] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kPairs; ++u) {
+            const int i = i0 + u * blockDim.x, m = i / p.R, k = i % p.R;
+            if (i >= M * p.R)
+                break;
+            float z = 0.f;
+#pragma unroll
+            for (int q = 0; q < kMaxCluster; ++q)
+                if (q < S) z = fmaf(invq_s[q * M + m], pv[u][q], z);
+            const float zc = z * p.inv_C;
+            if (k < L) {
+                const float a = zc * sigmoid_fast(zc);
+                act_s[(size_t)m * L + k] = a;
+                if (blockIdx.x == 0)
+                    p.act_out[(size_t)m * L + k] = a;
+            } else if (blockIdx.x == 0 && p.gate) {
+                p.gate[(size_t)m * p.gate_stride + (k - L)] = 2.0f * sigmoid_fast(zc);
+            }
+        }
+    }
+    const bool timed_out = !mbar_wait_bounded(bar, 0);
+    if (timed_out)
+        record_timeout(p.status);
+    __syncthreads();
+
+    if (h_ok) {  // warp-uniform
+        constexpr int NC = CC > 0 ? CC : 8;
+        const uint32_t *wr = reinterpret_cast<const uint32_t *>(w_s) + (size_t)hl * (L / 2);
+        const size_t cstride = (size_t)HB * (L / 2);
+        for (int t = 0; t < M; ++t) {
+            float nvh = 0.f, rt = rv[0], ot = ov[0], gt = gp[0];
+#pragma unroll
+            for (int u = 1; u < kFewMaxTokens; ++u)
+                if (u == t) { rt = rv[u]; ot = ov[u]; gt = gp[u]; }
+            if (holder) {
+                if (p.inj_out)
+                    rt = __bfloat162float(__float2bfloat16_rn(fmaf(ot, gt, rt)));
+                if (p.raw_out)  // the stored residual [M][C*H], whatever view it was read through
+                    p.raw_out[(size_t)t * p.W + (size_t)hc * p.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(rt));
+                nvh = rt * invq_s[(hc * p.sps) * M + t] * gval;
+            }
+            uint64_t a2[NC];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) a2[c] = 0;
+            const float *act_t = act_s + (size_t)t * L;
+#pragma unroll 2
+            for (int j = lane; j < L / 2; j += 32) {
+                const uint64_t xpair = *reinterpret_cast<const uint64_t *>(act_t + 2 * j);
+#pragma unroll
+                for (int c = 0; c < NC; ++c)
+                    if (CC > 0 || c < p.C)
+                        a2[c] = ffma2(bf16x2_as_f32x2(wr[c * cstride + j]), xpair, a2[c]);
+            }
+            float acc[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] = c < NC ? f32x2_sum(a2[c < NC ? c : 0]) : 0.f;
+            const float d = warp_transpose_sum8(acc, lane);
+            const float wv = sigmoid_fast(d);
+            if (p.w_out && holder)
+                p.w_out[(size_t)t * p.C * p.H + hc * p.H + h] = wv;
+            float term = holder ? wv * nvh : 0.f;
+            term += __shfl_xor_sync(0xffffffffu, term, 4);
+            term += __shfl_xor_sync(0xffffffffu, term, 8);
+            term += __shfl_xor_sync(0xffffffffu, term, 16);
+            if (lane == 0)
+                p.mixed[(size_t)t * p.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(term * p.inv_C));
+        }
+    }
+    if (timed_out)
+        mbar_wait_bounded(bar, 0);
+}
+
 
 __global__ void __launch_bounds__(256) hc_inject_kernel(const InjectParams p)
 {
@@ -1303,6 +1639,36 @@ bool one_token_ok(const DownParams &d, const UpParams &u)
     if (down1_groups(d) * down1_group_threads(d) > 1024 || up1_threads(u) > 1024)
         return false;
     return down1_layout(d).total <= kSmemBudget && up1_layout(u).total <= kSmemBudget;
+}
+
+int downm_threads(const DownParams &d) { return down1_groups(d) * down1_group_threads(d); }
+
+bool few_tokens_ok(const DownParams &d, const UpParams &u)
+{
+    if (d.M < 2 || d.M > kFewMaxTokens || d.down.type != 0 || u.up.type != 0 || d.S > kMaxCluster || d.C > 8 ||
+        u.HB > 32 || u.R > 1024 || d.M * d.S > kSsqStride)
+        return false;
+    if (downm_threads(d) > 1024 || up1_threads(u) > 1024)
+        return false;
+    return downm_layout(d, downm_threads(d) / 32).total <= kSmemBudget && upm_layout(u).total <= kSmemBudget;
+}
+
+cudaError_t launch_few_tokens(const DownParams &d, const UpParams &u, const LaunchCfg &cfg, cudaStream_t stream)
+{
+    if (!few_tokens_ok(d, u))
+        return cudaErrorInvalidConfiguration;
+    void (*ku)(UpParams) = u.C == 4 ? hc_upm_kernel<4> : hc_upm_kernel<0>;
+    const size_t sd = downm_layout(d, downm_threads(d) / 32).total, su = upm_layout(u).total;
+    cudaError_t e = allow_smem(hc_downm_kernel, sd);
+    if (e == cudaSuccess)
+        e = allow_smem(ku, su);
+    if (e != cudaSuccess)
+        return e;
+    const dim3 dgrid(d.S, (d.R + d.rows_per_block - 1) / d.rows_per_block, 1);
+    e = launch_ex(hc_downm_kernel, dgrid, dim3(downm_threads(d)), sd, stream, 0, cfg.pdl, d);
+    if (e != cudaSuccess)
+        return e;
+    return launch_ex(ku, dim3((u.H + u.HB - 1) / u.HB), dim3(up1_threads(u)), su, stream, 0, cfg.pdl, u);
 }
 
 cudaError_t launch_one_token(const DownParams &d, const UpParams &u, const LaunchCfg &cfg, cudaStream_t stream)

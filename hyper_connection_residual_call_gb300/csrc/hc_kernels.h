@@ -55,6 +55,11 @@ struct DownParams {
 
 // Copies of the one-token partials; up CTA b reads copy b % kPartCopies.
 constexpr int kPartCopies = 8;
+// The few-token path (2 <= M <= kFewMaxTokens, bf16 weights): the one-token
+// kernels' layout with a token loop inside. Each token adds a serial chain to
+// both kernels, so it beats the tensor-core path (about 13.5 µs per call at the
+// full shape from 2 to 16 tokens) at 2 tokens (10.4 µs) but not from 4.
+constexpr int kFewMaxTokens = 2;
 constexpr long kSsqStride = 64;  // floats between the copies of the sums of squares
 
 // Up projection + sigmoid + mean mix: CTA b owns h in [b*HB, b*HB + HB) of
@@ -91,7 +96,8 @@ struct UpParams {
     float eps, inv_H;
     float *act_out;           // [L]
     float *inv_out;           // [C]
-    float *gate;              // gates (R > L), or nullptr
+    float *gate;              // gates (R > L), or nullptr; token m's at gate + m * gate_stride
+    long gate_stride;
     // Optional debug output: w = sigmoid(up(act)) fp32 [M][W], or nullptr.
     float *w_out;
 };
@@ -165,6 +171,8 @@ cudaError_t launch_down(const DownParams &p, const LaunchCfg &cfg, cudaStream_t 
 // d.ssq1 and hc_up1_kernel reduces them (u.part1 / u.ssq1 point at the same
 // buffers). one_token_ok says whether a shape fits these kernels' limits.
 bool one_token_ok(const DownParams &d, const UpParams &u);
+bool few_tokens_ok(const DownParams &d, const UpParams &u);
+cudaError_t launch_few_tokens(const DownParams &d, const UpParams &u, const LaunchCfg &cfg, cudaStream_t stream);
 cudaError_t launch_one_token(const DownParams &d, const UpParams &u, const LaunchCfg &cfg, cudaStream_t stream);
 
 cudaError_t launch_up(const UpParams &p, const LaunchCfg &cfg, cudaStream_t stream);

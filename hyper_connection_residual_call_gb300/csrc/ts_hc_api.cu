@@ -243,9 +243,9 @@ WsLayout ws_layout(int M, int H, int C, int L)
     w.inv_rms = 0;
     w.act = align256(sizeof(float) * (size_t)M * C);
     w.total = w.act + align256(sizeof(float) * (size_t)M * L);
-    if (M == 1) {  // one token: the down kernel leaves partials, the up kernel reduces them
+    if (M >= 1 && M <= tshc::kFewMaxTokens) {  // the down kernel leaves partials, the up kernel reduces them
         w.part1 = w.total;
-        w.ssq1 = w.part1 + tshc::kPartCopies * align256(sizeof(float) * kPart1Chunks * ((size_t)L + C));
+        w.ssq1 = w.part1 + tshc::kPartCopies * align256(sizeof(float) * kPart1Chunks * (size_t)M * ((size_t)L + C));
         w.total = w.ssq1 + tshc::kPartCopies * sizeof(float) * tshc::kSsqStride;
     }
     if (tc_path_ok(M, H, C, L)) {  // normed hi/lo, per-chunk partials, act hi/lo
@@ -342,7 +342,11 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
     const bool all_int4 = down->type == TS_W_INT4_AFFINE && up->type == TS_W_INT4_AFFINE &&
                           (!inject || inject->type == TS_W_INT4_AFFINE) && down->group % 8 == 0 &&
                           up->group % 8 == 0;
-    if (tc_path_ok(M, H, C, L) && (all_bf16 || all_int4)) {
+    // From 2 to kFewMaxTokens tokens bf16 calls try the few-token kernels first
+    // (two kernels, no tensor cores), and take the tensor-core path when the
+    // shape does not fit them.
+    const bool few_first = all_bf16 && M >= 2 && M <= tshc::kFewMaxTokens;
+    auto run_tc = [&]() -> ts_status {
         const tshc::TcPlan pl = tshc::tc_plan(M, L, C, W);
         tshc::TcCall t{};
         const int R = L + (inject ? C : 0);
@@ -418,7 +422,10 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         if (e != cudaSuccess)
             return cuda_fail(e, "launching the tensor-core path");
         return TS_OK;
-    }
+    };
+    const bool tc_ok = tc_path_ok(M, H, C, L) && (all_bf16 || all_int4);
+    if (tc_ok && !few_first)
+        return run_tc();
 
     tshc::DownParams d{};
     d.raw = static_cast<const uint16_t *>(raw);
@@ -482,12 +489,13 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
 
     const tshc::LaunchCfg cfg{dev.sm_count, true};
     cudaError_t e;
-    if (M == 1) {
-        // One token: the down kernel leaves per-chunk partials and the up
-        // kernel reduces them, so neither kernel waits on another CTA.
+    if (M <= tshc::kFewMaxTokens) {
+        // One token (and, with bf16 weights, up to kFewMaxTokens): the down kernel
+        // leaves per-chunk partials and the up kernel reduces them, so neither
+        // kernel waits on another CTA.
         d.part1 = reinterpret_cast<float *>(wsb + wl.part1);
         d.ssq1 = reinterpret_cast<float *>(wsb + wl.ssq1);
-        d.part1_stride = (long)(align256(sizeof(float) * kPart1Chunks * ((size_t)L + C)) / sizeof(float));
+        d.part1_stride = (long)(align256(sizeof(float) * kPart1Chunks * (size_t)M * ((size_t)L + C)) / sizeof(float));
         u.part1 = d.part1;
         u.ssq1 = d.ssq1;
         u.part1_stride = d.part1_stride;
@@ -499,13 +507,22 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
         u.act_out = act;
         u.inv_out = inv_rms;
         u.gate = inject ? inject_w : nullptr;
-        if (d.S <= kPart1Chunks && tshc::one_token_ok(d, u)) {
+        u.gate_stride = inject_stride;
+        if (M == 1 && d.S <= kPart1Chunks && tshc::one_token_ok(d, u)) {
             e = tshc::launch_one_token(d, u, cfg, stream);
             if (e != cudaSuccess)
                 return cuda_fail(e, "launching the one-token kernels");
             return TS_OK;
         }
+        if (few_first && d.S <= kPart1Chunks && tshc::few_tokens_ok(d, u)) {
+            e = tshc::launch_few_tokens(d, u, cfg, stream);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "launching the few-token kernels");
+            return TS_OK;
+        }
     }
+    if (tc_ok)  // the few-token kernels do not take this shape
+        return run_tc();
     e = tshc::launch_down(d, cfg, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "launching the down kernel");

@@ -293,7 +293,7 @@ def run_stack_gpu_fused(st, H, C):
     return out, raw
 
 
-@pytest.mark.parametrize("M", [1, 3, 128])
+@pytest.mark.parametrize("M", [1, 2, 3, 128])
 def test_fused_inject_call_is_bit_identical(M):
     s = inputs.FULL_DECODE
     H, C, L = s.H, s.C, s.L
@@ -495,6 +495,7 @@ def test_stack_driver_rejects_bad_sublayer_outputs():
 
 
 @pytest.mark.parametrize("M,H,C,L,kind", [(1, 2560, 4, 320, "bf16"), (1, 256, 4, 32, "bf16"), (3, 256, 4, 32, "bf16"),
+                                          (2, 2560, 4, 320, "bf16"),
                                           (16, 2560, 4, 320, "bf16"), (1, 2560, 4, 320, "int4"),
                                           (64, 2560, 4, 320, "int4"), (3, 40, 3, 24, "bf16")])
 @pytest.mark.parametrize("with_inject", [True, False])
