@@ -19,8 +19,8 @@ results read back inside the timed region.
 
 ``other_configs`` (skipped with --no-configs) times the rest of the workload
 family the same way, each over distinct weight sets: the M=128 prefill
-micro-batch (attn_hc + mlp_hc per batch, tensor-core path), an 8-token decode
-batch, the INT4-affine full shape at M=1 and M=64, the decoder's exit (mixer +
+micro-batch (attn_hc + mlp_hc per batch, tensor-core path), a 2-token decode
+batch (two-token kernels) and an 8-token one (tensor cores), the INT4-affine full shape at M=1 and M=64, the decoder's exit (mixer +
 lm_head at a synthetic vocabulary of 32768) and the PLE gate at M=1 and M=16,
 and the 40-layer stack (entry fused into layer 0, 80 fused calls, exit mixer)
 at M=1 and M=16.
@@ -378,6 +378,19 @@ def measure_other_configs(B, inputs, torch, dev, stream, sets_bf16, peak):
         out[name] = {"M": Mx, "calls_per_s": n_calls / (ms / 1e3), "tokens_per_s": Mx * n_calls / (ms / 1e3),
                      "us_per_call": 1e3 * ms / n_calls, "bytes_per_call": bytes_call, "hbm_gbs": gbs,
                      "frac": gbs / peak, **(extra or {})}
+
+    # A 2-token decode batch (the few-token kernels): fused calls over distinct weight sets.
+    Md2 = 2
+    raw = inputs.make_residual(Md2, H, C, 7).to(dev)
+    outs = [inputs.make_sublayer_out(Md2, H, 7, i).to(dev) for i in range(4)]
+    gates = torch.zeros((2, Md2, C), dtype=torch.float32, device=dev)
+    slots = [(gates[0], C), (gates[1], C)]
+    mixed = torch.empty((Md2, H), dtype=torch.bfloat16, device=dev)
+    ws = B.workspace(Md2, H, C, L, dev)
+    n = 2 * len(sets_bf16)
+    ms = graph_ms(chain(raw, outs, gates, sets_bf16, n, mixed, ws, slots), 5)
+    record(f"decode_m{Md2}_bf16", Md2, ms, n, bytes_per_call(Md2, sets_bf16[0].nbytes),
+           {"path": "two-token kernels (the one-token layout with a token loop)"})
 
     # Prefill micro-batch: M = 128, attn_hc + inject then mlp_hc + inject per batch,
     # token t's gates at t*2C (attn) and t*2C + C (mlp).

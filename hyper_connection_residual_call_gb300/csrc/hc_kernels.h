@@ -57,9 +57,9 @@ struct DownParams {
 constexpr int kPartCopies = 8;
 // The few-token path (2 <= M <= kFewMaxTokens, bf16 weights): the one-token
 // kernels' layout with a token loop inside. Each token adds a serial chain to
-// both kernels, so it beats the tensor-core path (about 13.5 µs per call at the
-// full shape from 2 to 16 tokens) at 2 tokens (10.4 µs) but not from 4.
-constexpr int kFewMaxTokens = 2;
+// both kernels, so it beats the tensor-core path (about 13.6 µs per call at the
+// full shape from 2 to 16 tokens) at 2 and 3 tokens (9.4 and 11.7 µs) but not at 4.
+constexpr int kFewMaxTokens = 3;
 constexpr long kSsqStride = 64;  // floats between the copies of the sums of squares
 
 // Up projection + sigmoid + mean mix: CTA b owns h in [b*HB, b*HB + HB) of

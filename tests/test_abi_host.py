@@ -44,12 +44,12 @@ def test_workspace_size_and_layout(lib):
     # down kernel's per-chunk partials [nchunk][L+C][Mp] fp32 and the activations as
     # bf16 hi + lo [M][L] x 2. The K split aims at 152 CTAs: at M=128 (one 128-token
     # tile, 3 row tiles) 160 K blocks of 64 go 4 to a chunk, 40 chunks.
-    # At 2 tokens the few-token kernels' partials come first: 8 copies of up to 8 chunks x
-    # M tokens of per-row partials, and of the sums of squares.
+    # At 2 and 3 tokens the few-token kernels' partials come first: 8 copies of up to 8
+    # chunks x M tokens of per-row partials, and of the sums of squares.
     for M, nchunk, Mp in ((128, 40, 128), (2, 40, 16), (15, 40, 16), (16, 40, 16), (40, 40, 48),
-                          (300, 16, 384), (8, 40, 16)):
+                          (300, 16, 384), (8, 40, 16), (3, 40, 16)):
         tc = 2 * a256(2 * M * C * H) + a256(4 * nchunk * (L + C) * Mp) + 2 * a256(2 * M * L)
-        few = 8 * a256(4 * 8 * M * (L + C)) + 8 * 4 * 64 if M <= 2 else 0
+        few = 8 * a256(4 * 8 * M * (L + C)) + 8 * 4 * 64 if M <= 3 else 0
         assert B.ts_hc_workspace_bytes(M, H, C, L) == a256(4 * M * C) + a256(4 * M * L) + few + tc, M
     # shapes the tensor-core path does not take (lowrank not a multiple of 64): inv_rms, act
     assert B.ts_hc_workspace_bytes(15, H, C, 32) == a256(4 * 15 * C) + a256(4 * 15 * 32)

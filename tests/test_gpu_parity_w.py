@@ -85,6 +85,7 @@ PATHS = {
     "few-token bf16 full shape": (2, 2560, 4, 320, "bf16", 0),
     "few-token bf16 eight streams": (2, 1024, 8, 128, "bf16", 0),
     "few-token bf16 one stream, odd lowrank": (2, 96, 1, 40, "bf16", 0),
+    "few-token bf16 three tokens": (3, 2560, 4, 320, "bf16", 0),
     # from 2 tokens, shapes the tensor cores do not take: the cluster split-K kernels
     "cluster bf16 odd shape": (3, 40, 3, 24, "bf16", 0),
     "cluster bf16 five streams": (11, 96, 5, 40, "bf16", 0),
