@@ -610,3 +610,19 @@ def test_bounded_wait_records_a_timeout_and_the_context_stays_usable(orc):
 
 def test_device_status_clean():
     assert B.device_status() == B.TS_OK
+
+
+@pytest.mark.parametrize("M", [2, 3])
+def test_few_tokens_equal_one_token_calls(M):
+    """The few-token kernels keep the one-token kernels' layout and summation order, so M
+    tokens in one call give, bit for bit, what M one-token calls give (tokens are
+    independent: families/qwen4/mod.rs, "Chunked prefill is wired")."""
+    s = inputs.FULL_DECODE
+    H, C, L = s.H, s.C, s.L
+    w = inputs.make_hc_weights(H, C, L, 61).to("cuda")
+    raw = inputs.make_residual(M, H, C, 61).cuda()
+    mixed, gates = B.hc_call(raw, w, H=H, C=C)
+    for t in range(M):
+        m1, g1 = B.hc_call(raw[t:t + 1].clone(), w, H=H, C=C)
+        torch.cuda.synchronize()
+        assert torch.equal(m1, mixed[t:t + 1]) and torch.equal(g1, gates[t:t + 1]), f"token {t}"
