@@ -239,7 +239,7 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
     const int r0 = rt * kTileRows;
     const int KBT = p.W / kKBlock, kb0 = kc * p.KBc;
     const int KB = min(p.KBc, KBT - kb0);
-    const uint32_t ncols = tmem_cols(NT);
+    const uint32_t ncols = tmem_cols(2 * NT);  // columns [0, NT): W * B_hi, [NT, 2 NT): W * B_lo
 
     // Boxes of 32 rows making up this row tile: from W_down, from
     // block_inject_weight (rows beyond its C are zero-filled), or skipped.
@@ -383,8 +383,12 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
                 mbar_arrive(&fullp[s]);
         }
     } else if (warp == 1 && lane == 0) {
-        // MMA issuer.
-        const uint32_t idesc = umma_idesc_bf16(kTileRows, NT);
+        // MMA issuer. B_lo follows B_hi in the stage, a whole number of 8-row
+        // swizzle atoms later, so [B_hi; B_lo] is one K-major operand of 2 NT rows:
+        // one MMA of N = 2 NT per K step instead of one per part (an MMA
+        // instruction costs about the same from N = 16 to N = 128).
+        const uint32_t idesc2 = umma_idesc_bf16(kTileRows, 2 * NT);
+        const uint32_t idesc1 = umma_idesc_bf16(kTileRows, NT);
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % NS, u = kb / NS;
             if (!mbar_wait_bounded(&full[s], u & 1)) timed_out = true;
@@ -392,13 +396,12 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
             tc_fence_after();
             const uint32_t a = smem_addr(smem + lay.ring + s * lay.stage_bytes);
             const uint32_t al = a + lay.a_bytes;  // A_lo (INT4 weights)
-            const uint32_t bh = a + b_off, bl = bh + lay.b_bytes;
+            const uint32_t bh = a + b_off;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(bh + 32 * k), idesc, (kb | k) != 0);
-                umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(bl + 32 * k), idesc, 1);
-                if (WT == 1)  // the weight's lo part against the activation's hi part
-                    umma_bf16(tmem, umma_desc_sw128(al + 32 * k), umma_desc_sw128(bh + 32 * k), idesc, 1);
+                umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(bh + 32 * k), idesc2, (kb | k) != 0);
+                if (WT == 1)  // the weight's lo part against the activation's hi part (columns [0, NT))
+                    umma_bf16(tmem, umma_desc_sw128(al + 32 * k), umma_desc_sw128(bh + 32 * k), idesc1, 1);
             }
             umma_commit(&empty[s]);
         }
@@ -406,10 +409,10 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
     }
 
     // Epilogue on all 16 warps: warp w reads TMEM lanes 32*(w%4).. (the tile's
-    // rows) for the 16-column chunks 16*(w/4) + 64k -- all of them before the
-    // one wait -- and stores them to part[chunk][token][row]: the 32 lanes of a
-    // store write 32 consecutive rows of one token (coalesced). The barrier
-    // reconverges the single-thread roles.
+    // rows) for the 16-column chunks 16*(w/4) + 64k, the hi and the lo parts --
+    // all of them before the one wait -- adds the two, and stores them to
+    // part[chunk][token][row]: the 32 lanes of a store write 32 consecutive rows
+    // of one token (coalesced). The barrier reconverges the single-thread roles.
     __syncthreads();
     if (!mbar_wait_bounded(done, 0)) timed_out = true;
     __syncwarp();  // the TMEM loads below are .aligned
@@ -420,14 +423,18 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
         const int quad = warp & 3, part = warp >> 2;
         const int gr = r0 + quad * 32 + lane;
         const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16);
-        uint32_t v[kChunks][16];
+        uint32_t v[kChunks][16], w[kChunks][16];
 #pragma unroll
         for (int k = 0; k < kChunks; ++k)
-            if (16 * part + 16 * kParts * k < NT)  // warp-uniform
+            if (16 * part + 16 * kParts * k < NT) {  // warp-uniform
                 tmem_ld16_async(tbase + 16 * part + 16 * kParts * k, v[k]);
+                tmem_ld16_async(tbase + NT + 16 * part + 16 * kParts * k, w[k]);
+            }
 #pragma unroll
-        for (int k = 0; k < kChunks; ++k)
+        for (int k = 0; k < kChunks; ++k) {
             tmem_wait_ld(v[k]);
+            tmem_wait_ld(w[k]);
+        }
         if (gr < p.R) {
             float *dst = p.part + ((size_t)kc * p.Mp + (size_t)tile * NT) * p.R + gr;
 #pragma unroll
@@ -436,7 +443,7 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
                 if (c0 < NT) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        dst[(size_t)(c0 + j) * p.R] = __uint_as_float(v[k][j]);
+                        dst[(size_t)(c0 + j) * p.R] = __uint_as_float(v[k][j]) + __uint_as_float(w[k][j]);
                 }
             }
         }
@@ -554,7 +561,7 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
     const int h0 = blockIdx.x * HBt;
     const int tile = blockIdx.y;
     const int KB = p.L / kKBlock;
-    const uint32_t ncols = tmem_cols(NT);
+    const uint32_t ncols = tmem_cols(2 * NT);  // columns [0, NT): Wu * act_hi, [NT, 2 NT): Wu * act_lo
 
     pdl_launch_dependents();
     if (tid == 0) {
@@ -684,7 +691,10 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
     }
 
     if (warp == 1 && lane == 0) {
-        const uint32_t idesc = umma_idesc_bf16(kTileRows, NT);
+        // One MMA of N = 2 NT per K step over [act_hi; act_lo] (act_lo follows
+        // act_hi in the stage, a whole number of swizzle atoms later).
+        const uint32_t idesc2 = umma_idesc_bf16(kTileRows, 2 * NT);
+        const uint32_t idesc1 = umma_idesc_bf16(kTileRows, NT);
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % NS, u = kb / NS;
             if (!mbar_wait_bounded(&full[s], u & 1)) timed_out = true;
@@ -692,13 +702,12 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
             tc_fence_after();
             const uint32_t a = smem_addr(smem + lay.ring + s * lay.stage_bytes);
             const uint32_t al = a + lay.a_bytes;  // A_lo (INT4 weights)
-            const uint32_t b = a + b_off, bl = b + lay.b_bytes;
+            const uint32_t b = a + b_off;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(b + 32 * k), idesc, (kb | k) != 0);
-                umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(bl + 32 * k), idesc, 1);
-                if (WT == 1)  // the weight's lo part against act's hi part
-                    umma_bf16(tmem, umma_desc_sw128(al + 32 * k), umma_desc_sw128(b + 32 * k), idesc, 1);
+                umma_bf16(tmem, umma_desc_sw128(a + 32 * k), umma_desc_sw128(b + 32 * k), idesc2, (kb | k) != 0);
+                if (WT == 1)  // the weight's lo part against act's hi part (columns [0, NT))
+                    umma_bf16(tmem, umma_desc_sw128(al + 32 * k), umma_desc_sw128(b + 32 * k), idesc1, 1);
             }
             umma_commit(&empty[s]);
         }
@@ -741,24 +750,32 @@ hc_tc_up_kernel(const TcUpParams p, const __grid_constant__ CUtensorMap map_u,
             }
         };
         const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16);
-        uint32_t va[16], vb[16];
-        int c0 = 16 * part;
-        if (c0 < NT)  // warp-uniform
+        // NT <= 128 = 2 kStride: at most two chunks per warp; the hi and lo
+        // columns of both are loaded before the one wait, then added.
+        static_assert(2 * kStride >= 128, "two chunks per warp cover NT");
+        uint32_t va[16], vb[16], wa[16], wb[16];
+        const int c0 = 16 * part;
+        if (c0 < NT) {  // warp-uniform
             tmem_ld16_async(tbase + c0, va);
-        tmem_wait_ld(va);
-#pragma unroll 1
-        for (; c0 < NT; c0 += 2 * kStride) {
-            if (c0 + kStride < NT)
-                tmem_ld16_async(tbase + c0 + kStride, vb);
-            process(c0, va);
-            tmem_wait_ld(vb);
-            if (c0 + kStride >= NT)
-                break;
-            if (c0 + 2 * kStride < NT)
-                tmem_ld16_async(tbase + c0 + 2 * kStride, va);
-            process(c0 + kStride, vb);
-            tmem_wait_ld(va);
+            tmem_ld16_async(tbase + NT + c0, wa);
         }
+        if (c0 + kStride < NT) {
+            tmem_ld16_async(tbase + c0 + kStride, vb);
+            tmem_ld16_async(tbase + NT + c0 + kStride, wb);
+        }
+        tmem_wait_ld(va);
+        tmem_wait_ld(wa);
+        tmem_wait_ld(vb);
+        tmem_wait_ld(wb);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            va[j] = __float_as_uint(__uint_as_float(va[j]) + __uint_as_float(wa[j]));
+            vb[j] = __float_as_uint(__uint_as_float(vb[j]) + __uint_as_float(wb[j]));
+        }
+        if (c0 < NT)
+            process(c0, va);
+        if (c0 + kStride < NT)
+            process(c0 + kStride, vb);
     }
     tc_fence_before();
     __syncthreads();
