@@ -469,6 +469,15 @@ hc_tc_down_kernel(const TcDownParams p, const __grid_constant__ CUtensorMap map_
 // kernel may read the prep kernel's normed tiles before its own.
 constexpr int kReduceBatch = 40;
 
+// A load through L2 that the compiler keeps in program order with the other
+// loads of a batch (volatile), so that the batch is in flight at once.
+__device__ __forceinline__ float ld_cg_f32(const float *ptr)
+{
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
+    return v;
+}
+
 __global__ void __launch_bounds__(1024) hc_tc_reduce_kernel(const TcReduceParams p)
 {
     if (threadIdx.x < 32) {
@@ -494,9 +503,15 @@ __global__ void __launch_bounds__(1024) hc_tc_reduce_kernel(const TcReduceParams
     float z = 0.f;
     for (int kc = 0; kc < p.nchunk; kc += kReduceBatch) {
         float v[kReduceBatch];
+        if (kc + kReduceBatch <= p.nchunk) {  // a whole batch: every load issued before the first add
 #pragma unroll
-        for (int j = 0; j < kReduceBatch; ++j)
-            v[j] = kc + j < p.nchunk ? src[(size_t)(kc + j) * cstride] : 0.f;
+            for (int j = 0; j < kReduceBatch; ++j)
+                v[j] = ld_cg_f32(src + (size_t)(kc + j) * cstride);
+        } else {
+#pragma unroll
+            for (int j = 0; j < kReduceBatch; ++j)
+                v[j] = kc + j < p.nchunk ? ld_cg_f32(src + (size_t)(kc + j) * cstride) : 0.f;
+        }
 #pragma unroll
         for (int j = 0; j < kReduceBatch; ++j)
             z += v[j];
