@@ -390,7 +390,7 @@ def measure_other_configs(B, inputs, torch, dev, stream, sets_bf16, peak):
     n = 2 * len(sets_bf16)
     ms = graph_ms(chain(raw, outs, gates, sets_bf16, n, mixed, ws, slots), 5)
     record(f"decode_m{Md2}_bf16", Md2, ms, n, bytes_per_call(Md2, sets_bf16[0].nbytes),
-           {"path": "two-token kernels (the one-token layout with a token loop)"})
+           {"path": "few-token kernels (the one-token layout with a token loop)"})
 
     # Prefill micro-batch: M = 128, attn_hc + inject then mlp_hc + inject per batch,
     # token t's gates at t*2C (attn) and t*2C + C (mlp).
@@ -463,7 +463,7 @@ def measure_other_configs(B, inputs, torch, dev, stream, sets_bf16, peak):
         b = (bytes_per_call(Me, mixers[0].nbytes, inject=False) + 2 * Me * C * H + 2 * Me * H + 4 * Me * C
              + V * H * 2 + 4 * Me * V)
         record(f"exit_logits_m{Me}_v{V}", Me, ms, n, b,
-               {"path": "inject-add fused into the exit mixer, then the lm_head GEMV (dependent launch)",
+               {"path": "inject-add fused into the exit mixer, then the tensor-core lm_head GEMM (dependent launch)",
                 "vocab": V})
     del lm
 
@@ -488,7 +488,7 @@ def measure_other_configs(B, inputs, torch, dev, stream, sets_bf16, peak):
         b = (W * H * 2 + H * H * 2 + Mq * H * 2 + 3 * W * 2 + W * 4 * 2 + 2 * 9 * W * 4 + 2 * Mq * W * 2
              + Mq * 16 * 4)
         record(f"ple_m{Mq}", Mq, ms, n, b,
-               {"path": "row gather, key/value projections (GEMV kernel), gate, causal conv + residual add"})
+               {"path": "row gather, key and value projections (one tensor-core GEMM launch), gate, causal conv + residual add"})
     del psets
 
     # Full-depth stack through the native driver (ts_hc_stack): entry replication,
