@@ -870,7 +870,7 @@ __host__ __device__ inline Up1Smem up1_layout(const UpParams &p)
 }
 
 // CC: the stream count when it is a compile-time constant (4), else 0.
-template <int WT, int CC>
+template <int WT, int CC, bool PF>
 __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -902,6 +902,10 @@ __global__ void __launch_bounds__(1024, 1) hc_up1_kernel(const UpParams p)
             bulk_copy_g2s(smem + lay.w + (size_t)c * HB * row_bytes,
                           static_cast<const unsigned char *>(p.up.data) + ((size_t)c * p.H + h0) * row_bytes,
                           (uint32_t)(row_bytes * hb), bar);
+    }
+    if constexpr (PF) {  // the next kernel's weights, after this CTA's own (a separate instance:
+        if (warp == 1)    // the branch alone slowed the one-token call by 0.1 us)
+            prefetch_share_l2(p.l2_pf, p.l2_pf_bytes, lane, 32);
     }
     if constexpr (WT == 1) {
         for (int i = tid; i < p.C * hb * ng; i += blockDim.x) {
@@ -1676,9 +1680,15 @@ cudaError_t launch_one_token(const DownParams &d, const UpParams &u, const Launc
     if (!one_token_ok(d, u))
         return cudaErrorInvalidConfiguration;
     void (*kd)(DownParams) = d.down.type == 0 ? hc_down1_kernel<0> : hc_down1_kernel<1>;
-    void (*ku)(UpParams) = u.up.type != 0 ? (u.C == 4 ? hc_up1_kernel<1, 4> : hc_up1_kernel<1, 0>)
-                           : u.C == 4     ? hc_up1_kernel<0, 4>
-                                          : hc_up1_kernel<0, 0>;
+    void (*ku)(UpParams);
+    if (u.l2_pf_bytes)
+        ku = u.up.type != 0 ? (u.C == 4 ? hc_up1_kernel<1, 4, true> : hc_up1_kernel<1, 0, true>)
+           : u.C == 4       ? hc_up1_kernel<0, 4, true>
+                            : hc_up1_kernel<0, 0, true>;
+    else
+        ku = u.up.type != 0 ? (u.C == 4 ? hc_up1_kernel<1, 4, false> : hc_up1_kernel<1, 0, false>)
+           : u.C == 4       ? hc_up1_kernel<0, 4, false>
+                            : hc_up1_kernel<0, 0, false>;
     const size_t sd = down1_layout(d).total, su = up1_layout(u).total;
     cudaError_t e = allow_smem(kd, sd);
     if (e == cudaSuccess)

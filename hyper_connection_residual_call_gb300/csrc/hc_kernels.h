@@ -100,6 +100,11 @@ struct UpParams {
     long gate_stride;
     // Optional debug output: w = sigmoid(up(act)) fp32 [M][W], or nullptr.
     float *w_out;
+    // One-token path: optional L2 prefetch, before the dependency wait, of the
+    // next kernel's weights (the exit's lm_head): 16-byte aligned, a multiple of
+    // 16 bytes, or 0.
+    const void *l2_pf;
+    size_t l2_pf_bytes;
 };
 
 struct InjectParams {

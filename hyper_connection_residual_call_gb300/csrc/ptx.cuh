@@ -100,6 +100,19 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Asks L2 to fetch this CTA's share of [base, base + bytes) (the grid's CTAs in
+// order, pieces of at most 16 KB), issued by `lanes` threads, this one being
+// `lane` of them. base 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_share_l2(const void *base, size_t bytes, int lane, int lanes)
+{
+    constexpr size_t kPiece = 16384;
+    const size_t nb = (size_t)gridDim.x * gridDim.y, b = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
+    const size_t share = ((bytes + nb - 1) / nb + 15) & ~size_t(15);
+    const size_t lo = min(bytes, b * share), hi = min(bytes, lo + share);
+    for (size_t off = lo + (size_t)lane * kPiece; off < hi; off += (size_t)lanes * kPiece)
+        bulk_prefetch_l2(static_cast<const unsigned char *>(base) + off, (uint32_t)min(kPiece, hi - off));
+}
+
 // ---- programmatic dependent launch -----------------------------------------
 
 // Lets the next kernel in the stream start launching (its blocks then wait in

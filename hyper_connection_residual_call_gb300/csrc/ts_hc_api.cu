@@ -292,7 +292,7 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
                        const ts_weight *up, const ts_weight *inject, void *mixed, float *inject_w,
                        long inject_stride, int M, int H, int C, int L, float eps, void *workspace,
                        size_t workspace_bytes, cudaStream_t stream, const ResidualIO *fi = nullptr,
-                       float *w_out = nullptr)
+                       float *w_out = nullptr, const void *l2_pf = nullptr, size_t l2_pf_bytes = 0)
 {
     ts_status st = check_shape(M, H, C, L);
     if (st != TS_OK)
@@ -473,6 +473,8 @@ ts_status hc_call_impl(const void *raw, const void *hc_norm_w, const ts_weight *
     u.inv_C = d.inv_C;
     u.status = dev.status;
     u.w_out = w_out;
+    u.l2_pf = l2_pf;
+    u.l2_pf_bytes = l2_pf_bytes;
     if (fi) {
         u.raw_out = fi->raw_out;
         u.inj_out = fi->out;
@@ -614,6 +616,17 @@ bool gates_overlap(const float *a, long sa, const float *b, long sb, int M, int 
 
 }  // namespace
 
+namespace {
+
+// Bytes of lm_head that the exit's one-token mixer asks L2 to prefetch: about what
+// HBM delivers beside the mixer's own weights in its ~5.5 us (12, 24 and 40 MB
+// measured: 32.1, 31.95, 32.2 us per exit against 33.3). The batched mixers take
+// none: 32, 48 and 80 MB from the tensor-core up kernel did not shorten an exit at
+// 16 tokens (41.1 us against 41.4, 41.3, 43.3).
+size_t exit_prefetch_bytes(int M) { return M == 1 ? (size_t)24 << 20 : 0; }
+
+}  // namespace
+
 extern "C" {
 
 ts_status ts_hc_inject_call(void *raw, const void *out, const float *prev_inject_w, long prev_inject_stride,
@@ -669,8 +682,11 @@ ts_status ts_hc_exit_logits(void *raw, const void *out, const float *prev_inject
         return st;
     const ResidualIO io{(long)C * H, H, static_cast<uint16_t *>(raw), static_cast<const uint16_t *>(out),
                         prev_inject_w, prev_inject_stride};
+    // While a one-token mixer runs, its up kernel asks L2 for the first part of
+    // lm_head (the lm_head kernel then streams that part from L2, not HBM).
+    const size_t pf = std::min(exit_prefetch_bytes(M), (size_t)V * H * 2) & ~size_t(15);
     st = hc_call_impl(raw, hc_norm_w, down, up, nullptr, mixed, nullptr, 0, M, H, C, lowrank, eps, workspace,
-                      workspace_bytes, stream, out ? &io : nullptr);
+                      workspace_bytes, stream, out ? &io : nullptr, nullptr, lm_head, pf);
     if (st != TS_OK)
         return st;
     // lm_head over tiles of at most kLmHeadMaxTokens tokens, each a dependent of the launch before it.

@@ -229,7 +229,8 @@ ts_status ts_hc_inject_call(void *raw, const void *out, const float *prev_inject
  * lm_head runs on the tensor cores (bf16 operands, fp32 accumulation) in
  * launches of at most 16 tokens; each launches as a programmatic dependent of
  * the kernel before it and streams its first weight tiles before that kernel
- * has finished.
+ * has finished. With one token the mixer's up kernel also asks L2 to prefetch
+ * the first 24 MB of lm_head while the mixer runs.
  *
  *   raw             bf16 [M][C*H]; read, and written with the fused inject-add
  *   out, prev_inject_w, prev_inject_stride   as for ts_hc_inject_call, or
