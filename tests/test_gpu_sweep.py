@@ -8,7 +8,9 @@ Each runs the previous sublayer's inject-add fused into a call
 (`ts_hc_inject_call`: families/qwen4/mod.rs, decoder pseudocode, an inject-add
 followed by the next attn_hc / mlp_hc) and then the exit mixer on the result,
 and compares the residual, mixed, the gates, inv_rms and act with the fp64
-oracle fed the same inputs.
+oracle fed the same inputs; and the entry replication fused into a first call
+(`ts_hc_entry_call`) followed by `ts_hc_call_debug`, whose up-projection output
+w = sigmoid(up(act)) (mod.rs "Hyper-connections") is compared itself.
 """
 import numpy as np
 import pytest
@@ -33,12 +35,15 @@ def _cases(n=28, seed=20261203):
         L = int(rng.choice([8, 24, 32, 64, 96, 128, 192]))
         kind, group = "bf16", 64
         if H % 64 == 0 and L % 32 == 0 and rng.random() < 0.4:
-            kind, group = "int4", (64 if L % 64 == 0 and rng.random() < 0.5 else 32)
+            groups = [g for g in (128, 64, 32) if L % g == 0 and H % g == 0]
+            kind, group = "int4", groups[sum(c[5] == "int4" for c in out) % len(groups)]
         out.append((i, M, H, C, L, kind, group))
     return out
 
 
-CASES = _cases()
+# plus INT4 with groups of 128 on the one-token, cluster and tensor-core paths
+CASES = _cases() + [(28, 1, 256, 2, 128, "int4", 128), (29, 3, 384, 3, 256, "int4", 128),
+                    (30, 16, 512, 4, 128, "int4", 128)]
 
 
 def test_sweep_covers_every_path():
@@ -55,6 +60,8 @@ def test_sweep_covers_every_path():
         else:
             kinds.add("cluster")
     assert kinds >= {"one-token", "few-token", "tensor-core bf16", "tensor-core int4", "cluster"}, kinds
+    groups = {c[6] for c in CASES if c[5] == "int4"}
+    assert groups >= {32, 64, 128}, groups
 
 
 @pytest.fixture(scope="module")
@@ -109,3 +116,26 @@ def test_fused_call_then_mixer(orc, case):
     mixed2 = B.hc_mixer(raw_d, wm_d, H=H, C=C, eps=EPS)
     torch.cuda.synchronize()
     check_bf16(mixed2, ref_mix["mixed"], f"{tag} exit mixer")
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-M{c[1]}-H{c[2]}-C{c[3]}-L{c[4]}-{c[5]}")
+def test_entry_call_then_w(orc, case):
+    i, M, H, C, L, kind, group = case
+    seed = 9000 + i
+    w = inputs.make_hc_weights(H, C, L, seed, 0, kind=kind, group=group)
+    emb = inputs.make_residual(M, H, 1, seed)  # [M][H]
+    rep = orc.replicate_entry(emb, H=H, C=C)
+    ref = orc.hc_call(rep, w.g, w.down, w.up, w.inject, H=H, C=C, L=L, eps=EPS, want_w=True)
+
+    w_d = w.to("cuda")
+    tag = f"{kind} M={M} H={H} C={C} L={L} group={group}"
+    raw, mixed, gates = B.hc_entry_call(emb.cuda(), w_d, C=C, eps=EPS)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(raw), rep), f"{tag}: replicated residual"
+    check_bf16(mixed, ref["mixed"], f"{tag} entry call mixed")
+    check_fp32(gates, ref["gate"], f"{tag} entry call gates")
+
+    mixed2, gates2, wv = B.hc_call_debug(raw, w_d, H=H, C=C, eps=EPS)
+    torch.cuda.synchronize()
+    check_bf16(mixed2, ref["mixed"], f"{tag} mixed")
+    check_fp32(wv, ref["w"], f"{tag} w = sigmoid(up(act))")
