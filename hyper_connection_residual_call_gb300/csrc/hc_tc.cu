@@ -11,14 +11,17 @@
 //                      stored as bf16 hi + lo (normed = hi + lo to ~16
 //                      significant bits), so that the GEMMs keep fp32-level
 //                      accuracy with bf16 operands.
-//  hc_tc_down_kernel   D[128 rows][N tokens] = W[rows][K chunk] * normed^T, two
-//                      MMAs per K step (hi, lo); CTA (chunk, row tile, token
-//                      tile) writes its fp32 partial tile to part[chunk][token][row].
+//  hc_tc_down_kernel   D[128 rows][N tokens] = W[rows][K chunk] * normed^T, one
+//                      MMA of N = 2 * tokens per K step over the stacked hi and
+//                      lo tiles (their column halves added in the epilogue);
+//                      CTA (chunk, row tile, token tile) writes its fp32
+//                      partial tile to part[chunk][token][row].
 //  hc_tc_reduce_kernel z = sum over chunks (fixed order); act = silu(z / C)
 //                      (fp32, and bf16 hi + lo for the up GEMM), gates =
 //                      2 sigmoid(z / C).
 //  hc_tc_up_kernel     D[C*HBt rows][N] = Wu[rows {c*H + h}][L] * (act_hi + act_lo)^T,
-//                      two MMAs per K step, epilogue: w = sigmoid(D),
+//                      one stacked MMA per K step as in the down kernel,
+//                      epilogue: w = sigmoid(D),
 //                      mixed[h] = mean_c w * normed, with the normed tile
 //                      (hi + lo) staged by TMA. act keeps ~16 significant bits
 //                      so that w meets the fp32 bar where the sigmoid leaves
