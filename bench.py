@@ -621,19 +621,21 @@ def run_ours(args):
             print(f"ran {args.profile_exit or args.profile_ple} M={Mx} {what} (profiling run)")
         return
     if args.profile_graph:
-        # Replays of one CUDA graph of 8 dependent fused M-token calls (the prefill
-        # chain of other_configs), for a profiler that measures whole graphs: DRAM
-        # traffic of the chain as the kernels overlap in it.
+        # Replays of one CUDA graph of dependent fused M-token calls, for a profiler
+        # that measures whole graphs: DRAM traffic of the chain as the kernels
+        # overlap in it. One distinct weight set per call, more bytes of them than
+        # the 129 MB L2 holds (16 bf16 sets of 13.2 MB, 48 INT4 sets of 3.8 MB), so
+        # that a replay does not find the previous replay's weights in L2.
         Mp = args.profile_tokens
-        psets = sets[:8] if not args.profile_int4 else [
-            inputs.make_hc_weights(H, C, L, 4, i, kind="int4").to(dev) for i in range(8)]
+        psets = sets[:16] if not args.profile_int4 else [
+            inputs.make_hc_weights(H, C, L, 4, i, kind="int4").to(dev) for i in range(48)]
         rawp = inputs.make_residual(Mp, H, C, 2).to(dev)
         outp = [inputs.make_sublayer_out(Mp, H, 2, i).to(dev) for i in range(2)]
         gatep = torch.zeros((Mp, 2 * C), dtype=torch.float32, device=dev)
         slots = [(gatep[:, :C], 2 * C), (gatep[:, C:], 2 * C)]
         mixedp = torch.empty((Mp, H), dtype=torch.bfloat16, device=dev)
         wsp2 = B.workspace(Mp, H, C, L, dev)
-        body = fused_chain(B, rawp, outp, psets, 8, mixedp, wsp2, slots)
+        body = fused_chain(B, rawp, outp, psets, len(psets), mixedp, wsp2, slots)
         with torch.cuda.stream(stream):
             body()
         stream.synchronize()
@@ -645,7 +647,7 @@ def run_ours(args):
                 g.replay()
         stream.synchronize()
         if rank == 0:
-            print(f"replayed a graph of 8 M={Mp} fused calls {args.profile_graph} times (profiling run)")
+            print(f"replayed a graph of {len(psets)} M={Mp} fused calls {args.profile_graph} times (profiling run)")
         return
     if args.profile_calls:
         # A short eager chain of the fused call for a profiler that captures
@@ -853,8 +855,9 @@ def main():
     ap.add_argument("--profile-ple", type=int, default=0,
                     help="eager PLE gates at M = --profile-tokens, for a profiler")
     ap.add_argument("--profile-graph", type=int, default=0,
-                    help="replays of a CUDA graph of 8 fused M-token calls (--profile-tokens, --profile-int4), "
-                         "for a profiler that measures whole graphs; no timing")
+                    help="replays of a CUDA graph of fused M-token calls over distinct weight sets larger than "
+                         "L2 in all (--profile-tokens, --profile-int4), for a profiler that measures whole graphs; "
+                         "no timing")
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="run this many eager fused calls of the workload and exit (for ncu captures)")
     args = ap.parse_args()
